@@ -1,0 +1,174 @@
+"""CPU oracle for the ragged grouped GEMM — TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline / reference
+leg of ``bench.py`` may import this package.  The product path (the
+``ragged_matmul_gb300`` package and its CUDA library) never does, and shares
+no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain C, one thread per slice of output
+rows); this module only compiles it with gcc, loads it with ctypes and
+marshals numpy arrays.  See ``oracle.c`` for the definition it implements and
+the page sections it follows (Modular "grouped_matmul_sm100_persistent",
+section "Args"; Modular "multistage_gemm_q", section "Parameters").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+BAD_OFFSETS = 1
+BAD_EXPERT_ID = 2
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so beside it (portable flags: x86_64 and aarch64)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(
+            ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-pthread",
+             "-o", tmp, _SRC, "-lm"],
+            check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        I = ctypes.c_int
+        lib.oracle_gmm_bf16.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I]
+        lib.oracle_gmm_bf16.restype = I
+        lib.oracle_gmm_int4.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I]
+        lib.oracle_gmm_int4.restype = I
+        lib.oracle_dequant_int4.argtypes = [P, P, P, I, I, I]
+        lib.oracle_dequant_int4.restype = None
+        lib.oracle_round_bf16_array.argtypes = [P, P, ctypes.c_int64]
+        lib.oracle_round_bf16_array.restype = None
+        lib.oracle_validate.argtypes = [P, P, I, I, P]
+        lib.oracle_validate.restype = I
+        _lib = lib
+    return _lib
+
+
+def _ptr(x):
+    return None if x is None else x.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c_u16(x, shape=None):
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    if shape is not None:
+        assert x.shape == tuple(shape), (x.shape, shape)
+    return x
+
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover - non-Linux
+        return os.cpu_count() or 1
+
+
+@dataclass
+class OracleResult:
+    c: np.ndarray          # uint16 bf16 bits [rows_alloc, N]; untouched rows keep c_init
+    ref32: np.ndarray      # float32 sums (NaN where no active group wrote)
+    ref64: np.ndarray | None
+    stats: np.ndarray      # uint32 copy of expert_usage_stats after the call
+    flags: int             # BAD_OFFSETS | BAD_EXPERT_ID
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """fp32 -> bf16 bits, round to nearest even (the oracle's own rounding)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_round_bf16_array(_ptr(out), _ptr(x), x.size)
+    return out
+
+
+def validate(a_offsets, expert_ids, num_experts: int):
+    off = np.ascontiguousarray(a_offsets, dtype=np.uint32)
+    ids = np.ascontiguousarray(expert_ids, dtype=np.int32)
+    cnt = np.zeros(1, dtype=np.uint32)
+    flags = _load().oracle_validate(_ptr(off), _ptr(ids), ids.size, num_experts, _ptr(cnt))
+    return flags, int(cnt[0])
+
+
+def gmm_bf16(a_bits, a_offsets, b_bits, expert_ids, *, c_init=None, stats_init=None,
+             want64: bool = False, nthreads: int | None = None) -> OracleResult:
+    """Grouped GEMM on bf16 bit arrays: a [rows, K], b [E, N, K]."""
+    a = _c_u16(a_bits)
+    b = _c_u16(b_bits)
+    E, N, K = b.shape
+    rows = a.shape[0]
+    assert a.shape[1] == K
+    off = np.ascontiguousarray(a_offsets, dtype=np.uint32)
+    ids = np.ascontiguousarray(expert_ids, dtype=np.int32)
+    G = ids.size
+    assert off.size == G + 1
+    c = (np.zeros((rows, N), np.uint16) if c_init is None
+         else np.array(c_init, dtype=np.uint16, copy=True).reshape(rows, N))
+    ref32 = np.full((rows, N), np.nan, np.float32)
+    ref64 = np.full((rows, N), np.nan, np.float64) if want64 else None
+    stats = (np.zeros(4, np.uint32) if stats_init is None
+             else np.array(stats_init, dtype=np.uint32, copy=True))
+    flags = _load().oracle_gmm_bf16(
+        _ptr(c), _ptr(ref32), _ptr(ref64), _ptr(a), _ptr(off), _ptr(b), _ptr(ids), _ptr(stats),
+        G, E, N, K, nthreads or default_threads())
+    if flags < 0:
+        raise MemoryError("oracle allocation failed")
+    return OracleResult(c, ref32, ref64, stats, flags)
+
+
+def dequant_int4(packed, scales, group_size: int) -> np.ndarray:
+    """packed [N, K/8] uint32 + scales [N, K/group_size] bf16 bits -> bf16 bits [N, K]."""
+    p = np.ascontiguousarray(packed, dtype=np.uint32)
+    s = _c_u16(scales)
+    N, kw = p.shape
+    K = kw * 8
+    assert s.shape == (N, K // group_size)
+    w = np.empty((N, K), np.uint16)
+    _load().oracle_dequant_int4(_ptr(w), _ptr(p), _ptr(s), N, K, group_size)
+    return w
+
+
+def gmm_int4(a_bits, a_offsets, packed, scales, expert_ids, *, group_size: int = 128,
+             c_init=None, stats_init=None, want64: bool = False,
+             nthreads: int | None = None) -> OracleResult:
+    """4-bit grouped GEMM: packed [E, N, K/8] uint32, scales [E, N, K/group_size] bf16 bits."""
+    a = _c_u16(a_bits)
+    p = np.ascontiguousarray(packed, dtype=np.uint32)
+    s = _c_u16(scales)
+    E, N, kw = p.shape
+    K = kw * 8
+    rows = a.shape[0]
+    assert a.shape[1] == K and s.shape == (E, N, K // group_size)
+    off = np.ascontiguousarray(a_offsets, dtype=np.uint32)
+    ids = np.ascontiguousarray(expert_ids, dtype=np.int32)
+    G = ids.size
+    assert off.size == G + 1
+    c = (np.zeros((rows, N), np.uint16) if c_init is None
+         else np.array(c_init, dtype=np.uint16, copy=True).reshape(rows, N))
+    ref32 = np.full((rows, N), np.nan, np.float32)
+    ref64 = np.full((rows, N), np.nan, np.float64) if want64 else None
+    stats = (np.zeros(4, np.uint32) if stats_init is None
+             else np.array(stats_init, dtype=np.uint32, copy=True))
+    flags = _load().oracle_gmm_int4(
+        _ptr(c), _ptr(ref32), _ptr(ref64), _ptr(a), _ptr(off), _ptr(p), _ptr(s), _ptr(ids),
+        _ptr(stats), G, E, N, K, group_size, nthreads or default_threads())
+    if flags == -2:
+        raise ValueError("K must be a multiple of 8 and of group_size")
+    if flags < 0:
+        raise MemoryError("oracle allocation failed")
+    return OracleResult(c, ref32, ref64, stats, flags)

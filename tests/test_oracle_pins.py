@@ -1,0 +1,347 @@
+"""Pins for the CPU oracle, checked against things other than itself.
+
+Each test ties the oracle to something fixed outside its own code: hand-worked
+values (tests/golden), a library routine the special case reduces to (numpy
+matmul / einsum in fp64, torch's bf16 cast), closed forms, invariants, and
+brute force on tiny inputs.  Together they fail on a dropped term, a wrong
+sign, a transposed operand, a wrong expert index, a wrong skip rule, a wrong
+stats entry, a wrong nibble order, zero point or scale index.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from ragged_matmul_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_bits(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_f32(h):
+    return (np.asarray(h, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------------ rounding
+
+def test_round_bf16_matches_torch_cast():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * 10,
+        (rng.integers(0, 2**32, 20000, dtype=np.uint64).astype(np.uint32)).view(np.float32),
+        np.array([0.0, -0.0, np.inf, -np.inf, 1.0 + 2**-8, 1.0 + 3 * 2**-8, 1e-40, -1e-40,
+                  3.3895314e38, 3.40282e38], np.float32),
+    ])
+    # exact ties: upper 16 bits arbitrary, lower 16 bits = 0x8000
+    ties = ((rng.integers(0, 2**16, 5000).astype(np.uint32) << 16) | 0x8000).view(np.float32)
+    x = np.concatenate([x, ties])
+    mine = oracle.round_bf16(x)
+    ref = bf16_bits(x)
+    nan = np.isnan(x)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert np.all(np.isnan(bits_to_f32(mine[nan])))
+
+
+# ------------------------------------------------------------------ hand-worked fixtures
+
+def _parse_golden_bf16():
+    lines = [l.split() for l in open(os.path.join(GOLDEN, "hand_worked_bf16.txt")) if l.strip() and not l.startswith("#")]
+    d, i = {}, 0
+    while i < len(lines):
+        key = lines[i][0]
+        if key in ("E", "N", "K", "stats1"):
+            d[key] = int(lines[i][1]); i += 1
+        elif key in ("offsets", "ids"):
+            d[key] = [int(v) for v in lines[i][1:]]; i += 1
+        elif key in ("A", "B0", "B1", "C"):
+            rows = []
+            i += 1
+            while i < len(lines) and lines[i][0] not in ("A", "B0", "B1", "C", "stats1"):
+                rows.append(lines[i]); i += 1
+            d[key] = rows
+        else:
+            raise ValueError(key)
+    return d
+
+
+def test_hand_worked_bf16_example():
+    d = _parse_golden_bf16()
+    A = np.array([[float(v) for v in r] for r in d["A"]], np.float32)
+    B = np.stack([np.array([[float(v) for v in r] for r in d[f"B{e}"]], np.float32) for e in range(d["E"])])
+    assert B.shape == (d["E"], d["N"], d["K"])
+    c0 = wl.sentinel_c(A.shape[0], d["N"])
+    res = oracle.gmm_bf16(bf16_bits(A), d["offsets"], bf16_bits(B), d["ids"], c_init=c0,
+                          stats_init=np.full(4, wl.SENTINEL_STATS, np.uint32))
+    assert res.flags == 0
+    for r, row in enumerate(d["C"]):
+        for n, v in enumerate(row):
+            if v == "untouched":
+                assert res.c[r, n] == wl.SENTINEL_BF16
+            else:
+                assert bits_to_f32(res.c[r, n]) == float(v), (r, n)
+    assert res.stats[1] == d["stats1"]
+    assert res.stats[0] == wl.SENTINEL_STATS and res.stats[2] == wl.SENTINEL_STATS
+
+
+def test_hand_worked_int4_example():
+    d = {}
+    for l in open(os.path.join(GOLDEN, "hand_worked_int4.txt")):
+        if l.strip() and not l.startswith("#"):
+            k, *v = l.split()
+            d[k] = v
+    K, gs = int(d["K"][0]), int(d["group_size"][0])
+    words = np.array([[int(w, 16) for w in d["words"]]], np.uint32)
+    scales = bf16_bits(np.array([[float(s) for s in d["scales"]]], np.float32))
+    w = oracle.dequant_int4(words, scales, gs)
+    assert np.array_equal(bits_to_f32(w[0]), np.array([float(v) for v in d["W"]], np.float32))
+    A = np.zeros((3, K), np.float32)
+    A[0] = 1.0
+    A[1, 3] = 1.0
+    A[2, 9] = 1.0
+    res = oracle.gmm_int4(bf16_bits(A), [0, 3], words[None], scales[None], [0], group_size=gs)
+    got = bits_to_f32(res.c[:, 0])
+    assert got.tolist() == [float(d["A_ones"][0]), float(d["A_unit3"][0]), float(d["A_unit9"][0])]
+
+
+# ------------------------------------------------------------------ library special cases
+
+def _rand_problem(seed, E, N, K, loads, ids, base=0, dist=("uniform", -1.0, 1.0)):
+    r = wl.make_routing("t", E, N, K, loads, ids, a_dist=dist, b_dist=dist, base=base)
+    v = wl.host_values(r, seed)
+    return r, v
+
+
+def test_single_group_is_dense_matmul():
+    """G = 1 reduces to C = A @ B[e]^T; fp32 accumulation stays within its error bound."""
+    r, v = _rand_problem(1, E=3, N=40, K=72, loads=[37], ids=[2])
+    res = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, want64=True)
+    A = bits_to_f32(v["a"]).astype(np.float64)
+    B = bits_to_f32(v["b"]).astype(np.float64)
+    exact = A @ B[2].T
+    bound = r.K * 2.0**-24 * (np.abs(A) @ np.abs(B[2]).T) * 1.01 + 1e-30
+    assert np.all(np.abs(res.ref32 - exact) <= bound)
+    assert np.allclose(res.ref64, exact, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(res.c, bf16_bits(res.ref32))
+
+
+def test_multi_group_matches_gathered_einsum():
+    """Per-row expert gather + einsum (a different route) agrees with the oracle's fp64 sums."""
+    loads = [5, 0, 9, 1, 14, 3, 7]
+    ids = [3, 0, -1, 1, 3, 2, -1]
+    r, v = _rand_problem(2, E=4, N=24, K=40, loads=loads, ids=ids)
+    res = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, want64=True,
+                          c_init=wl.sentinel_c(r.rows, r.N))
+    expert_of_row = np.repeat(np.asarray(ids), loads)
+    live = expert_of_row >= 0
+    A = bits_to_f32(v["a"]).astype(np.float64)
+    B = bits_to_f32(v["b"]).astype(np.float64)
+    ref = np.einsum("rk,rnk->rn", A[live], B[expert_of_row[live]])
+    assert np.allclose(res.ref64[live], ref, rtol=1e-12, atol=1e-12)
+    assert np.all(res.c[~live] == wl.SENTINEL_BF16)
+    assert res.stats[1] == 5
+
+
+def test_unit_rows_select_weight_entries():
+    """A row equal to the unit vector e_k yields C[r, n] = B[e, n, k] exactly (pins B's layout)."""
+    E, N, K = 3, 5, 7
+    rng = np.random.default_rng(3)
+    B = bf16_bits(rng.uniform(-2, 2, (E, N, K)).astype(np.float32))
+    loads, ids = [K, K, K], [2, 0, 1]
+    A = np.zeros((3 * K, K), np.float32)
+    for g in range(3):
+        for k in range(K):
+            A[g * K + k, k] = 1.0
+    res = oracle.gmm_bf16(bf16_bits(A), wl.offsets_from_loads(loads), B, ids)
+    for g in range(3):
+        for k in range(K):
+            assert np.array_equal(res.c[g * K + k], B[ids[g], :, k])
+
+
+def test_small_integers_are_exact():
+    """Integer operands in [-3, 3]: every sum is an exact integer; compare with int64 matmul."""
+    rng = np.random.default_rng(4)
+    E, N, K = 4, 48, 28
+    loads, ids = [6, 11, 0, 17, 4], [1, 3, 0, -1, 2]
+    off = wl.offsets_from_loads(loads)
+    Ai = rng.integers(-3, 4, (off[-1], K))
+    Bi = rng.integers(-3, 4, (E, N, K))
+    res = oracle.gmm_bf16(bf16_bits(Ai), off, bf16_bits(Bi), ids)
+    for g, e in enumerate(ids):
+        if e < 0:
+            continue
+        rows = slice(off[g], off[g + 1])
+        want = Ai[rows] @ Bi[e].T
+        assert np.array_equal(bits_to_f32(res.c[rows]), want.astype(np.float32))
+
+
+# ------------------------------------------------------------------ invariants
+
+def test_group_permutation_invariance():
+    loads = [13, 2, 0, 21, 8, 5]
+    ids = [1, 0, 2, -1, 3, 1]
+    r, v = _rand_problem(5, E=4, N=32, K=64, loads=loads, ids=ids)
+    base = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, c_init=wl.sentinel_c(r.rows, r.N))
+    perm = np.random.default_rng(6).permutation(len(loads))
+    off = r.a_offsets.astype(np.int64)
+    blocks = [np.arange(off[g], off[g + 1]) for g in range(len(loads))]
+    row_perm = np.concatenate([blocks[g] for g in perm]).astype(np.int64)
+    loads_p = np.asarray(loads)[perm]
+    ids_p = np.asarray(ids)[perm]
+    res = oracle.gmm_bf16(v["a"][row_perm], wl.offsets_from_loads(loads_p), v["b"], ids_p,
+                          c_init=wl.sentinel_c(r.rows, r.N))
+    assert np.array_equal(res.c, base.c[row_perm])
+    assert res.stats[1] == base.stats[1]
+
+
+def test_skipped_groups_with_rows_stay_untouched_and_stats_count():
+    loads = [4, 9, 3, 0, 6]
+    ids = [-1, 2, -7, 1, -1]
+    r, v = _rand_problem(7, E=3, N=16, K=32, loads=loads, ids=ids, base=5)
+    rows_alloc = r.rows + 3            # rows before a_offsets[0] and after a_offsets[G] exist too
+    a = np.concatenate([v["a"], v["a"][:3]])
+    c0 = wl.sentinel_c(rows_alloc, r.N)
+    stats0 = np.array([11, 22, 33, 44], np.uint32)
+    res = oracle.gmm_bf16(a, r.a_offsets, v["b"], r.expert_ids, c_init=c0, stats_init=stats0)
+    live = np.zeros(rows_alloc, bool)
+    live[r.a_offsets[1]:r.a_offsets[2]] = True
+    assert np.all(res.c[~live] == wl.SENTINEL_BF16)
+    assert not np.any(res.c[live] == wl.SENTINEL_BF16)
+    assert res.stats.tolist() == [11, 2, 33, 44]      # ids 2 and 1 are active (the empty group counts)
+
+
+def test_invalid_inputs_are_flagged():
+    b = np.zeros((2, 8, 8), np.uint16)
+    a = np.zeros((10, 8), np.uint16)
+    c0 = wl.sentinel_c(10, 8)
+    res = oracle.gmm_bf16(a, [0, 6, 4, 10], b, [0, 1, 0], c_init=c0)
+    assert res.flags & oracle.BAD_OFFSETS
+    assert np.all(res.c == wl.SENTINEL_BF16)            # nothing computed
+    assert res.stats[1] == 3
+    res = oracle.gmm_bf16(a, [0, 4, 10], b, [0, 2], c_init=c0)
+    assert res.flags == oracle.BAD_EXPERT_ID
+    assert np.all(res.c[4:] == wl.SENTINEL_BF16) and not np.any(res.c[:4] == wl.SENTINEL_BF16)
+    assert res.stats[1] == 1
+
+
+def test_empty_problem_writes_only_stats():
+    b = np.zeros((2, 8, 8), np.uint16)
+    res = oracle.gmm_bf16(np.zeros((0, 8), np.uint16), [0], b, np.zeros(0, np.int32),
+                          stats_init=np.full(4, 7, np.uint32))
+    assert res.stats.tolist() == [7, 0, 7, 7] and res.flags == 0
+
+
+def test_fp32_result_within_bound_of_fp64():
+    r, v = _rand_problem(8, E=2, N=64, K=1024, loads=[40, 30], ids=[1, 0], dist=("normal", 1.0))
+    res = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, want64=True)
+    A = np.abs(bits_to_f32(v["a"]).astype(np.float64))
+    B = np.abs(bits_to_f32(v["b"]).astype(np.float64))
+    expert_of_row = np.repeat(r.expert_ids, r.loads)
+    bound = r.K * 2.0**-24 * np.einsum("rk,rnk->rn", A, B[expert_of_row])
+    assert np.all(np.abs(res.ref32 - res.ref64) <= bound)
+
+
+def test_thread_count_does_not_change_bits():
+    r, v = _rand_problem(9, E=3, N=40, K=96, loads=[17, 3, 29, 1], ids=[0, 2, 1, 0])
+    one = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, nthreads=1)
+    many = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, nthreads=7)
+    assert np.array_equal(one.c, many.c)
+    assert np.array_equal(one.ref32.view(np.uint32), many.ref32.view(np.uint32))
+
+
+def test_tiny_workload_brute_force():
+    """The tiny named workload against plain Python loops in double precision."""
+    r = wl.routing("tiny")
+    v = wl.host_values(r, 0)
+    res = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, want64=True,
+                          c_init=wl.sentinel_c(r.rows, r.N))
+    A = bits_to_f32(v["a"]).tolist()
+    B = bits_to_f32(v["b"])
+    rng = np.random.default_rng(10)
+    off = r.a_offsets.tolist()
+    for g, e in enumerate(r.expert_ids.tolist()):
+        for row in range(off[g], off[g + 1]):
+            for n in rng.choice(r.N, 24, replace=False):
+                if e < 0:
+                    assert res.c[row, n] == wl.SENTINEL_BF16
+                    continue
+                w = B[e, n].tolist()
+                s = 0.0
+                for k in range(r.K):
+                    s += A[row][k] * w[k]
+                assert abs(res.ref64[row, n] - s) <= 1e-12 * (1 + abs(s))
+                assert abs(res.ref32[row, n] - s) <= 1e-4
+    assert res.stats[1] == 3
+
+
+# ------------------------------------------------------------------ 4-bit variant
+
+def test_int4_dequant_matches_independent_unpack():
+    rng = np.random.default_rng(11)
+    N, K, gs = 6, 64, 16
+    q = rng.integers(0, 16, (N, K))
+    words = np.zeros((N, K // 8), np.uint64)
+    for k in range(K):                                    # pack by explicit place value
+        words[:, k // 8] += q[:, k].astype(np.uint64) * (16 ** (k % 8))
+    words = words.astype(np.uint32)
+    s = rng.uniform(0.005, 0.02, (N, K // gs)).astype(np.float32)
+    sb = bf16_bits(s)
+    w = oracle.dequant_int4(words, sb, gs)
+    want = bf16_bits((q - 8).astype(np.float32) * np.repeat(bits_to_f32(sb), gs, axis=1))
+    assert np.array_equal(w, want)
+    # the generator's packer agrees with the place-value packing
+    assert np.array_equal(wl.pack_nibbles(q), words)
+
+
+def test_int4_zero_point_gives_zero():
+    N, K = 8, 32
+    words = wl.pack_nibbles(np.full((1, N, K), 8))
+    scales = bf16_bits(np.full((1, N, K // 16), 0.013, np.float32))
+    a = bf16_bits(np.random.default_rng(12).standard_normal((5, K)).astype(np.float32))
+    res = oracle.gmm_int4(a, [0, 5], words, scales, [0], group_size=16)
+    assert np.all(bits_to_f32(res.c) == 0.0)
+
+
+def test_int4_integer_case_is_exact():
+    rng = np.random.default_rng(13)
+    E, N, K, gs = 3, 16, 64, 32
+    q = rng.integers(0, 16, (E, N, K))
+    scales = bf16_bits(np.ones((E, N, K // gs), np.float32))
+    Ai = rng.integers(-2, 3, (20, K))
+    loads, ids = [7, 0, 13], [2, 1, 0]
+    off = wl.offsets_from_loads(loads)
+    res = oracle.gmm_int4(bf16_bits(Ai), off, wl.pack_nibbles(q), scales, ids, group_size=gs)
+    for g, e in enumerate(ids):
+        rows = slice(off[g], off[g + 1])
+        assert np.array_equal(bits_to_f32(res.c[rows]), (Ai[rows] @ (q[e] - 8).T).astype(np.float32))
+
+
+def test_int4_equals_bf16_path_on_dequantised_weights():
+    """The 4-bit oracle is the bf16 oracle applied to the dequantised weights."""
+    r = wl.make_routing("q", 4, 32, 256, [9, 0, 23, 4], [3, 1, -1, 0], a_dist=("normal", 1.0),
+                        b_dist=None, int4=True, group_size=128)
+    v = wl.host_values(r, 14)
+    res4 = oracle.gmm_int4(v["a"], r.a_offsets, v["packed"], v["scales"], r.expert_ids, group_size=128)
+    w = np.stack([oracle.dequant_int4(v["packed"][e], v["scales"][e], 128) for e in range(r.E)])
+    res16 = oracle.gmm_bf16(v["a"], r.a_offsets, w, r.expert_ids)
+    assert np.array_equal(res4.c, res16.c)
+    assert res4.stats[1] == res16.stats[1] == 3
+
+
+# ------------------------------------------------------------------ generators
+
+def test_named_routings_have_the_stated_structure():
+    t = wl.routing("tiny")
+    assert t.loads.tolist() == [3, 17, 0, 40] and t.expert_ids.tolist() == [2, 0, -1, 3]
+    d = wl.routing("decode")
+    assert d.rows == 2048 and d.G == 64 and (d.N, d.K) == (2816, 2048)
+    p = wl.routing("prefill")
+    assert p.rows == 32768 and np.all(np.abs(p.loads - 4096) <= 409.6)
+    f = wl.routing("fine_grained")
+    assert f.rows == 32768 and int((f.expert_ids < 0).sum()) == 13 and (f.N, f.K) == (4096, 7168)
+    q = wl.routing("int4")
+    assert q.rows == 8192 and q.int4 and (q.N, q.K, q.group_size) == (4096, 4096, 128)
