@@ -1,0 +1,120 @@
+/*
+ * gmm.h — C ABI of the GB300 (sm_103a) ragged grouped GEMM library (libgmm.so).
+ *
+ * The operation (Modular "grouped_matmul_sm100_persistent" API page, section
+ * "Args"): for every group g whose expert id e = expert_ids[g] satisfies
+ * 0 <= e < num_experts,
+ *
+ *     C[r, n] = bf16( sum_k A[r, k] * B[e, n, k] )
+ *         for r in [a_offsets[g], a_offsets[g+1]), n in [0, N)
+ *
+ * accumulated in fp32 on the tensor cores and rounded to nearest even.
+ *   - A  : bf16 [rows, K], row-major (K contiguous).  rows >= a_offsets[num_groups].
+ *   - B  : bf16 [num_experts, N, K], row-major — the transposed-B convention of the
+ *          page (each expert's weight matrix is stored N x K).
+ *   - C  : bf16 [rows, N], row-major.
+ *   - a_offsets          : uint32 [num_groups + 1], non-decreasing prefix sum of rows per group.
+ *   - expert_ids         : int32  [num_groups]; a negative id skips the group.
+ *   - expert_usage_stats : uint32 [>= 2]; index 1 receives the number of groups with
+ *                          0 <= id < num_experts.  No other entry is read or written.
+ * Rows of C that no active group covers keep their previous contents, bit for bit.
+ *
+ * Device-side conventions (checked on the device, reported by gmm_query_status):
+ *   - a decreasing a_offsets entry: nothing is computed, stats[1] is still written,
+ *     status GMM_ERR_BAD_INPUT;
+ *   - an expert id >= num_experts: that group is skipped and not counted,
+ *     status GMM_ERR_BAD_INPUT.
+ *
+ * All pointers passed to the run calls are DEVICE pointers on the handle's device
+ * and are owned by the caller.  The run calls are asynchronous on `stream`: they
+ * validate the arguments on the host, launch one persistent kernel and return;
+ * they do not synchronise and allocate nothing.
+ *
+ * A handle owns a small device workspace (a status word and per-CTA tensor-map
+ * slots) that every launch made through it rewrites.  Launches made through the
+ * same handle must therefore not overlap on the GPU: issue them on one stream, or
+ * use one handle per stream.
+ */
+#ifndef GMM_H_
+#define GMM_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes.  0 is success; everything else is negative. */
+#define GMM_OK                  0
+#define GMM_ERR_INVALID_ARG    -1  /* null pointer, negative size, misaligned or badly shaped operand */
+#define GMM_ERR_UNSUPPORTED    -2  /* valid request outside what the kernels implement (e.g. too many groups) */
+#define GMM_ERR_CUDA           -3  /* a CUDA runtime/driver call failed (allocation, launch, copy) */
+#define GMM_ERR_DEVICE_TIMEOUT -4  /* a kernel gave up waiting on its own pipeline (reported by gmm_query_status) */
+#define GMM_ERR_BAD_INPUT      -5  /* decreasing a_offsets or an expert id >= num_experts (gmm_query_status) */
+#define GMM_ERR_NO_DEVICE      -6  /* the device is not an sm_103 GPU, or none is present */
+
+typedef struct gmm_ctx *gmm_handle_t;
+
+/*
+ * Create a handle for `device` and `num_experts` experts (E, the leading
+ * dimension of B; used for the id bounds check and the B tensor map).
+ * Allocates the handle's device workspace on `device` (cudaMalloc).  The
+ * caller's current device is left unchanged.
+ * Errors: GMM_ERR_INVALID_ARG (out == NULL, num_experts < 1),
+ *         GMM_ERR_NO_DEVICE (no such device, or not compute capability 10.3),
+ *         GMM_ERR_CUDA (allocation failed).  *out is NULL on error.
+ */
+int gmm_create(gmm_handle_t *out, int num_experts, int device);
+
+/*
+ * bf16 ragged grouped GEMM (see the header comment for the operation).
+ * N and K: multiples of 8 (16-byte rows, a TMA requirement), both >= 8.
+ * c, a, b: 16-byte aligned.  num_groups: 0 .. 4096.
+ * With num_groups == 0 only expert_usage_stats[1] = 0 is written.
+ * Errors (nothing is launched): GMM_ERR_INVALID_ARG, GMM_ERR_UNSUPPORTED,
+ *         GMM_ERR_CUDA (tensor-map encoding or launch failed).
+ */
+int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, const void *b,
+            const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
+            cudaStream_t stream);
+
+/*
+ * 4-bit grouped GEMM (the grouped path with the weights of Modular's
+ * "multistage_gemm_q", section "Parameters": pack_factor 4-bit values per uint32 and
+ * one scale per group_size K elements).  B[e, n, k] is replaced by
+ *     w = bf16( (q - 8) * scale[e, n, k / group_size] ),
+ *     q = bits [4*(k%8), 4*(k%8)+4) of b_packed[e, n, k/8]   (low nibble first),
+ * b_packed: uint32 [num_experts, N, K/8] (16-byte aligned);
+ * b_scales: bf16 [num_experts, N, K/group_size] (2-byte aligned).
+ * Requirements: those of gmm_run, plus group_size a multiple of 64 that divides K.
+ * Errors: as gmm_run.
+ */
+int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets,
+                 const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
+                 uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
+                 cudaStream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the device status that the kernels of
+ * this handle accumulated since the last query.  Returns GMM_OK,
+ * GMM_ERR_BAD_INPUT or GMM_ERR_DEVICE_TIMEOUT (timeout wins when both are set),
+ * or GMM_ERR_CUDA when the synchronisation or the copy fails (for instance after
+ * an earlier asynchronous fault).
+ */
+int gmm_query_status(gmm_handle_t h, cudaStream_t stream);
+
+/* Static, NUL-terminated description of a return code. */
+const char *gmm_error_string(int code);
+
+/*
+ * Release the handle and its workspace.  The caller must make sure no launch made
+ * through the handle is still running (synchronise first).  NULL is accepted.
+ */
+int gmm_destroy(gmm_handle_t h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GMM_H_ */

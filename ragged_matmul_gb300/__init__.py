@@ -1,0 +1,11 @@
+"""GB300 (sm_103a) ragged grouped GEMM for mixture-of-experts layers.
+
+The compute lives in libgmm.so (hand-written CUDA, C ABI in include/gmm.h);
+this package holds its ctypes binding, the in-tree build step and the seeded
+workload generators.  Importing the package does not load the library; the
+first call does, and raises if the library is missing.
+"""
+from .binding import (EXPORTED, GMM_ERR_BAD_INPUT, GMM_ERR_CUDA, GMM_ERR_DEVICE_TIMEOUT,  # noqa: F401
+                      GMM_ERR_INVALID_ARG, GMM_ERR_NO_DEVICE, GMM_ERR_UNSUPPORTED, GMM_OK, GmmError,
+                      Handle, gmm_create, gmm_destroy, gmm_error_string, gmm_query_status, gmm_run,
+                      gmm_run_int4, library_path, load_library)

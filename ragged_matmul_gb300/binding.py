@@ -1,0 +1,196 @@
+"""Thin ctypes binding over libgmm.so (the C ABI in include/gmm.h).
+
+Argument marshalling only: every step of the grouped GEMM runs in the CUDA
+kernels of libgmm.so.  If the library is missing this module raises; there is
+no fallback of any kind.  The functions keep the C names:
+
+    h = gmm_create(num_experts, device)
+    gmm_run(h, c, a, a_offsets, b, expert_ids, expert_usage_stats)
+    gmm_run_int4(h, c, a, a_offsets, b_packed, b_scales, expert_ids, expert_usage_stats, group_size)
+    gmm_query_status(h)            # syncs the stream; returns the code
+    gmm_error_string(code)
+    gmm_destroy(h)
+
+Tensors are torch CUDA tensors: c/a/b bf16, a_offsets uint32 (or int32 holding
+the same bits), expert_ids int32, expert_usage_stats uint32/int32 with at least
+2 entries, b_packed int32/uint32 words, b_scales bf16.  `stream` defaults to
+torch's current stream on the handle's device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+GMM_OK = 0
+GMM_ERR_INVALID_ARG = -1
+GMM_ERR_UNSUPPORTED = -2
+GMM_ERR_CUDA = -3
+GMM_ERR_DEVICE_TIMEOUT = -4
+GMM_ERR_BAD_INPUT = -5
+GMM_ERR_NO_DEVICE = -6
+
+EXPORTED = ("gmm_create", "gmm_run", "gmm_run_int4", "gmm_query_status", "gmm_error_string",
+            "gmm_destroy")
+
+_lib = None
+
+
+class GmmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {gmm_error_string(code)} ({code})")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load libgmm.so (raises RuntimeError if it is not built)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is not built; call ragged_matmul_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    lib.gmm_create.argtypes = [ctypes.POINTER(P), I, I]
+    lib.gmm_create.restype = I
+    lib.gmm_run.argtypes = [P, P, P, P, P, P, P, I, I, I, P]
+    lib.gmm_run.restype = I
+    lib.gmm_run_int4.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, P]
+    lib.gmm_run_int4.restype = I
+    lib.gmm_query_status.argtypes = [P, P]
+    lib.gmm_query_status.restype = I
+    lib.gmm_error_string.argtypes = [I]
+    lib.gmm_error_string.restype = ctypes.c_char_p
+    lib.gmm_destroy.argtypes = [P]
+    lib.gmm_destroy.restype = I
+    if path == library_path():
+        _lib = lib
+    return lib
+
+
+def gmm_error_string(code: int) -> str:
+    return load_library().gmm_error_string(int(code)).decode()
+
+
+class Handle:
+    """Owns a gmm_handle_t; released by gmm_destroy or at garbage collection."""
+
+    def __init__(self, ptr: int, device: int, num_experts: int):
+        self.ptr = ptr
+        self.device = device
+        self.num_experts = num_experts
+
+    def __del__(self):
+        try:
+            gmm_destroy(self)
+        except Exception:
+            pass
+
+
+def gmm_create(num_experts: int, device: int | None = None) -> Handle:
+    import torch
+    if device is None:
+        device = torch.cuda.current_device()
+    h = ctypes.c_void_p()
+    rc = load_library().gmm_create(ctypes.byref(h), int(num_experts), int(device))
+    if rc != GMM_OK:
+        raise GmmError(rc, "gmm_create")
+    return Handle(h.value, int(device), int(num_experts))
+
+
+def gmm_destroy(h: Handle) -> None:
+    if h is not None and h.ptr:
+        ptr, h.ptr = h.ptr, None
+        rc = load_library().gmm_destroy(ptr)
+        if rc != GMM_OK:
+            raise GmmError(rc, "gmm_destroy")
+
+
+def stream_handle(device: int, stream=None) -> ctypes.c_void_p:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(t, name, dtypes, device, min_numel=0):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda" or t.device.index != device:
+        raise ValueError(f"{name} must live on cuda:{device}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} needs at least {min_numel} elements")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _i32_types():
+    import torch
+    return (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+
+
+def _routing_args(h, a_offsets, expert_ids, stats):
+    import torch
+    G = expert_ids.numel()
+    return (_check(a_offsets, "a_offsets", _i32_types(), h.device, G + 1),
+            _check(expert_ids, "expert_ids", (torch.int32,), h.device),
+            _check(stats, "expert_usage_stats", _i32_types(), h.device, 2), G)
+
+
+def gmm_run(h: Handle, c, a, a_offsets, b, expert_ids, expert_usage_stats, stream=None,
+            check: bool = True) -> int:
+    """C[r, :] = A[r, :] @ B[expert_ids[g]].T for rows of active groups (asynchronous)."""
+    import torch
+    if a.dim() != 2 or b.dim() != 3 or c.dim() != 2:
+        raise ValueError("a must be [rows, K], b [E, N, K], c [rows, N]")
+    E, N, K = b.shape
+    if a.shape[1] != K or c.shape[1] != N or c.shape[0] != a.shape[0] or E != h.num_experts:
+        raise ValueError(f"shape mismatch: a {tuple(a.shape)}, b {tuple(b.shape)}, c {tuple(c.shape)}, "
+                         f"handle E={h.num_experts}")
+    bf = (torch.bfloat16,)
+    pc = _check(c, "c", bf, h.device)
+    pa = _check(a, "a", bf, h.device)
+    pb = _check(b, "b", bf, h.device)
+    po, pi, ps, G = _routing_args(h, a_offsets, expert_ids, expert_usage_stats)
+    rc = load_library().gmm_run(h.ptr, pc, pa, po, pb, pi, ps, G, N, K, stream_handle(h.device, stream))
+    if check and rc != GMM_OK:
+        raise GmmError(rc, "gmm_run")
+    return rc
+
+
+def gmm_run_int4(h: Handle, c, a, a_offsets, b_packed, b_scales, expert_ids, expert_usage_stats,
+                 group_size: int = 128, stream=None, check: bool = True) -> int:
+    """4-bit variant: b_packed [E, N, K/8] 32-bit words, b_scales [E, N, K/group_size] bf16."""
+    import torch
+    if a.dim() != 2 or b_packed.dim() != 3 or c.dim() != 2 or b_scales.dim() != 3:
+        raise ValueError("a must be [rows, K], b_packed [E, N, K/8], b_scales [E, N, K/gs], c [rows, N]")
+    E, N, KW = b_packed.shape
+    K = KW * 8
+    if (a.shape[1] != K or c.shape[1] != N or c.shape[0] != a.shape[0] or E != h.num_experts
+            or group_size <= 0 or tuple(b_scales.shape) != (E, N, K // group_size)):
+        raise ValueError("shape mismatch between a, b_packed, b_scales, c")
+    bf = (torch.bfloat16,)
+    pc = _check(c, "c", bf, h.device)
+    pa = _check(a, "a", bf, h.device)
+    pq = _check(b_packed, "b_packed", _i32_types(), h.device)
+    psc = _check(b_scales, "b_scales", bf, h.device)
+    po, pi, ps, G = _routing_args(h, a_offsets, expert_ids, expert_usage_stats)
+    rc = load_library().gmm_run_int4(h.ptr, pc, pa, po, pq, psc, pi, ps, G, N, K, int(group_size),
+                                     stream_handle(h.device, stream))
+    if check and rc != GMM_OK:
+        raise GmmError(rc, "gmm_run_int4")
+    return rc
+
+
+def gmm_query_status(h: Handle, stream=None) -> int:
+    return load_library().gmm_query_status(h.ptr, stream_handle(h.device, stream))

@@ -1,0 +1,285 @@
+// Host side of the C ABI declared in include/gmm.h: handle management,
+// argument validation, tensor-map encoding and the kernel launch.  No call
+// here synchronises except gmm_query_status, and gmm_run / gmm_run_int4
+// allocate nothing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "gmm.h"
+#include "gmm_kernel.cuh"
+
+namespace {
+
+using gmm::GmmParams;
+
+constexpr size_t kStatusBytes = 256;
+
+struct DeviceGuard {
+  int prev = -1;
+  bool switched = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) switched = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (switched) cudaSetDevice(prev);
+  }
+};
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+struct gmm_ctx {
+  int device = 0;
+  int num_experts = 0;
+  int num_sms = 0;
+  int stages_bf16 = 0;
+  size_t smem_bf16 = 0;
+  int stages_int4 = 0;
+  size_t smem_int4 = 0;
+  uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
+  size_t ws_bytes = 0;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+};
+
+namespace {
+
+int encode_map(gmm_ctx *h, CUtensorMap *m, CUtensorMapDataType type, uint32_t rank, const void *base,
+               const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+               CUtensorMapSwizzle swizzle) {
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = h->encode(m, type, rank, const_cast<void *>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GMM_OK : GMM_ERR_CUDA;
+}
+
+// Token (A) maps: {K, rows} bf16 with 128-row and 16-row boxes.  The row extent
+// written here is a placeholder: the kernel patches it to a_offsets[G].
+int encode_token_maps(gmm_ctx *h, GmmParams &p, const void *a, int K) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), 256};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  cuuint32_t box128[2] = {gmm::kBK, 128};
+  cuuint32_t box16[2] = {gmm::kBK, 16};
+  int rc = encode_map(h, &p.tok_map128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, dims, strides, box128,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  return encode_map(h, &p.tok_map16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, dims, strides, box16,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+int check_common(gmm_ctx *h, void *c, const void *a, const uint32_t *a_offsets, const int32_t *ids,
+                 uint32_t *stats, int G, int N, int K) {
+  if (!h || !c || !a || !a_offsets || !ids || !stats) return GMM_ERR_INVALID_ARG;
+  if (G < 0 || N < 8 || K < 8 || (N % 8) || (K % 8)) return GMM_ERR_INVALID_ARG;
+  if (N > (1 << 24) || K > (1 << 24)) return GMM_ERR_UNSUPPORTED;
+  if (G > gmm::kMaxGroups) return GMM_ERR_UNSUPPORTED;
+  if (!aligned16(c) || !aligned16(a)) return GMM_ERR_INVALID_ARG;
+  return GMM_OK;
+}
+
+void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, const int32_t *ids,
+                 uint32_t *stats, int G, int N, int K) {
+  p.c = static_cast<__nv_bfloat16 *>(c);
+  p.a_offsets = a_offsets;
+  p.expert_ids = ids;
+  p.stats = stats;
+  p.status = reinterpret_cast<uint32_t *>(h->ws);
+  p.map_slots = h->ws + kStatusBytes;
+  p.num_groups = G;
+  p.num_experts = h->num_experts;
+  p.N = N;
+  p.K = K;
+}
+
+// Deepest ring that fits next to the kernel's static shared memory: the number of
+// pipeline stages is chosen from the shared-memory budget of the device.
+int pick_stages(const void *kernel, int stage_bytes, int optin, size_t *dyn_bytes) {
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return 0;
+  const long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024;
+  long s = budget / stage_bytes;
+  if (s > gmm::kMaxStages) s = gmm::kMaxStages;
+  if (s < 2) return 0;
+  *dyn_bytes = static_cast<size_t>(s) * stage_bytes + 1024;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(*dyn_bytes)) != cudaSuccess)
+    return 0;
+  return static_cast<int>(s);
+}
+
+template <bool kInt4>
+int launch(gmm_ctx *h, const GmmParams &p, cudaStream_t stream) {
+  DeviceGuard guard(h->device);
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(h->num_sms));
+  cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : gmm::kThreads);
+  cfg.dynamicSmemBytes = kInt4 ? h->smem_int4 : h->smem_bf16;
+  cfg.stream = stream;
+  if (cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4>, p) != cudaSuccess) {
+    cudaGetLastError();
+    return GMM_ERR_CUDA;
+  }
+  return GMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *gmm_error_string(int code) {
+  switch (code) {
+    case GMM_OK: return "success";
+    case GMM_ERR_INVALID_ARG: return "invalid argument";
+    case GMM_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case GMM_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case GMM_ERR_DEVICE_TIMEOUT: return "kernel pipeline wait timed out";
+    case GMM_ERR_BAD_INPUT: return "decreasing a_offsets or expert id out of range";
+    case GMM_ERR_NO_DEVICE: return "no sm_103 device";
+    default: return "unknown error code";
+  }
+}
+
+int gmm_create(gmm_handle_t *out, int num_experts, int device) {
+  if (!out) return GMM_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (num_experts < 1) return GMM_ERR_INVALID_ARG;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return GMM_ERR_NO_DEVICE;
+  }
+  int major = 0, minor = 0, sms = 0, optin = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  if (major != 10 || minor != 3 || sms < 1) return GMM_ERR_NO_DEVICE;
+
+  gmm_ctx *h = new (std::nothrow) gmm_ctx;
+  if (!h) return GMM_ERR_CUDA;
+  h->device = device;
+  h->num_experts = num_experts;
+  h->num_sms = sms;
+
+  DeviceGuard guard(device);
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    cudaGetLastError();
+    delete h;
+    return GMM_ERR_CUDA;
+  }
+  h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+
+  h->stages_bf16 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<false>),
+                               gmm::kStageBytes, optin, &h->smem_bf16);
+  h->stages_int4 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<true>),
+                               gmm::kInt4StageBytes, optin, &h->smem_int4);
+  if (!h->stages_bf16 || !h->stages_int4) {
+    cudaGetLastError();
+    delete h;
+    return GMM_ERR_CUDA;
+  }
+
+  h->ws_bytes = kStatusBytes + static_cast<size_t>(sms) * gmm::kMapSlotBytes;
+  if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess ||
+      cudaMemset(h->ws, 0, h->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    if (h->ws) cudaFree(h->ws);
+    delete h;
+    return GMM_ERR_CUDA;
+  }
+  *out = h;
+  return GMM_OK;
+}
+
+int gmm_destroy(gmm_handle_t h) {
+  if (!h) return GMM_OK;
+  DeviceGuard guard(h->device);
+  int rc = GMM_OK;
+  if (h->ws && cudaFree(h->ws) != cudaSuccess) rc = GMM_ERR_CUDA;
+  delete h;
+  return rc;
+}
+
+int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, const void *b,
+            const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
+            cudaStream_t stream) {
+  int rc = check_common(h, c, a, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  if (rc) return rc;
+  if (!b || !aligned16(b)) return GMM_ERR_INVALID_ARG;
+
+  GmmParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(h->num_experts)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(N) * K * 2};
+    cuuint32_t box[3] = {gmm::kBK, gmm::kBlockN, 1};
+    rc = encode_map(h, &p.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  }
+  rc = encode_token_maps(h, p, a, K);
+  if (rc) return rc;
+  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  p.num_stages = h->stages_bf16;
+  return launch<false>(h, p, stream);
+}
+
+int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets,
+                 const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
+                 uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
+                 cudaStream_t stream) {
+  int rc = check_common(h, c, a, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  if (rc) return rc;
+  if (!b_packed || !b_scales) return GMM_ERR_INVALID_ARG;
+  if (!aligned16(b_packed) || (reinterpret_cast<uintptr_t>(b_scales) & 1u)) return GMM_ERR_INVALID_ARG;
+  if (group_size < gmm::kBK || group_size % gmm::kBK || K % group_size) return GMM_ERR_UNSUPPORTED;
+
+  GmmParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    // Packed weights as 32-bit words {K/8, N, E}; one box = 128 rows x 64 K (8 words, 32 B).
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(h->num_experts)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 8) * 4, static_cast<cuuint64_t>(N) * (K / 8) * 4};
+    cuuint32_t box[3] = {gmm::kBK / 8, gmm::kBlockN, 1};
+    rc = encode_map(h, &p.w_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, b_packed, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  }
+  rc = encode_token_maps(h, p, a, K);
+  if (rc) return rc;
+  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  p.num_stages = h->stages_int4;
+  p.scales = static_cast<const __nv_bfloat16 *>(b_scales);
+  p.group_size = group_size;
+  return launch<true>(h, p, stream);
+}
+
+int gmm_query_status(gmm_handle_t h, cudaStream_t stream) {
+  if (!h) return GMM_ERR_INVALID_ARG;
+  DeviceGuard guard(h->device);
+  uint32_t status = 0;
+  if (cudaMemcpyAsync(&status, h->ws, sizeof(status), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaMemsetAsync(h->ws, 0, sizeof(status), stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GMM_ERR_CUDA;
+  }
+  if (status & gmm::kStatusTimeout) return GMM_ERR_DEVICE_TIMEOUT;
+  if (status) return GMM_ERR_BAD_INPUT;
+  return GMM_OK;
+}
+
+}  // extern "C"

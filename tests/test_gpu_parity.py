@@ -1,0 +1,277 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small and medium shapes are compared element by element; the full-size
+workloads are compared on sampled rows and columns that the oracle computes,
+in the same launch configuration the bench times.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from ragged_matmul_gb300 import binding
+from ragged_matmul_gb300 import workloads as wl
+
+from gpu_util import (assert_close, bits_of, check_against_oracle, live_row_mask, run_gpu,
+                      sentinel_dev, to_dev_i32)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from ragged_matmul_gb300 import build
+    build.build()
+    torch.cuda.set_device(0)
+
+
+_handles = {}
+
+
+def handle(E):
+    if E not in _handles:
+        _handles[E] = binding.gmm_create(E, 0)
+    return _handles[E]
+
+
+def routing(E, N, K, loads, ids, dist=("uniform", -1.0, 1.0), base=0, int4=False, gs=128):
+    return wl.make_routing("t", E, N, K, loads, ids, a_dist=dist, b_dist=None if int4 else dist,
+                           base=base, int4=int4, group_size=gs)
+
+
+# ---------------------------------------------------------------- named tiny workload
+
+def test_tiny_workload():
+    r = wl.routing("tiny")
+    v = wl.host_values(r, 0)
+    _, _, status, _ = check_against_oracle(handle(r.E), r, v, where="tiny")
+    assert status == binding.GMM_OK
+
+
+# ---------------------------------------------------------------- exact arithmetic
+
+def test_small_integers_bit_exact():
+    """Integer operands in [-3, 3], K <= 28: every sum is exact, so C must match bit for bit."""
+    r = routing(5, 136, 24, [1, 17, 0, 130, 33, 256, 7], [4, 0, 2, 3, -1, 1, 4], dist=("int", -3, 3))
+    v = wl.host_values(r, 1)
+    check_against_oracle(handle(5), r, v, exact=True, where="int")
+
+
+def test_unit_rows_select_weight_columns():
+    """A rows that are unit vectors e_k return B[e, n, k] exactly: pins operand orientation."""
+    E, N, K = 3, 256, 64
+    rng = np.random.default_rng(2)
+    b = wl._to_bf16_bits(rng.uniform(-2, 2, (E, N, K)).astype(np.float32))
+    A = np.zeros((3 * K, K), np.float32)
+    for g in range(3):
+        A[g * K + np.arange(K), np.arange(K)] = 1.0
+    ids = [2, 0, 1]
+    off = wl.offsets_from_loads([K, K, K])
+    got, stats, status = run_gpu(handle(E), wl._to_bf16_bits(A), off, ids, b_bits=b, N=N)
+    for g in range(3):
+        for k in range(K):
+            assert np.array_equal(got[g * K + k], b[ids[g], :, k]), (g, k)
+    assert stats[1] == 3 and status == binding.GMM_OK
+
+
+# ---------------------------------------------------------------- ragged shapes and tails
+
+@pytest.mark.parametrize("N,K", [(384, 320), (136, 200), (256, 64), (1024, 1096)])
+def test_ragged_groups_tails(N, K):
+    loads = [1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 300, 513, 0, 2]
+    ids = [3, 0, 5, 1, 7, 2, 6, 4, 3, 0, 1, 2, 6, 7]
+    r = routing(8, N, K, loads, ids, dist=("normal", 1.0))
+    v = wl.host_values(r, 3)
+    _, _, status, _ = check_against_oracle(handle(8), r, v, where=f"ragged N={N} K={K}")
+    assert status == binding.GMM_OK
+
+
+def test_single_group_dense():
+    r = routing(2, 512, 512, [700], [1], dist=("normal", 1.0))
+    v = wl.host_values(r, 4)
+    check_against_oracle(handle(2), r, v, where="single group")
+
+
+def test_offset_base_and_trailing_rows_untouched():
+    """a_offsets[0] > 0 and rows after a_offsets[G]: both stay untouched."""
+    r = routing(4, 128, 128, [40, 9, 100], [1, -1, 3], base=37)
+    rows_alloc = r.rows + 21
+    v = wl.host_values(r, 5, rows=rows_alloc)
+    check_against_oracle(handle(4), r, v, rows_alloc=rows_alloc, where="offset base")
+
+
+def test_skipped_groups_with_rows_and_duplicates():
+    r = routing(4, 256, 192, [50, 300, 20, 64, 64], [-1, 2, -5, 2, 0])
+    v = wl.host_values(r, 6)
+    _, _, status, _ = check_against_oracle(handle(4), r, v, where="skips")
+    assert status == binding.GMM_OK
+
+
+def test_all_groups_skipped_and_empty_problem():
+    r = routing(4, 128, 64, [30, 40], [-1, -1])
+    v = wl.host_values(r, 7)
+    check_against_oracle(handle(4), r, v, where="all skipped")
+    r0 = routing(4, 128, 64, [], [])
+    got, stats, status = run_gpu(handle(4), np.zeros((16, 64), np.uint16), r0.a_offsets, r0.expert_ids,
+                                 b_bits=np.zeros((4, 128, 64), np.uint16), N=128)
+    assert stats.tolist() == [0xFFFFFFFF, 0, 0xFFFFFFFF, 0xFFFFFFFF]
+    assert np.all(got == wl.SENTINEL_BF16) and status == binding.GMM_OK
+
+
+def test_bad_offsets_compute_nothing_and_report():
+    r = routing(4, 128, 64, [30, 40, 10], [0, 1, 2])
+    v = wl.host_values(r, 8)
+    off = np.array([0, 30, 20, 80], np.uint32)       # decreasing at g = 1
+    got, stats, status = run_gpu(handle(4), v["a"], off, r.expert_ids, b_bits=v["b"], N=128, rows_alloc=80)
+    ref = oracle.gmm_bf16(v["a"], off, v["b"], r.expert_ids, c_init=wl.sentinel_c(80, 128),
+                          stats_init=np.full(4, 0xFFFFFFFF, np.uint32))
+    assert ref.flags & oracle.BAD_OFFSETS
+    assert np.array_equal(got, ref.c) and np.array_equal(stats, ref.stats)
+    assert status == binding.GMM_ERR_BAD_INPUT
+    assert binding.gmm_query_status(handle(4)) == binding.GMM_OK    # the query cleared it
+
+
+def test_expert_id_out_of_range_is_skipped_and_reported():
+    r = routing(4, 128, 64, [30, 40, 10], [0, 9, 2])
+    v = wl.host_values(r, 9)
+    _, ref, status, _ = check_against_oracle(handle(4), r, v, where="bad id")
+    assert ref.flags == oracle.BAD_EXPERT_ID
+    assert status == binding.GMM_ERR_BAD_INPUT
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_group_permutation_and_determinism():
+    loads = [300, 7, 129, 0, 64, 511]
+    ids = [1, 0, 3, 2, -1, 1]
+    r = routing(4, 640, 256, loads, ids, dist=("normal", 1.0))
+    v = wl.host_values(r, 10)
+    h = handle(4)
+    base, _, _ = run_gpu(h, v["a"], r.a_offsets, r.expert_ids, b_bits=v["b"], N=r.N)
+    again, _, _ = run_gpu(h, v["a"], r.a_offsets, r.expert_ids, b_bits=v["b"], N=r.N)
+    assert np.array_equal(base, again), "repeated runs differ"
+    perm = np.random.default_rng(11).permutation(len(loads))
+    off = r.a_offsets.astype(np.int64)
+    row_perm = np.concatenate([np.arange(off[g], off[g + 1]) for g in perm]).astype(np.int64)
+    got, _, _ = run_gpu(h, v["a"][row_perm], wl.offsets_from_loads(np.asarray(loads)[perm]),
+                        np.asarray(ids)[perm], b_bits=v["b"], N=r.N)
+    assert np.array_equal(got, base[row_perm])
+
+
+def test_argument_validation_codes():
+    import torch
+    h = handle(4)
+    a = torch.zeros((16, 60), dtype=torch.bfloat16, device=DEV)       # K = 60: not a multiple of 8
+    b = torch.zeros((4, 64, 60), dtype=torch.bfloat16, device=DEV)
+    c = torch.zeros((16, 64), dtype=torch.bfloat16, device=DEV)
+    off = to_dev_i32([0, 16], DEV)
+    ids = to_dev_i32([0], DEV)
+    st = to_dev_i32([0, 0], DEV)
+    assert binding.gmm_run(h, c, a, off, b, ids, st, check=False) == binding.GMM_ERR_INVALID_ARG
+    big = torch.zeros(4097, dtype=torch.int32, device=DEV)
+    a = torch.zeros((16, 64), dtype=torch.bfloat16, device=DEV)
+    b = torch.zeros((4, 64, 64), dtype=torch.bfloat16, device=DEV)
+    offs = torch.zeros(4098, dtype=torch.int32, device=DEV)
+    assert binding.gmm_run(h, c, a, offs, b, big, st, check=False) == binding.GMM_ERR_UNSUPPORTED
+    q = torch.zeros((4, 64, 8), dtype=torch.int32, device=DEV)
+    s = torch.zeros((4, 64, 2), dtype=torch.bfloat16, device=DEV)
+    assert binding.gmm_run_int4(h, c, a, off, q, s, ids, st, group_size=32, check=False) \
+        == binding.GMM_ERR_UNSUPPORTED
+
+
+# ---------------------------------------------------------------- scaled-down named workloads
+
+def _scaled(name, N, K):
+    full = wl.routing(name)
+    return wl.make_routing(name + "_small", full.E, N, K, full.loads, full.expert_ids, a_dist=full.a_dist,
+                           b_dist=full.b_dist, int4=full.int4, group_size=full.group_size,
+                           scale_range=full.scale_range)
+
+
+@pytest.mark.parametrize("name,N,K", [("decode", 2816, 256), ("prefill", 512, 512),
+                                      ("fine_grained", 256, 448), ("int4", 512, 512)])
+def test_named_workload_routing_at_reduced_width(name, N, K):
+    """The full routing (all rows, all groups, skips) with N and K cut down."""
+    r = _scaled(name, N, K)
+    v = wl.host_values(r, 12)
+    _, _, status, _ = check_against_oracle(handle(r.E), r, v, where=name)
+    assert status == binding.GMM_OK
+
+
+# ---------------------------------------------------------------- 4-bit variant
+
+def test_int4_integer_case_bit_exact():
+    rng = np.random.default_rng(13)
+    E, N, K, gs = 3, 256, 256, 128
+    r = routing(E, N, K, [7, 0, 130, 45], [2, 1, 0, 2], int4=True, gs=gs)
+    a = wl._to_bf16_bits(rng.integers(-2, 3, (r.rows, K)).astype(np.float32))
+    q = rng.integers(0, 16, (E, N, K))
+    v = {"a": a, "packed": wl.pack_nibbles(q),
+         "scales": wl._to_bf16_bits(np.ones((E, N, K // gs), np.float32))}
+    check_against_oracle(handle(E), r, v, exact=True, where="int4 exact")
+
+
+@pytest.mark.parametrize("gs", [64, 128, 256])
+def test_int4_random(gs):
+    r = routing(6, 384, 512, [33, 0, 257, 16, 100, 1], [5, 0, 1, -1, 3, 2], dist=("normal", 1.0),
+                int4=True, gs=gs)
+    v = wl.host_values(r, 14)
+    _, _, status, _ = check_against_oracle(handle(6), r, v, where=f"int4 gs={gs}")
+    assert status == binding.GMM_OK
+
+
+# ---------------------------------------------------------------- full-size sampled parity
+
+def sampled_full_size(name, rows_per_group=2, ncols=96, seed=0):
+    """Run the full named workload on the GPU; check sampled outputs against the oracle."""
+    import torch
+    r = wl.routing(name)
+    v = wl.device_values(r, seed, device=DEV)
+    h = handle(r.E)
+    c = sentinel_dev(r.rows, r.N, DEV)
+    stats = to_dev_i32(np.full(4, 0xFFFFFFFF, np.uint32), DEV)
+    off_d, ids_d = to_dev_i32(r.a_offsets, DEV), to_dev_i32(r.expert_ids, DEV)
+    if r.int4:
+        binding.gmm_run_int4(h, c, v["a"], off_d, v["packed"], v["scales"], ids_d, stats, group_size=r.group_size)
+    else:
+        binding.gmm_run(h, c, v["a"], off_d, v["b"], ids_d, stats)
+    assert binding.gmm_query_status(h) == binding.GMM_OK
+    assert stats.cpu().numpy().view(np.uint32).tolist() == [0xFFFFFFFF, int(r.active_mask().sum()),
+                                                            0xFFFFFFFF, 0xFFFFFFFF]
+    live = live_row_mask(r.rows, r.a_offsets, r.expert_ids, r.E)
+    dead = torch.from_numpy(~live).to(DEV)      # rows outside active groups: still all sentinel
+    assert bool((c.view(torch.int16)[dead] == wl.SENTINEL_BF16).all())
+    rng = np.random.default_rng(seed + 100)
+    rows, loads = [], []
+    for g in range(r.G):
+        lo, hi = int(r.a_offsets[g]), int(r.a_offsets[g + 1])
+        pick = sorted(set([lo, hi - 1] + rng.integers(lo, hi, rows_per_group).tolist())) if hi > lo else []
+        rows += pick
+        loads.append(len(pick))
+    rows = np.asarray(rows, np.int64)
+    cols = np.unique(np.concatenate([[0, r.N - 1], rng.choice(r.N, ncols, replace=False)]))
+    rows_t = torch.from_numpy(rows).to(DEV)
+    cols_t = torch.from_numpy(cols).to(DEV)
+    a_s = bits_of(v["a"][rows_t])
+    off_s = wl.offsets_from_loads(loads)
+    if r.int4:
+        q_s = v["packed"][:, cols_t, :].contiguous().cpu().numpy().view(np.uint32)
+        s_s = bits_of(v["scales"][:, cols_t, :])
+        ref = oracle.gmm_int4(a_s, off_s, q_s, s_s, r.expert_ids, group_size=r.group_size)
+    else:
+        b_s = bits_of(v["b"][:, cols_t, :])
+        ref = oracle.gmm_bf16(a_s, off_s, b_s, r.expert_ids)
+    got = bits_of(c[rows_t][:, cols_t])
+    live_s = live_row_mask(len(rows), off_s, r.expert_ids, r.E)
+    err = assert_close(got, ref.ref32, live_s, where=name)
+    assert np.all(got[~live_s] == wl.SENTINEL_BF16)
+    return err
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "fine_grained", "int4"])
+def test_full_size_sampled(name):
+    sampled_full_size(name)
