@@ -1,0 +1,409 @@
+"""Benchmark of the ragged grouped GEMM on GB300: useful TFLOP/s and fraction of roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|fine_grained|int4|tiny]
+                    [--impl ours|reference]
+
+One step = one gmm_run (gmm_run_int4 for the int4 workload) over the whole
+workload: every group, every row, all N columns.  Inputs are seeded synthetic
+tensors already resident in HBM; between steps L2 is flushed by writing a
+512 MiB buffer (outside the timed events).  Each step is timed with CUDA events
+on the launching stream; `value` is useful FLOPs / mean step time.
+
+The default workload is decode (256 tokens top-8 over 64 experts: 2048 rows,
+K=2048, N=2816).  Under torchrun each rank runs its own replica of the workload
+(the groups are independent problems and need no exchange), so scaling is weak
+and `value` = FLOPs of all ranks / the slowest rank's time.
+
+--impl reference times the CPU oracle (oracle/, plain C, all host cores of this
+process) on a bounded sample of the same workload: the first rows of every
+active group, all N columns.  It is a baseline for context, not the target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ragged_matmul_gb300 import workloads as wl  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FLUSH_BYTES = 512 << 20
+METRIC = "grouped GEMM useful TFLOP/s and % of roofline (tensor or HBM) per config, 1xGB300"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def work_counts(r: wl.Routing):
+    """Useful FLOPs and algorithmic bytes of one pass (padding and L2 re-reads not counted)."""
+    act = r.active_mask()
+    rows = int(r.loads[act].sum())
+    flops = 2.0 * r.N * r.K * rows
+    experts = np.unique(r.expert_ids[act])
+    if r.int4:
+        wbytes = r.N * r.K // 2 + r.N * (r.K // r.group_size) * 2
+    else:
+        wbytes = r.N * r.K * 2
+    nbytes = len(experts) * wbytes + rows * r.K * 2 + rows * r.N * 2 + 4 * (2 * r.G + 2)
+    return flops, float(nbytes), rows
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ragged_matmul_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel."""
+    path = os.path.join(ROOT, "profiles", f"gmm_grouped_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    hm = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or not hm or hm.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 100 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        use = inside or [p for t, p in self.samples]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in use if num(p[1]) is not None]
+        mx = [num(p[2]) for p in use if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i in range(4) if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside), "samples_total": len(self.samples)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle arm
+
+def oracle_sample(r: wl.Routing, vals_dev, rows_per_group: int):
+    """First rows_per_group rows of every active group, all N columns, as host arrays."""
+    import torch
+    act = r.active_mask()
+    rows, loads, ids = [], [], []
+    for g in range(r.G):
+        if not act[g]:
+            continue
+        lo = int(r.a_offsets[g])
+        n = min(int(r.loads[g]), rows_per_group)
+        rows += range(lo, lo + n)
+        loads.append(n)
+        ids.append(int(r.expert_ids[g]))
+    idx = torch.tensor(rows, dtype=torch.int64, device=vals_dev["a"].device)
+    a = vals_dev["a"][idx].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    sample = {"a": a, "off": wl.offsets_from_loads(loads), "ids": np.asarray(ids, np.int32)}
+    if r.int4:
+        sample["packed"] = vals_dev["packed"].cpu().numpy().view(np.uint32)
+        sample["scales"] = vals_dev["scales"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    else:
+        sample["b"] = vals_dev["b"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    sample["flops"] = 2.0 * r.N * r.K * sum(loads)
+    return sample
+
+
+def run_oracle(r: wl.Routing, s, nthreads):
+    import oracle
+    t0 = time.perf_counter()
+    if r.int4:
+        oracle.gmm_int4(s["a"], s["off"], s["packed"], s["scales"], s["ids"], group_size=r.group_size,
+                        nthreads=nthreads)
+    else:
+        oracle.gmm_bf16(s["a"], s["off"], s["b"], s["ids"], nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def pick_oracle_rows(r, vals_dev, nthreads, target_s):
+    """Rows per group so that one oracle pass takes about target_s seconds."""
+    probe = oracle_sample(r, vals_dev, 1)
+    dt = max(run_oracle(r, probe, nthreads), 1e-3)
+    rate = probe["flops"] / dt
+    act_groups = int(r.active_mask().sum())
+    rows = int(target_s * rate / (2.0 * r.N * r.K * max(act_groups, 1)))
+    return max(1, min(rows, int(r.loads.max()))), rate
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="decode", choices=[n for n in wl.WORKLOAD_NAMES])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--oracle-seconds", type=float, default=2.0,
+                    help="CPU oracle work per step of the reference arm / per cpu_baseline pass")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_env()
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+
+    r = wl.routing(args.workload)
+    flops, nbytes, rows = work_counts(r)
+    peaks, peaks_kind = load_peaks()
+    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_tensor >= t_hbm else "hbm"
+    config = {"workload": args.workload, "E": r.E, "N": r.N, "K": r.K, "groups": r.G,
+              "active_groups": int(r.active_mask().sum()), "rows": rows,
+              "useful_flops": flops, "algorithmic_bytes": nbytes,
+              "l2": "flushed between steps (512 MiB write)", "weights": "int4" if r.int4 else "bf16"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            barrier(world)
+            return
+        vals = wl.device_values(r, 0, device=dev)
+        nthreads = len(os.sched_getaffinity(0))
+        per_step_rows, _ = pick_oracle_rows(r, vals, nthreads, args.oracle_seconds)
+        s = oracle_sample(r, vals, per_step_rows)
+        del vals
+        for _ in range(min(args.warmup, 1)):
+            run_oracle(r, s, nthreads)
+        times = [run_oracle(r, s, nthreads) for _ in range(args.steps)]
+        t = statistics.mean(times)
+        value = s["flops"] / t / 1e12
+        sample_desc = (f"first {per_step_rows} rows of each active group ({s['a'].shape[0]} rows), "
+                       f"all N={r.N} columns, K={r.K}")
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 inputs, fp32 accumulation (C, CPU)",
+            "data": "synthetic (seeded)", "config": config,
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+                             "sample": sample_desc},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }), flush=True)
+        barrier(world)
+        return
+
+    from ragged_matmul_gb300 import binding
+    from ragged_matmul_gb300 import build as gbuild
+    if rank == 0:
+        gbuild.build()
+    barrier(world)
+
+    vals = wl.device_values(r, rank, device=dev)
+    h = binding.gmm_create(r.E, local)
+    c = torch.full((r.rows, r.N), wl.SENTINEL_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
+    off = torch.from_numpy(r.a_offsets.view(np.int32)).to(dev)
+    ids = torch.from_numpy(r.expert_ids).to(dev)
+    stats = torch.zeros(4, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(cc=c, aa=vals["a"], oo=off, ii=ids, ss=stats):
+        if r.int4:
+            binding.gmm_run_int4(h, cc, aa, oo, vals["packed"], vals["scales"], ii, ss,
+                                 group_size=r.group_size, stream=stream)
+        else:
+            binding.gmm_run(h, cc, aa, oo, vals["b"], ii, ss, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    status = binding.gmm_query_status(h)
+    if status != binding.GMM_OK:
+        raise RuntimeError(f"device status after warm-up: {binding.gmm_error_string(status)}")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.time()
+    for i in range(args.steps):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    w1 = time.time()
+    sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    mean_ms = statistics.mean(step_ms)
+    status = binding.gmm_query_status(h)
+    if status != binding.GMM_OK:
+        raise RuntimeError(f"device status after timing: {binding.gmm_error_string(status)}")
+    max_ms = reduce_max(mean_ms, world, dev)
+    value = world * flops / (max_ms * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: H2D of the step's inputs
+    # (activations, offsets, ids) from pinned memory, the kernel, D2H of C and stats.
+    e2e = None
+    if not args.no_e2e:
+        a_h = vals["a"].cpu().pin_memory()
+        off_h, ids_h = off.cpu().pin_memory(), ids.cpu().pin_memory()
+        c_h = torch.empty_like(c, device="cpu").pin_memory()
+        st_h = torch.empty_like(stats, device="cpu").pin_memory()
+        a_d, off_d, ids_d = torch.empty_like(vals["a"]), torch.empty_like(off), torch.empty_like(ids)
+        h2d = a_h.numel() * 2 + off_h.numel() * 4 + ids_h.numel() * 4
+        d2h = c_h.numel() * 2 + st_h.numel() * 4
+
+        def e2e_step():
+            a_d.copy_(a_h, non_blocking=True)
+            off_d.copy_(off_h, non_blocking=True)
+            ids_d.copy_(ids_h, non_blocking=True)
+            step(c, a_d, off_d, ids_d, stats)
+            c_h.copy_(c, non_blocking=True)
+            st_h.copy_(stats, non_blocking=True)
+
+        for _ in range(args.warmup):
+            flush.zero_()
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = []
+        barrier(world)
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            e2e_step()
+            e1.record(stream)
+            e1.synchronize()
+            e_ms.append(e0.elapsed_time(e1))
+        e2e_max = reduce_max(statistics.mean(e_ms), world, dev)
+        e2e = {"value": world * flops / (e2e_max * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_max}
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nthreads = len(os.sched_getaffinity(0))
+        per_rows, _ = pick_oracle_rows(r, vals, nthreads, args.oracle_seconds)
+        s = oracle_sample(r, vals, per_rows)
+        t = run_oracle(r, s, nthreads)
+        cpu_baseline = {"value": s["flops"] / t / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
+                        "sample": f"first {per_rows} rows of each active group ({s['a'].shape[0]} rows), "
+                                  f"all N={r.N} columns, K={r.K}; {t:.2f} s"}
+
+    if rank == 0:
+        t_s = mean_ms * 1e-3
+        if bound == "hbm":
+            achieved, peak, unit = nbytes / t_s / 1e9, peaks["hbm_gbs"], "GB/s"
+        else:
+            achieved, peak, unit = flops / t_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                    "traffic": profiled_traffic(args.workload), "peak_source": f"{peaks_kind} (burst)",
+                    "roofline_time_ms": max(t_tensor, t_hbm) * 1e3,
+                    "kernel": "gmm_grouped_kernel<%s>" % ("true" if r.int4 else "false")}
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if not r.int4 else "int4 weights, bf16 MMA",
+            "data": "synthetic (seeded, generated on device)", "config": config,
+            "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": sampler.summary(w0, w1), "region_wall_ms": (w1 - w0) * 1e3,
+            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+        }
+        print(json.dumps(line), flush=True)
+    binding.gmm_destroy(h)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -71,7 +71,7 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device);
  * bf16 ragged grouped GEMM (see the header comment for the operation).
  * N and K: multiples of 8 (16-byte rows, a TMA requirement), both >= 8.
  * c, a, b: 16-byte aligned.  num_groups: 0 .. 4096.
- * With num_groups == 0 only expert_usage_stats[1] = 0 is written.
+ * With num_groups == 0 only expert_usage_stats[1] = 0 is written (expert_ids may then be NULL).
  * Errors (nothing is launched): GMM_ERR_INVALID_ARG, GMM_ERR_UNSUPPORTED,
  *         GMM_ERR_CUDA (tensor-map encoding or launch failed).
  */

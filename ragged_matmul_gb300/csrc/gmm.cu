@@ -75,7 +75,8 @@ int encode_token_maps(gmm_ctx *h, GmmParams &p, const void *a, int K) {
 
 int check_common(gmm_ctx *h, void *c, const void *a, const uint32_t *a_offsets, const int32_t *ids,
                  uint32_t *stats, int G, int N, int K) {
-  if (!h || !c || !a || !a_offsets || !ids || !stats) return GMM_ERR_INVALID_ARG;
+  if (!h || !c || !a || !a_offsets || !stats) return GMM_ERR_INVALID_ARG;
+  if (!ids && G > 0) return GMM_ERR_INVALID_ARG;   // never read when there are no groups
   if (G < 0 || N < 8 || K < 8 || (N % 8) || (K % 8)) return GMM_ERR_INVALID_ARG;
   if (N > (1 << 24) || K > (1 << 24)) return GMM_ERR_UNSUPPORTED;
   if (G > gmm::kMaxGroups) return GMM_ERR_UNSUPPORTED;
