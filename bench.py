@@ -15,8 +15,9 @@ K=2048, N=2816).  Under torchrun each rank runs its own replica of the workload
 and `value` = FLOPs of all ranks / the slowest rank's time.
 
 --impl reference times the CPU oracle (oracle/, plain C, all host cores of this
-process) on a bounded sample of the same workload: the first rows of every
-active group, all N columns.  It is a baseline for context, not the target.
+process) on a bounded sample of the same workload: the first whole groups in
+routing order, all N columns, grown until one pass takes a few seconds.  It is
+a baseline for context, not the target.
 """
 from __future__ import annotations
 
@@ -38,6 +39,11 @@ sys.path.insert(0, ROOT)
 
 from ragged_matmul_gb300 import workloads as wl  # noqa: E402
 
+# Roofline denominators.  MEASURED_PEAKS.json (written per GPU pool: a STREAM-style copy and a
+# cuBLAS bf16 8192^3 GEMM, burst and sustained) wins when present; RECORDED_PEAKS is the copy of
+# that measurement taken on the GB300s, used when the file is absent; FALLBACK_PEAKS is
+# an older single GB300 measurement.
+RECORDED_PEAKS = {"hbm_gbs": 6782.8, "bf16_tflops": 1921.8, "bf16_tflops_sustained": 1713.6}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 512 << 20
 METRIC = "grouped GEMM useful TFLOP/s and % of roofline (tensor or HBM) per config, 1xGB300"
@@ -49,7 +55,7 @@ def load_peaks():
         with open(path) as f:
             d = json.load(f)
         return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
-    return dict(FALLBACK_PEAKS), "fallback"
+    return dict(RECORDED_PEAKS), "measured (recorded copy)"
 
 
 def work_counts(r: wl.Routing):
@@ -167,28 +173,30 @@ def barrier(world):
 
 # ------------------------------------------------------------------ CPU oracle arm
 
-def oracle_sample(r: wl.Routing, vals_dev, rows_per_group: int):
-    """First rows_per_group rows of every active group, all N columns, as host arrays."""
+def oracle_sample(r: wl.Routing, vals_dev, n_groups: int):
+    """The first n_groups active groups, all of their rows, all N columns, as host arrays."""
     import torch
-    act = r.active_mask()
+    act = np.flatnonzero(r.active_mask())[:n_groups]
     rows, loads, ids = [], [], []
-    for g in range(r.G):
-        if not act[g]:
-            continue
-        lo = int(r.a_offsets[g])
-        n = min(int(r.loads[g]), rows_per_group)
-        rows += range(lo, lo + n)
-        loads.append(n)
+    for g in act:
+        lo, hi = int(r.a_offsets[g]), int(r.a_offsets[g + 1])
+        rows += range(lo, hi)
+        loads.append(hi - lo)
         ids.append(int(r.expert_ids[g]))
     idx = torch.tensor(rows, dtype=torch.int64, device=vals_dev["a"].device)
     a = vals_dev["a"][idx].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    sample = {"a": a, "off": wl.offsets_from_loads(loads), "ids": np.asarray(ids, np.int32)}
+    sample = {"a": a, "off": wl.offsets_from_loads(loads), "ids": np.asarray(ids, np.int32),
+              "groups": len(act), "rows": len(rows)}
+    used = sorted(set(ids))
+    remap = {e: i for i, e in enumerate(used)}           # keep only the experts the sample uses
+    sample["ids"] = np.asarray([remap[e] for e in ids], np.int32)
+    sel = torch.tensor(used, dtype=torch.int64, device=vals_dev["a"].device)
     if r.int4:
-        sample["packed"] = vals_dev["packed"].cpu().numpy().view(np.uint32)
-        sample["scales"] = vals_dev["scales"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        sample["packed"] = vals_dev["packed"][sel].cpu().numpy().view(np.uint32)
+        sample["scales"] = vals_dev["scales"][sel].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     else:
-        sample["b"] = vals_dev["b"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    sample["flops"] = 2.0 * r.N * r.K * sum(loads)
+        sample["b"] = vals_dev["b"][sel].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    sample["flops"] = 2.0 * r.N * r.K * len(rows)
     return sample
 
 
@@ -203,14 +211,21 @@ def run_oracle(r: wl.Routing, s, nthreads):
     return time.perf_counter() - t0
 
 
-def pick_oracle_rows(r, vals_dev, nthreads, target_s):
-    """Rows per group so that one oracle pass takes about target_s seconds."""
-    probe = oracle_sample(r, vals_dev, 1)
-    dt = max(run_oracle(r, probe, nthreads), 1e-3)
-    rate = probe["flops"] / dt
-    act_groups = int(r.active_mask().sum())
-    rows = int(target_s * rate / (2.0 * r.N * r.K * max(act_groups, 1)))
-    return max(1, min(rows, int(r.loads.max()))), rate
+def pick_oracle_sample(r, vals_dev, nthreads, target_s):
+    """Grow the number of whole groups (doubling) until one oracle pass takes about target_s."""
+    n_active = int(r.active_mask().sum())
+    n = 1
+    while True:
+        s = oracle_sample(r, vals_dev, n)
+        dt = run_oracle(r, s, nthreads)
+        if dt >= 0.5 * target_s or n >= n_active:
+            return s, dt
+        n = min(n_active, n * 2 if dt <= 0 else max(n + 1, int(n * min(4.0, target_s / dt))))
+
+
+def sample_desc(r, s):
+    return (f"first {s['groups']} active groups in routing order ({s['rows']} rows), "
+            f"all N={r.N} columns, K={r.K}")
 
 
 # ------------------------------------------------------------------ main
@@ -222,7 +237,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode", choices=[n for n in wl.WORKLOAD_NAMES])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--oracle-seconds", type=float, default=2.0,
+    ap.add_argument("--oracle-seconds", type=float, default=10.0,
                     help="CPU oracle work per step of the reference arm / per cpu_baseline pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -255,23 +270,21 @@ def main():
             return
         vals = wl.device_values(r, 0, device=dev)
         nthreads = len(os.sched_getaffinity(0))
-        per_step_rows, _ = pick_oracle_rows(r, vals, nthreads, args.oracle_seconds)
-        s = oracle_sample(r, vals, per_step_rows)
+        per_step = max(0.2, min(args.oracle_seconds, 150.0 / (args.steps + 1)))   # whole run: minutes
+        s, _ = pick_oracle_sample(r, vals, nthreads, per_step)
         del vals
         for _ in range(min(args.warmup, 1)):
             run_oracle(r, s, nthreads)
         times = [run_oracle(r, s, nthreads) for _ in range(args.steps)]
         t = statistics.mean(times)
         value = s["flops"] / t / 1e12
-        sample_desc = (f"first {per_step_rows} rows of each active group ({s['a'].shape[0]} rows), "
-                       f"all N={r.N} columns, K={r.K}")
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16 inputs, fp32 accumulation (C, CPU)",
             "data": "synthetic (seeded)", "config": config,
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-                             "sample": sample_desc},
+                             "sample": sample_desc(r, s)},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }), flush=True)
         barrier(world)
@@ -372,12 +385,9 @@ def main():
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = len(os.sched_getaffinity(0))
-        per_rows, _ = pick_oracle_rows(r, vals, nthreads, args.oracle_seconds)
-        s = oracle_sample(r, vals, per_rows)
-        t = run_oracle(r, s, nthreads)
+        s, t = pick_oracle_sample(r, vals, nthreads, args.oracle_seconds)
         cpu_baseline = {"value": s["flops"] / t / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-                        "sample": f"first {per_rows} rows of each active group ({s['a'].shape[0]} rows), "
-                                  f"all N={r.N} columns, K={r.K}; {t:.2f} s"}
+                        "sample": sample_desc(r, s) + f"; {t:.2f} s"}
 
     if rank == 0:
         t_s = mean_ms * 1e-3
