@@ -96,6 +96,38 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
                  cudaStream_t stream);
 
 /*
+ * Allocation-free variant of gmm_run, for callers that cannot call cudaMalloc when
+ * they need the GEMM: code running inside an allocator or memory-pool callback, a
+ * framework that has reserved all device memory for its own pool, or a runtime that
+ * forbids allocations after start-up.  The pages have no counterpart to this call.
+ *
+ * It computes exactly what gmm_run computes, with the same kernel, on the CALLER'S
+ * CURRENT DEVICE (all pointers must live there), and needs no handle: num_experts is
+ * passed directly.  The caller still provides every input and output buffer.  The
+ * kernel's scratch (a status word and one 256-byte tensor-map slot per CTA) comes from
+ * a fixed array compiled into the library, 65,792 bytes on every GPU that loads it,
+ * held until the process exits.  That array has slots for at most 256 CTAs; the grid
+ * is one CTA per SM, so a device with more than 256 SMs gets GMM_ERR_UNSUPPORTED.
+ *
+ * The first call on a device does a one-time set-up (looks up the array's device
+ * address, the tensor-map encoder, and the kernel's shared-memory setting); make that
+ * first call before any stream capture.  No call allocates or frees device memory.
+ *
+ * Every call shares the one array and finds the previous call's contents in it; the
+ * call clears the status word itself (stream-ordered on `stream`) and rewrites the
+ * tensor-map slots.  Calls whose kernels overlap on the GPU (different streams, or
+ * concurrent threads) race on the array: order them on one stream.  The device
+ * status (bad offsets / ids) is not reported by this call; the device still applies
+ * the same rules (see the header comment).
+ * Errors (nothing is launched): those of gmm_run, plus GMM_ERR_INVALID_ARG
+ * (num_experts < 1), GMM_ERR_NO_DEVICE (current device is not sm_103),
+ * GMM_ERR_UNSUPPORTED (more than 256 SMs, or a device index >= 64).
+ */
+int gmm_run_noalloc(void *c, const void *a, const uint32_t *a_offsets, const void *b,
+                    const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_experts,
+                    int num_groups, int N, int K, cudaStream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the device status that the kernels of
  * this handle accumulated since the last query.  Returns GMM_OK,
  * GMM_ERR_BAD_INPUT or GMM_ERR_DEVICE_TIMEOUT (timeout wins when both are set),

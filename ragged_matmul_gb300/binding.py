@@ -31,8 +31,8 @@ GMM_ERR_DEVICE_TIMEOUT = -4
 GMM_ERR_BAD_INPUT = -5
 GMM_ERR_NO_DEVICE = -6
 
-EXPORTED = ("gmm_create", "gmm_run", "gmm_run_int4", "gmm_query_status", "gmm_error_string",
-            "gmm_destroy")
+EXPORTED = ("gmm_create", "gmm_run", "gmm_run_int4", "gmm_run_noalloc", "gmm_query_status",
+            "gmm_error_string", "gmm_destroy")
 
 _lib = None
 
@@ -63,6 +63,8 @@ def load_library(path: str | None = None):
     lib.gmm_run.restype = I
     lib.gmm_run_int4.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, P]
     lib.gmm_run_int4.restype = I
+    lib.gmm_run_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
+    lib.gmm_run_noalloc.restype = I
     lib.gmm_query_status.argtypes = [P, P]
     lib.gmm_query_status.restype = I
     lib.gmm_error_string.argtypes = [I]

@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "gmm.h"
@@ -284,3 +285,122 @@ int gmm_query_status(gmm_handle_t h, cudaStream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point (gmm_run_noalloc).
+//
+// Some callers cannot call cudaMalloc at the moment they need a grouped GEMM:
+// code running inside a custom allocator or memory-pool callback, a framework
+// that has reserved the whole device for its own pool, or an inference runtime
+// that forbids allocations after start-up.  gmm_run_noalloc serves them: it
+// launches the same bf16 kernel as gmm_run, but takes the kernel's scratch (its
+// status word and the per-CTA patched tensor maps) from the fixed array below
+// instead of a handle's cudaMalloc'd workspace, and it creates no handle.
+//
+// g_noalloc_scratch lives in every GPU that loads this library, until the
+// process exits.  In host code its name is only a host-side stand-in, so the
+// host never passes it to a kernel: it passes the device address obtained from
+// cudaGetSymbolAddress once per device.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kNoAllocMaxCtas = 256;   // persistent grid = SM count; 152 on GB300
+constexpr size_t kNoAllocScratchBytes = kStatusBytes + static_cast<size_t>(kNoAllocMaxCtas) * gmm::kMapSlotBytes;
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];   // 65,792 bytes
+
+struct NoAllocDevice {
+  bool ready = false;
+  int rc = GMM_OK;    // outcome of the one-time set-up
+  gmm_ctx ctx;        // static storage; ctx.ws points into g_noalloc_scratch on this device
+};
+
+NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
+std::mutex g_noalloc_mutex;
+
+// One-time set-up for the current device: resolve the scratch array's device
+// address, the tensor-map encoder and the kernel's shared-memory configuration.
+int noalloc_setup(int device, gmm_ctx **out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  NoAllocDevice &d = g_noalloc_devices[device];
+  if (d.ready) {
+    *out = &d.ctx;
+    return d.rc;
+  }
+  int major = 0, minor = 0, sms = 0, optin = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  int rc = GMM_OK;
+  if (major != 10 || minor != 3 || sms < 1) rc = GMM_ERR_NO_DEVICE;
+  else if (sms > kNoAllocMaxCtas) rc = GMM_ERR_UNSUPPORTED;   // scratch holds 256 CTA slots
+  void *scratch = nullptr;
+  if (rc == GMM_OK && cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess) rc = GMM_ERR_CUDA;
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (rc == GMM_OK &&
+      (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+           cudaSuccess ||
+       q != cudaDriverEntryPointSuccess || !fn))
+    rc = GMM_ERR_CUDA;
+  if (rc == GMM_OK) {
+    d.ctx.device = device;
+    d.ctx.num_sms = sms;
+    d.ctx.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    d.ctx.stages_bf16 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<false>),
+                                    gmm::kStageBytes, optin, &d.ctx.smem_bf16);
+    if (!d.ctx.stages_bf16) rc = GMM_ERR_CUDA;
+    d.ctx.ws = static_cast<uint8_t *>(scratch);
+    d.ctx.ws_bytes = kNoAllocScratchBytes;
+  }
+  if (rc != GMM_OK) cudaGetLastError();
+  d.rc = rc;
+  d.ready = true;
+  *out = &d.ctx;
+  return rc;
+}
+
+}  // namespace
+
+extern "C" int gmm_run_noalloc(void *c, const void *a, const uint32_t *a_offsets, const void *b,
+                               const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_experts,
+                               int num_groups, int N, int K, cudaStream_t stream) {
+  if (num_experts < 1) return GMM_ERR_INVALID_ARG;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0) {
+    cudaGetLastError();
+    return GMM_ERR_NO_DEVICE;
+  }
+  if (device >= kNoAllocMaxDevices) return GMM_ERR_UNSUPPORTED;
+  gmm_ctx *h = nullptr;
+  int rc = noalloc_setup(device, &h);
+  if (rc) return rc;
+  rc = check_common(h, c, a, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  if (rc) return rc;
+  if (!b || !aligned16(b)) return GMM_ERR_INVALID_ARG;
+
+  GmmParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(num_experts)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(N) * K * 2};
+    cuuint32_t box[3] = {gmm::kBK, gmm::kBlockN, 1};
+    rc = encode_map(h, &p.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  }
+  rc = encode_token_maps(h, p, a, K);
+  if (rc) return rc;
+  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  p.num_experts = num_experts;
+  p.num_stages = h->stages_bf16;
+  // The status word keeps the previous call's flags: clear it (stream-ordered, no allocation).
+  if (cudaMemsetAsync(h->ws, 0, sizeof(uint32_t), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return GMM_ERR_CUDA;
+  }
+  return launch<false>(h, p, stream);
+}
