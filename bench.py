@@ -27,7 +27,6 @@ import json
 import os
 import re
 import statistics
-import subprocess
 import sys
 import threading
 import time
@@ -95,57 +94,80 @@ def profiled_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 100 ms while running."""
+    """SM clock, power and clock-event reasons, sampled every 10 ms from a thread.
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    Reads them through NVML (libnvidia-ml, shipped with the driver) with ctypes:
+    read-only queries, no setting of the GPU is touched.  Falls back to no samples
+    when NVML cannot be loaded.
+    """
 
-    def __init__(self, index: int):
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, period_s: float = 0.01):
         self.index = index
+        self.period = period_s
         self.samples = []
-        self.proc = None
+        self._stop = threading.Event()
         self.thread = None
+        self.nvml = None
+        self.handle = None
+        self.max_mhz = None
+
+    def _open(self):
+        import ctypes
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                lib = None
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+            return False
+        self.nvml, self.handle = lib, h
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # 1 = SM clock
+            self.max_mhz = mx.value
+        return True
+
+    def _poll(self):
+        import ctypes
+        lib, h = self.nvml, self.handle
+        mhz, mw, reasons = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(mhz)) == 0
+            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+            get_reasons(h, ctypes.byref(reasons))
+            if ok:
+                self.samples.append((time.time(), mhz.value, mw.value / 1000.0, reasons.value))
+            self._stop.wait(self.period)
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            if not self._open():
+                return
+        except Exception:
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread = threading.Thread(target=self._poll, daemon=True)
         self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
-                self.samples.append((time.time(), parts))
-
     def stop(self):
-        if self.proc:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        self._stop.set()
+        if self.thread:
+            self.thread.join(timeout=2)
 
     def summary(self, t0, t1):
-        inside = [p for t, p in self.samples if t0 <= t <= t1]
-        use = inside or [p for t, p in self.samples]
-        def num(x):
-            try:
-                return float(x)
-            except ValueError:
-                return None
-        sm = [num(p[1]) for p in use if num(p[1]) is not None]
-        mx = [num(p[2]) for p in use if num(p[2]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for p in use for i in range(4) if p[5 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(inside), "samples_total": len(self.samples)}
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        reasons = sorted({name for x in inside for bit, name in self.REASONS.items() if x[3] & bit})
+        return {"sm_mhz": statistics.median([x[1] for x in inside]) if inside else None,
+                "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "power_w_max": max((x[2] for x in inside), default=None),
+                "samples": len(inside), "source": "nvml" if self.nvml else "unavailable"}
 
 
 def dist_env():
@@ -233,7 +255,7 @@ def sample_desc(r, s):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode", choices=[n for n in wl.WORKLOAD_NAMES])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -241,6 +263,10 @@ def main():
                     help="CPU oracle work per step of the reference arm / per cpu_baseline pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--groups", type=int, default=0,
+                    help="profile-sized sub-workload: only the first G groups of the named routing")
+    ap.add_argument("--variant", default=None, choices=["pair", "single"],
+                    help="kernel variant (default: the library's choice, CTA pairs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -254,12 +280,14 @@ def main():
     dev = torch.device(f"cuda:{local}")
 
     r = wl.routing(args.workload)
+    if args.groups:
+        r = wl.first_groups(r, args.groups)
     flops, nbytes, rows = work_counts(r)
     peaks, peaks_kind = load_peaks()
     t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if t_tensor >= t_hbm else "hbm"
-    config = {"workload": args.workload, "E": r.E, "N": r.N, "K": r.K, "groups": r.G,
+    config = {"workload": r.name, "E": r.E, "N": r.N, "K": r.K, "groups": r.G,
               "active_groups": int(r.active_mask().sum()), "rows": rows,
               "useful_flops": flops, "algorithmic_bytes": nbytes,
               "l2": "flushed between steps (512 MiB write)", "weights": "int4" if r.int4 else "bf16"}
@@ -297,6 +325,8 @@ def main():
     barrier(world)
 
     vals = wl.device_values(r, rank, device=dev)
+    if args.variant:
+        os.environ["GMM_VARIANT"] = args.variant
     h = binding.gmm_create(r.E, local)
     c = torch.full((r.rows, r.N), wl.SENTINEL_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
     off = torch.from_numpy(r.a_offsets.view(np.int32)).to(dev)
@@ -398,7 +428,8 @@ def main():
         roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                     "traffic": profiled_traffic(args.workload), "peak_source": f"{peaks_kind} (burst)",
                     "roofline_time_ms": max(t_tensor, t_hbm) * 1e3,
-                    "kernel": "gmm_grouped_kernel<%s>" % ("true" if r.int4 else "false")}
+                    "kernel": "gmm_grouped_kernel<%s, %s>" % ("true" if r.int4 else "false",
+                                                              "false" if args.variant == "single" else "true")}
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",

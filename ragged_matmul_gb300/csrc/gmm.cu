@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -35,6 +36,13 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+// One launch configuration per kernel variant.
+struct gmm_variant {
+  int stages = 0;
+  size_t smem = 0;
+  int grid = 0;   // CTAs: the SM count, or (pairs) twice the co-resident clusters of two
+};
+
 struct gmm_ctx {
   int device = 0;
   int num_experts = 0;
@@ -43,6 +51,9 @@ struct gmm_ctx {
   size_t smem_bf16 = 0;
   int stages_int4 = 0;
   size_t smem_int4 = 0;
+  gmm_variant pair_bf16;
+  gmm_variant pair_int4;
+  int use_pairs = 1;              // 1: CTA-pair kernels (cta_group::2), 0: one CTA per tile
   uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
   size_t ws_bytes = 0;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -85,6 +96,10 @@ int check_common(gmm_ctx *h, void *c, const void *a, const uint32_t *a_offsets, 
   return GMM_OK;
 }
 
+// Token blocks per band of the tile order: as many 256-row blocks of A as fit in
+// about 40 MB, a third of the GB300's L2, so a band's activations stay resident.
+constexpr double kBandBytes = 40e6;
+
 void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, const int32_t *ids,
                  uint32_t *stats, int G, int N, int K) {
   p.c = static_cast<__nv_bfloat16 *>(c);
@@ -97,34 +112,92 @@ void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, c
   p.num_experts = h->num_experts;
   p.N = N;
   p.K = K;
+  const double block_bytes = static_cast<double>(gmm::kMaxTok) * K * 2.0;
+  const double band = kBandBytes / block_bytes;
+  p.tok_band = band < 1.0 ? 1 : (band > 1e6 ? 1000000 : static_cast<int>(band));
+  if (const char *env = getenv("GMM_TOK_BAND")) {   // tuning override
+    const int v = atoi(env);
+    if (v > 0) p.tok_band = v;
+  }
+  p.two_ended = 0;
+  if (const char *env = getenv("GMM_TWO_ENDED")) p.two_ended = atoi(env) != 0;   // tuning override
+  p.cache_hints = 1;
+  if (const char *env = getenv("GMM_CACHE_HINTS")) p.cache_hints = atoi(env) != 0;   // tuning override
 }
 
 // Deepest ring that fits next to the kernel's static shared memory: the number of
 // pipeline stages is chosen from the shared-memory budget of the device.
-int pick_stages(const void *kernel, int stage_bytes, int optin, size_t *dyn_bytes) {
+int pick_stages(const void *kernel, int stage_bytes, int optin, size_t *dyn_bytes, int fixed_bytes = 0) {
   cudaFuncAttributes attr;
   if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return 0;
-  const long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024;
+  const long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024 - fixed_bytes;
   long s = budget / stage_bytes;
   if (s > gmm::kMaxStages) s = gmm::kMaxStages;
   if (s < 2) return 0;
-  *dyn_bytes = static_cast<size_t>(s) * stage_bytes + 1024;
+  *dyn_bytes = static_cast<size_t>(s) * stage_bytes + fixed_bytes + 1024;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(*dyn_bytes)) != cudaSuccess)
     return 0;
   return static_cast<int>(s);
 }
 
+// Configure a CTA-pair kernel: ring depth from the shared-memory budget, grid from
+// the number of clusters of two that fit on the device at once.
 template <bool kInt4>
-int launch(gmm_ctx *h, const GmmParams &p, cudaStream_t stream) {
+int setup_pair(gmm_variant *v, int stage_bytes, int optin, int num_sms) {
+  const void *kernel = reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<kInt4, true>);
+  v->stages = pick_stages(kernel, stage_bytes, optin, &v->smem, kInt4 ? gmm::kQRingBytes : 0);
+  if (!v->stages) return GMM_ERR_CUDA;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+  cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : gmm::kThreads);
+  cfg.dynamicSmemBytes = v->smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  if (cudaOccupancyMaxActiveClusters(&clusters, gmm::gmm_grouped_kernel<kInt4, true>, &cfg) != cudaSuccess ||
+      clusters < 1) {
+    cudaGetLastError();
+    return GMM_ERR_CUDA;
+  }
+  v->grid = 2 * clusters < (num_sms & ~1) ? 2 * clusters : (num_sms & ~1);
+  return GMM_OK;
+}
+
+template <bool kInt4>
+int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   DeviceGuard guard(h->device);
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>(h->num_sms));
+  cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : gmm::kThreads);
-  cfg.dynamicSmemBytes = kInt4 ? h->smem_int4 : h->smem_bf16;
   cfg.stream = stream;
-  if (cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4>, p) != cudaSuccess) {
+  cudaError_t err;
+  if (h->use_pairs) {
+    const gmm_variant &v = kInt4 ? h->pair_int4 : h->pair_bf16;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(v.grid));
+    cfg.dynamicSmemBytes = v.smem;
+    p.num_stages = v.stages;
+    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, true>, p);
+  } else {
+    cfg.gridDim = dim3(static_cast<unsigned>(h->num_sms));
+    cfg.dynamicSmemBytes = kInt4 ? h->smem_int4 : h->smem_bf16;
+    p.num_stages = kInt4 ? h->stages_int4 : h->stages_bf16;
+    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, false>, p);
+  }
+  if (err != cudaSuccess) {
     cudaGetLastError();
     return GMM_ERR_CUDA;
   }
@@ -182,10 +255,16 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
   }
   h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 
-  h->stages_bf16 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<false>),
+  h->stages_bf16 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<false, false>),
                                gmm::kStageBytes, optin, &h->smem_bf16);
-  h->stages_int4 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<true>),
-                               gmm::kInt4StageBytes, optin, &h->smem_int4);
+  h->stages_int4 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<true, false>),
+                               gmm::kInt4StageBytes, optin, &h->smem_int4, gmm::kQRingBytes);
+  const char *variant = getenv("GMM_VARIANT");   // tuning override: "single" or "pair"
+  h->use_pairs = !(variant && std::strcmp(variant, "single") == 0) && sms >= 2;
+  if (h->use_pairs &&
+      (setup_pair<false>(&h->pair_bf16, gmm::kPairStageBytes, optin, sms) != GMM_OK ||
+       setup_pair<true>(&h->pair_int4, gmm::kPairInt4StageBytes, optin, sms) != GMM_OK))
+    h->use_pairs = 0;
   if (!h->stages_bf16 || !h->stages_int4) {
     cudaGetLastError();
     delete h;
@@ -234,7 +313,6 @@ int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, c
   rc = encode_token_maps(h, p, a, K);
   if (rc) return rc;
   fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
-  p.num_stages = h->stages_bf16;
   return launch<false>(h, p, stream);
 }
 
@@ -263,7 +341,6 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
   rc = encode_token_maps(h, p, a, K);
   if (rc) return rc;
   fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
-  p.num_stages = h->stages_int4;
   p.scales = static_cast<const __nv_bfloat16 *>(b_scales);
   p.group_size = group_size;
   return launch<true>(h, p, stream);
@@ -349,8 +426,9 @@ int noalloc_setup(int device, gmm_ctx **out) {
     d.ctx.device = device;
     d.ctx.num_sms = sms;
     d.ctx.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    d.ctx.stages_bf16 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<false>),
+    d.ctx.stages_bf16 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<false, false>),
                                     gmm::kStageBytes, optin, &d.ctx.smem_bf16);
+    d.ctx.use_pairs = 0;   // one CTA per tile: the grid is the SM count, one scratch slot per CTA
     if (!d.ctx.stages_bf16) rc = GMM_ERR_CUDA;
     d.ctx.ws = static_cast<uint8_t *>(scratch);
     d.ctx.ws_bytes = kNoAllocScratchBytes;

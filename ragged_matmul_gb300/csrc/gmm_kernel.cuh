@@ -26,8 +26,10 @@
 //   warps 2..5  epilogue: TMEM -> registers -> bf16 -> C, masking token rows past
 //               the group's end and columns past N.  Two accumulators let the
 //               epilogue of one tile overlap the main loop of the next.
-//   warps 6..9  (4-bit variant only) dequantise the packed slab of each stage
-//               into the bf16 weight slab the MMA reads.
+//   warp 6      (4-bit variant) TMA producer of the packed 4-bit slabs, into
+//               their own 8-deep ring so they run well ahead of the MMA.
+//   warps 7..14 (4-bit variant) dequantise packed slabs into the bf16 weight slab
+//               of the W/T stage the MMA reads next.
 //
 // Row bounds.  The host does not know how many rows A has (that is
 // a_offsets[G], on the device), so the token tensor maps are encoded with a
@@ -53,12 +55,19 @@ constexpr int kBK = 64;                       // K per stage: one 128-byte swizz
 constexpr int kMaxStages = 8;
 constexpr int kMaxGroups = 4096;
 constexpr int kThreads = 192;                 // bf16 kernel: producer, MMA, 4 epilogue warps
-constexpr int kInt4Threads = 320;             // 4-bit kernel: + 4 dequantisation warps
+constexpr int kDequantThreads = 256;          // 4-bit kernel: 8 dequantisation warps, two threads per weight row
+constexpr int kInt4Threads = kThreads + 32 + kDequantThreads;   // + one packed-slab producer warp
+constexpr int kQStages = 8;                   // 4-bit kernel: depth of the packed-slab ring
 constexpr int kWBytes = kBlockN * kBK * 2;    // 16 KB weight slab
 constexpr int kTBytes = kMaxTok * kBK * 2;    // 32 KB token slab
 constexpr int kStageBytes = kWBytes + kTBytes;
 constexpr int kQBytes = kBlockN * kBK / 2;    // 4 KB packed 4-bit slab (128 rows x 8 words)
-constexpr int kInt4StageBytes = kStageBytes + kQBytes;
+constexpr int kInt4StageBytes = kStageBytes;  // per W/T stage; the packed ring (kQRingBytes) is extra
+constexpr int kQRingBytes = kQStages * kQBytes;
+// CTA-pair variant: each CTA holds 128 weight rows and half of the (<= 256) tokens.
+constexpr int kPairTBytes = kTBytes / 2;      // 16 KB token half-slab
+constexpr int kPairStageBytes = kWBytes + kPairTBytes;
+constexpr int kPairInt4StageBytes = kPairStageBytes;
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr int kMapSlotBytes = 256;            // per-CTA workspace: two patched 128-byte tensor maps
@@ -89,10 +98,14 @@ struct alignas(128) GmmParams {
   int num_stages;
   const __nv_bfloat16 *scales;   // 4-bit path: [E, N, K / group_size]
   int group_size;                // 4-bit path: multiple of 64 dividing K
+  int tok_band;                  // token blocks per band of the tile order (see decode_tile)
+  int two_ended;                 // 1: interleave tiles from both ends of the tile order (see tile_of)
+  int cache_hints;               // 1: L2 eviction priorities on the TMA loads (see the producer)
 };
 
 struct Tile {
   int32_t e;
+  uint32_t single_block;   // the group fits one token block: its weight panels are read once
   uint32_t row0;   // first token row of the tile
   uint32_t nrows;  // token rows that belong to the group (<= 256)
   uint32_t ntok;   // nrows rounded up to 16: the MMA's N
@@ -100,8 +113,11 @@ struct Tile {
 };
 
 struct __align__(8) Ctrl {
-  uint64_t full[kMaxStages];    // TMA bytes of the stage landed
-  uint64_t wfull[kMaxStages];   // 4-bit path: dequantised weight slab written
+  uint64_t full[kMaxStages];    // TMA bytes of the stage landed (pair: both CTAs', on the leader)
+  uint64_t qfull[kQStages];     // 4-bit path: a packed slab landed (this CTA)
+  uint64_t qempty[kQStages];    // 4-bit path: the dequantisation warps are done with a packed slab
+  uint64_t wfull[kMaxStages];   // 4-bit path: dequantised weight slab written (pair leader: both CTAs')
+  uint64_t wlocal[kMaxStages];  // 4-bit pair peer: its own slab written (forwarded to the leader)
   uint64_t empty[kMaxStages];   // MMAs that read the stage completed
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
@@ -137,16 +153,23 @@ __device__ __forceinline__ bool wait_phase_for(uint32_t bar, uint32_t parity, ui
   return true;
 }
 
-// Tiles of one group: token blocks of 256 rows times n-blocks of 128 columns.
+// Work-unit geometry of the two variants.
+template <bool kPair>
+struct TileShape {
+  static constexpr uint32_t kRows = kPair ? 2 * kBlockN : kBlockN;   // weight rows (C columns) per tile
+  static constexpr uint32_t kTokAlign = kPair ? 32 : 16;             // token granule: MMA N (pair: 2 x 16)
+};
+
+// Tiles of one group: token blocks of 256 rows times n-blocks of kRows columns.
 __device__ __forceinline__ unsigned long long group_tiles(uint32_t rows, uint32_t n_blocks) {
   return static_cast<unsigned long long>((rows + kMaxTok - 1) / kMaxTok) * n_blocks;
 }
 
 // Scan a_offsets / expert_ids into prefix[g] = first tile of group g (all NT threads).
-template <int NT>
+template <int NT, bool kPair>
 __device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix) {
   const int G = p.num_groups;
-  const uint32_t n_blocks = static_cast<uint32_t>((p.N + kBlockN - 1) / kBlockN);
+  const uint32_t n_blocks = static_cast<uint32_t>((p.N + TileShape<kPair>::kRows - 1) / TileShape<kPair>::kRows);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chunk = (G + NT - 1) / NT;
   const int g_begin = min(G, tid * chunk), g_end = min(G, g_begin + chunk);
@@ -196,6 +219,13 @@ __device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix) 
   __syncthreads();
 }
 
+// Tile t -> (group, n-block, token block).  Within a group the token blocks are cut
+// into bands of p.tok_band blocks; a band is walked n-block by n-block with its token
+// blocks fastest.  CTAs running at the same time then share one weight panel, and the
+// band's activations (tok_band x 256 rows x K) stay in L2 while the weight panels of
+// the whole expert stream past; without bands a large group would re-read all of its
+// activations from DRAM for every wave of n-blocks.
+template <bool kPair>
 __device__ __forceinline__ Tile decode_tile(uint32_t t, const uint32_t *prefix, const GmmParams &p) {
   int lo = 0, hi = p.num_groups - 1;   // last group whose first tile is <= t
   while (lo < hi) {
@@ -206,15 +236,33 @@ __device__ __forceinline__ Tile decode_tile(uint32_t t, const uint32_t *prefix, 
   const uint32_t r0 = __ldg(p.a_offsets + lo);
   const uint32_t rows = __ldg(p.a_offsets + lo + 1) - r0;
   const uint32_t n_tok_blocks = (rows + kMaxTok - 1) / kMaxTok;
-  const uint32_t nb = local / n_tok_blocks;
-  const uint32_t tb = local - nb * n_tok_blocks;
+  const uint32_t n_blocks = (static_cast<uint32_t>(p.N) + TileShape<kPair>::kRows - 1) / TileShape<kPair>::kRows;
+  const uint32_t band = static_cast<uint32_t>(p.tok_band);
+  const uint32_t band_idx = local / (band * n_blocks);
+  const uint32_t in_band = local - band_idx * band * n_blocks;
+  const uint32_t band_len = min(band, n_tok_blocks - band_idx * band);
+  const uint32_t nb = in_band / band_len;
+  const uint32_t tb = band_idx * band + (in_band - nb * band_len);
+  constexpr uint32_t kAlign = TileShape<kPair>::kTokAlign;
   Tile x;
   x.e = __ldg(p.expert_ids + lo);
   x.row0 = r0 + tb * kMaxTok;
   x.nrows = min(static_cast<uint32_t>(kMaxTok), rows - tb * kMaxTok);
-  x.ntok = (x.nrows + 15u) & ~15u;
-  x.n0 = nb * kBlockN;
+  x.ntok = (x.nrows + kAlign - 1) & ~(kAlign - 1);
+  x.n0 = nb * TileShape<kPair>::kRows;
+  x.single_block = n_tok_blocks == 1;
   return x;
+}
+
+// Work slot c -> tile index.  With p.two_ended the even slots walk the tile order
+// from the front and the odd slots from the back (a bijection on [0, total)).  Groups
+// come largest first, so CTAs working on the compute-heavy tiles of large groups run
+// alongside CTAs streaming the weights of small groups, and the two bounds overlap
+// instead of following each other.  Slots of one parity stay consecutive, so CTAs
+// running at the same time still share weight panels.
+__device__ __forceinline__ uint32_t tile_of(uint32_t c, uint32_t total, int two_ended) {
+  if (!two_ended) return c;
+  return (c & 1u) ? total - 1u - (c >> 1) : (c >> 1);
 }
 
 // Dequantise one packed word (8 four-bit values, k = 8j .. 8j+7, low nibble first)
@@ -240,12 +288,39 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
   return out;
 }
 
+// Bounded wait with cluster-scope acquire (for barriers the peer CTA arrives on).
+__device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((spin & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // kInt4 = false: bf16 weights, 192 threads.  kInt4 = true: packed 4-bit weights
-// dequantised by warps 6..9 into the stage's bf16 slab ahead of the MMA, 320 threads.
-template <bool kInt4>
+// streamed by warp 6 and dequantised by warps 7..14 into the stage's bf16 slab ahead
+// of the MMA, 480 threads.
+// kPair = false: one CTA per tile, tcgen05 cta_group::1, M = 128.
+// kPair = true: a cluster of two CTAs per tile, tcgen05 cta_group::2, M = 256: CTA r
+//   loads weight rows n0 + 128 r .. + 128 and token rows half r of the tile; the
+//   leader (r = 0) waits for both halves, issues every MMA and commits to both
+//   CTAs' barriers; each CTA's epilogue stores its own 128 columns of C.
+template <bool kInt4, bool kPair>
 __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     gmm_grouped_kernel(const __grid_constant__ GmmParams p) {
   constexpr int NT = kInt4 ? kInt4Threads : kThreads;
+  constexpr uint32_t kTBytesCta = kPair ? kPairTBytes : kTBytes;   // token slab per CTA
+  constexpr uint32_t kWIn = kInt4 ? 0u : static_cast<uint32_t>(kWBytes);   // weight bytes through `full`
+  constexpr uint32_t kEpiArrivals = (kPair ? 2 : 1) * 4;                         // one per epilogue warp
+  constexpr uint32_t kDequantWarps = kDequantThreads / 32;
+  constexpr uint32_t kDequantArrivals = kDequantWarps + (kPair ? 1 : 0);   // + the peer's forwarded arrive
   __shared__ Ctrl ctl;
   __shared__ uint32_t prefix[kMaxGroups + 1];
   extern __shared__ uint8_t dyn_smem[];
@@ -253,23 +328,32 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = p.num_stages;
   const int KB = (p.K + kBK - 1) / kBK;
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const uint32_t unit0 = kPair ? cluster_id_x() : blockIdx.x;      // first tile of this CTA / pair
+  const uint32_t unit_step = kPair ? cluster_count_x() : gridDim.x;
 
   // 1024-byte aligned ring: S weight slabs, S token slabs, then (4-bit) S packed slabs.
+  // Identical offsets in both CTAs of a pair.
   const uint32_t dyn_base = smem_addr(dyn_smem);
   const uint32_t ring = (dyn_base + 1023u) & ~1023u;
   const uint32_t w_ring = ring;
   const uint32_t t_ring = ring + S * kWBytes;
-  const uint32_t q_ring = t_ring + S * kTBytes;
+  const uint32_t q_ring = t_ring + S * kTBytesCta;   // 4-bit: kQStages packed slabs
 
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_addr(&ctl.full[s]), 1);
-      mbar_init(smem_addr(&ctl.wfull[s]), 4 * 32);
+      mbar_init(smem_addr(&ctl.wfull[s]), kDequantArrivals);
+      mbar_init(smem_addr(&ctl.wlocal[s]), kDequantWarps);
       mbar_init(smem_addr(&ctl.empty[s]), 1);
+    }
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(smem_addr(&ctl.qfull[s]), 1);
+      mbar_init(smem_addr(&ctl.qempty[s]), kDequantWarps);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_addr(&ctl.acc_full[a]), 1);
-      mbar_init(smem_addr(&ctl.acc_empty[a]), 4 * 32);
+      mbar_init(smem_addr(&ctl.acc_empty[a]), kEpiArrivals);
     }
     ctl.abort = 0;
     ctl.active = 0;
@@ -277,12 +361,18 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
-    tmem_relinquish();
+    if constexpr (kPair) {
+      tmem_alloc_pair(smem_addr(&ctl.tmem_base), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
+      tmem_relinquish();
+    }
     tc_fence_before_sync();
   }
   __syncthreads();
-  build_schedule<NT>(p, ctl, prefix);
+  build_schedule<NT, kPair>(p, ctl, prefix);
+  if constexpr (kPair) cluster_sync();   // the peer's barriers are initialised before anyone signals them
 
   if (blockIdx.x == 0 && tid == 0) {
     p.stats[1] = ctl.active;
@@ -315,78 +405,123 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const CUtensorMap *tok16 = reinterpret_cast<const CUtensorMap *>(slot + 128);
       prefetch_tensormap(&p.w_map);
 
+      const uint64_t pol_first = l2_policy_evict_first();
+      const uint64_t pol_last = l2_policy_evict_last();
+      const uint64_t pol_normal = l2_policy_evict_normal();
       uint32_t stage = 0, phase = 0;
       uint32_t pending = 0;     // bit s: stage s has copies whose completion this thread has not seen
       uint32_t pend_phase = 0;  // bit s: the phase in which they complete
       bool ok = true;
-      for (uint32_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile ti = decode_tile(t, prefix, p);
-        const uint32_t tx = (kInt4 ? kQBytes : kWBytes) + ti.ntok * (kBK * 2);
+      for (uint32_t t = unit0; t < total && ok; t += unit_step) {
+        const Tile ti = decode_tile<kPair>(tile_of(t, total, p.two_ended), prefix, p);
+        const uint32_t my_tok = kPair ? ti.ntok / 2 : ti.ntok;     // token rows this CTA loads
+        const uint32_t tx = (kPair ? 2u : 1u) * (kWIn + my_tok * (kBK * 2));
+        const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
+        // L2 priorities: a weight panel that only one token block of its group reads is
+        // streamed once (evict first); token slabs are read again by every n-block of the
+        // group (evict last), so streaming weights do not wash them out of L2.
+        const uint64_t w_pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
+        const uint64_t t_pol = p.cache_hints ? pol_last : pol_normal;
         for (int kb = 0; kb < KB; ++kb) {
-          const uint32_t full = smem_addr(&ctl.full[stage]);
+          const uint32_t full_local = smem_addr(&ctl.full[stage]);
           if (!wait_phase(smem_addr(&ctl.empty[stage]), phase ^ 1u, abort)) { ok = false; break; }
-          mbar_arrive_expect_tx(full, tx);
           const int32_t k0 = kb * kBK;
-          if (kInt4)
-            tma_load_3d(q_ring + stage * kQBytes, &p.w_map, full, k0 / 8, static_cast<int32_t>(ti.n0), ti.e);
-          else
-            tma_load_3d(w_ring + stage * kWBytes, &p.w_map, full, k0, static_cast<int32_t>(ti.n0), ti.e);
-          uint32_t dst_t = t_ring + stage * kTBytes;
-          int32_t r = static_cast<int32_t>(ti.row0);
-          uint32_t left = ti.ntok;
-          for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
-            tma_load_2d(dst_t, tok128, full, k0, r);
-          for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
-            tma_load_2d(dst_t, tok16, full, k0, r);
+          if (rank == 0) mbar_arrive_expect_tx(full_local, tx);
+          uint32_t dst_t = t_ring + stage * kTBytesCta;
+          int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok);
+          uint32_t left = my_tok;
+          if constexpr (kPair) {
+            const uint32_t full_leader = map_to_rank(full_local, 0);
+            if (!kInt4) tma_load_3d_pair(w_ring + stage * kWBytes, &p.w_map, full_leader, k0, w_row, ti.e, w_pol);
+            for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
+              tma_load_2d_pair(dst_t, tok128, full_leader, k0, r, t_pol);
+            for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
+              tma_load_2d_pair(dst_t, tok16, full_leader, k0, r, t_pol);
+          } else {
+            if (!kInt4) tma_load_3d_hint(w_ring + stage * kWBytes, &p.w_map, full_local, k0, w_row, ti.e, w_pol);
+            for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
+              tma_load_2d_hint(dst_t, tok128, full_local, k0, r, t_pol);
+            for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
+              tma_load_2d_hint(dst_t, tok16, full_local, k0, r, t_pol);
+          }
           pending |= 1u << stage;
           pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
           if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
         }
       }
       if (!ok) {
-        // Let the copies already issued land before the CTA can exit.
+        // Let the copies already issued land before the CTA can exit.  In a pair only the
+        // leader can observe `full` (it counts both CTAs' bytes); the peer is held at the
+        // final cluster barrier until the leader has drained.
         for (int s = 0; s < S; ++s)
           if (pending & (1u << s))
-            wait_phase_for(smem_addr(&ctl.full[s]), (pend_phase >> s) & 1u, kDrainLimitNs);
+            if (rank == 0) wait_phase_for(smem_addr(&ctl.full[s]), (pend_phase >> s) & 1u, kDrainLimitNs);
         atomicOr(p.status, kStatusTimeout);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && total > 0) {
+    // ------------------------------------------------------------ MMA issuer (the leader of a pair)
+    if (lane == 0 && total > 0 && rank == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (uint32_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        const Tile ti = decode_tile(t, prefix, p);
-        if (!wait_phase(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort)) { ok = false; break; }
+      for (uint32_t t = unit0; t < total && ok; t += unit_step) {
+        const Tile ti = decode_tile<kPair>(tile_of(t, total, p.two_ended), prefix, p);
+        const bool got = kPair ? wait_phase_cluster(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort)
+                               : wait_phase(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort);
+        if (!got) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        const uint32_t idesc = idesc_bf16_f32(kBlockN, ti.ntok);
+        const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBlockN : kBlockN, ti.ntok);
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_phase(smem_addr(&ctl.full[stage]), phase, abort)) { ok = false; break; }
-          if (kInt4 && !wait_phase(smem_addr(&ctl.wfull[stage]), phase, abort)) { ok = false; break; }
+          if (kInt4) {
+            const bool w_ok = kPair ? wait_phase_cluster(smem_addr(&ctl.wfull[stage]), phase, abort)
+                                    : wait_phase(smem_addr(&ctl.wfull[stage]), phase, abort);
+            if (!w_ok) { ok = false; break; }
+          }
           tc_fence_after_sync();
           const uint64_t a_desc = smem_desc_k_sw128(w_ring + stage * kWBytes);
-          const uint64_t b_desc = smem_desc_k_sw128(t_ring + stage * kTBytes);
+          const uint64_t b_desc = smem_desc_k_sw128(t_ring + stage * kTBytesCta);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)   // +32 bytes along K per step: +2 in the >>4 address field
-            mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0);
-          mma_commit(smem_addr(&ctl.empty[stage]));
+          for (int k = 0; k < kBK / 16; ++k) {   // +32 bytes along K per step: +2 in the >>4 address field
+            if constexpr (kPair)
+              mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0);
+            else
+              mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0);
+          }
+          if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.empty[stage]), 0x3);
+          else mma_commit(smem_addr(&ctl.empty[stage]));
           if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        mma_commit(smem_addr(&ctl.acc_full[acc]));
+        if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.acc_full[acc]), 0x3);
+        else mma_commit(smem_addr(&ctl.acc_full[acc]));
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
+      if (!ok) atomicOr(p.status, kStatusTimeout);
+    } else if (kInt4 && kPair && lane == 0 && total > 0 && rank != 0) {
+      // Forwarder of the pair's peer: one cluster-scope arrive per stage on the leader's
+      // wfull once this CTA's eight dequantisation warps have written their slab.
+      const uint32_t wfull_leader0 = map_to_rank(smem_addr(&ctl.wfull[0]), 0);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (uint32_t t = unit0; t < total && ok; t += unit_step)
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_phase(smem_addr(&ctl.wlocal[stage]), phase, abort)) { ok = false; break; }
+          mbar_arrive_cluster(wfull_leader0 + stage * sizeof(uint64_t));
+          if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+        }
       if (!ok) atomicOr(p.status, kStatusTimeout);
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
     const uint32_t quad = static_cast<uint32_t>(warp & 3);   // TMEM lanes this warp may read
+    const uint32_t acc_empty0 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[0]), 0) : smem_addr(&ctl.acc_empty[0]);
+    const uint32_t acc_empty1 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[1]), 0) : smem_addr(&ctl.acc_empty[1]);
     uint32_t acc = 0, acc_phase = 0;
-    for (uint32_t t = blockIdx.x; t < total; t += gridDim.x) {
-      const Tile ti = decode_tile(t, prefix, p);
+    for (uint32_t t = unit0; t < total; t += unit_step) {
+      const Tile ti = decode_tile<kPair>(tile_of(t, total, p.two_ended), prefix, p);
       int ok = 1;
       if (lane == 0) ok = wait_phase(smem_addr(&ctl.acc_full[acc]), acc_phase, abort);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -395,7 +530,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const uint32_t n = ti.n0 + quad * 32 + static_cast<uint32_t>(lane);
+      const uint32_t n = ti.n0 + rank * kBlockN + quad * 32 + static_cast<uint32_t>(lane);
       const bool col_ok = n < static_cast<uint32_t>(p.N);
       __nv_bfloat16 *cp = p.c + static_cast<size_t>(ti.row0) * p.N + n;
       const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * kAccCols;
@@ -411,46 +546,109 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         }
       }
       tc_fence_before_sync();
-      mbar_arrive(smem_addr(&ctl.acc_empty[acc]));
+      __syncwarp();
+      if (lane == 0) {
+        if constexpr (kPair) mbar_arrive_cluster(acc ? acc_empty1 : acc_empty0);
+        else mbar_arrive(acc ? acc_empty1 : acc_empty0);
+      }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+  } else if (kInt4 && warp == 6) {
+    // ------------------------------------------------------------ packed-slab producer (4-bit)
+    if (lane == 0 && total > 0) {
+      prefetch_tensormap(&p.w_map);
+      uint32_t qs = 0, qphase = 0;
+      uint32_t pending = 0, pend_phase = 0;
+      bool ok = true;
+      for (uint32_t t = unit0; t < total && ok; t += unit_step) {
+        const Tile ti = decode_tile<kPair>(tile_of(t, total, p.two_ended), prefix, p);
+        const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!wait_phase(smem_addr(&ctl.qempty[qs]), qphase ^ 1u, abort)) { ok = false; break; }
+          const uint32_t qfull = smem_addr(&ctl.qfull[qs]);
+          mbar_arrive_expect_tx(qfull, kQBytes);
+          tma_load_3d(q_ring + qs * kQBytes, &p.w_map, qfull, kb * (kBK / 8), w_row, ti.e);
+          pending |= 1u << qs;
+          pend_phase = (pend_phase & ~(1u << qs)) | (qphase << qs);
+          if (++qs == static_cast<uint32_t>(kQStages)) { qs = 0; qphase ^= 1u; }
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < kQStages; ++s)
+          if (pending & (1u << s)) wait_phase_for(smem_addr(&ctl.qfull[s]), (pend_phase >> s) & 1u, kDrainLimitNs);
+        atomicOr(p.status, kStatusTimeout);
+      }
+    }
   } else if (kInt4) {
     // ------------------------------------------------------------ 4-bit dequantisation
-    // Thread r (0..127) owns weight row n0 + r of every stage: 8 packed words in,
-    // 8 swizzled 16-byte bf16 chunks out (chunk j of row r lands at j ^ (r % 8)).
-    const uint32_t r = static_cast<uint32_t>(tid - 6 * 32);
+    // Thread u (0..255) owns half of weight row r = u / 2: packed words 4h .. 4h+3
+    // (h = u % 2) in, 16 consecutive bytes of the packed slab, so a warp's loads are
+    // conflict-free; four 16-byte bf16 chunks out, chunk j of row r landing at
+    // j ^ (r % 8) (the 128-byte swizzle).  A packed slab is consumed from the deep
+    // packed ring as soon as it lands and the W slot of the stage is free (the MMA
+    // that last read it has completed).  Scales are loaded four k-steps ahead.
+    const uint32_t u = static_cast<uint32_t>(tid - (kThreads + 32));
+    const uint32_t r = u >> 1, h = u & 1u;
     const int spr = p.K / p.group_size;   // scales per weight row
-    uint32_t stage = 0, phase = 0;
+    const int kb_per_scale = p.group_size / kBK;
+    const unsigned short *sbits = reinterpret_cast<const unsigned short *>(p.scales);
+    const uint32_t wdone0 = smem_addr(kPair && rank != 0 ? &ctl.wlocal[0] : &ctl.wfull[0]);
+    uint32_t stage = 0, phase = 0, qs = 0, qphase = 0;
     bool ok = true;
-    for (uint32_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
-      const Tile ti = decode_tile(t, prefix, p);
-      const uint32_t n = ti.n0 + r;
+    for (uint32_t t = unit0; t < total && ok; t += unit_step) {
+      const Tile ti = decode_tile<kPair>(tile_of(t, total, p.two_ended), prefix, p);
+      const uint32_t n = ti.n0 + rank * kBlockN + r;
       const bool row_ok = n < static_cast<uint32_t>(p.N);
-      const __nv_bfloat16 *srow = p.scales + (static_cast<size_t>(ti.e) * p.N + (row_ok ? n : 0)) * spr;
-      for (int kb = 0; kb < KB; ++kb) {
-        const __nv_bfloat16 s = row_ok ? srow[(kb * kBK) / p.group_size] : __float2bfloat16_rn(0.0f);
-        if (!wait_phase(smem_addr(&ctl.full[stage]), phase, abort)) { ok = false; break; }
-        const uint4 *q = reinterpret_cast<const uint4 *>(dyn_smem + (q_ring - dyn_base) + stage * kQBytes + r * 32);
-        const uint4 q0 = q[0], q1 = q[1];
-        const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-        const __nv_bfloat162 s2 = __halves2bfloat162(s, s);
-        uint8_t *wrow = dyn_smem + (w_ring - dyn_base) + stage * kWBytes + r * 128;
+      const unsigned short *srow = sbits + (static_cast<size_t>(ti.e) * p.N + (row_ok ? n : 0)) * spr;
+      auto scale_at = [&](int kb) -> unsigned short {
+        return (row_ok && kb < KB) ? __ldg(srow + kb / kb_per_scale) : static_cast<unsigned short>(0);
+      };
+      // Scale of k-step kb sits in sq[kb % 4], loaded four k-steps before it is used
+      // (the loop is unrolled by four so each slot stays in its own register).
+      unsigned short sq[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4 *>(wrow + ((j ^ (r & 7)) << 4)) = dequant_word(words[j], s2);
-        fence_async_smem();   // generic-proxy writes -> visible to the tensor core's reads
-        mbar_arrive(smem_addr(&ctl.wfull[stage]));
-        if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+      for (int j = 0; j < 4; ++j) sq[j] = scale_at(j);
+      for (int kb0 = 0; kb0 < KB && ok; kb0 += 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int kb = kb0 + j;
+          if (kb >= KB || !ok) continue;
+          const unsigned short s = sq[j];
+          sq[j] = scale_at(kb + 4);
+          const bool landed = wait_phase(smem_addr(&ctl.qfull[qs]), qphase, abort) &&
+                              wait_phase(smem_addr(&ctl.empty[stage]), phase ^ 1u, abort);
+          if (!__all_sync(0xffffffffu, landed)) { ok = false; continue; }   // the warp aborts together
+          const uint4 q = *reinterpret_cast<const uint4 *>(dyn_smem + (q_ring - dyn_base) + qs * kQBytes + u * 16);
+          const __nv_bfloat16 sb = __ushort_as_bfloat16(s);
+          const __nv_bfloat162 s2v = __halves2bfloat162(sb, sb);
+          uint8_t *wrow = dyn_smem + (w_ring - dyn_base) + stage * kWBytes + r * 128;
+          const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const uint32_t jc = 4 * h + jj;
+            *reinterpret_cast<uint4 *>(wrow + ((jc ^ (r & 7u)) << 4)) = dequant_word(words[jj], s2v);
+          }
+          fence_async_smem();   // generic-proxy writes -> visible to the tensor core's reads
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(smem_addr(&ctl.qempty[qs]));
+            mbar_arrive(wdone0 + stage * sizeof(uint64_t));
+          }
+          if (++qs == static_cast<uint32_t>(kQStages)) { qs = 0; qphase ^= 1u; }
+          if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+        }
       }
     }
     if (!ok) atomicOr(p.status, kStatusTimeout);
   }
 
   __syncthreads();
+  if constexpr (kPair) cluster_sync();   // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if constexpr (kPair) tmem_dealloc_pair(tmem_base, kTmemCols);
+    else tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 

@@ -151,6 +151,17 @@ def routing(name: str, seed: int | None = None) -> Routing:
     raise KeyError(name)
 
 
+def first_groups(r: Routing, G: int) -> Routing:
+    """The sub-workload made of the first G groups of r (rows, ids and distributions kept;
+    E shrunk to the largest expert id used + 1)."""
+    ids = r.expert_ids[:G]
+    valid = ids[(ids >= 0) & (ids < r.E)]
+    E = int(valid.max()) + 1 if valid.size else 1
+    return Routing(f"{r.name}[:{G}]", E, r.N, r.K, r.loads[:G].copy(), ids.copy(),
+                   offsets_from_loads(r.loads[:G]), r.a_dist, r.b_dist, r.int4, r.group_size,
+                   r.scale_range)
+
+
 # ---------------------------------------------------------------- host values (numpy)
 
 def _to_bf16_bits(x: np.ndarray) -> np.ndarray:

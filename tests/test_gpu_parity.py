@@ -31,11 +31,24 @@ def _built():
 
 _handles = {}
 
+VARIANTS = ("pair", "single")   # CTA-pair kernels (default) and one CTA per tile
 
-def handle(E):
-    if E not in _handles:
-        _handles[E] = binding.gmm_create(E, 0)
-    return _handles[E]
+
+def handle(E, variant="pair"):
+    """A handle per (E, kernel variant); the variant is fixed when the handle is created."""
+    import os
+    key = (E, variant)
+    if key not in _handles:
+        old = os.environ.get("GMM_VARIANT")
+        os.environ["GMM_VARIANT"] = variant
+        try:
+            _handles[key] = binding.gmm_create(E, 0)
+        finally:
+            if old is None:
+                del os.environ["GMM_VARIANT"]
+            else:
+                os.environ["GMM_VARIANT"] = old
+    return _handles[key]
 
 
 def routing(E, N, K, loads, ids, dist=("uniform", -1.0, 1.0), base=0, int4=False, gs=128):
@@ -45,23 +58,26 @@ def routing(E, N, K, loads, ids, dist=("uniform", -1.0, 1.0), base=0, int4=False
 
 # ---------------------------------------------------------------- named tiny workload
 
-def test_tiny_workload():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_tiny_workload(variant):
     r = wl.routing("tiny")
     v = wl.host_values(r, 0)
-    _, _, status, _ = check_against_oracle(handle(r.E), r, v, where="tiny")
+    _, _, status, _ = check_against_oracle(handle(r.E, variant), r, v, where="tiny")
     assert status == binding.GMM_OK
 
 
 # ---------------------------------------------------------------- exact arithmetic
 
-def test_small_integers_bit_exact():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_small_integers_bit_exact(variant):
     """Integer operands in [-3, 3], K <= 28: every sum is exact, so C must match bit for bit."""
-    r = routing(5, 136, 24, [1, 17, 0, 130, 33, 256, 7], [4, 0, 2, 3, -1, 1, 4], dist=("int", -3, 3))
+    r = routing(5, 392, 24, [1, 17, 0, 130, 33, 256, 7, 300], [4, 0, 2, 3, -1, 1, 4, 2], dist=("int", -3, 3))
     v = wl.host_values(r, 1)
-    check_against_oracle(handle(5), r, v, exact=True, where="int")
+    check_against_oracle(handle(5, variant), r, v, exact=True, where="int")
 
 
-def test_unit_rows_select_weight_columns():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_unit_rows_select_weight_columns(variant):
     """A rows that are unit vectors e_k return B[e, n, k] exactly: pins operand orientation."""
     E, N, K = 3, 256, 64
     rng = np.random.default_rng(2)
@@ -71,7 +87,7 @@ def test_unit_rows_select_weight_columns():
         A[g * K + np.arange(K), np.arange(K)] = 1.0
     ids = [2, 0, 1]
     off = wl.offsets_from_loads([K, K, K])
-    got, stats, status = run_gpu(handle(E), wl._to_bf16_bits(A), off, ids, b_bits=b, N=N)
+    got, stats, status = run_gpu(handle(E, variant), wl._to_bf16_bits(A), off, ids, b_bits=b, N=N)
     for g in range(3):
         for k in range(K):
             assert np.array_equal(got[g * K + k], b[ids[g], :, k]), (g, k)
@@ -80,13 +96,14 @@ def test_unit_rows_select_weight_columns():
 
 # ---------------------------------------------------------------- ragged shapes and tails
 
-@pytest.mark.parametrize("N,K", [(384, 320), (136, 200), (256, 64), (1024, 1096)])
-def test_ragged_groups_tails(N, K):
-    loads = [1, 15, 16, 17, 127, 128, 129, 255, 256, 257, 300, 513, 0, 2]
-    ids = [3, 0, 5, 1, 7, 2, 6, 4, 3, 0, 1, 2, 6, 7]
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("N,K", [(384, 320), (136, 200), (256, 64), (1024, 1096), (648, 512)])
+def test_ragged_groups_tails(N, K, variant):
+    loads = [1, 15, 16, 17, 31, 32, 33, 127, 128, 129, 255, 256, 257, 300, 513, 0, 2]
+    ids = [3, 0, 5, 1, 7, 2, 6, 4, 3, 0, 1, 2, 6, 7, 5, 1, 4]
     r = routing(8, N, K, loads, ids, dist=("normal", 1.0))
     v = wl.host_values(r, 3)
-    _, _, status, _ = check_against_oracle(handle(8), r, v, where=f"ragged N={N} K={K}")
+    _, _, status, _ = check_against_oracle(handle(8, variant), r, v, where=f"ragged N={N} K={K} {variant}")
     assert status == binding.GMM_OK
 
 
@@ -145,12 +162,13 @@ def test_expert_id_out_of_range_is_skipped_and_reported():
 
 # ---------------------------------------------------------------- invariants
 
-def test_group_permutation_and_determinism():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_group_permutation_and_determinism(variant):
     loads = [300, 7, 129, 0, 64, 511]
     ids = [1, 0, 3, 2, -1, 1]
     r = routing(4, 640, 256, loads, ids, dist=("normal", 1.0))
     v = wl.host_values(r, 10)
-    h = handle(4)
+    h = handle(4, variant)
     base, _, _ = run_gpu(h, v["a"], r.a_offsets, r.expert_ids, b_bits=v["b"], N=r.N)
     again, _, _ = run_gpu(h, v["a"], r.a_offsets, r.expert_ids, b_bits=v["b"], N=r.N)
     assert np.array_equal(base, again), "repeated runs differ"
@@ -192,19 +210,21 @@ def _scaled(name, N, K):
                            scale_range=full.scale_range)
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("name,N,K", [("decode", 2816, 256), ("prefill", 512, 512),
                                       ("fine_grained", 256, 448), ("int4", 512, 512)])
-def test_named_workload_routing_at_reduced_width(name, N, K):
+def test_named_workload_routing_at_reduced_width(name, N, K, variant):
     """The full routing (all rows, all groups, skips) with N and K cut down."""
     r = _scaled(name, N, K)
     v = wl.host_values(r, 12)
-    _, _, status, _ = check_against_oracle(handle(r.E), r, v, where=name)
+    _, _, status, _ = check_against_oracle(handle(r.E, variant), r, v, where=f"{name} {variant}")
     assert status == binding.GMM_OK
 
 
 # ---------------------------------------------------------------- 4-bit variant
 
-def test_int4_integer_case_bit_exact():
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_int4_integer_case_bit_exact(variant):
     rng = np.random.default_rng(13)
     E, N, K, gs = 3, 256, 256, 128
     r = routing(E, N, K, [7, 0, 130, 45], [2, 1, 0, 2], int4=True, gs=gs)
@@ -212,15 +232,16 @@ def test_int4_integer_case_bit_exact():
     q = rng.integers(0, 16, (E, N, K))
     v = {"a": a, "packed": wl.pack_nibbles(q),
          "scales": wl._to_bf16_bits(np.ones((E, N, K // gs), np.float32))}
-    check_against_oracle(handle(E), r, v, exact=True, where="int4 exact")
+    check_against_oracle(handle(E, variant), r, v, exact=True, where="int4 exact")
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("gs", [64, 128, 256])
-def test_int4_random(gs):
+def test_int4_random(gs, variant):
     r = routing(6, 384, 512, [33, 0, 257, 16, 100, 1], [5, 0, 1, -1, 3, 2], dist=("normal", 1.0),
                 int4=True, gs=gs)
     v = wl.host_values(r, 14)
-    _, _, status, _ = check_against_oracle(handle(6), r, v, where=f"int4 gs={gs}")
+    _, _, status, _ = check_against_oracle(handle(6, variant), r, v, where=f"int4 gs={gs} {variant}")
     assert status == binding.GMM_OK
 
 
