@@ -428,8 +428,9 @@ def main():
         roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                     "traffic": profiled_traffic(args.workload), "peak_source": f"{peaks_kind} (burst)",
                     "roofline_time_ms": max(t_tensor, t_hbm) * 1e3,
-                    "kernel": "gmm_grouped_kernel<%s, %s>" % ("true" if r.int4 else "false",
-                                                              "false" if args.variant == "single" else "true")}
+                    "kernel": "gmm_grouped_kernel<%s, %s>" % (
+                        "true" if r.int4 else "false",
+                        "true" if (args.variant == "pair" or (args.variant is None and not r.int4)) else "false")}
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",

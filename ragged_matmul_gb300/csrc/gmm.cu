@@ -38,22 +38,18 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 // One launch configuration per kernel variant.
 struct gmm_variant {
-  int stages = 0;
-  size_t smem = 0;
-  int grid = 0;   // CTAs: the SM count, or (pairs) twice the co-resident clusters of two
+  int stages = 0;     // depth of the W+T stage ring
+  size_t smem = 0;    // dynamic shared memory
+  int grid = 0;       // CTAs: the SM count, or (pairs) twice the co-resident clusters of two
 };
 
 struct gmm_ctx {
   int device = 0;
   int num_experts = 0;
   int num_sms = 0;
-  int stages_bf16 = 0;
-  size_t smem_bf16 = 0;
-  int stages_int4 = 0;
-  size_t smem_int4 = 0;
-  gmm_variant pair_bf16;
-  gmm_variant pair_int4;
-  int use_pairs = 1;              // 1: CTA-pair kernels (cta_group::2), 0: one CTA per tile
+  gmm_variant var[2][2];          // [4-bit][pair]
+  int use_pairs = 1;              // bf16 path: 1 = CTA-pair kernels (cta_group::2), 0 = one CTA per tile
+  int use_pairs_int4 = 0;         // 4-bit path: one CTA per tile by default (measured faster)
   uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
   size_t ws_bytes = 0;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -101,7 +97,7 @@ int check_common(gmm_ctx *h, void *c, const void *a, const uint32_t *a_offsets, 
 constexpr double kBandBytes = 40e6;
 
 void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, const int32_t *ids,
-                 uint32_t *stats, int G, int N, int K) {
+                 uint32_t *stats, int G, int N, int K, uint32_t max_tok) {
   p.c = static_cast<__nv_bfloat16 *>(c);
   p.a_offsets = a_offsets;
   p.expert_ids = ids;
@@ -112,7 +108,7 @@ void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, c
   p.num_experts = h->num_experts;
   p.N = N;
   p.K = K;
-  const double block_bytes = static_cast<double>(gmm::kMaxTok) * K * 2.0;
+  const double block_bytes = static_cast<double>(max_tok) * K * 2.0;
   const double band = kBandBytes / block_bytes;
   p.tok_band = band < 1.0 ? 1 : (band > 1e6 ? 1000000 : static_cast<int>(band));
   if (const char *env = getenv("GMM_TOK_BAND")) {   // tuning override
@@ -125,76 +121,70 @@ void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, c
   if (const char *env = getenv("GMM_CACHE_HINTS")) p.cache_hints = atoi(env) != 0;   // tuning override
 }
 
-// Deepest ring that fits next to the kernel's static shared memory: the number of
-// pipeline stages is chosen from the shared-memory budget of the device.
-int pick_stages(const void *kernel, int stage_bytes, int optin, size_t *dyn_bytes, int fixed_bytes = 0) {
+// Ring depths from the device's shared-memory budget (the pages' launcher likewise
+// derives its pipeline depth from the shared memory available), and the grid: one
+// CTA per SM, or for pairs twice the number of clusters of two that fit at once.
+template <bool kInt4, bool kPair>
+int configure(gmm_variant *v, int optin, int num_sms) {
+  using G = gmm::Geom<kInt4, kPair>;
+  auto kernel = gmm::gmm_grouped_kernel<kInt4, kPair>;
   cudaFuncAttributes attr;
-  if (cudaFuncGetAttributes(&attr, kernel) != cudaSuccess) return 0;
-  const long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024 - fixed_bytes;
-  long s = budget / stage_bytes;
-  if (s > gmm::kMaxStages) s = gmm::kMaxStages;
-  if (s < 2) return 0;
-  *dyn_bytes = static_cast<size_t>(s) * stage_bytes + fixed_bytes + 1024;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(*dyn_bytes)) != cudaSuccess)
-    return 0;
-  return static_cast<int>(s);
-}
-
-// Configure a CTA-pair kernel: ring depth from the shared-memory budget, grid from
-// the number of clusters of two that fit on the device at once.
-template <bool kInt4>
-int setup_pair(gmm_variant *v, int stage_bytes, int optin, int num_sms) {
-  const void *kernel = reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<kInt4, true>);
-  v->stages = pick_stages(kernel, stage_bytes, optin, &v->smem, kInt4 ? gmm::kQRingBytes : 0);
-  if (!v->stages) return GMM_ERR_CUDA;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
-  cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : gmm::kThreads);
-  cfg.dynamicSmemBytes = v->smem;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int clusters = 0;
-  if (cudaOccupancyMaxActiveClusters(&clusters, gmm::gmm_grouped_kernel<kInt4, true>, &cfg) != cudaSuccess ||
-      clusters < 1) {
-    cudaGetLastError();
+  if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(kernel)) != cudaSuccess) return GMM_ERR_CUDA;
+  long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024;
+  if (kInt4) budget -= gmm::kQRingBytes;   // the packed-slab ring
+  v->stages = static_cast<int>(budget / static_cast<long>(gmm::kWBytes + G::kTSlot));
+  if (v->stages > gmm::kMaxStages) v->stages = gmm::kMaxStages;
+  if (v->stages < 2) return GMM_ERR_UNSUPPORTED;
+  v->smem = static_cast<size_t>(v->stages) * (gmm::kWBytes + G::kTSlot) +
+            (kInt4 ? gmm::kQRingBytes : 0) + 1024;
+  if (cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(v->smem)) != cudaSuccess)
     return GMM_ERR_CUDA;
+  v->grid = num_sms;
+  if (kPair) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute la[1];
+    la[0].id = cudaLaunchAttributeClusterDimension;
+    la[0].val.clusterDim.x = 2;
+    la[0].val.clusterDim.y = 1;
+    la[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+    cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : gmm::kThreads);
+    cfg.dynamicSmemBytes = v->smem;
+    cfg.attrs = la;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1)
+      return GMM_ERR_CUDA;
+    v->grid = 2 * clusters < (num_sms & ~1) ? 2 * clusters : (num_sms & ~1);
   }
-  v->grid = 2 * clusters < (num_sms & ~1) ? 2 * clusters : (num_sms & ~1);
   return GMM_OK;
 }
 
 template <bool kInt4>
 int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   DeviceGuard guard(h->device);
+  const int pairs = kInt4 ? h->use_pairs_int4 : h->use_pairs;
+  const gmm_variant &v = h->var[kInt4][pairs];
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cudaLaunchAttribute attr[1];
   cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : gmm::kThreads);
+  cfg.gridDim = dim3(static_cast<unsigned>(v.grid));
+  cfg.dynamicSmemBytes = v.smem;
   cfg.stream = stream;
+  p.num_stages = v.stages;
   cudaError_t err;
-  if (h->use_pairs) {
-    const gmm_variant &v = kInt4 ? h->pair_int4 : h->pair_bf16;
+  if (pairs) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(v.grid));
-    cfg.dynamicSmemBytes = v.smem;
-    p.num_stages = v.stages;
     err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, true>, p);
   } else {
-    cfg.gridDim = dim3(static_cast<unsigned>(h->num_sms));
-    cfg.dynamicSmemBytes = kInt4 ? h->smem_int4 : h->smem_bf16;
-    p.num_stages = kInt4 ? h->stages_int4 : h->stages_bf16;
     err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, false>, p);
   }
   if (err != cudaSuccess) {
@@ -202,6 +192,11 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
     return GMM_ERR_CUDA;
   }
   return GMM_OK;
+}
+
+uint32_t max_tok(const gmm_ctx *h, bool int4) {
+  if (int4) return h->use_pairs_int4 ? gmm::Geom<true, true>::kMaxTok : gmm::Geom<true, false>::kMaxTok;
+  return h->use_pairs ? gmm::Geom<false, true>::kMaxTok : gmm::Geom<false, false>::kMaxTok;
 }
 
 }  // namespace
@@ -255,17 +250,15 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
   }
   h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 
-  h->stages_bf16 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<false, false>),
-                               gmm::kStageBytes, optin, &h->smem_bf16);
-  h->stages_int4 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<true, false>),
-                               gmm::kInt4StageBytes, optin, &h->smem_int4, gmm::kQRingBytes);
-  const char *variant = getenv("GMM_VARIANT");   // tuning override: "single" or "pair"
-  h->use_pairs = !(variant && std::strcmp(variant, "single") == 0) && sms >= 2;
-  if (h->use_pairs &&
-      (setup_pair<false>(&h->pair_bf16, gmm::kPairStageBytes, optin, sms) != GMM_OK ||
-       setup_pair<true>(&h->pair_int4, gmm::kPairInt4StageBytes, optin, sms) != GMM_OK))
-    h->use_pairs = 0;
-  if (!h->stages_bf16 || !h->stages_int4) {
+  const int single_ok = configure<false, false>(&h->var[0][0], optin, sms) == GMM_OK &&
+                        configure<true, false>(&h->var[1][0], optin, sms) == GMM_OK;
+  // Tuning override GMM_VARIANT: "single" or "pair" forces both paths to that variant.
+  const char *variant = getenv("GMM_VARIANT");
+  const bool pairs_ok = sms >= 2 && configure<false, true>(&h->var[0][1], optin, sms) == GMM_OK &&
+                        configure<true, true>(&h->var[1][1], optin, sms) == GMM_OK;
+  h->use_pairs = pairs_ok && !(variant && std::strcmp(variant, "single") == 0);
+  h->use_pairs_int4 = pairs_ok && variant && std::strcmp(variant, "pair") == 0;
+  if (!single_ok) {
     cudaGetLastError();
     delete h;
     return GMM_ERR_CUDA;
@@ -312,7 +305,7 @@ int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, c
   }
   rc = encode_token_maps(h, p, a, K);
   if (rc) return rc;
-  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K, max_tok(h, false));
   return launch<false>(h, p, stream);
 }
 
@@ -340,7 +333,7 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
   }
   rc = encode_token_maps(h, p, a, K);
   if (rc) return rc;
-  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K, max_tok(h, true));
   p.scales = static_cast<const __nv_bfloat16 *>(b_scales);
   p.group_size = group_size;
   return launch<true>(h, p, stream);
@@ -426,10 +419,8 @@ int noalloc_setup(int device, gmm_ctx **out) {
     d.ctx.device = device;
     d.ctx.num_sms = sms;
     d.ctx.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    d.ctx.stages_bf16 = pick_stages(reinterpret_cast<const void *>(gmm::gmm_grouped_kernel<false, false>),
-                                    gmm::kStageBytes, optin, &d.ctx.smem_bf16);
     d.ctx.use_pairs = 0;   // one CTA per tile: the grid is the SM count, one scratch slot per CTA
-    if (!d.ctx.stages_bf16) rc = GMM_ERR_CUDA;
+    if (configure<false, false>(&d.ctx.var[0][0], optin, sms) != GMM_OK) rc = GMM_ERR_CUDA;
     d.ctx.ws = static_cast<uint8_t *>(scratch);
     d.ctx.ws_bytes = kNoAllocScratchBytes;
   }
@@ -472,9 +463,8 @@ extern "C" int gmm_run_noalloc(void *c, const void *a, const uint32_t *a_offsets
   }
   rc = encode_token_maps(h, p, a, K);
   if (rc) return rc;
-  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K, max_tok(h, false));
   p.num_experts = num_experts;
-  p.num_stages = h->stages_bf16;
   // The status word keeps the previous call's flags: clear it (stream-ordered, no allocation).
   if (cudaMemsetAsync(h->ws, 0, sizeof(uint32_t), stream) != cudaSuccess) {
     cudaGetLastError();

@@ -6,30 +6,39 @@
 //
 // Orientation.  The page's launcher swaps A and B so that the weights play the
 // MMA's M role.  This kernel does the same for every tile: the MMA computes
-//   D[n, t] = sum_k W[n, k] * T[t, k]      (M = 128 weight rows, N = tokens)
-// so a tile holds 128 output columns of C and up to 256 token rows, and the
-// token count of a tile only has to be a multiple of 16.  Small groups (decode)
-// therefore pay for at most 15 padded tokens instead of a 128-row tile.
+//   D[n, t] = sum_k W[n, k] * T[t, k]      (M = weight rows, N = tokens)
+// so the token count of a tile only has to be a multiple of 16 (32 for a CTA
+// pair).  Small groups (decode) pay for at most a few padded tokens instead of a
+// 128-row tile.
 //
-// Work decomposition.  A tile is (group g, n-block of 128 weight rows, token
-// block of <= 256 rows of the group).  Every CTA scans a_offsets / expert_ids
-// into a shared-memory prefix sum of tiles per group and walks tiles
-// t = blockIdx.x, blockIdx.x + gridDim.x, ...; token blocks are the fastest
-// index, so CTAs running at the same time share one weight panel in L2.
+// Work decomposition.  A tile is (group g, n-block of weight rows, token block of
+// the group).  Every CTA scans a_offsets / expert_ids into a shared-memory prefix
+// sum of tiles per group and walks its share of tiles; within a group the token
+// blocks are the fastest index (in L2-sized bands), so CTAs running at the same
+// time share one weight panel in L2.
+//
+// Variants (template parameters):
+//   kPair = false  one CTA per tile, 128 weight rows, tcgen05 cta_group::1 (M = 128).
+//   kPair = true   a cluster of two CTAs per tile, 256 weight rows, cta_group::2
+//                  (M = 256): CTA r holds weight rows n0 + 128 r .. + 128 and half
+//                  of the tokens; the leader (r = 0) issues the MMAs and commits to
+//                  both CTAs' barriers; each CTA stores its own 128 columns of C.
+//   kInt4 = false  bf16 weights, loaded by TMA into the stage together with tokens.
+//   kInt4 = true   packed 4-bit weights: a dedicated TMA warp streams packed slabs
+//                  through their own 8-deep ring, and eight warps dequantise them into
+//                  the bf16 weight slab of each stage; the MMA waits for the stage's
+//                  tokens (full) and its dequantised weights (wfull).
 //
 // Roles:
-//   warp 0      TMA producer: weight slab [128 x 64] via a 3-D map over B
-//               [E, N, K] (or the packed 4-bit words) and token slab [ntok x 64]
-//               via 2-D maps over A, 128-byte swizzle, into an S-stage ring.
-//   warp 1      TMEM allocation (512 columns = two 128 x 256 fp32 accumulators)
-//               and the single MMA-issuing thread (tcgen05.mma kind::f16).
-//   warps 2..5  epilogue: TMEM -> registers -> bf16 -> C, masking token rows past
-//               the group's end and columns past N.  Two accumulators let the
-//               epilogue of one tile overlap the main loop of the next.
-//   warp 6      (4-bit variant) TMA producer of the packed 4-bit slabs, into
-//               their own 8-deep ring so they run well ahead of the MMA.
-//   warps 7..14 (4-bit variant) dequantise packed slabs into the bf16 weight slab
-//               of the W/T stage the MMA reads next.
+//   warp 0       TMA producer of token slabs (and of bf16 weight slabs).
+//   warp 1       TMEM allocation (512 columns = two fp32 accumulators) and the
+//                single MMA-issuing thread (tcgen05.mma kind::f16); in a 4-bit
+//                pair's second CTA, the forwarder of its weight-slab readiness.
+//   warps 2..5   epilogue: TMEM -> registers -> bf16 -> C, masking token rows past
+//                the group's end and columns past N; two accumulators let it
+//                overlap the next tile's main loop.
+//   warp 6       (4-bit) TMA producer of packed slabs.
+//   warps 7..14  (4-bit) dequantisation.
 //
 // Row bounds.  The host does not know how many rows A has (that is
 // a_offsets[G], on the device), so the token tensor maps are encoded with a
@@ -49,25 +58,17 @@
 
 namespace gmm {
 
-constexpr int kBlockN = 128;                  // weight rows per tile (MMA M)
-constexpr int kMaxTok = 256;                  // token rows per tile (MMA N, multiple of 16)
+constexpr int kBlockN = 128;                  // weight rows per CTA and tile (MMA M of one CTA)
 constexpr int kBK = 64;                       // K per stage: one 128-byte swizzle row of bf16
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;                // deepest W+T stage ring
 constexpr int kMaxGroups = 4096;
 constexpr int kThreads = 192;                 // bf16 kernel: producer, MMA, 4 epilogue warps
 constexpr int kDequantThreads = 256;          // 4-bit kernel: 8 dequantisation warps, two threads per weight row
 constexpr int kInt4Threads = kThreads + 32 + kDequantThreads;   // + one packed-slab producer warp
 constexpr int kQStages = 8;                   // 4-bit kernel: depth of the packed-slab ring
-constexpr int kWBytes = kBlockN * kBK * 2;    // 16 KB weight slab
-constexpr int kTBytes = kMaxTok * kBK * 2;    // 32 KB token slab
-constexpr int kStageBytes = kWBytes + kTBytes;
+constexpr int kWBytes = kBlockN * kBK * 2;    // 16 KB bf16 weight slab
 constexpr int kQBytes = kBlockN * kBK / 2;    // 4 KB packed 4-bit slab (128 rows x 8 words)
-constexpr int kInt4StageBytes = kStageBytes;  // per W/T stage; the packed ring (kQRingBytes) is extra
 constexpr int kQRingBytes = kQStages * kQBytes;
-// CTA-pair variant: each CTA holds 128 weight rows and half of the (<= 256) tokens.
-constexpr int kPairTBytes = kTBytes / 2;      // 16 KB token half-slab
-constexpr int kPairStageBytes = kWBytes + kPairTBytes;
-constexpr int kPairInt4StageBytes = kPairStageBytes;
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr int kMapSlotBytes = 256;            // per-CTA workspace: two patched 128-byte tensor maps
@@ -79,6 +80,19 @@ constexpr uint32_t kStatusTooLarge = 8u;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // give up on a pipeline wait after 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // and on draining copies after 0.2 s
+
+// Geometry of one kernel variant.
+template <bool kInt4, bool kPair>
+struct Geom {
+  static constexpr uint32_t kRows = kPair ? 2 * kBlockN : kBlockN;   // weight rows (C columns) per tile
+  static constexpr uint32_t kTokAlign = kPair ? 32 : 16;             // MMA N granule (pair: 2 x 16)
+  // Token rows per tile.  The 4-bit path keeps slabs small so its token ring can be
+  // deep: its MMA per stage is short (about 128 tokens), and the token copies come
+  // from L2 with microsecond latency.
+  static constexpr uint32_t kMaxTok = kInt4 ? 160 : 256;
+  static constexpr uint32_t kTSlot = (kPair ? kMaxTok / 2 : kMaxTok) * kBK * 2;   // token slab per CTA
+  static_assert(kTSlot % 1024 == 0, "token slabs must keep the 1024-byte swizzle alignment");
+};
 
 struct alignas(128) GmmParams {
   CUtensorMap w_map;       // bf16 path: B {K, N, E}, box {64, 128, 1}, 128 B swizzle
@@ -95,7 +109,7 @@ struct alignas(128) GmmParams {
   int num_experts;
   int N;
   int K;
-  int num_stages;
+  int num_stages;                // depth of the W+T stage ring
   const __nv_bfloat16 *scales;   // 4-bit path: [E, N, K / group_size]
   int group_size;                // 4-bit path: multiple of 64 dividing K
   int tok_band;                  // token blocks per band of the tile order (see decode_tile)
@@ -106,19 +120,19 @@ struct alignas(128) GmmParams {
 struct Tile {
   int32_t e;
   uint32_t single_block;   // the group fits one token block: its weight panels are read once
-  uint32_t row0;   // first token row of the tile
-  uint32_t nrows;  // token rows that belong to the group (<= 256)
-  uint32_t ntok;   // nrows rounded up to 16: the MMA's N
-  uint32_t n0;     // first weight row / C column
+  uint32_t row0;           // first token row of the tile
+  uint32_t nrows;          // token rows that belong to the group
+  uint32_t ntok;           // nrows rounded up to the MMA granule: the MMA's N
+  uint32_t n0;             // first weight row / C column of the tile
 };
 
 struct __align__(8) Ctrl {
-  uint64_t full[kMaxStages];    // TMA bytes of the stage landed (pair: both CTAs', on the leader)
-  uint64_t qfull[kQStages];     // 4-bit path: a packed slab landed (this CTA)
-  uint64_t qempty[kQStages];    // 4-bit path: the dequantisation warps are done with a packed slab
-  uint64_t wfull[kMaxStages];   // 4-bit path: dequantised weight slab written (pair leader: both CTAs')
-  uint64_t wlocal[kMaxStages];  // 4-bit pair peer: its own slab written (forwarded to the leader)
-  uint64_t empty[kMaxStages];   // MMAs that read the stage completed
+  uint64_t full[kMaxStages];     // stage's TMA bytes landed (pair: both CTAs' bytes, on the leader)
+  uint64_t empty[kMaxStages];    // MMAs that read the stage completed
+  uint64_t wfull[kMaxStages];    // 4-bit: stage's weight slab written (pair leader: both CTAs')
+  uint64_t wlocal[kMaxStages];   // 4-bit pair peer: its own slab written (forwarded to the leader)
+  uint64_t qfull[kQStages];      // 4-bit: a packed slab landed (this CTA)
+  uint64_t qempty[kQStages];     // 4-bit: the dequantisation warps are done with a packed slab
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint32_t tmem_base;
@@ -127,6 +141,17 @@ struct __align__(8) Ctrl {
   uint32_t active;
   uint32_t flags;
   unsigned long long warp_tiles[kInt4Threads / 32];
+};
+
+// A ring position: slot index and the parity of the slot's current use.
+struct Ring {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void next(uint32_t depth) {
+    if (++slot == depth) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
 };
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's abort
@@ -146,6 +171,22 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
+// The same with cluster-scope acquire, for barriers the peer CTA arrives on.
+__device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((spin & 63u) == 0) {
+      if (*abort) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ bool wait_phase_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity))
@@ -153,26 +194,14 @@ __device__ __forceinline__ bool wait_phase_for(uint32_t bar, uint32_t parity, ui
   return true;
 }
 
-// Work-unit geometry of the two variants.
-template <bool kPair>
-struct TileShape {
-  static constexpr uint32_t kRows = kPair ? 2 * kBlockN : kBlockN;   // weight rows (C columns) per tile
-  static constexpr uint32_t kTokAlign = kPair ? 32 : 16;             // token granule: MMA N (pair: 2 x 16)
-};
-
-// Tiles of one group: token blocks of 256 rows times n-blocks of kRows columns.
-__device__ __forceinline__ unsigned long long group_tiles(uint32_t rows, uint32_t n_blocks) {
-  return static_cast<unsigned long long>((rows + kMaxTok - 1) / kMaxTok) * n_blocks;
-}
-
 // Scan a_offsets / expert_ids into prefix[g] = first tile of group g (all NT threads).
-template <int NT, bool kPair>
+template <int NT, class G>
 __device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix) {
-  const int G = p.num_groups;
-  const uint32_t n_blocks = static_cast<uint32_t>((p.N + TileShape<kPair>::kRows - 1) / TileShape<kPair>::kRows);
+  const int Gn = p.num_groups;
+  const uint32_t n_blocks = static_cast<uint32_t>((p.N + G::kRows - 1) / G::kRows);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int chunk = (G + NT - 1) / NT;
-  const int g_begin = min(G, tid * chunk), g_end = min(G, g_begin + chunk);
+  const int chunk = (Gn + NT - 1) / NT;
+  const int g_begin = min(Gn, tid * chunk), g_end = min(Gn, g_begin + chunk);
 
   unsigned long long mine = 0;
   uint32_t active = 0, flags = 0;
@@ -183,7 +212,7 @@ __device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix) 
     if (e >= p.num_experts) flags |= kStatusBadExpert;
     if (e >= 0 && e < p.num_experts) {
       ++active;
-      if (r1 > r0) mine += group_tiles(r1 - r0, n_blocks);
+      if (r1 > r0) mine += static_cast<unsigned long long>((r1 - r0 + G::kMaxTok - 1) / G::kMaxTok) * n_blocks;
     }
     prefix[g + 1] = static_cast<uint32_t>(mine);   // running sum within the chunk, fixed up below
   }
@@ -219,13 +248,21 @@ __device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix) 
   __syncthreads();
 }
 
+// Work slot c -> tile index.  With p.two_ended the even slots walk the tile order
+// from the front and the odd slots from the back (a bijection on [0, total)), so
+// CTAs on compute-heavy tiles of large groups run beside CTAs streaming the weights
+// of small groups.  Off by default: on the measured workloads it was slower.
+__device__ __forceinline__ uint32_t tile_of(uint32_t c, uint32_t total, int two_ended) {
+  if (!two_ended) return c;
+  return (c & 1u) ? total - 1u - (c >> 1) : (c >> 1);
+}
+
 // Tile t -> (group, n-block, token block).  Within a group the token blocks are cut
 // into bands of p.tok_band blocks; a band is walked n-block by n-block with its token
 // blocks fastest.  CTAs running at the same time then share one weight panel, and the
-// band's activations (tok_band x 256 rows x K) stay in L2 while the weight panels of
-// the whole expert stream past; without bands a large group would re-read all of its
-// activations from DRAM for every wave of n-blocks.
-template <bool kPair>
+// band's activations stay in L2 while the weight panels of the whole expert stream
+// past.
+template <class G>
 __device__ __forceinline__ Tile decode_tile(uint32_t t, const uint32_t *prefix, const GmmParams &p) {
   int lo = 0, hi = p.num_groups - 1;   // last group whose first tile is <= t
   while (lo < hi) {
@@ -235,34 +272,22 @@ __device__ __forceinline__ Tile decode_tile(uint32_t t, const uint32_t *prefix, 
   const uint32_t local = t - prefix[lo];
   const uint32_t r0 = __ldg(p.a_offsets + lo);
   const uint32_t rows = __ldg(p.a_offsets + lo + 1) - r0;
-  const uint32_t n_tok_blocks = (rows + kMaxTok - 1) / kMaxTok;
-  const uint32_t n_blocks = (static_cast<uint32_t>(p.N) + TileShape<kPair>::kRows - 1) / TileShape<kPair>::kRows;
+  const uint32_t n_tok_blocks = (rows + G::kMaxTok - 1) / G::kMaxTok;
+  const uint32_t n_blocks = (static_cast<uint32_t>(p.N) + G::kRows - 1) / G::kRows;
   const uint32_t band = static_cast<uint32_t>(p.tok_band);
   const uint32_t band_idx = local / (band * n_blocks);
   const uint32_t in_band = local - band_idx * band * n_blocks;
   const uint32_t band_len = min(band, n_tok_blocks - band_idx * band);
   const uint32_t nb = in_band / band_len;
   const uint32_t tb = band_idx * band + (in_band - nb * band_len);
-  constexpr uint32_t kAlign = TileShape<kPair>::kTokAlign;
   Tile x;
   x.e = __ldg(p.expert_ids + lo);
-  x.row0 = r0 + tb * kMaxTok;
-  x.nrows = min(static_cast<uint32_t>(kMaxTok), rows - tb * kMaxTok);
-  x.ntok = (x.nrows + kAlign - 1) & ~(kAlign - 1);
-  x.n0 = nb * TileShape<kPair>::kRows;
   x.single_block = n_tok_blocks == 1;
+  x.row0 = r0 + tb * G::kMaxTok;
+  x.nrows = min(G::kMaxTok, rows - tb * G::kMaxTok);
+  x.ntok = (x.nrows + G::kTokAlign - 1) & ~(G::kTokAlign - 1);
+  x.n0 = nb * G::kRows;
   return x;
-}
-
-// Work slot c -> tile index.  With p.two_ended the even slots walk the tile order
-// from the front and the odd slots from the back (a bijection on [0, total)).  Groups
-// come largest first, so CTAs working on the compute-heavy tiles of large groups run
-// alongside CTAs streaming the weights of small groups, and the two bounds overlap
-// instead of following each other.  Slots of one parity stay consecutive, so CTAs
-// running at the same time still share weight panels.
-__device__ __forceinline__ uint32_t tile_of(uint32_t c, uint32_t total, int two_ended) {
-  if (!two_ended) return c;
-  return (c & 1u) ? total - 1u - (c >> 1) : (c >> 1);
 }
 
 // Dequantise one packed word (8 four-bit values, k = 8j .. 8j+7, low nibble first)
@@ -288,66 +313,44 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
   return out;
 }
 
-// Bounded wait with cluster-scope acquire (for barriers the peer CTA arrives on).
-__device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, volatile int *abort) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t spin = 1;; ++spin) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((spin & 63u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        return false;
-      }
-    }
-  }
-}
-
-// kInt4 = false: bf16 weights, 192 threads.  kInt4 = true: packed 4-bit weights
-// streamed by warp 6 and dequantised by warps 7..14 into the stage's bf16 slab ahead
-// of the MMA, 480 threads.
-// kPair = false: one CTA per tile, tcgen05 cta_group::1, M = 128.
-// kPair = true: a cluster of two CTAs per tile, tcgen05 cta_group::2, M = 256: CTA r
-//   loads weight rows n0 + 128 r .. + 128 and token rows half r of the tile; the
-//   leader (r = 0) waits for both halves, issues every MMA and commits to both
-//   CTAs' barriers; each CTA's epilogue stores its own 128 columns of C.
 template <bool kInt4, bool kPair>
 __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     gmm_grouped_kernel(const __grid_constant__ GmmParams p) {
+  using G = Geom<kInt4, kPair>;
   constexpr int NT = kInt4 ? kInt4Threads : kThreads;
-  constexpr uint32_t kTBytesCta = kPair ? kPairTBytes : kTBytes;   // token slab per CTA
-  constexpr uint32_t kWIn = kInt4 ? 0u : static_cast<uint32_t>(kWBytes);   // weight bytes through `full`
-  constexpr uint32_t kEpiArrivals = (kPair ? 2 : 1) * 4;                         // one per epilogue warp
+  constexpr uint32_t kEpiArrivals = (kPair ? 2 : 1) * 4;   // one per epilogue warp of each CTA
   constexpr uint32_t kDequantWarps = kDequantThreads / 32;
-  constexpr uint32_t kDequantArrivals = kDequantWarps + (kPair ? 1 : 0);   // + the peer's forwarded arrive
+  constexpr uint32_t kWArrivals = kDequantWarps + (kPair ? 1 : 0);   // + the peer's forwarded arrive
   __shared__ Ctrl ctl;
   __shared__ uint32_t prefix[kMaxGroups + 1];
   extern __shared__ uint8_t dyn_smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int S = p.num_stages;
+  const uint32_t ST = static_cast<uint32_t>(p.num_stages);   // W+T stage ring
+  const uint32_t SW = ST;
   const int KB = (p.K + kBK - 1) / kBK;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
-  const uint32_t unit0 = kPair ? cluster_id_x() : blockIdx.x;      // first tile of this CTA / pair
+  const uint32_t unit0 = kPair ? cluster_id_x() : blockIdx.x;      // first work slot of this CTA / pair
   const uint32_t unit_step = kPair ? cluster_count_x() : gridDim.x;
 
-  // 1024-byte aligned ring: S weight slabs, S token slabs, then (4-bit) S packed slabs.
-  // Identical offsets in both CTAs of a pair.
+  // 1024-byte aligned rings, at identical offsets in both CTAs of a pair:
+  // SW weight slabs, ST token slabs, then (4-bit) kQStages packed slabs.
   const uint32_t dyn_base = smem_addr(dyn_smem);
   const uint32_t ring = (dyn_base + 1023u) & ~1023u;
   const uint32_t w_ring = ring;
-  const uint32_t t_ring = ring + S * kWBytes;
-  const uint32_t q_ring = t_ring + S * kTBytesCta;   // 4-bit: kQStages packed slabs
+  const uint32_t t_ring = ring + SW * kWBytes;
+  const uint32_t q_ring = t_ring + ST * G::kTSlot;
 
   if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (uint32_t s = 0; s < ST; ++s) {
       mbar_init(smem_addr(&ctl.full[s]), 1);
-      mbar_init(smem_addr(&ctl.wfull[s]), kDequantArrivals);
-      mbar_init(smem_addr(&ctl.wlocal[s]), kDequantWarps);
       mbar_init(smem_addr(&ctl.empty[s]), 1);
     }
-    for (int s = 0; s < kQStages; ++s) {
+    for (uint32_t s = 0; s < SW && kInt4; ++s) {
+      mbar_init(smem_addr(&ctl.wfull[s]), kWArrivals);
+      mbar_init(smem_addr(&ctl.wlocal[s]), kDequantWarps);
+    }
+    for (int s = 0; s < kQStages && kInt4; ++s) {
       mbar_init(smem_addr(&ctl.qfull[s]), 1);
       mbar_init(smem_addr(&ctl.qempty[s]), kDequantWarps);
     }
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     tc_fence_before_sync();
   }
   __syncthreads();
-  build_schedule<NT, kPair>(p, ctl, prefix);
+  build_schedule<NT, G>(p, ctl, prefix);
   if constexpr (kPair) cluster_sync();   // the peer's barriers are initialised before anyone signals them
 
   if (blockIdx.x == 0 && tid == 0) {
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   volatile int *abort = &ctl.abort;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ token (and bf16 weight) producer
     if (lane == 0 && total > 0) {
       uint8_t *slot = p.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlotBytes;
       const uint4 *src128 = reinterpret_cast<const uint4 *>(&p.tok_map128);
@@ -404,18 +407,18 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const CUtensorMap *tok128 = reinterpret_cast<const CUtensorMap *>(slot);
       const CUtensorMap *tok16 = reinterpret_cast<const CUtensorMap *>(slot + 128);
       prefetch_tensormap(&p.w_map);
-
       const uint64_t pol_first = l2_policy_evict_first();
       const uint64_t pol_last = l2_policy_evict_last();
       const uint64_t pol_normal = l2_policy_evict_normal();
-      uint32_t stage = 0, phase = 0;
+
+      Ring rt;
       uint32_t pending = 0;     // bit s: stage s has copies whose completion this thread has not seen
       uint32_t pend_phase = 0;  // bit s: the phase in which they complete
       bool ok = true;
-      for (uint32_t t = unit0; t < total && ok; t += unit_step) {
-        const Tile ti = decode_tile<kPair>(tile_of(t, total, p.two_ended), prefix, p);
+      for (uint32_t c = unit0; c < total && ok; c += unit_step) {
+        const Tile ti = decode_tile<G>(tile_of(c, total, p.two_ended), prefix, p);
         const uint32_t my_tok = kPair ? ti.ntok / 2 : ti.ntok;     // token rows this CTA loads
-        const uint32_t tx = (kPair ? 2u : 1u) * (kWIn + my_tok * (kBK * 2));
+        const uint32_t tx = (kPair ? 2u : 1u) * ((kInt4 ? 0u : static_cast<uint32_t>(kWBytes)) + my_tok * (kBK * 2));
         const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
         // L2 priorities: a weight panel that only one token block of its group reads is
         // streamed once (evict first); token slabs are read again by every n-block of the
@@ -423,65 +426,66 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         const uint64_t w_pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
         const uint64_t t_pol = p.cache_hints ? pol_last : pol_normal;
         for (int kb = 0; kb < KB; ++kb) {
-          const uint32_t full_local = smem_addr(&ctl.full[stage]);
-          if (!wait_phase(smem_addr(&ctl.empty[stage]), phase ^ 1u, abort)) { ok = false; break; }
+          const uint32_t full_local = smem_addr(&ctl.full[rt.slot]);
+          if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
           const int32_t k0 = kb * kBK;
           if (rank == 0) mbar_arrive_expect_tx(full_local, tx);
-          uint32_t dst_t = t_ring + stage * kTBytesCta;
+          uint32_t dst_t = t_ring + rt.slot * G::kTSlot;
           int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok);
           uint32_t left = my_tok;
           if constexpr (kPair) {
             const uint32_t full_leader = map_to_rank(full_local, 0);
-            if (!kInt4) tma_load_3d_pair(w_ring + stage * kWBytes, &p.w_map, full_leader, k0, w_row, ti.e, w_pol);
+            if (!kInt4) tma_load_3d_pair(w_ring + rt.slot * kWBytes, &p.w_map, full_leader, k0, w_row, ti.e, w_pol);
             for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
               tma_load_2d_pair(dst_t, tok128, full_leader, k0, r, t_pol);
             for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
               tma_load_2d_pair(dst_t, tok16, full_leader, k0, r, t_pol);
           } else {
-            if (!kInt4) tma_load_3d_hint(w_ring + stage * kWBytes, &p.w_map, full_local, k0, w_row, ti.e, w_pol);
+            if (!kInt4) tma_load_3d_hint(w_ring + rt.slot * kWBytes, &p.w_map, full_local, k0, w_row, ti.e, w_pol);
             for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
               tma_load_2d_hint(dst_t, tok128, full_local, k0, r, t_pol);
             for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
               tma_load_2d_hint(dst_t, tok16, full_local, k0, r, t_pol);
           }
-          pending |= 1u << stage;
-          pend_phase = (pend_phase & ~(1u << stage)) | (phase << stage);
-          if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+          pending |= 1u << rt.slot;
+          pend_phase = (pend_phase & ~(1u << rt.slot)) | (rt.phase << rt.slot);
+          rt.next(ST);
         }
       }
       if (!ok) {
         // Let the copies already issued land before the CTA can exit.  In a pair only the
         // leader can observe `full` (it counts both CTAs' bytes); the peer is held at the
         // final cluster barrier until the leader has drained.
-        for (int s = 0; s < S; ++s)
-          if (pending & (1u << s))
-            if (rank == 0) wait_phase_for(smem_addr(&ctl.full[s]), (pend_phase >> s) & 1u, kDrainLimitNs);
+        for (uint32_t s = 0; s < ST; ++s)
+          if ((pending & (1u << s)) && rank == 0)
+            wait_phase_for(smem_addr(&ctl.full[s]), (pend_phase >> s) & 1u, kDrainLimitNs);
         atomicOr(p.status, kStatusTimeout);
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (the leader of a pair)
     if (lane == 0 && total > 0 && rank == 0) {
-      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      // ---------------------------------------------------------- MMA issuer (the leader of a pair)
+      Ring rt;
+      uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
-      for (uint32_t t = unit0; t < total && ok; t += unit_step) {
-        const Tile ti = decode_tile<kPair>(tile_of(t, total, p.two_ended), prefix, p);
+      for (uint32_t c = unit0; c < total && ok; c += unit_step) {
+        const Tile ti = decode_tile<G>(tile_of(c, total, p.two_ended), prefix, p);
         const bool got = kPair ? wait_phase_cluster(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort)
                                : wait_phase(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort);
         if (!got) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        const uint32_t idesc = idesc_bf16_f32(kPair ? 2 * kBlockN : kBlockN, ti.ntok);
+        const uint32_t idesc = idesc_bf16_f32(G::kRows, ti.ntok);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!wait_phase(smem_addr(&ctl.full[stage]), phase, abort)) { ok = false; break; }
+          if (!wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort)) { ok = false; break; }
           if (kInt4) {
-            const bool w_ok = kPair ? wait_phase_cluster(smem_addr(&ctl.wfull[stage]), phase, abort)
-                                    : wait_phase(smem_addr(&ctl.wfull[stage]), phase, abort);
+            const bool w_ok = kPair ? wait_phase_cluster(smem_addr(&ctl.wfull[rt.slot]), rt.phase, abort)
+                                    : wait_phase(smem_addr(&ctl.wfull[rt.slot]), rt.phase, abort);
             if (!w_ok) { ok = false; break; }
           }
           tc_fence_after_sync();
-          const uint64_t a_desc = smem_desc_k_sw128(w_ring + stage * kWBytes);
-          const uint64_t b_desc = smem_desc_k_sw128(t_ring + stage * kTBytesCta);
+          const uint64_t a_desc = smem_desc_k_sw128(w_ring + rt.slot * kWBytes);
+          const uint64_t b_desc = smem_desc_k_sw128(t_ring + rt.slot * G::kTSlot);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {   // +32 bytes along K per step: +2 in the >>4 address field
             if constexpr (kPair)
@@ -489,9 +493,9 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
             else
               mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0);
           }
-          if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.empty[stage]), 0x3);
-          else mma_commit(smem_addr(&ctl.empty[stage]));
-          if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+          if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.empty[rt.slot]), 0x3);
+          else mma_commit(smem_addr(&ctl.empty[rt.slot]));
+          rt.next(ST);
         }
         if (!ok) break;
         if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.acc_full[acc]), 0x3);
@@ -501,16 +505,17 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       }
       if (!ok) atomicOr(p.status, kStatusTimeout);
     } else if (kInt4 && kPair && lane == 0 && total > 0 && rank != 0) {
-      // Forwarder of the pair's peer: one cluster-scope arrive per stage on the leader's
-      // wfull once this CTA's eight dequantisation warps have written their slab.
+      // ---------------------------------------------------------- forwarder (4-bit pair, second CTA)
+      // One cluster-scope arrive per weight slab on the leader's wfull, once this CTA's
+      // eight dequantisation warps have written their half of it.
       const uint32_t wfull_leader0 = map_to_rank(smem_addr(&ctl.wfull[0]), 0);
-      uint32_t stage = 0, phase = 0;
+      Ring rw;
       bool ok = true;
-      for (uint32_t t = unit0; t < total && ok; t += unit_step)
+      for (uint32_t c = unit0; c < total && ok; c += unit_step)
         for (int kb = 0; kb < KB; ++kb) {
-          if (!wait_phase(smem_addr(&ctl.wlocal[stage]), phase, abort)) { ok = false; break; }
-          mbar_arrive_cluster(wfull_leader0 + stage * sizeof(uint64_t));
-          if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+          if (!wait_phase(smem_addr(&ctl.wlocal[rw.slot]), rw.phase, abort)) { ok = false; break; }
+          mbar_arrive_cluster(wfull_leader0 + rw.slot * sizeof(uint64_t));
+          rw.next(SW);
         }
       if (!ok) atomicOr(p.status, kStatusTimeout);
     }
@@ -520,8 +525,8 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     const uint32_t acc_empty0 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[0]), 0) : smem_addr(&ctl.acc_empty[0]);
     const uint32_t acc_empty1 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[1]), 0) : smem_addr(&ctl.acc_empty[1]);
     uint32_t acc = 0, acc_phase = 0;
-    for (uint32_t t = unit0; t < total; t += unit_step) {
-      const Tile ti = decode_tile<kPair>(tile_of(t, total, p.two_ended), prefix, p);
+    for (uint32_t c = unit0; c < total; c += unit_step) {
+      const Tile ti = decode_tile<G>(tile_of(c, total, p.two_ended), prefix, p);
       int ok = 1;
       if (lane == 0) ok = wait_phase(smem_addr(&ctl.acc_full[acc]), acc_phase, abort);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -558,20 +563,23 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     // ------------------------------------------------------------ packed-slab producer (4-bit)
     if (lane == 0 && total > 0) {
       prefetch_tensormap(&p.w_map);
-      uint32_t qs = 0, qphase = 0;
+      const uint64_t pol_first = l2_policy_evict_first();
+      const uint64_t pol_normal = l2_policy_evict_normal();
+      Ring rq;
       uint32_t pending = 0, pend_phase = 0;
       bool ok = true;
-      for (uint32_t t = unit0; t < total && ok; t += unit_step) {
-        const Tile ti = decode_tile<kPair>(tile_of(t, total, p.two_ended), prefix, p);
+      for (uint32_t c = unit0; c < total && ok; c += unit_step) {
+        const Tile ti = decode_tile<G>(tile_of(c, total, p.two_ended), prefix, p);
         const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
+        const uint64_t pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!wait_phase(smem_addr(&ctl.qempty[qs]), qphase ^ 1u, abort)) { ok = false; break; }
-          const uint32_t qfull = smem_addr(&ctl.qfull[qs]);
+          if (!wait_phase(smem_addr(&ctl.qempty[rq.slot]), rq.phase ^ 1u, abort)) { ok = false; break; }
+          const uint32_t qfull = smem_addr(&ctl.qfull[rq.slot]);
           mbar_arrive_expect_tx(qfull, kQBytes);
-          tma_load_3d(q_ring + qs * kQBytes, &p.w_map, qfull, kb * (kBK / 8), w_row, ti.e);
-          pending |= 1u << qs;
-          pend_phase = (pend_phase & ~(1u << qs)) | (qphase << qs);
-          if (++qs == static_cast<uint32_t>(kQStages)) { qs = 0; qphase ^= 1u; }
+          tma_load_3d_hint(q_ring + rq.slot * kQBytes, &p.w_map, qfull, kb * (kBK / 8), w_row, ti.e, pol);
+          pending |= 1u << rq.slot;
+          pend_phase = (pend_phase & ~(1u << rq.slot)) | (rq.phase << rq.slot);
+          rq.next(kQStages);
         }
       }
       if (!ok) {
@@ -585,19 +593,19 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     // Thread u (0..255) owns half of weight row r = u / 2: packed words 4h .. 4h+3
     // (h = u % 2) in, 16 consecutive bytes of the packed slab, so a warp's loads are
     // conflict-free; four 16-byte bf16 chunks out, chunk j of row r landing at
-    // j ^ (r % 8) (the 128-byte swizzle).  A packed slab is consumed from the deep
-    // packed ring as soon as it lands and the W slot of the stage is free (the MMA
-    // that last read it has completed).  Scales are loaded four k-steps ahead.
+    // j ^ (r % 8) (the 128-byte swizzle).  A packed slab is consumed as soon as it
+    // lands and the next weight slot is free (the MMA that last read it completed).
+    // Scales are loaded four k-steps ahead.
     const uint32_t u = static_cast<uint32_t>(tid - (kThreads + 32));
     const uint32_t r = u >> 1, h = u & 1u;
     const int spr = p.K / p.group_size;   // scales per weight row
     const int kb_per_scale = p.group_size / kBK;
     const unsigned short *sbits = reinterpret_cast<const unsigned short *>(p.scales);
     const uint32_t wdone0 = smem_addr(kPair && rank != 0 ? &ctl.wlocal[0] : &ctl.wfull[0]);
-    uint32_t stage = 0, phase = 0, qs = 0, qphase = 0;
+    Ring rw, rq;
     bool ok = true;
-    for (uint32_t t = unit0; t < total && ok; t += unit_step) {
-      const Tile ti = decode_tile<kPair>(tile_of(t, total, p.two_ended), prefix, p);
+    for (uint32_t c = unit0; c < total && ok; c += unit_step) {
+      const Tile ti = decode_tile<G>(tile_of(c, total, p.two_ended), prefix, p);
       const uint32_t n = ti.n0 + rank * kBlockN + r;
       const bool row_ok = n < static_cast<uint32_t>(p.N);
       const unsigned short *srow = sbits + (static_cast<size_t>(ti.e) * p.N + (row_ok ? n : 0)) * spr;
@@ -616,13 +624,15 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           if (kb >= KB || !ok) continue;
           const unsigned short s = sq[j];
           sq[j] = scale_at(kb + 4);
-          const bool landed = wait_phase(smem_addr(&ctl.qfull[qs]), qphase, abort) &&
-                              wait_phase(smem_addr(&ctl.empty[stage]), phase ^ 1u, abort);
+          // Packed slab landed and the stage's weight slot free (the MMA that last read
+          // it completed).
+          const bool landed = wait_phase(smem_addr(&ctl.qfull[rq.slot]), rq.phase, abort) &&
+                              wait_phase(smem_addr(&ctl.empty[rw.slot]), rw.phase ^ 1u, abort);
           if (!__all_sync(0xffffffffu, landed)) { ok = false; continue; }   // the warp aborts together
-          const uint4 q = *reinterpret_cast<const uint4 *>(dyn_smem + (q_ring - dyn_base) + qs * kQBytes + u * 16);
+          const uint4 q = *reinterpret_cast<const uint4 *>(dyn_smem + (q_ring - dyn_base) + rq.slot * kQBytes + u * 16);
           const __nv_bfloat16 sb = __ushort_as_bfloat16(s);
           const __nv_bfloat162 s2v = __halves2bfloat162(sb, sb);
-          uint8_t *wrow = dyn_smem + (w_ring - dyn_base) + stage * kWBytes + r * 128;
+          uint8_t *wrow = dyn_smem + (w_ring - dyn_base) + rw.slot * kWBytes + r * 128;
           const uint32_t words[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
@@ -632,11 +642,11 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           fence_async_smem();   // generic-proxy writes -> visible to the tensor core's reads
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(smem_addr(&ctl.qempty[qs]));
-            mbar_arrive(wdone0 + stage * sizeof(uint64_t));
+            mbar_arrive(smem_addr(&ctl.qempty[rq.slot]));
+            mbar_arrive(wdone0 + rw.slot * sizeof(uint64_t));
           }
-          if (++qs == static_cast<uint32_t>(kQStages)) { qs = 0; qphase ^= 1u; }
-          if (++stage == static_cast<uint32_t>(S)) { stage = 0; phase ^= 1u; }
+          rq.next(kQStages);
+          rw.next(SW);
         }
       }
     }
