@@ -177,7 +177,8 @@ def dist_env():
     return world, rank, local
 
 
-def reduce_max(x: float, world: int, device) -> float:
+def reduce_max(x: float, world: int, device="cpu") -> float:
+    """Maximum of x over the ranks (the slowest rank's time)."""
     if world == 1:
         return x
     import torch
@@ -187,6 +188,11 @@ def reduce_max(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def aggregate_tflops(world: int, flops_per_rank: float, slowest_ms: float) -> float:
+    """Whole-job throughput of `world` replicas: every rank's FLOPs over the slowest rank's time."""
+    return world * flops_per_rank / (slowest_ms * 1e-3) / 1e12
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -194,6 +200,19 @@ def barrier(world):
 
 
 # ------------------------------------------------------------------ CPU oracle arm
+
+def host_values_as_tensors(r: wl.Routing, seed: int = 0):
+    """Seeded host-generated operands as CPU torch tensors (for hosts without a GPU)."""
+    import torch
+    v = wl.host_values(r, seed)
+    out = {"a": torch.from_numpy(v["a"].view(np.int16)).view(torch.bfloat16)}
+    if r.int4:
+        out["packed"] = torch.from_numpy(v["packed"].view(np.int32))
+        out["scales"] = torch.from_numpy(v["scales"].view(np.int16)).view(torch.bfloat16)
+    else:
+        out["b"] = torch.from_numpy(v["b"].view(np.int16)).view(torch.bfloat16)
+    return out
+
 
 def oracle_sample(r: wl.Routing, vals_dev, n_groups: int):
     """The first n_groups active groups, all of their rows, all N columns, as host arrays."""
@@ -273,11 +292,6 @@ def main():
 
     world, rank, local = dist_env()
     import torch
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
-    torch.cuda.set_device(local)
-    dev = torch.device(f"cuda:{local}")
 
     r = wl.routing(args.workload)
     if args.groups:
@@ -293,10 +307,13 @@ def main():
               "l2": "flushed between steps (512 MiB write)", "weights": "int4" if r.int4 else "bf16"}
 
     if args.impl == "reference":
+        # The CPU oracle, timed on this host's cores; under torchrun only rank 0 works.
         if rank != 0:
-            barrier(world)
             return
-        vals = wl.device_values(r, 0, device=dev)
+        if torch.cuda.is_available():
+            vals = wl.device_values(r, 0, device=torch.device(f"cuda:{local}"))
+        else:
+            vals = host_values_as_tensors(r, 0)
         nthreads = len(os.sched_getaffinity(0))
         per_step = max(0.2, min(args.oracle_seconds, 150.0 / (args.steps + 1)))   # whole run: minutes
         s, _ = pick_oracle_sample(r, vals, nthreads, per_step)
@@ -315,8 +332,13 @@ def main():
                              "sample": sample_desc(r, s)},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }), flush=True)
-        barrier(world)
         return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
 
     from ragged_matmul_gb300 import binding
     from ragged_matmul_gb300 import build as gbuild
@@ -372,7 +394,7 @@ def main():
     if status != binding.GMM_OK:
         raise RuntimeError(f"device status after timing: {binding.gmm_error_string(status)}")
     max_ms = reduce_max(mean_ms, world, dev)
-    value = world * flops / (max_ms * 1e-3) / 1e12
+    value = aggregate_tflops(world, flops, max_ms)
 
     # end to end through the public API with host buffers: H2D of the step's inputs
     # (activations, offsets, ids) from pinned memory, the kernel, D2H of C and stats.
@@ -409,7 +431,7 @@ def main():
             e1.synchronize()
             e_ms.append(e0.elapsed_time(e1))
         e2e_max = reduce_max(statistics.mean(e_ms), world, dev)
-        e2e = {"value": world * flops / (e2e_max * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": aggregate_tflops(world, flops, e2e_max), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_max}
 
     cpu_baseline = None
