@@ -5,9 +5,12 @@
 
 One step = one gmm_run (gmm_run_int4 for the int4 workload) over the whole
 workload: every group, every row, all N columns.  Inputs are seeded synthetic
-tensors already resident in HBM; between steps L2 is flushed by writing a
-512 MiB buffer (outside the timed events).  Each step is timed with CUDA events
-on the launching stream; `value` is useful FLOPs / mean step time.
+tensors already resident in HBM.  Between steps, outside the timed events, L2
+is flushed: a 512 MiB buffer is written, then a different 512 MiB buffer is
+read, so each step starts with a cold L2 that holds no dirty lines (without the
+read, the timed kernel would also pay for writing the flush's dirty lines back
+to HBM).  Each step is timed with CUDA events on the launching stream; `value`
+is useful FLOPs / mean step time.
 
 The default workload is decode (256 tokens top-8 over 64 experts: 2048 rows,
 K=2048, N=2816).  Under torchrun each rank runs its own replica of the workload
@@ -304,7 +307,8 @@ def main():
     config = {"workload": r.name, "E": r.E, "N": r.N, "K": r.K, "groups": r.G,
               "active_groups": int(r.active_mask().sum()), "rows": rows,
               "useful_flops": flops, "algorithmic_bytes": nbytes,
-              "l2": "flushed between steps (512 MiB write)", "weights": "int4" if r.int4 else "bf16"}
+              "l2": "flushed between steps (512 MiB written, then another 512 MiB read: cold, clean L2)",
+              "weights": "int4" if r.int4 else "bf16"}
 
     if args.impl == "reference":
         # The CPU oracle, timed on this host's cores; under torchrun only rank 0 works.
@@ -354,7 +358,12 @@ def main():
     off = torch.from_numpy(r.a_offsets.view(np.int32)).to(dev)
     ids = torch.from_numpy(r.expert_ids).to(dev)
     stats = torch.zeros(4, dtype=torch.int32, device=dev)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        flush_r.sum()
     stream = torch.cuda.current_stream(dev)
 
     def step(cc=c, aa=vals["a"], oo=off, ii=ids, ss=stats):
@@ -365,7 +374,7 @@ def main():
             binding.gmm_run(h, cc, aa, oo, vals["b"], ii, ss, stream=stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     torch.cuda.synchronize()
     status = binding.gmm_query_status(h)
@@ -380,7 +389,7 @@ def main():
     torch.cuda.synchronize()
     w0 = time.time()
     for i in range(args.steps):
-        flush.zero_()
+        flush_l2()
         evs[i][0].record(stream)
         step()
         evs[i][1].record(stream)
@@ -417,13 +426,13 @@ def main():
             st_h.copy_(stats, non_blocking=True)
 
         for _ in range(args.warmup):
-            flush.zero_()
+            flush_l2()
             e2e_step()
         torch.cuda.synchronize()
         e_ms = []
         barrier(world)
         for _ in range(args.steps):
-            flush.zero_()
+            flush_l2()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             e2e_step()
