@@ -19,7 +19,11 @@ namespace {
 
 using gmm::GmmParams;
 
+// Workspace layout: a 256-byte block with the status word at byte 0 and the two
+// tile-scheduling counters at byte 64 (zero between launches), then one tensor-map
+// slot per CTA.
 constexpr size_t kStatusBytes = 256;
+constexpr size_t kTileCounterOffset = 64;
 
 struct DeviceGuard {
   int prev = -1;
@@ -103,6 +107,7 @@ void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, c
   p.expert_ids = ids;
   p.stats = stats;
   p.status = reinterpret_cast<uint32_t *>(h->ws);
+  p.tile_counter = reinterpret_cast<uint32_t *>(h->ws + kTileCounterOffset);
   p.map_slots = h->ws + kStatusBytes;
   p.num_groups = G;
   p.num_experts = h->num_experts;
@@ -115,8 +120,6 @@ void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, c
     const int v = atoi(env);
     if (v > 0) p.tok_band = v;
   }
-  p.two_ended = 0;
-  if (const char *env = getenv("GMM_TWO_ENDED")) p.two_ended = atoi(env) != 0;   // tuning override
   p.cache_hints = 1;
   if (const char *env = getenv("GMM_CACHE_HINTS")) p.cache_hints = atoi(env) != 0;   // tuning override
 }

@@ -13,9 +13,14 @@
 //
 // Work decomposition.  A tile is (group g, n-block of weight rows, token block of
 // the group).  Every CTA scans a_offsets / expert_ids into a shared-memory prefix
-// sum of tiles per group and walks its share of tiles; within a group the token
-// blocks are the fastest index (in L2-sized bands), so CTAs running at the same
-// time share one weight panel in L2.
+// sum of tiles per group; within a group the token blocks are the fastest index
+// (in L2-sized bands), so CTAs running at the same time share one weight panel in
+// L2.  The producer thread (of the pair leader) decides the tile sequence and
+// publishes it in a small shared-memory queue that every other role reads in order.
+// With many tiles per CTA (at least kDynamicTilesPerUnit) it claims tiles from a
+// global counter, one tile ahead of its loads, so CTAs that draw cheaper tiles
+// simply take more; with few tiles per CTA the claim costs more than the balance
+// gains, and it takes the static round-robin share t = unit, unit + units, ...
 //
 // Variants (template parameters):
 //   kPair = false  one CTA per tile, 128 weight rows, tcgen05 cta_group::1 (M = 128).
@@ -72,6 +77,9 @@ constexpr int kQRingBytes = kQStages * kQBytes;
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr int kMapSlotBytes = 256;            // per-CTA workspace: two patched 128-byte tensor maps
+constexpr int kTileQueue = 4;                 // entries of the shared-memory tile queue
+constexpr uint32_t kDynamicTilesPerUnit = 16; // dynamic tile claiming from this many tiles per CTA (pair)
+constexpr uint32_t kNoTile = 0xffffffffu;     // queue entry meaning "no more tiles"
 
 constexpr uint32_t kStatusBadOffsets = 1u;
 constexpr uint32_t kStatusBadExpert = 2u;
@@ -113,7 +121,7 @@ struct alignas(128) GmmParams {
   const __nv_bfloat16 *scales;   // 4-bit path: [E, N, K / group_size]
   int group_size;                // 4-bit path: multiple of 64 dividing K
   int tok_band;                  // token blocks per band of the tile order (see decode_tile)
-  int two_ended;                 // 1: interleave tiles from both ends of the tile order (see tile_of)
+  uint32_t *tile_counter;        // workspace: [0] next unclaimed tile, [1] CTAs finished (both 0 between launches)
   int cache_hints;               // 1: L2 eviction priorities on the TMA loads (see the producer)
 };
 
@@ -135,6 +143,9 @@ struct __align__(8) Ctrl {
   uint64_t qempty[kQStages];     // 4-bit: the dequantisation warps are done with a packed slab
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
+  uint64_t tq_full[kTileQueue];  // tile queue entry published
+  uint64_t tq_empty[kTileQueue]; // every reader has taken the entry (pair: both CTAs', on the leader)
+  uint32_t tq_tile[kTileQueue];
   uint32_t tmem_base;
   int abort;
   uint32_t total_tiles;
@@ -248,15 +259,6 @@ __device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix) 
   __syncthreads();
 }
 
-// Work slot c -> tile index.  With p.two_ended the even slots walk the tile order
-// from the front and the odd slots from the back (a bijection on [0, total)), so
-// CTAs on compute-heavy tiles of large groups run beside CTAs streaming the weights
-// of small groups.  Off by default: on the measured workloads it was slower.
-__device__ __forceinline__ uint32_t tile_of(uint32_t c, uint32_t total, int two_ended) {
-  if (!two_ended) return c;
-  return (c & 1u) ? total - 1u - (c >> 1) : (c >> 1);
-}
-
 // Tile t -> (group, n-block, token block).  Within a group the token blocks are cut
 // into bands of p.tok_band blocks; a band is walked n-block by n-block with its token
 // blocks fastest.  CTAs running at the same time then share one weight panel, and the
@@ -313,6 +315,58 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
   return out;
 }
 
+// Reader of the tile queue (one thread).  Returns 1 with *tile set, 0 when the work
+// is done, -1 when a wait gave up.  `empty0` is the address of the leader CTA's
+// tq_empty[0] (a cluster address in the pair's second CTA, which then arrives
+// remotely; that CTA's entries are published by the leader, so it waits with
+// cluster scope).
+struct TileQueueReader {
+  uint32_t pos = 0;
+  __device__ __forceinline__ int next(Ctrl &ctl, uint32_t empty0, bool remote, volatile int *abort,
+                                      uint32_t *tile) {
+    const uint32_t slot = pos % kTileQueue, parity = (pos / kTileQueue) & 1u;
+    const uint32_t full = smem_addr(&ctl.tq_full[slot]);
+    if (!(remote ? wait_phase_cluster(full, parity, abort) : wait_phase(full, parity, abort))) return -1;
+    *tile = *reinterpret_cast<volatile uint32_t *>(&ctl.tq_tile[slot]);
+    const uint32_t empty = empty0 + slot * static_cast<uint32_t>(sizeof(uint64_t));
+    if (remote) mbar_arrive_cluster(empty); else mbar_arrive(empty);
+    ++pos;
+    return *tile == kNoTile ? 0 : 1;
+  }
+};
+
+// Where a role gets its tiles: with few tiles per CTA the static round-robin share
+// (unit, unit + units, ...), computed by every role itself; with many, the queue.
+struct TileSource {
+  bool dynamic;
+  uint32_t next_static, units, total;
+  TileQueueReader q;
+  __device__ __forceinline__ TileSource(bool dyn, uint32_t unit0, uint32_t units_, uint32_t total_)
+      : dynamic(dyn), next_static(unit0), units(units_), total(total_) {}
+  __device__ __forceinline__ int next(Ctrl &ctl, uint32_t empty0, bool remote, volatile int *abort,
+                                      uint32_t *tile) {
+    if (!dynamic) {
+      if (next_static >= total) return 0;
+      *tile = next_static;
+      next_static += units;
+      return 1;
+    }
+    return q.next(ctl, empty0, remote, abort, tile);
+  }
+};
+
+// The same for a whole warp: lane 0 reads, the warp agrees.
+__device__ __forceinline__ int next_tile_warp(TileSource &src, Ctrl &ctl, uint32_t empty0, bool remote,
+                                              volatile int *abort, uint32_t *tile) {
+  if (!src.dynamic) return src.next(ctl, empty0, remote, abort, tile);
+  int r = 0;
+  uint32_t t = kNoTile;
+  if ((threadIdx.x & 31) == 0) r = src.next(ctl, empty0, remote, abort, &t);
+  r = __shfl_sync(0xffffffffu, r, 0);
+  *tile = __shfl_sync(0xffffffffu, t, 0);
+  return r;
+}
+
 template <bool kInt4, bool kPair>
 __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     gmm_grouped_kernel(const __grid_constant__ GmmParams p) {
@@ -330,8 +384,12 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   const uint32_t SW = ST;
   const int KB = (p.K + kBK - 1) / kBK;
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
-  const uint32_t unit0 = kPair ? cluster_id_x() : blockIdx.x;      // first work slot of this CTA / pair
-  const uint32_t unit_step = kPair ? cluster_count_x() : gridDim.x;
+  // Readers of each tile-queue entry: per CTA the MMA thread (leader only), the four
+  // epilogue warps and (4-bit) the packed-slab producer and eight dequantisation
+  // warps; in the pair's second CTA also its token producer and (4-bit) forwarder.
+  constexpr uint32_t kLeaderReaders = 1 + 4 + (kInt4 ? 1 + kDequantThreads / 32 : 0);
+  constexpr uint32_t kPeerReaders = 1 + 4 + (kInt4 ? 1 + kDequantThreads / 32 + 1 : 0);
+  constexpr uint32_t kQueueArrivals = kLeaderReaders + (kPair ? kPeerReaders : 0);
 
   // 1024-byte aligned rings, at identical offsets in both CTAs of a pair:
   // SW weight slabs, ST token slabs, then (4-bit) kQStages packed slabs.
@@ -357,6 +415,10 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_addr(&ctl.acc_full[a]), 1);
       mbar_init(smem_addr(&ctl.acc_empty[a]), kEpiArrivals);
+    }
+    for (int q = 0; q < kTileQueue; ++q) {
+      mbar_init(smem_addr(&ctl.tq_full[q]), 1);
+      mbar_init(smem_addr(&ctl.tq_empty[q]), kQueueArrivals);
     }
     ctl.abort = 0;
     ctl.active = 0;
@@ -386,6 +448,13 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   const uint32_t tmem_base = ctl.tmem_base;
   const uint32_t total = ctl.total_tiles;
   volatile int *abort = &ctl.abort;
+  // Tile-queue plumbing: readers arrive on the leader's tq_empty (remotely from the
+  // pair's second CTA, which also waits on its entries with cluster scope).
+  const uint32_t unit0 = kPair ? cluster_id_x() : blockIdx.x;   // this CTA's (pair's) static share
+  const uint32_t units = kPair ? cluster_count_x() : gridDim.x;
+  const bool dynamic = total >= kDynamicTilesPerUnit * units;   // every CTA agrees: same total and grid
+  const bool q_remote = kPair && rank != 0;
+  const uint32_t q_empty0 = q_remote ? map_to_rank(smem_addr(&ctl.tq_empty[0]), 0) : smem_addr(&ctl.tq_empty[0]);
 
   if (warp == 0) {
     // ------------------------------------------------------------ token (and bf16 weight) producer
@@ -415,8 +484,49 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       uint32_t pending = 0;     // bit s: stage s has copies whose completion this thread has not seen
       uint32_t pend_phase = 0;  // bit s: the phase in which they complete
       bool ok = true;
-      for (uint32_t c = unit0; c < total && ok; c += unit_step) {
-        const Tile ti = decode_tile<G>(tile_of(c, total, p.two_ended), prefix, p);
+      // The leader's producer decides the tile sequence and publishes it one tile
+      // ahead of its own loads, so the other roles (the packed-slab producer, the
+      // pair's second CTA) can cross tile boundaries without waiting; dynamic claims
+      // run two tiles ahead so the atomic's latency stays hidden.  Elsewhere the
+      // producer reads the queue like every other role.
+      TileSource reader(dynamic, unit0, units, total);
+      uint32_t qpos = 0;
+      auto claim = [&]() -> uint32_t { return atomicAdd(p.tile_counter, 1u); };
+      auto publish = [&](uint32_t t) -> bool {
+        const uint32_t slot = qpos % kTileQueue, parity = (qpos / kTileQueue) & 1u;
+        const uint32_t empty = smem_addr(&ctl.tq_empty[slot]);
+        if (!(kPair ? wait_phase_cluster(empty, parity ^ 1u, abort) : wait_phase(empty, parity ^ 1u, abort)))
+          return false;
+        ctl.tq_tile[slot] = t;
+        if constexpr (kPair) {   // the second CTA's copy of the entry, then its signal
+          st_shared_cluster_u32(map_to_rank(smem_addr(&ctl.tq_tile[slot]), 1), t);
+          mbar_arrive_cluster(map_to_rank(smem_addr(&ctl.tq_full[slot]), 1));
+        }
+        mbar_arrive(smem_addr(&ctl.tq_full[slot]));
+        ++qpos;
+        return true;
+      };
+      auto valid = [&](uint32_t t) -> uint32_t { return t < total ? t : kNoTile; };
+      const bool publisher = dynamic && rank == 0;
+      uint32_t cur = kNoTile, nxt = kNoTile;   // tile being loaded; tile already published after it
+      if (publisher) {
+        cur = valid(claim());
+        nxt = cur == kNoTile ? kNoTile : valid(claim());
+        ok = publish(cur) && (cur == kNoTile || publish(nxt));
+      }
+      for (; ok;) {
+        uint32_t tile;
+        uint32_t after = kNoTile;   // claimed now, published when `nxt` starts
+        if (publisher) {
+          tile = cur;
+          if (tile == kNoTile) break;
+          if (nxt != kNoTile) after = claim();
+        } else {
+          const int got = reader.next(ctl, q_empty0, q_remote, abort, &tile);
+          if (got < 0) ok = false;
+          if (got <= 0) break;
+        }
+        const Tile ti = decode_tile<G>(tile, prefix, p);
         const uint32_t my_tok = kPair ? ti.ntok / 2 : ti.ntok;     // token rows this CTA loads
         const uint32_t tx = (kPair ? 2u : 1u) * ((kInt4 ? 0u : static_cast<uint32_t>(kWBytes)) + my_tok * (kBK * 2));
         const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
@@ -451,6 +561,14 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           pend_phase = (pend_phase & ~(1u << rt.slot)) | (rt.phase << rt.slot);
           rt.next(ST);
         }
+        if (!ok) break;
+        if (publisher) {
+          cur = nxt;
+          if (cur != kNoTile) {
+            nxt = valid(after);
+            if (!publish(nxt)) { ok = false; break; }
+          }
+        }
       }
       if (!ok) {
         // Let the copies already issued land before the CTA can exit.  In a pair only the
@@ -468,11 +586,16 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       Ring rt;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
-      for (uint32_t c = unit0; c < total && ok; c += unit_step) {
-        const Tile ti = decode_tile<G>(tile_of(c, total, p.two_ended), prefix, p);
-        const bool got = kPair ? wait_phase_cluster(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort)
-                               : wait_phase(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort);
-        if (!got) { ok = false; break; }
+      TileSource reader(dynamic, unit0, units, total);
+      for (;;) {
+        uint32_t tile;
+        const int got = reader.next(ctl, q_empty0, q_remote, abort, &tile);
+        if (got < 0) ok = false;
+        if (got <= 0) break;
+        const Tile ti = decode_tile<G>(tile, prefix, p);
+        const bool acc_free = kPair ? wait_phase_cluster(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort)
+                                    : wait_phase(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort);
+        if (!acc_free) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
         const uint32_t idesc = idesc_bf16_f32(G::kRows, ti.ntok);
@@ -511,12 +634,19 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const uint32_t wfull_leader0 = map_to_rank(smem_addr(&ctl.wfull[0]), 0);
       Ring rw;
       bool ok = true;
-      for (uint32_t c = unit0; c < total && ok; c += unit_step)
+      TileSource reader(dynamic, unit0, units, total);
+      for (;;) {
+        uint32_t tile;
+        const int got = reader.next(ctl, q_empty0, q_remote, abort, &tile);
+        if (got < 0) ok = false;
+        if (got <= 0) break;
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_phase(smem_addr(&ctl.wlocal[rw.slot]), rw.phase, abort)) { ok = false; break; }
           mbar_arrive_cluster(wfull_leader0 + rw.slot * sizeof(uint64_t));
           rw.next(SW);
         }
+        if (!ok) break;
+      }
       if (!ok) atomicOr(p.status, kStatusTimeout);
     }
   } else if (warp < 6) {
@@ -525,8 +655,14 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     const uint32_t acc_empty0 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[0]), 0) : smem_addr(&ctl.acc_empty[0]);
     const uint32_t acc_empty1 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[1]), 0) : smem_addr(&ctl.acc_empty[1]);
     uint32_t acc = 0, acc_phase = 0;
-    for (uint32_t c = unit0; c < total; c += unit_step) {
-      const Tile ti = decode_tile<G>(tile_of(c, total, p.two_ended), prefix, p);
+    TileSource reader(dynamic, unit0, units, total);
+    for (;;) {
+      if (total == 0) break;
+      uint32_t tile;
+      const int got = next_tile_warp(reader, ctl, q_empty0, q_remote, abort, &tile);
+      if (got < 0 && lane == 0) atomicOr(p.status, kStatusTimeout);
+      if (got <= 0) break;
+      const Tile ti = decode_tile<G>(tile, prefix, p);
       int ok = 1;
       if (lane == 0) ok = wait_phase(smem_addr(&ctl.acc_full[acc]), acc_phase, abort);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -568,8 +704,13 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       Ring rq;
       uint32_t pending = 0, pend_phase = 0;
       bool ok = true;
-      for (uint32_t c = unit0; c < total && ok; c += unit_step) {
-        const Tile ti = decode_tile<G>(tile_of(c, total, p.two_ended), prefix, p);
+      TileSource reader(dynamic, unit0, units, total);
+      for (;;) {
+        uint32_t tile;
+        const int got = reader.next(ctl, q_empty0, q_remote, abort, &tile);
+        if (got < 0) ok = false;
+        if (got <= 0) break;
+        const Tile ti = decode_tile<G>(tile, prefix, p);
         const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
         const uint64_t pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
         for (int kb = 0; kb < KB; ++kb) {
@@ -581,6 +722,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           pend_phase = (pend_phase & ~(1u << rq.slot)) | (rq.phase << rq.slot);
           rq.next(kQStages);
         }
+        if (!ok) break;
       }
       if (!ok) {
         for (int s = 0; s < kQStages; ++s)
@@ -604,8 +746,14 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     const uint32_t wdone0 = smem_addr(kPair && rank != 0 ? &ctl.wlocal[0] : &ctl.wfull[0]);
     Ring rw, rq;
     bool ok = true;
-    for (uint32_t c = unit0; c < total && ok; c += unit_step) {
-      const Tile ti = decode_tile<G>(tile_of(c, total, p.two_ended), prefix, p);
+    TileSource reader(dynamic, unit0, units, total);
+    for (;;) {
+      if (total == 0) break;
+      uint32_t tile;
+      const int got = next_tile_warp(reader, ctl, q_empty0, q_remote, abort, &tile);
+      if (got < 0) ok = false;
+      if (got <= 0) break;
+      const Tile ti = decode_tile<G>(tile, prefix, p);
       const uint32_t n = ti.n0 + rank * kBlockN + r;
       const bool row_ok = n < static_cast<uint32_t>(p.N);
       const unsigned short *srow = sbits + (static_cast<size_t>(ti.e) * p.N + (row_ok ? n : 0)) * spr;
@@ -649,12 +797,22 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           rw.next(SW);
         }
       }
+      if (!ok) break;
     }
     if (!ok) atomicOr(p.status, kStatusTimeout);
   }
 
   __syncthreads();
   if constexpr (kPair) cluster_sync();   // no CTA leaves while its peer may still signal it
+  if (tid == 0) {
+    // The last CTA to finish returns the tile counter to zero for the next launch
+    // (launches through one workspace are stream-ordered, never concurrent).
+    __threadfence();
+    if (atomicAdd(p.tile_counter + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.tile_counter, 0u);
+      atomicExch(p.tile_counter + 1, 0u);
+    }
+  }
   if (warp == 1) {
     tc_fence_after_sync();
     if constexpr (kPair) tmem_dealloc_pair(tmem_base, kTmemCols);
