@@ -287,6 +287,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--groups", type=int, default=0,
                     help="profile-sized sub-workload: only the first G groups of the named routing")
+    ap.add_argument("--group-range", default=None,
+                    help="sub-workload lo:hi - groups lo .. hi-1 of the named routing")
     ap.add_argument("--variant", default=None, choices=["pair", "single"],
                     help="kernel variant (default: the library's choice, CTA pairs)")
     args = ap.parse_args()
@@ -299,6 +301,9 @@ def main():
     r = wl.routing(args.workload)
     if args.groups:
         r = wl.first_groups(r, args.groups)
+    if args.group_range:
+        lo, hi = (int(x) for x in args.group_range.split(":"))
+        r = wl.group_range(r, lo, hi)
     flops, nbytes, rows = work_counts(r)
     peaks, peaks_kind = load_peaks()
     t_tensor = flops / (peaks["bf16_tflops"] * 1e12)

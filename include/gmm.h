@@ -30,8 +30,9 @@
  * validate the arguments on the host, launch one persistent kernel and return;
  * they do not synchronise and allocate nothing.
  *
- * A handle owns a small device workspace (a status word, two tile-scheduling
- * counters that each launch returns to zero, and per-CTA tensor-map slots) that
+ * A handle owns a small device workspace (a status word, a 64-bit tile-claim
+ * word and a finished-CTA counter that each launch returns to zero, and per-CTA
+ * tensor-map slots) that
  * every launch made through it rewrites.  Launches made through the
  * same handle must therefore not overlap on the GPU: issue them on one stream, or
  * use one handle per stream.
@@ -116,8 +117,8 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
  *
  * Every call shares the one array and finds the previous call's contents in it; the
  * call clears the status word itself (stream-ordered on `stream`), rewrites the
- * tensor-map slots, and its kernel returns the array's two tile-scheduling counters
- * to zero when it finishes (they are zero when the library is loaded).  Calls whose kernels overlap on the GPU (different streams, or
+ * tensor-map slots, and its kernel returns the array's tile-claim word and
+ * finished-CTA counter to zero when it finishes (they are zero when the library is loaded).  Calls whose kernels overlap on the GPU (different streams, or
  * concurrent threads) race on the array: order them on one stream.  The device
  * status (bad offsets / ids) is not reported by this call; the device still applies
  * the same rules (see the header comment).

@@ -19,9 +19,9 @@ namespace {
 
 using gmm::GmmParams;
 
-// Workspace layout: a 256-byte block with the status word at byte 0 and the two
-// tile-scheduling counters at byte 64 (zero between launches), then one tensor-map
-// slot per CTA.
+// Workspace layout: a 256-byte block with the status word at byte 0, the 64-bit
+// tile-claim word (front count | back count << 32) at byte 64 and the finished-CTA
+// counter at byte 72 (all zero between launches), then one tensor-map slot per CTA.
 constexpr size_t kStatusBytes = 256;
 constexpr size_t kTileCounterOffset = 64;
 
@@ -135,10 +135,10 @@ int configure(gmm_variant *v, int optin, int num_sms) {
   if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(kernel)) != cudaSuccess) return GMM_ERR_CUDA;
   long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024;
   if (kInt4) budget -= gmm::kQRingBytes;   // the packed-slab ring
-  v->stages = static_cast<int>(budget / static_cast<long>(gmm::kWBytes + G::kTSlot));
+  v->stages = static_cast<int>(budget / static_cast<long>(G::kStageBytes));
   if (v->stages > gmm::kMaxStages) v->stages = gmm::kMaxStages;
   if (v->stages < 2) return GMM_ERR_UNSUPPORTED;
-  v->smem = static_cast<size_t>(v->stages) * (gmm::kWBytes + G::kTSlot) +
+  v->smem = static_cast<size_t>(v->stages) * G::kStageBytes +
             (kInt4 ? gmm::kQRingBytes : 0) + 1024;
   if (cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(v->smem)) != cudaSuccess)

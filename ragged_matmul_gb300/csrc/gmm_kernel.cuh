@@ -17,7 +17,7 @@
 // (in L2-sized bands), so CTAs running at the same time share one weight panel in
 // L2.  The producer thread (of the pair leader) decides the tile sequence and
 // publishes it in a small shared-memory queue that every other role reads in order.
-// With many tiles per CTA (at least kDynamicTilesPerUnit) it claims tiles from a
+// With many tiles per CTA (at least kDynamicTilesPerUnit, or ...4) it claims tiles from a
 // global counter, one tile ahead of its loads, so CTAs that draw cheaper tiles
 // simply take more; with few tiles per CTA the claim costs more than the balance
 // gains, and it takes the static round-robin share t = unit, unit + units, ...
@@ -78,7 +78,9 @@ constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr int kMapSlotBytes = 256;            // per-CTA workspace: two patched 128-byte tensor maps
 constexpr int kTileQueue = 4;                 // entries of the shared-memory tile queue
-constexpr uint32_t kDynamicTilesPerUnit = 16; // dynamic tile claiming from this many tiles per CTA (pair)
+constexpr uint32_t kDynamicTilesPerUnit = 16; // bf16: dynamic tile claiming from this many tiles per CTA (pair)
+constexpr uint32_t kDynamicTilesPerUnit4 = 8; // 4-bit: the same (its tiles are longer, measured better lower)
+constexpr uint32_t kUnevenRatio = 4;          // groups this uneven get the two-ended claim order
 constexpr uint32_t kNoTile = 0xffffffffu;     // queue entry meaning "no more tiles"
 
 constexpr uint32_t kStatusBadOffsets = 1u;
@@ -100,6 +102,11 @@ struct Geom {
   static constexpr uint32_t kMaxTok = kInt4 ? 160 : 256;
   static constexpr uint32_t kTSlot = (kPair ? kMaxTok / 2 : kMaxTok) * kBK * 2;   // token slab per CTA
   static_assert(kTSlot % 1024 == 0, "token slabs must keep the 1024-byte swizzle alignment");
+  // 64-wide K sub-slabs per pipeline stage.  The bf16 pair kernel takes 128 of K per
+  // stage (8 MMAs per barrier wait and commit): the MMA thread's fixed cost per stage
+  // (wait, fence, commit, loop) is then spread over twice the tensor work.
+  static constexpr uint32_t kSub = (kPair && !kInt4) ? 2 : 1;
+  static constexpr uint32_t kStageBytes = kSub * (kWBytes + kTSlot);
 };
 
 struct alignas(128) GmmParams {
@@ -121,7 +128,8 @@ struct alignas(128) GmmParams {
   const __nv_bfloat16 *scales;   // 4-bit path: [E, N, K / group_size]
   int group_size;                // 4-bit path: multiple of 64 dividing K
   int tok_band;                  // token blocks per band of the tile order (see decode_tile)
-  uint32_t *tile_counter;        // workspace: [0] next unclaimed tile, [1] CTAs finished (both 0 between launches)
+  uint32_t *tile_counter;        // workspace, 8-byte aligned, zero between launches: [0..1] one 64-bit claim
+                                 // word (tiles claimed from the front | from the back << 32), [2] CTAs finished
   int cache_hints;               // 1: L2 eviction priorities on the TMA loads (see the producer)
 };
 
@@ -149,6 +157,8 @@ struct __align__(8) Ctrl {
   uint32_t tmem_base;
   int abort;
   uint32_t total_tiles;
+  uint32_t max_group_tiles;      // largest and smallest non-zero tile count of a group
+  uint32_t min_group_tiles;
   uint32_t active;
   uint32_t flags;
   unsigned long long warp_tiles[kInt4Threads / 32];
@@ -215,7 +225,7 @@ __device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix) 
   const int g_begin = min(Gn, tid * chunk), g_end = min(Gn, g_begin + chunk);
 
   unsigned long long mine = 0;
-  uint32_t active = 0, flags = 0;
+  uint32_t active = 0, flags = 0, gmax = 0, gmin = 0xffffffffu;
   for (int g = g_begin; g < g_end; ++g) {
     const uint32_t r0 = __ldg(p.a_offsets + g), r1 = __ldg(p.a_offsets + g + 1);
     const int32_t e = __ldg(p.expert_ids + g);
@@ -223,12 +233,21 @@ __device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix) 
     if (e >= p.num_experts) flags |= kStatusBadExpert;
     if (e >= 0 && e < p.num_experts) {
       ++active;
-      if (r1 > r0) mine += static_cast<unsigned long long>((r1 - r0 + G::kMaxTok - 1) / G::kMaxTok) * n_blocks;
+      if (r1 > r0) {
+        const uint32_t tb = (r1 - r0 + G::kMaxTok - 1) / G::kMaxTok;
+        mine += static_cast<unsigned long long>(tb) * n_blocks;
+        gmax = max(gmax, tb);
+        gmin = min(gmin, tb);
+      }
     }
     prefix[g + 1] = static_cast<uint32_t>(mine);   // running sum within the chunk, fixed up below
   }
   if (flags) atomicOr(&ctl.flags, flags);
   if (active) atomicAdd(&ctl.active, active);
+  if (gmax) {
+    atomicMax(&ctl.max_group_tiles, gmax);
+    atomicMin(&ctl.min_group_tiles, gmin);
+  }
 
   unsigned long long incl = mine;
 #pragma unroll
@@ -382,7 +401,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t ST = static_cast<uint32_t>(p.num_stages);   // W+T stage ring
   const uint32_t SW = ST;
-  const int KB = (p.K + kBK - 1) / kBK;
+  const int KB = (p.K + static_cast<int>(G::kSub * kBK) - 1) / static_cast<int>(G::kSub * kBK);   // stages per tile
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   // Readers of each tile-queue entry: per CTA the MMA thread (leader only), the four
   // epilogue warps and (4-bit) the packed-slab producer and eight dequantisation
@@ -396,8 +415,8 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   const uint32_t dyn_base = smem_addr(dyn_smem);
   const uint32_t ring = (dyn_base + 1023u) & ~1023u;
   const uint32_t w_ring = ring;
-  const uint32_t t_ring = ring + SW * kWBytes;
-  const uint32_t q_ring = t_ring + ST * G::kTSlot;
+  const uint32_t t_ring = ring + SW * G::kSub * kWBytes;
+  const uint32_t q_ring = t_ring + ST * G::kSub * G::kTSlot;
 
   if (tid == 0) {
     for (uint32_t s = 0; s < ST; ++s) {
@@ -423,6 +442,8 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     ctl.abort = 0;
     ctl.active = 0;
     ctl.flags = 0;
+    ctl.max_group_tiles = 0;
+    ctl.min_group_tiles = 0xffffffffu;
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -452,7 +473,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   // pair's second CTA, which also waits on its entries with cluster scope).
   const uint32_t unit0 = kPair ? cluster_id_x() : blockIdx.x;   // this CTA's (pair's) static share
   const uint32_t units = kPair ? cluster_count_x() : gridDim.x;
-  const bool dynamic = total >= kDynamicTilesPerUnit * units;   // every CTA agrees: same total and grid
+  const bool dynamic = total >= (kInt4 ? kDynamicTilesPerUnit4 : kDynamicTilesPerUnit) * units;   // all CTAs agree
   const bool q_remote = kPair && rank != 0;
   const uint32_t q_empty0 = q_remote ? map_to_rank(smem_addr(&ctl.tq_empty[0]), 0) : smem_addr(&ctl.tq_empty[0]);
 
@@ -491,7 +512,22 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       // producer reads the queue like every other role.
       TileSource reader(dynamic, unit0, units, total);
       uint32_t qpos = 0;
-      auto claim = [&]() -> uint32_t { return atomicAdd(p.tile_counter, 1u); };
+      // When group sizes are very uneven (the largest group has kUnevenRatio times the
+      // token blocks of the smallest), half of the CTAs (pairs) claim from the back of
+      // the tile order: they stream the weights of the small groups while the others
+      // run the compute-heavy tiles of the large groups from the front, so the tensor
+      // and HBM bounds overlap.  Both ends share one 64-bit claim word and meet
+      // exactly; where they meet adapts to how fast each side goes.  With even groups
+      // every claim comes from the front, which keeps more reuse in L2.
+      const bool two_ended = ctl.max_group_tiles >= kUnevenRatio * ctl.min_group_tiles;
+      const bool from_back = two_ended && (unit0 & 1u);
+      auto claim = [&]() -> uint32_t {
+        const unsigned long long old =
+            atomicAdd(reinterpret_cast<unsigned long long *>(p.tile_counter), from_back ? (1ull << 32) : 1ull);
+        const uint32_t front = static_cast<uint32_t>(old), back = static_cast<uint32_t>(old >> 32);
+        if (static_cast<unsigned long long>(front) + back >= total) return kNoTile;
+        return from_back ? total - 1u - back : front;
+      };
       auto publish = [&](uint32_t t) -> bool {
         const uint32_t slot = qpos % kTileQueue, parity = (qpos / kTileQueue) & 1u;
         const uint32_t empty = smem_addr(&ctl.tq_empty[slot]);
@@ -506,7 +542,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         ++qpos;
         return true;
       };
-      auto valid = [&](uint32_t t) -> uint32_t { return t < total ? t : kNoTile; };
+      auto valid = [](uint32_t t) -> uint32_t { return t; };   // claim() already returns kNoTile at the end
       const bool publisher = dynamic && rank == 0;
       uint32_t cur = kNoTile, nxt = kNoTile;   // tile being loaded; tile already published after it
       if (publisher) {
@@ -528,7 +564,8 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         }
         const Tile ti = decode_tile<G>(tile, prefix, p);
         const uint32_t my_tok = kPair ? ti.ntok / 2 : ti.ntok;     // token rows this CTA loads
-        const uint32_t tx = (kPair ? 2u : 1u) * ((kInt4 ? 0u : static_cast<uint32_t>(kWBytes)) + my_tok * (kBK * 2));
+        const uint32_t tx =
+            (kPair ? 2u : 1u) * G::kSub * ((kInt4 ? 0u : static_cast<uint32_t>(kWBytes)) + my_tok * (kBK * 2));
         const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
         // L2 priorities: a weight panel that only one token block of its group reads is
         // streamed once (evict first); token slabs are read again by every n-block of the
@@ -538,24 +575,30 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         for (int kb = 0; kb < KB; ++kb) {
           const uint32_t full_local = smem_addr(&ctl.full[rt.slot]);
           if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
-          const int32_t k0 = kb * kBK;
           if (rank == 0) mbar_arrive_expect_tx(full_local, tx);
-          uint32_t dst_t = t_ring + rt.slot * G::kTSlot;
-          int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok);
-          uint32_t left = my_tok;
-          if constexpr (kPair) {
-            const uint32_t full_leader = map_to_rank(full_local, 0);
-            if (!kInt4) tma_load_3d_pair(w_ring + rt.slot * kWBytes, &p.w_map, full_leader, k0, w_row, ti.e, w_pol);
-            for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
-              tma_load_2d_pair(dst_t, tok128, full_leader, k0, r, t_pol);
-            for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
-              tma_load_2d_pair(dst_t, tok16, full_leader, k0, r, t_pol);
-          } else {
-            if (!kInt4) tma_load_3d_hint(w_ring + rt.slot * kWBytes, &p.w_map, full_local, k0, w_row, ti.e, w_pol);
-            for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
-              tma_load_2d_hint(dst_t, tok128, full_local, k0, r, t_pol);
-            for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
-              tma_load_2d_hint(dst_t, tok16, full_local, k0, r, t_pol);
+#pragma unroll
+          for (uint32_t sub = 0; sub < G::kSub; ++sub) {
+            // Sub-slab `sub` of the stage: K from k0, weights at +sub*16 KB, tokens at
+            // +sub*kTSlot.  A sub-slab past K is zero-filled by TMA and adds nothing.
+            const int32_t k0 = (kb * static_cast<int32_t>(G::kSub) + static_cast<int32_t>(sub)) * kBK;
+            const uint32_t dst_w = w_ring + (rt.slot * G::kSub + sub) * kWBytes;
+            uint32_t dst_t = t_ring + (rt.slot * G::kSub + sub) * G::kTSlot;
+            int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok);
+            uint32_t left = my_tok;
+            if constexpr (kPair) {
+              const uint32_t full_leader = map_to_rank(full_local, 0);
+              if (!kInt4) tma_load_3d_pair(dst_w, &p.w_map, full_leader, k0, w_row, ti.e, w_pol);
+              for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
+                tma_load_2d_pair(dst_t, tok128, full_leader, k0, r, t_pol);
+              for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
+                tma_load_2d_pair(dst_t, tok16, full_leader, k0, r, t_pol);
+            } else {
+              if (!kInt4) tma_load_3d_hint(dst_w, &p.w_map, full_local, k0, w_row, ti.e, w_pol);
+              for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
+                tma_load_2d_hint(dst_t, tok128, full_local, k0, r, t_pol);
+              for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
+                tma_load_2d_hint(dst_t, tok16, full_local, k0, r, t_pol);
+            }
           }
           pending |= 1u << rt.slot;
           pend_phase = (pend_phase & ~(1u << rt.slot)) | (rt.phase << rt.slot);
@@ -607,14 +650,18 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
             if (!w_ok) { ok = false; break; }
           }
           tc_fence_after_sync();
-          const uint64_t a_desc = smem_desc_k_sw128(w_ring + rt.slot * kWBytes);
-          const uint64_t b_desc = smem_desc_k_sw128(t_ring + rt.slot * G::kTSlot);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {   // +32 bytes along K per step: +2 in the >>4 address field
-            if constexpr (kPair)
-              mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0);
-            else
-              mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (kb | k) != 0);
+          for (uint32_t sub = 0; sub < G::kSub; ++sub) {
+            const uint64_t a_desc = smem_desc_k_sw128(w_ring + (rt.slot * G::kSub + sub) * kWBytes);
+            const uint64_t b_desc = smem_desc_k_sw128(t_ring + (rt.slot * G::kSub + sub) * G::kTSlot);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {   // +32 bytes along K per step: +2 in the >>4 address field
+              const uint32_t accumulate = (kb | static_cast<int>(sub) | k) != 0;
+              if constexpr (kPair)
+                mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
+              else
+                mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
+            }
           }
           if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.empty[rt.slot]), 0x3);
           else mma_commit(smem_addr(&ctl.empty[rt.slot]));
@@ -808,9 +855,9 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     // The last CTA to finish returns the tile counter to zero for the next launch
     // (launches through one workspace are stream-ordered, never concurrent).
     __threadfence();
-    if (atomicAdd(p.tile_counter + 1, 1u) == gridDim.x - 1) {
-      atomicExch(p.tile_counter, 0u);
-      atomicExch(p.tile_counter + 1, 0u);
+    if (atomicAdd(p.tile_counter + 2, 1u) == gridDim.x - 1) {
+      atomicExch(reinterpret_cast<unsigned long long *>(p.tile_counter), 0ull);
+      atomicExch(p.tile_counter + 2, 0u);
     }
   }
   if (warp == 1) {

@@ -151,6 +151,14 @@ def routing(name: str, seed: int | None = None) -> Routing:
     raise KeyError(name)
 
 
+def group_range(r: Routing, lo: int, hi: int) -> Routing:
+    """The sub-workload made of groups lo .. hi-1 of r (rows renumbered from 0, E kept)."""
+    loads = r.loads[lo:hi].copy()
+    ids = r.expert_ids[lo:hi].copy()
+    return Routing(f"{r.name}[{lo}:{hi}]", r.E, r.N, r.K, loads, ids, offsets_from_loads(loads), r.a_dist,
+                   r.b_dist, r.int4, r.group_size, r.scale_range)
+
+
 def first_groups(r: Routing, G: int) -> Routing:
     """The sub-workload made of the first G groups of r (rows, ids and distributions kept;
     E shrunk to the largest expert id used + 1)."""
