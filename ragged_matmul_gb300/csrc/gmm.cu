@@ -51,9 +51,8 @@ struct gmm_ctx {
   int device = 0;
   int num_experts = 0;
   int num_sms = 0;
-  gmm_variant var[2][2];          // [4-bit][pair]
+  gmm_variant var[2][2];          // [4-bit][pair]; the 4-bit path has only the one-CTA kernel
   int use_pairs = 1;              // bf16 path: 1 = CTA-pair kernels (cta_group::2), 0 = one CTA per tile
-  int use_pairs_int4 = 0;         // 4-bit path: one CTA per tile by default (measured faster)
   uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
   size_t ws_bytes = 0;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -134,7 +133,7 @@ int configure(gmm_variant *v, int optin, int num_sms) {
   cudaFuncAttributes attr;
   if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(kernel)) != cudaSuccess) return GMM_ERR_CUDA;
   long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024;
-  if (kInt4) budget -= gmm::kQRingBytes;   // the packed-slab ring
+  if (kInt4) budget -= gmm::kQRingBytes;   // the packed-slab ring (the weights themselves are in TMEM)
   v->stages = static_cast<int>(budget / static_cast<long>(G::kStageBytes));
   if (v->stages > gmm::kMaxStages) v->stages = gmm::kMaxStages;
   if (v->stages < 2) return GMM_ERR_UNSUPPORTED;
@@ -168,7 +167,7 @@ int configure(gmm_variant *v, int optin, int num_sms) {
 template <bool kInt4>
 int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   DeviceGuard guard(h->device);
-  const int pairs = kInt4 ? h->use_pairs_int4 : h->use_pairs;
+  const int pairs = kInt4 ? 0 : h->use_pairs;
   const gmm_variant &v = h->var[kInt4][pairs];
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
@@ -179,16 +178,18 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   cfg.stream = stream;
   p.num_stages = v.stages;
   cudaError_t err;
-  if (pairs) {
+  if constexpr (kInt4) {
+    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<true, false>, p);
+  } else if (pairs) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, true>, p);
+    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<false, true>, p);
   } else {
-    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, false>, p);
+    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<false, false>, p);
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
@@ -198,7 +199,7 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
 }
 
 uint32_t max_tok(const gmm_ctx *h, bool int4) {
-  if (int4) return h->use_pairs_int4 ? gmm::Geom<true, true>::kMaxTok : gmm::Geom<true, false>::kMaxTok;
+  if (int4) return gmm::Geom<true, false>::kMaxTok;
   return h->use_pairs ? gmm::Geom<false, true>::kMaxTok : gmm::Geom<false, false>::kMaxTok;
 }
 
@@ -255,12 +256,10 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
 
   const int single_ok = configure<false, false>(&h->var[0][0], optin, sms) == GMM_OK &&
                         configure<true, false>(&h->var[1][0], optin, sms) == GMM_OK;
-  // Tuning override GMM_VARIANT: "single" or "pair" forces both paths to that variant.
+  // Tuning override GMM_VARIANT=single: the bf16 path runs its one-CTA kernel.
   const char *variant = getenv("GMM_VARIANT");
-  const bool pairs_ok = sms >= 2 && configure<false, true>(&h->var[0][1], optin, sms) == GMM_OK &&
-                        configure<true, true>(&h->var[1][1], optin, sms) == GMM_OK;
+  const bool pairs_ok = sms >= 2 && configure<false, true>(&h->var[0][1], optin, sms) == GMM_OK;
   h->use_pairs = pairs_ok && !(variant && std::strcmp(variant, "single") == 0);
-  h->use_pairs_int4 = pairs_ok && variant && std::strcmp(variant, "pair") == 0;
   if (!single_ok) {
     cudaGetLastError();
     delete h;

@@ -29,16 +29,19 @@
 //                  of the tokens; the leader (r = 0) issues the MMAs and commits to
 //                  both CTAs' barriers; each CTA stores its own 128 columns of C.
 //   kInt4 = false  bf16 weights, loaded by TMA into the stage together with tokens.
-//   kInt4 = true   packed 4-bit weights: a dedicated TMA warp streams packed slabs
-//                  through their own 8-deep ring, and eight warps dequantise them into
-//                  the bf16 weight slab of each stage; the MMA waits for the stage's
-//                  tokens (full) and its dequantised weights (wfull).
+//   kInt4 = true   packed 4-bit weights (one CTA per tile only): a dedicated TMA warp
+//                  streams packed slabs through their own ring, and eight warps
+//                  dequantise them straight into tensor memory, where the MMA takes
+//                  its A operand from (tcgen05.mma with A in TMEM).  The dequantised
+//                  weights never touch shared memory, so shared memory carries only
+//                  the token slabs and the packed slabs, and no proxy fence sits
+//                  between the dequantisation and the MMA.
 //
 // Roles:
 //   warp 0       TMA producer of token slabs (and of bf16 weight slabs).
-//   warp 1       TMEM allocation (512 columns = two fp32 accumulators) and the
-//                single MMA-issuing thread (tcgen05.mma kind::f16); in a 4-bit
-//                pair's second CTA, the forwarder of its weight-slab readiness.
+//   warp 1       TMEM allocation (512 columns: two fp32 accumulators, and in the
+//                4-bit kernel a ring of dequantised weight slabs between them) and
+//                the single MMA-issuing thread (tcgen05.mma kind::f16).
 //   warps 2..5   epilogue: TMEM -> registers -> bf16 -> C, masking token rows past
 //                the group's end and columns past N; two accumulators let it
 //                overlap the next tile's main loop.
@@ -68,14 +71,24 @@ constexpr int kBK = 64;                       // K per stage: one 128-byte swizz
 constexpr int kMaxStages = 12;                // deepest W+T stage ring
 constexpr int kMaxGroups = 4096;
 constexpr int kThreads = 192;                 // bf16 kernel: producer, MMA, 4 epilogue warps
-constexpr int kDequantThreads = 256;          // 4-bit kernel: 8 dequantisation warps, two threads per weight row
+constexpr int kDequantThreads = 256;          // 4-bit kernel: 8 dequantisation warps, one thread per row and K half
 constexpr int kInt4Threads = kThreads + 32 + kDequantThreads;   // + one packed-slab producer warp
-constexpr int kQStages = 8;                   // 4-bit kernel: depth of the packed-slab ring
 constexpr int kWBytes = kBlockN * kBK * 2;    // 16 KB bf16 weight slab
 constexpr int kQBytes = kBlockN * kBK / 2;    // 4 KB packed 4-bit slab (128 rows x 8 words)
-constexpr int kQRingBytes = kQStages * kQBytes;
+constexpr int kQStages = 6;                   // 4-bit kernel: depth of the packed ring (one 128-K stage per slot)
+constexpr int kQSlotBytes = 2 * kQBytes;
+constexpr int kQRingBytes = kQStages * kQSlotBytes;
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
+// 4-bit kernel: dequantised weight slabs live in TMEM (128 lanes = weight rows, 32
+// columns = 64 bf16 of K per 64-wide slab) in the columns the accumulators leave
+// free: an accumulator holds at most 160 token columns (kMaxTok), so columns
+// 160..255 and 416..511 hold six slabs, three 128-K stages of two slabs each.
+constexpr uint32_t kAStages = 3;
+__device__ __forceinline__ uint32_t a_slab_col(uint32_t stage, uint32_t sub) {
+  const uint32_t i = 2 * stage + sub;   // 0..5
+  return i < 3 ? 160u + 32u * i : 416u + 32u * (i - 3u);
+}
 constexpr int kMapSlotBytes = 256;            // per-CTA workspace: two patched 128-byte tensor maps
 constexpr int kTileQueue = 4;                 // entries of the shared-memory tile queue
 constexpr uint32_t kDynamicTilesPerUnit = 16; // bf16: dynamic tile claiming from this many tiles per CTA (pair)
@@ -89,24 +102,27 @@ constexpr uint32_t kStatusTimeout = 4u;
 constexpr uint32_t kStatusTooLarge = 8u;
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // give up on a pipeline wait after 2 s
+constexpr uint32_t kSuspendNs = 1u << 20;            // longest suspension of one mbarrier test (~1 ms)
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // and on draining copies after 0.2 s
 
 // Geometry of one kernel variant.
 template <bool kInt4, bool kPair>
 struct Geom {
+  static_assert(!(kInt4 && kPair), "the 4-bit kernel runs one CTA per tile");
   static constexpr uint32_t kRows = kPair ? 2 * kBlockN : kBlockN;   // weight rows (C columns) per tile
   static constexpr uint32_t kTokAlign = kPair ? 32 : 16;             // MMA N granule (pair: 2 x 16)
   // Token rows per tile.  The 4-bit path keeps slabs small so its token ring can be
   // deep: its MMA per stage is short (about 128 tokens), and the token copies come
   // from L2 with microsecond latency.
-  static constexpr uint32_t kMaxTok = kInt4 ? 160 : 256;
+  static constexpr uint32_t kMaxTok = kInt4 ? 160 : 256;   // 4-bit: also bounded by the TMEM layout above
   static constexpr uint32_t kTSlot = (kPair ? kMaxTok / 2 : kMaxTok) * kBK * 2;   // token slab per CTA
   static_assert(kTSlot % 1024 == 0, "token slabs must keep the 1024-byte swizzle alignment");
-  // 64-wide K sub-slabs per pipeline stage.  The bf16 pair kernel takes 128 of K per
-  // stage (8 MMAs per barrier wait and commit): the MMA thread's fixed cost per stage
-  // (wait, fence, commit, loop) is then spread over twice the tensor work.
-  static constexpr uint32_t kSub = (kPair && !kInt4) ? 2 : 1;
-  static constexpr uint32_t kStageBytes = kSub * (kWBytes + kTSlot);
+  // 64-wide K sub-slabs per pipeline stage.  The pair and 4-bit kernels take 128 of K
+  // per stage (8 MMAs per barrier wait and commit): the MMA thread's fixed cost per
+  // stage (wait, fence, commit, loop) is then spread over twice the tensor work.
+  static constexpr uint32_t kSub = (kPair || kInt4) ? 2 : 1;
+  // Shared memory of one stage of the W+T ring (the 4-bit kernel's weights are in TMEM).
+  static constexpr uint32_t kStageBytes = kSub * ((kInt4 ? 0 : kWBytes) + kTSlot);
 };
 
 struct alignas(128) GmmParams {
@@ -145,10 +161,10 @@ struct Tile {
 struct __align__(8) Ctrl {
   uint64_t full[kMaxStages];     // stage's TMA bytes landed (pair: both CTAs' bytes, on the leader)
   uint64_t empty[kMaxStages];    // MMAs that read the stage completed
-  uint64_t wfull[kMaxStages];    // 4-bit: stage's weight slab written (pair leader: both CTAs')
-  uint64_t wlocal[kMaxStages];   // 4-bit pair peer: its own slab written (forwarded to the leader)
-  uint64_t qfull[kQStages];      // 4-bit: a packed slab landed (this CTA)
-  uint64_t qempty[kQStages];     // 4-bit: the dequantisation warps are done with a packed slab
+  uint64_t afull[kAStages];      // 4-bit: a TMEM weight stage written by the eight dequantisation warps
+  uint64_t aempty[kAStages];     // 4-bit: the MMAs that read a TMEM weight stage completed
+  uint64_t qfull[kQStages];      // 4-bit: a packed stage landed
+  uint64_t qempty[kQStages];     // 4-bit: the dequantisation warps are done with a packed stage
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t tq_full[kTileQueue];  // tile queue entry published
@@ -176,41 +192,41 @@ struct Ring {
 };
 
 // Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's abort
-// flag) after kWaitLimitNs, or as soon as another role has aborted.
+// flag) after kWaitLimitNs, or as soon as another role has aborted.  Each test may
+// suspend the thread for up to kSuspendNs (it resumes as soon as the phase
+// completes), so a waiting role does not spin on the issue slots that the dequant,
+// epilogue and MMA-issuing warps of its SM need; the abort flag and the clock are
+// checked after every test.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t spin = 1;; ++spin) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((spin & 63u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
     }
+    if (mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
   }
 }
 
 // The same with cluster-scope acquire, for barriers the peer CTA arrives on.
 __device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, volatile int *abort) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
+  if (mbar_try_wait_cluster_hint(bar, parity, kSuspendNs)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t spin = 1;; ++spin) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((spin & 63u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort = 1;
+      return false;
     }
+    if (mbar_try_wait_cluster_hint(bar, parity, kSuspendNs)) return true;
   }
 }
 
 __device__ __forceinline__ bool wait_phase_for(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity))
+  while (!mbar_try_wait_hint(bar, parity, kSuspendNs))
     if (global_timer_ns() - t0 > limit_ns) return false;
   return true;
 }
@@ -312,7 +328,7 @@ __device__ __forceinline__ Tile decode_tile(uint32_t t, const uint32_t *prefix, 
 }
 
 // Dequantise one packed word (8 four-bit values, k = 8j .. 8j+7, low nibble first)
-// into the 16-byte bf16 chunk the MMA expects: w_i = bf16((q_i - 8) * s).
+// into four bf16 pairs in K order (one TMEM column each): w_i = bf16((q_i - 8) * s).
 // 0x4300 | q is the bf16 encoding of 128 + q (q < 16 fits the 7-bit mantissa at
 // exponent 7), so subtracting 136 gives q - 8 exactly; the bf16x2 multiply then
 // rounds the exact product (q - 8) * s once, to nearest even.
@@ -393,39 +409,38 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   constexpr int NT = kInt4 ? kInt4Threads : kThreads;
   constexpr uint32_t kEpiArrivals = (kPair ? 2 : 1) * 4;   // one per epilogue warp of each CTA
   constexpr uint32_t kDequantWarps = kDequantThreads / 32;
-  constexpr uint32_t kWArrivals = kDequantWarps + (kPair ? 1 : 0);   // + the peer's forwarded arrive
   __shared__ Ctrl ctl;
   __shared__ uint32_t prefix[kMaxGroups + 1];
   extern __shared__ uint8_t dyn_smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t ST = static_cast<uint32_t>(p.num_stages);   // W+T stage ring
-  const uint32_t SW = ST;
+  const uint32_t ST = static_cast<uint32_t>(p.num_stages);   // W+T stage ring (4-bit: tokens only)
+  const uint32_t SW = kInt4 ? 0u : ST;                         // weight slabs in shared memory
   const int KB = (p.K + static_cast<int>(G::kSub * kBK) - 1) / static_cast<int>(G::kSub * kBK);   // stages per tile
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   // Readers of each tile-queue entry: per CTA the MMA thread (leader only), the four
   // epilogue warps and (4-bit) the packed-slab producer and eight dequantisation
-  // warps; in the pair's second CTA also its token producer and (4-bit) forwarder.
-  constexpr uint32_t kLeaderReaders = 1 + 4 + (kInt4 ? 1 + kDequantThreads / 32 : 0);
-  constexpr uint32_t kPeerReaders = 1 + 4 + (kInt4 ? 1 + kDequantThreads / 32 + 1 : 0);
+  // warps; in the pair's second CTA also its token producer.
+  constexpr uint32_t kLeaderReaders = 1 + 4 + (kInt4 ? 1 + kDequantWarps : 0);
+  constexpr uint32_t kPeerReaders = 1 + 4;
   constexpr uint32_t kQueueArrivals = kLeaderReaders + (kPair ? kPeerReaders : 0);
 
   // 1024-byte aligned rings, at identical offsets in both CTAs of a pair:
-  // SW weight slabs, ST token slabs, then (4-bit) kQStages packed slabs.
+  // SW weight slabs (bf16), ST token slabs, then (4-bit) kQStages packed slabs.
   const uint32_t dyn_base = smem_addr(dyn_smem);
   const uint32_t ring = (dyn_base + 1023u) & ~1023u;
   const uint32_t w_ring = ring;
   const uint32_t t_ring = ring + SW * G::kSub * kWBytes;
-  const uint32_t q_ring = t_ring + ST * G::kSub * G::kTSlot;
+  const uint32_t q_ring = t_ring + ST * G::kSub * G::kTSlot;   // 4-bit only
 
   if (tid == 0) {
     for (uint32_t s = 0; s < ST; ++s) {
       mbar_init(smem_addr(&ctl.full[s]), 1);
       mbar_init(smem_addr(&ctl.empty[s]), 1);
     }
-    for (uint32_t s = 0; s < SW && kInt4; ++s) {
-      mbar_init(smem_addr(&ctl.wfull[s]), kWArrivals);
-      mbar_init(smem_addr(&ctl.wlocal[s]), kDequantWarps);
+    for (uint32_t s = 0; s < kAStages && kInt4; ++s) {
+      mbar_init(smem_addr(&ctl.afull[s]), kDequantWarps);
+      mbar_init(smem_addr(&ctl.aempty[s]), 1);
     }
     for (int s = 0; s < kQStages && kInt4; ++s) {
       mbar_init(smem_addr(&ctl.qfull[s]), 1);
@@ -626,7 +641,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && total > 0 && rank == 0) {
       // ---------------------------------------------------------- MMA issuer (the leader of a pair)
-      Ring rt;
+      Ring rt, ra;   // token stage, TMEM weight stage (4-bit)
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
       TileSource reader(dynamic, unit0, units, total);
@@ -644,27 +659,36 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         const uint32_t idesc = idesc_bf16_f32(G::kRows, ti.ntok);
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort)) { ok = false; break; }
-          if (kInt4) {
-            const bool w_ok = kPair ? wait_phase_cluster(smem_addr(&ctl.wfull[rt.slot]), rt.phase, abort)
-                                    : wait_phase(smem_addr(&ctl.wfull[rt.slot]), rt.phase, abort);
-            if (!w_ok) { ok = false; break; }
-          }
+          if (kInt4 && !wait_phase(smem_addr(&ctl.afull[ra.slot]), ra.phase, abort)) { ok = false; break; }
           tc_fence_after_sync();
 #pragma unroll
           for (uint32_t sub = 0; sub < G::kSub; ++sub) {
-            const uint64_t a_desc = smem_desc_k_sw128(w_ring + (rt.slot * G::kSub + sub) * kWBytes);
             const uint64_t b_desc = smem_desc_k_sw128(t_ring + (rt.slot * G::kSub + sub) * G::kTSlot);
+            if constexpr (kInt4) {
+              const uint32_t a_tmem = tmem_base + a_slab_col(ra.slot, sub);
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {   // +32 bytes along K per step: +2 in the >>4 address field
-              const uint32_t accumulate = (kb | static_cast<int>(sub) | k) != 0;
-              if constexpr (kPair)
-                mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
-              else
-                mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
+              for (int k = 0; k < kBK / 16; ++k) {   // A: +8 TMEM columns per K step; B: +32 bytes
+                const uint32_t accumulate = (kb | static_cast<int>(sub) | k) != 0;
+                mma_bf16_ts(d_tmem, a_tmem + 8u * k, b_desc + 2u * k, idesc, accumulate);
+              }
+            } else {
+              const uint64_t a_desc = smem_desc_k_sw128(w_ring + (rt.slot * G::kSub + sub) * kWBytes);
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k) {   // +32 bytes along K per step: +2 in the >>4 address field
+                const uint32_t accumulate = (kb | static_cast<int>(sub) | k) != 0;
+                if constexpr (kPair)
+                  mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
+                else
+                  mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
+              }
             }
           }
           if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.empty[rt.slot]), 0x3);
           else mma_commit(smem_addr(&ctl.empty[rt.slot]));
+          if constexpr (kInt4) {
+            mma_commit(smem_addr(&ctl.aempty[ra.slot]));
+            ra.next(kAStages);
+          }
           rt.next(ST);
         }
         if (!ok) break;
@@ -672,27 +696,6 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         else mma_commit(smem_addr(&ctl.acc_full[acc]));
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
-      }
-      if (!ok) atomicOr(p.status, kStatusTimeout);
-    } else if (kInt4 && kPair && lane == 0 && total > 0 && rank != 0) {
-      // ---------------------------------------------------------- forwarder (4-bit pair, second CTA)
-      // One cluster-scope arrive per weight slab on the leader's wfull, once this CTA's
-      // eight dequantisation warps have written their half of it.
-      const uint32_t wfull_leader0 = map_to_rank(smem_addr(&ctl.wfull[0]), 0);
-      Ring rw;
-      bool ok = true;
-      TileSource reader(dynamic, unit0, units, total);
-      for (;;) {
-        uint32_t tile;
-        const int got = reader.next(ctl, q_empty0, q_remote, abort, &tile);
-        if (got < 0) ok = false;
-        if (got <= 0) break;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!wait_phase(smem_addr(&ctl.wlocal[rw.slot]), rw.phase, abort)) { ok = false; break; }
-          mbar_arrive_cluster(wfull_leader0 + rw.slot * sizeof(uint64_t));
-          rw.next(SW);
-        }
-        if (!ok) break;
       }
       if (!ok) atomicOr(p.status, kStatusTimeout);
     }
@@ -758,13 +761,17 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         if (got < 0) ok = false;
         if (got <= 0) break;
         const Tile ti = decode_tile<G>(tile, prefix, p);
-        const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
+        const int32_t w_row = static_cast<int32_t>(ti.n0);
         const uint64_t pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_phase(smem_addr(&ctl.qempty[rq.slot]), rq.phase ^ 1u, abort)) { ok = false; break; }
           const uint32_t qfull = smem_addr(&ctl.qfull[rq.slot]);
-          mbar_arrive_expect_tx(qfull, kQBytes);
-          tma_load_3d_hint(q_ring + rq.slot * kQBytes, &p.w_map, qfull, kb * (kBK / 8), w_row, ti.e, pol);
+          mbar_arrive_expect_tx(qfull, kQSlotBytes);
+          // Two 64-K packed slabs per stage; one past K is zero-filled by TMA.
+#pragma unroll
+          for (uint32_t sub = 0; sub < 2; ++sub)
+            tma_load_3d_hint(q_ring + rq.slot * kQSlotBytes + sub * kQBytes, &p.w_map, qfull,
+                             (kb * 2 + static_cast<int32_t>(sub)) * (kBK / 8), w_row, ti.e, pol);
           pending |= 1u << rq.slot;
           pend_phase = (pend_phase & ~(1u << rq.slot)) | (rq.phase << rq.slot);
           rq.next(kQStages);
@@ -779,19 +786,19 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     }
   } else if (kInt4) {
     // ------------------------------------------------------------ 4-bit dequantisation
-    // Thread u (0..255) owns half of weight row r = u / 2: packed words 4h .. 4h+3
-    // (h = u % 2) in, 16 consecutive bytes of the packed slab, so a warp's loads are
-    // conflict-free; four 16-byte bf16 chunks out, chunk j of row r landing at
-    // j ^ (r % 8) (the 128-byte swizzle).  A packed slab is consumed as soon as it
-    // lands and the next weight slot is free (the MMA that last read it completed).
-    // Scales are loaded four k-steps ahead.
-    const uint32_t u = static_cast<uint32_t>(tid - (kThreads + 32));
-    const uint32_t r = u >> 1, h = u & 1u;
+    // Warp w (7..14) may write the TMEM lanes of quadrant w % 4, so its thread `lane`
+    // owns weight row r = 32 (w % 4) + lane, and the warp takes one 64-wide K half
+    // (h = 0 for warps 7..10, 1 for 11..14) of every 128-K stage: 8 packed words in
+    // (32 bytes of the packed slab), 32 TMEM columns of bf16 pairs out.  A stage's
+    // packed slab is consumed as soon as it lands and the TMEM stage is free (the
+    // MMAs that last read it completed).  Scales are loaded four stages ahead.
+    const uint32_t quad = static_cast<uint32_t>(warp & 3);
+    const uint32_t h = static_cast<uint32_t>(warp - 7) >> 2;
+    const uint32_t r = quad * 32u + static_cast<uint32_t>(lane);
     const int spr = p.K / p.group_size;   // scales per weight row
-    const int kb_per_scale = p.group_size / kBK;
     const unsigned short *sbits = reinterpret_cast<const unsigned short *>(p.scales);
-    const uint32_t wdone0 = smem_addr(kPair && rank != 0 ? &ctl.wlocal[0] : &ctl.wfull[0]);
-    Ring rw, rq;
+    const uint32_t lane_field = (quad * 32u) << 16;
+    Ring ra, rq;
     bool ok = true;
     TileSource reader(dynamic, unit0, units, total);
     for (;;) {
@@ -801,13 +808,16 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       if (got < 0) ok = false;
       if (got <= 0) break;
       const Tile ti = decode_tile<G>(tile, prefix, p);
-      const uint32_t n = ti.n0 + rank * kBlockN + r;
+      const uint32_t n = ti.n0 + r;
       const bool row_ok = n < static_cast<uint32_t>(p.N);
       const unsigned short *srow = sbits + (static_cast<size_t>(ti.e) * p.N + (row_ok ? n : 0)) * spr;
+      // Scale of this thread's K half of stage kb; zero past K (the half is then all
+      // zeros, matching the zero-filled tokens) or past N.
       auto scale_at = [&](int kb) -> unsigned short {
-        return (row_ok && kb < KB) ? __ldg(srow + kb / kb_per_scale) : static_cast<unsigned short>(0);
+        const int k0 = kb * 2 * kBK + static_cast<int>(h) * kBK;
+        return (row_ok && kb < KB && k0 < p.K) ? __ldg(srow + k0 / p.group_size) : static_cast<unsigned short>(0);
       };
-      // Scale of k-step kb sits in sq[kb % 4], loaded four k-steps before it is used
+      // Scale of stage kb sits in sq[kb % 4], loaded four stages before it is used
       // (the loop is unrolled by four so each slot stays in its own register).
       unsigned short sq[4];
 #pragma unroll
@@ -819,29 +829,35 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           if (kb >= KB || !ok) continue;
           const unsigned short s = sq[j];
           sq[j] = scale_at(kb + 4);
-          // Packed slab landed and the stage's weight slot free (the MMA that last read
-          // it completed).
           const bool landed = wait_phase(smem_addr(&ctl.qfull[rq.slot]), rq.phase, abort) &&
-                              wait_phase(smem_addr(&ctl.empty[rw.slot]), rw.phase ^ 1u, abort);
+                              wait_phase(smem_addr(&ctl.aempty[ra.slot]), ra.phase ^ 1u, abort);
           if (!__all_sync(0xffffffffu, landed)) { ok = false; continue; }   // the warp aborts together
-          const uint4 q = *reinterpret_cast<const uint4 *>(dyn_smem + (q_ring - dyn_base) + rq.slot * kQBytes + u * 16);
+          tc_fence_after_sync();   // the MMAs' reads of this TMEM stage precede the overwrite
+          const uint8_t *qrow = dyn_smem + (q_ring - dyn_base) + rq.slot * kQSlotBytes + h * kQBytes + r * 32u;
+          const uint4 q0 = *reinterpret_cast<const uint4 *>(qrow);
+          const uint4 q1 = *reinterpret_cast<const uint4 *>(qrow + 16);
           const __nv_bfloat16 sb = __ushort_as_bfloat16(s);
           const __nv_bfloat162 s2v = __halves2bfloat162(sb, sb);
-          uint8_t *wrow = dyn_smem + (w_ring - dyn_base) + rw.slot * kWBytes + r * 128;
-          const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+          const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          uint32_t cols[32];
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const uint32_t jc = 4 * h + jj;
-            *reinterpret_cast<uint4 *>(wrow + ((jc ^ (r & 7u)) << 4)) = dequant_word(words[jj], s2v);
+          for (int j8 = 0; j8 < 8; ++j8) {
+            const uint4 d = dequant_word(words[j8], s2v);
+            cols[4 * j8 + 0] = d.x;
+            cols[4 * j8 + 1] = d.y;
+            cols[4 * j8 + 2] = d.z;
+            cols[4 * j8 + 3] = d.w;
           }
-          fence_async_smem();   // generic-proxy writes -> visible to the tensor core's reads
+          tmem_st_x32(tmem_base + lane_field + a_slab_col(ra.slot, h), cols);
+          tmem_st_wait();
+          tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(smem_addr(&ctl.qempty[rq.slot]));
-            mbar_arrive(wdone0 + rw.slot * sizeof(uint64_t));
+            mbar_arrive(smem_addr(&ctl.afull[ra.slot]));
           }
           rq.next(kQStages);
-          rw.next(SW);
+          ra.next(kAStages);
         }
       }
       if (!ok) break;

@@ -245,6 +245,16 @@ def test_int4_random(gs, variant):
     assert status == binding.GMM_OK
 
 
+@pytest.mark.parametrize("N,K,gs", [(136, 192, 64), (200, 320, 64), (128, 64, 64), (72, 1088, 64)])
+def test_int4_k_and_n_tails(N, K, gs):
+    """K an odd multiple of 64 (the last 128-wide K stage has one half past K) and N
+    not a multiple of 128 (rows past N in the last weight block)."""
+    r = routing(5, N, K, [1, 17, 160, 161, 40], [4, 0, 2, 3, -1], dist=("normal", 1.0), int4=True, gs=gs)
+    v = wl.host_values(r, 15)
+    _, _, status, _ = check_against_oracle(handle(5), r, v, where=f"int4 tails N={N} K={K}")
+    assert status == binding.GMM_OK
+
+
 # ---------------------------------------------------------------- full-size sampled parity
 
 def sampled_full_size(name, rows_per_group=2, ncols=96, seed=0):
