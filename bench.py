@@ -290,8 +290,7 @@ def main():
     ap.add_argument("--group-range", default=None,
                     help="sub-workload lo:hi - groups lo .. hi-1 of the named routing")
     ap.add_argument("--variant", default=None, choices=["pair", "single"],
-                    help="bf16 kernel variant (default: the library's choice, CTA pairs); "
-                         "the 4-bit path always runs one CTA per tile")
+                    help="kernel variant (default: the library's choice, CTA pairs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -467,7 +466,7 @@ def main():
                     "roofline_time_ms": max(t_tensor, t_hbm) * 1e3,
                     "kernel": "gmm_grouped_kernel<%s, %s>" % (
                         "true" if r.int4 else "false",
-                        "false" if (r.int4 or args.variant == "single") else "true")}
+                        "true" if (args.variant == "pair" or (args.variant is None and not r.int4)) else "false")}
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",

@@ -51,8 +51,9 @@ struct gmm_ctx {
   int device = 0;
   int num_experts = 0;
   int num_sms = 0;
-  gmm_variant var[2][2];          // [4-bit][pair]; the 4-bit path has only the one-CTA kernel
+  gmm_variant var[2][2];          // [4-bit][pair]
   int use_pairs = 1;              // bf16 path: 1 = CTA-pair kernels (cta_group::2), 0 = one CTA per tile
+  int use_pairs_int4 = 0;         // 4-bit path: the same (default one CTA per tile)
   uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
   size_t ws_bytes = 0;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -136,6 +137,8 @@ int configure(gmm_variant *v, int optin, int num_sms) {
   if (kInt4) budget -= gmm::kQRingBytes;   // the packed-slab ring (the weights themselves are in TMEM)
   v->stages = static_cast<int>(budget / static_cast<long>(G::kStageBytes));
   if (v->stages > gmm::kMaxStages) v->stages = gmm::kMaxStages;
+  // The 4-bit stage ring also holds the TMEM weight slabs: exactly kAStages deep.
+  if (kInt4) v->stages = v->stages >= static_cast<int>(gmm::kAStages) ? static_cast<int>(gmm::kAStages) : 0;
   if (v->stages < 2) return GMM_ERR_UNSUPPORTED;
   v->smem = static_cast<size_t>(v->stages) * G::kStageBytes +
             (kInt4 ? gmm::kQRingBytes : 0) + 1024;
@@ -167,7 +170,7 @@ int configure(gmm_variant *v, int optin, int num_sms) {
 template <bool kInt4>
 int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   DeviceGuard guard(h->device);
-  const int pairs = kInt4 ? 0 : h->use_pairs;
+  const int pairs = kInt4 ? h->use_pairs_int4 : h->use_pairs;
   const gmm_variant &v = h->var[kInt4][pairs];
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
@@ -178,18 +181,16 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   cfg.stream = stream;
   p.num_stages = v.stages;
   cudaError_t err;
-  if constexpr (kInt4) {
-    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<true, false>, p);
-  } else if (pairs) {
+  if (pairs) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<false, true>, p);
+    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, true>, p);
   } else {
-    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<false, false>, p);
+    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, false>, p);
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
@@ -199,7 +200,7 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
 }
 
 uint32_t max_tok(const gmm_ctx *h, bool int4) {
-  if (int4) return gmm::Geom<true, false>::kMaxTok;
+  if (int4) return h->use_pairs_int4 ? gmm::Geom<true, true>::kMaxTok : gmm::Geom<true, false>::kMaxTok;
   return h->use_pairs ? gmm::Geom<false, true>::kMaxTok : gmm::Geom<false, false>::kMaxTok;
 }
 
@@ -256,10 +257,15 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
 
   const int single_ok = configure<false, false>(&h->var[0][0], optin, sms) == GMM_OK &&
                         configure<true, false>(&h->var[1][0], optin, sms) == GMM_OK;
-  // Tuning override GMM_VARIANT=single: the bf16 path runs its one-CTA kernel.
+  // Tuning override GMM_VARIANT: "single" forces the one-CTA kernels, "pair" the pairs.
   const char *variant = getenv("GMM_VARIANT");
-  const bool pairs_ok = sms >= 2 && configure<false, true>(&h->var[0][1], optin, sms) == GMM_OK;
+  const bool pairs_ok = sms >= 2 && configure<false, true>(&h->var[0][1], optin, sms) == GMM_OK &&
+                        configure<true, true>(&h->var[1][1], optin, sms) == GMM_OK;
   h->use_pairs = pairs_ok && !(variant && std::strcmp(variant, "single") == 0);
+  // The 4-bit path runs one CTA per tile unless GMM_VARIANT=pair: its pair kernel's
+  // cross-CTA signal that both halves of a weight stage are in TMEM costs more than
+  // the halved token traffic saves.
+  h->use_pairs_int4 = pairs_ok && variant && std::strcmp(variant, "pair") == 0;
   if (!single_ok) {
     cudaGetLastError();
     delete h;

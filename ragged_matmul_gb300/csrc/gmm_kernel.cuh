@@ -29,7 +29,7 @@
 //                  of the tokens; the leader (r = 0) issues the MMAs and commits to
 //                  both CTAs' barriers; each CTA stores its own 128 columns of C.
 //   kInt4 = false  bf16 weights, loaded by TMA into the stage together with tokens.
-//   kInt4 = true   packed 4-bit weights (one CTA per tile only): a dedicated TMA warp
+//   kInt4 = true   packed 4-bit weights: a dedicated TMA warp
 //                  streams packed slabs through their own ring, and eight warps
 //                  dequantise them straight into tensor memory, where the MMA takes
 //                  its A operand from (tcgen05.mma with A in TMEM).  The dequantised
@@ -46,7 +46,7 @@
 //                the group's end and columns past N; two accumulators let it
 //                overlap the next tile's main loop.
 //   warp 6       (4-bit) TMA producer of packed slabs.
-//   warps 7..14  (4-bit) dequantisation.
+//   warps 7..22  (4-bit) dequantisation.
 //
 // Row bounds.  The host does not know how many rows A has (that is
 // a_offsets[G], on the device), so the token tensor maps are encoded with a
@@ -71,11 +71,11 @@ constexpr int kBK = 64;                       // K per stage: one 128-byte swizz
 constexpr int kMaxStages = 12;                // deepest W+T stage ring
 constexpr int kMaxGroups = 4096;
 constexpr int kThreads = 192;                 // bf16 kernel: producer, MMA, 4 epilogue warps
-constexpr int kDequantThreads = 256;          // 4-bit kernel: 8 dequantisation warps, one thread per row and K half
+constexpr int kDequantThreads = 512;          // 4-bit kernel: 16 dequantisation warps, one thread per row and K quarter
 constexpr int kInt4Threads = kThreads + 32 + kDequantThreads;   // + one packed-slab producer warp
 constexpr int kWBytes = kBlockN * kBK * 2;    // 16 KB bf16 weight slab
 constexpr int kQBytes = kBlockN * kBK / 2;    // 4 KB packed 4-bit slab (128 rows x 8 words)
-constexpr int kQStages = 6;                   // 4-bit kernel: depth of the packed ring (one 128-K stage per slot)
+constexpr int kQStages = 8;                   // 4-bit kernel: depth of the packed ring (one 128-K stage per slot)
 constexpr int kQSlotBytes = 2 * kQBytes;
 constexpr int kQRingBytes = kQStages * kQSlotBytes;
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
@@ -83,7 +83,12 @@ constexpr uint32_t kTmemCols = 2 * kAccCols;
 // 4-bit kernel: dequantised weight slabs live in TMEM (128 lanes = weight rows, 32
 // columns = 64 bf16 of K per 64-wide slab) in the columns the accumulators leave
 // free: an accumulator holds at most 160 token columns (kMaxTok), so columns
-// 160..255 and 416..511 hold six slabs, three 128-K stages of two slabs each.
+// 160..255 and 416..511 hold six slabs, three 128-K stages of two slabs each.  The
+// 4-bit kernel's stage ring is therefore three deep, and a stage is its token slab
+// and its TMEM weight slabs together: one barrier tells the MMA that both are ready,
+// one commit frees both (the MMA-issuing thread's cost per stage is what bounds this
+// kernel).  Three stages hide the token copies' latency from L2 in the CTA-pair
+// kernel, whose CTAs each load half of a stage's tokens.
 constexpr uint32_t kAStages = 3;
 __device__ __forceinline__ uint32_t a_slab_col(uint32_t stage, uint32_t sub) {
   const uint32_t i = 2 * stage + sub;   // 0..5
@@ -108,7 +113,6 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;   // and on draining copies aft
 // Geometry of one kernel variant.
 template <bool kInt4, bool kPair>
 struct Geom {
-  static_assert(!(kInt4 && kPair), "the 4-bit kernel runs one CTA per tile");
   static constexpr uint32_t kRows = kPair ? 2 * kBlockN : kBlockN;   // weight rows (C columns) per tile
   static constexpr uint32_t kTokAlign = kPair ? 32 : 16;             // MMA N granule (pair: 2 x 16)
   // Token rows per tile.  The 4-bit path keeps slabs small so its token ring can be
@@ -159,10 +163,10 @@ struct Tile {
 };
 
 struct __align__(8) Ctrl {
-  uint64_t full[kMaxStages];     // stage's TMA bytes landed (pair: both CTAs' bytes, on the leader)
+  uint64_t full[kMaxStages];     // stage's TMA bytes landed (pair: both CTAs' bytes, on the leader);
+                                 // 4-bit: and its TMEM weight slabs written by every dequantisation
+                                 // warp (pair: of both CTAs)
   uint64_t empty[kMaxStages];    // MMAs that read the stage completed
-  uint64_t afull[kAStages];      // 4-bit: a TMEM weight stage written by the eight dequantisation warps
-  uint64_t aempty[kAStages];     // 4-bit: the MMAs that read a TMEM weight stage completed
   uint64_t qfull[kQStages];      // 4-bit: a packed stage landed
   uint64_t qempty[kQStages];     // 4-bit: the dequantisation warps are done with a packed stage
   uint64_t acc_full[2];
@@ -409,6 +413,9 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   constexpr int NT = kInt4 ? kInt4Threads : kThreads;
   constexpr uint32_t kEpiArrivals = (kPair ? 2 : 1) * 4;   // one per epilogue warp of each CTA
   constexpr uint32_t kDequantWarps = kDequantThreads / 32;
+  // Arrivals per phase of a stage's `full` barrier: the token producer's (which also
+  // sets the expected bytes) and, 4-bit, one per dequantisation warp of each CTA.
+  constexpr uint32_t kFullArrivals = 1 + (kInt4 ? (kPair ? 2 : 1) * kDequantWarps : 0);
   __shared__ Ctrl ctl;
   __shared__ uint32_t prefix[kMaxGroups + 1];
   extern __shared__ uint8_t dyn_smem[];
@@ -419,10 +426,10 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   const int KB = (p.K + static_cast<int>(G::kSub * kBK) - 1) / static_cast<int>(G::kSub * kBK);   // stages per tile
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   // Readers of each tile-queue entry: per CTA the MMA thread (leader only), the four
-  // epilogue warps and (4-bit) the packed-slab producer and eight dequantisation
+  // epilogue warps and (4-bit) the packed-slab producer and the dequantisation
   // warps; in the pair's second CTA also its token producer.
   constexpr uint32_t kLeaderReaders = 1 + 4 + (kInt4 ? 1 + kDequantWarps : 0);
-  constexpr uint32_t kPeerReaders = 1 + 4;
+  constexpr uint32_t kPeerReaders = 1 + 4 + (kInt4 ? 1 + kDequantWarps : 0);
   constexpr uint32_t kQueueArrivals = kLeaderReaders + (kPair ? kPeerReaders : 0);
 
   // 1024-byte aligned rings, at identical offsets in both CTAs of a pair:
@@ -435,12 +442,8 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
 
   if (tid == 0) {
     for (uint32_t s = 0; s < ST; ++s) {
-      mbar_init(smem_addr(&ctl.full[s]), 1);
+      mbar_init(smem_addr(&ctl.full[s]), kFullArrivals);
       mbar_init(smem_addr(&ctl.empty[s]), 1);
-    }
-    for (uint32_t s = 0; s < kAStages && kInt4; ++s) {
-      mbar_init(smem_addr(&ctl.afull[s]), kDequantWarps);
-      mbar_init(smem_addr(&ctl.aempty[s]), 1);
     }
     for (int s = 0; s < kQStages && kInt4; ++s) {
       mbar_init(smem_addr(&ctl.qfull[s]), 1);
@@ -639,40 +642,54 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && total > 0 && rank == 0) {
+    if (total > 0 && rank == 0) {
       // ---------------------------------------------------------- MMA issuer (the leader of a pair)
-      Ring rt, ra;   // token stage, TMEM weight stage (4-bit)
+      // The whole warp runs this loop with identical values in every lane, so the MMA
+      // operands are warp-uniform; the tcgen05 wrappers issue from one elected lane.
+      // Descriptors are a per-ring base plus a constant offset in the >>4 address field
+      // (shared-memory addresses stay below 256 KB, so the 14-bit field never carries).
+      Ring rt;
       uint32_t acc = 0, acc_phase = 0;
       bool ok = true;
       TileSource reader(dynamic, unit0, units, total);
+      const uint64_t t_desc0 = smem_desc_k_sw128(t_ring);
+      const uint64_t w_desc0 = smem_desc_k_sw128(w_ring);
       for (;;) {
         uint32_t tile;
-        const int got = reader.next(ctl, q_empty0, q_remote, abort, &tile);
+        const int got = next_tile_warp(reader, ctl, q_empty0, q_remote, abort, &tile);
         if (got < 0) ok = false;
         if (got <= 0) break;
         const Tile ti = decode_tile<G>(tile, prefix, p);
-        const bool acc_free = kPair ? wait_phase_cluster(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort)
-                                    : wait_phase(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort);
+        const bool acc_free = __all_sync(
+            0xffffffffu, kPair ? wait_phase_cluster(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort)
+                               : wait_phase(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort));
         if (!acc_free) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
         const uint32_t idesc = idesc_bf16_f32(G::kRows, ti.ntok);
         for (int kb = 0; kb < KB; ++kb) {
-          if (!wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort)) { ok = false; break; }
-          if (kInt4 && !wait_phase(smem_addr(&ctl.afull[ra.slot]), ra.phase, abort)) { ok = false; break; }
+          // The 4-bit pair's stage is also signalled by the second CTA's dequantisation
+          // warps (cluster-scope release), so it is acquired at cluster scope.
+          const bool staged = __all_sync(
+              0xffffffffu, (kInt4 && kPair) ? wait_phase_cluster(smem_addr(&ctl.full[rt.slot]), rt.phase, abort)
+                                            : wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort));
+          if (!staged) { ok = false; break; }
           tc_fence_after_sync();
 #pragma unroll
           for (uint32_t sub = 0; sub < G::kSub; ++sub) {
-            const uint64_t b_desc = smem_desc_k_sw128(t_ring + (rt.slot * G::kSub + sub) * G::kTSlot);
+            const uint64_t b_desc = t_desc0 + (((rt.slot * G::kSub + sub) * G::kTSlot) >> 4);
             if constexpr (kInt4) {
-              const uint32_t a_tmem = tmem_base + a_slab_col(ra.slot, sub);
+              const uint32_t a_tmem = tmem_base + a_slab_col(rt.slot, sub);
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k) {   // A: +8 TMEM columns per K step; B: +32 bytes
                 const uint32_t accumulate = (kb | static_cast<int>(sub) | k) != 0;
-                mma_bf16_ts(d_tmem, a_tmem + 8u * k, b_desc + 2u * k, idesc, accumulate);
+                if constexpr (kPair)
+                  mma_bf16_ts_pair(d_tmem, a_tmem + 8u * k, b_desc + 2u * k, idesc, accumulate);
+                else
+                  mma_bf16_ts(d_tmem, a_tmem + 8u * k, b_desc + 2u * k, idesc, accumulate);
               }
             } else {
-              const uint64_t a_desc = smem_desc_k_sw128(w_ring + (rt.slot * G::kSub + sub) * kWBytes);
+              const uint64_t a_desc = w_desc0 + (((rt.slot * G::kSub + sub) * kWBytes) >> 4);
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k) {   // +32 bytes along K per step: +2 in the >>4 address field
                 const uint32_t accumulate = (kb | static_cast<int>(sub) | k) != 0;
@@ -685,10 +702,6 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           }
           if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.empty[rt.slot]), 0x3);
           else mma_commit(smem_addr(&ctl.empty[rt.slot]));
-          if constexpr (kInt4) {
-            mma_commit(smem_addr(&ctl.aempty[ra.slot]));
-            ra.next(kAStages);
-          }
           rt.next(ST);
         }
         if (!ok) break;
@@ -697,7 +710,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
-      if (!ok) atomicOr(p.status, kStatusTimeout);
+      if (!ok && lane == 0) atomicOr(p.status, kStatusTimeout);
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
@@ -761,7 +774,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         if (got < 0) ok = false;
         if (got <= 0) break;
         const Tile ti = decode_tile<G>(tile, prefix, p);
-        const int32_t w_row = static_cast<int32_t>(ti.n0);
+        const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
         const uint64_t pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
         for (int kb = 0; kb < KB; ++kb) {
           if (!wait_phase(smem_addr(&ctl.qempty[rq.slot]), rq.phase ^ 1u, abort)) { ok = false; break; }
@@ -786,19 +799,26 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     }
   } else if (kInt4) {
     // ------------------------------------------------------------ 4-bit dequantisation
-    // Warp w (7..14) may write the TMEM lanes of quadrant w % 4, so its thread `lane`
-    // owns weight row r = 32 (w % 4) + lane, and the warp takes one 64-wide K half
-    // (h = 0 for warps 7..10, 1 for 11..14) of every 128-K stage: 8 packed words in
-    // (32 bytes of the packed slab), 32 TMEM columns of bf16 pairs out.  A stage's
-    // packed slab is consumed as soon as it lands and the TMEM stage is free (the
-    // MMAs that last read it completed).  Scales are loaded four stages ahead.
+    // Warp w (7..22) may write the TMEM lanes of quadrant w % 4, so its thread `lane`
+    // owns weight row r = 32 (w % 4) + lane; the four warps of a quadrant split every
+    // 128-K stage into 32-wide K quarters (quarter x = (w - 7) / 4): 4 packed words in
+    // (16 bytes of the packed slab), 16 TMEM columns of bf16 pairs out.  Sixteen
+    // warps with short chains keep the dequantisation latency per stage below the
+    // MMAs' time.  A stage's packed slab is consumed as soon as it lands and the TMEM
+    // stage is free (the MMAs that last read it completed).  Scales are loaded four
+    // stages ahead.
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
-    const uint32_t h = static_cast<uint32_t>(warp - 7) >> 2;
+    const uint32_t x = static_cast<uint32_t>(warp - 7) >> 2;   // K quarter of each stage
     const uint32_t r = quad * 32u + static_cast<uint32_t>(lane);
     const int spr = p.K / p.group_size;   // scales per weight row
+    const uint32_t gq = static_cast<uint32_t>(p.group_size) / 32u;   // K quarters per scale (>= 2)
     const unsigned short *sbits = reinterpret_cast<const unsigned short *>(p.scales);
     const uint32_t lane_field = (quad * 32u) << 16;
-    Ring ra, rq;
+    const uint32_t qoff = (x >> 1) * kQBytes + (x & 1u) * 16u + r * 32u;   // this thread's 16 packed bytes
+    const uint32_t col_off = (x & 1u) * 16u;                               // and its TMEM columns in the slab
+    Ring rs, rq;   // stage ring (token slab + TMEM weight slabs), packed ring
+    // The stage's `full` barrier lives in the leader CTA of a pair.
+    const uint32_t full0 = kPair ? map_to_rank(smem_addr(&ctl.full[0]), 0) : smem_addr(&ctl.full[0]);
     bool ok = true;
     TileSource reader(dynamic, unit0, units, total);
     for (;;) {
@@ -808,56 +828,71 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       if (got < 0) ok = false;
       if (got <= 0) break;
       const Tile ti = decode_tile<G>(tile, prefix, p);
-      const uint32_t n = ti.n0 + r;
+      const uint32_t n = ti.n0 + rank * kBlockN + r;
       const bool row_ok = n < static_cast<uint32_t>(p.N);
       const unsigned short *srow = sbits + (static_cast<size_t>(ti.e) * p.N + (row_ok ? n : 0)) * spr;
-      // Scale of this thread's K half of stage kb; zero past K (the half is then all
-      // zeros, matching the zero-filled tokens) or past N.
-      auto scale_at = [&](int kb) -> unsigned short {
-        const int k0 = kb * 2 * kBK + static_cast<int>(h) * kBK;
-        return (row_ok && kb < KB && k0 < p.K) ? __ldg(srow + k0 / p.group_size) : static_cast<unsigned short>(0);
+      // The K quarter of stage kb is u = 4 kb + x (32 of K each); its scale is number
+      // u / gq, tracked incrementally (no division in the loop) for the prefetch
+      // position kb + 4.  Past K (the last stage's second half when K is an odd
+      // multiple of 64) or past N the scale is zero, so the weights there are zero,
+      // matching the zero-filled tokens.
+      const uint32_t quarters = static_cast<uint32_t>(p.K) / 32u;
+      uint32_t pu = x, pidx = x / gq, prem = x % gq;   // prefetch position: quarter, scale index, remainder
+      auto scale_next = [&]() -> unsigned short {
+        const unsigned short v =
+            (row_ok && pu < quarters) ? __ldg(srow + pidx) : static_cast<unsigned short>(0);
+        pu += 4u;
+        prem += 4u;
+        while (prem >= gq) {
+          prem -= gq;
+          ++pidx;
+        }
+        return v;
       };
       // Scale of stage kb sits in sq[kb % 4], loaded four stages before it is used
       // (the loop is unrolled by four so each slot stays in its own register).
       unsigned short sq[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) sq[j] = scale_at(j);
+      for (int j = 0; j < 4; ++j) sq[j] = scale_next();
       for (int kb0 = 0; kb0 < KB && ok; kb0 += 4) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int kb = kb0 + j;
           if (kb >= KB || !ok) continue;
           const unsigned short s = sq[j];
-          sq[j] = scale_at(kb + 4);
-          const bool landed = wait_phase(smem_addr(&ctl.qfull[rq.slot]), rq.phase, abort) &&
-                              wait_phase(smem_addr(&ctl.aempty[ra.slot]), ra.phase ^ 1u, abort);
-          if (!__all_sync(0xffffffffu, landed)) { ok = false; continue; }   // the warp aborts together
-          tc_fence_after_sync();   // the MMAs' reads of this TMEM stage precede the overwrite
-          const uint8_t *qrow = dyn_smem + (q_ring - dyn_base) + rq.slot * kQSlotBytes + h * kQBytes + r * 32u;
-          const uint4 q0 = *reinterpret_cast<const uint4 *>(qrow);
-          const uint4 q1 = *reinterpret_cast<const uint4 *>(qrow + 16);
+          sq[j] = scale_next();
+          // The arithmetic needs only the packed slab: dequantise into registers and
+          // release the packed slot first, and only then wait for the TMEM stage, so
+          // the loop from an MMA's completion to the next write of its TMEM stage is
+          // just the store.
+          if (!__all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.qfull[rq.slot]), rq.phase, abort))) {
+            ok = false;   // the warp aborts together
+            continue;
+          }
+          const uint4 q = *reinterpret_cast<const uint4 *>(dyn_smem + (q_ring - dyn_base) + rq.slot * kQSlotBytes + qoff);
           const __nv_bfloat16 sb = __ushort_as_bfloat16(s);
           const __nv_bfloat162 s2v = __halves2bfloat162(sb, sb);
-          const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          uint32_t cols[32];
-#pragma unroll
-          for (int j8 = 0; j8 < 8; ++j8) {
-            const uint4 d = dequant_word(words[j8], s2v);
-            cols[4 * j8 + 0] = d.x;
-            cols[4 * j8 + 1] = d.y;
-            cols[4 * j8 + 2] = d.z;
-            cols[4 * j8 + 3] = d.w;
+          const uint4 d0 = dequant_word(q.x, s2v), d1 = dequant_word(q.y, s2v);
+          const uint4 d2 = dequant_word(q.z, s2v), d3 = dequant_word(q.w, s2v);
+          const uint32_t cols[16] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w,
+                                     d2.x, d2.y, d2.z, d2.w, d3.x, d3.y, d3.z, d3.w};
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_addr(&ctl.qempty[rq.slot]));   // the loads above are done
+          if (!__all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.empty[rs.slot]), rs.phase ^ 1u, abort))) {
+            ok = false;
+            continue;
           }
-          tmem_st_x32(tmem_base + lane_field + a_slab_col(ra.slot, h), cols);
+          tc_fence_after_sync();   // the MMAs' reads of this TMEM stage precede the overwrite
+          tmem_st_x16(tmem_base + lane_field + a_slab_col(rs.slot, x >> 1) + col_off, cols);
           tmem_st_wait();
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(smem_addr(&ctl.qempty[rq.slot]));
-            mbar_arrive(smem_addr(&ctl.afull[ra.slot]));
+            const uint32_t full = full0 + rs.slot * static_cast<uint32_t>(sizeof(uint64_t));
+            if constexpr (kPair) mbar_arrive_cluster(full); else mbar_arrive(full);
           }
           rq.next(kQStages);
-          ra.next(kAStages);
+          rs.next(ST);
         }
       }
       if (!ok) break;
