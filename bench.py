@@ -452,8 +452,15 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = len(os.sched_getaffinity(0))
         s, t = pick_oracle_sample(r, vals, nthreads, args.oracle_seconds)
-        cpu_baseline = {"value": s["flops"] / t / 1e12, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
-                        "sample": sample_desc(r, s) + f"; {t:.2f} s"}
+        # A workload whose whole oracle pass is short is timed over repeated passes,
+        # so the baseline still rests on about half the target seconds of CPU work.
+        passes, total = 1, t
+        while total < 0.5 * args.oracle_seconds and passes < 1000:
+            total += run_oracle(r, s, nthreads)
+            passes += 1
+        cpu_baseline = {"value": passes * s["flops"] / total / 1e12, "unit": "TFLOP/s", "cores": nthreads,
+                        "kind": "oracle",
+                        "sample": sample_desc(r, s) + f"; {passes} pass(es), {total:.2f} s"}
 
     if rank == 0:
         t_s = mean_ms * 1e-3
