@@ -330,13 +330,14 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
   GmmParams p;
   std::memset(&p, 0, sizeof(p));
   {
-    // Packed weights as 32-bit words {K/8, N, E}; one box = 128 rows x 64 K (8 words, 32 B).
+    // Packed weights as 32-bit words {K/8, N, E}; one box = 128 rows x 32 words (128 B,
+    // two 128-K stages), 128-byte swizzle.
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N),
                           static_cast<cuuint64_t>(h->num_experts)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 8) * 4, static_cast<cuuint64_t>(N) * (K / 8) * 4};
-    cuuint32_t box[3] = {gmm::kBK / 8, gmm::kBlockN, 1};
+    cuuint32_t box[3] = {gmm::kQRowBytes / 4, gmm::kBlockN, 1};
     rc = encode_map(h, &p.w_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, b_packed, dims, strides, box,
-                    CU_TENSOR_MAP_SWIZZLE_NONE);
+                    CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
   rc = encode_token_maps(h, p, a, K);

@@ -46,7 +46,7 @@
 //                the group's end and columns past N; two accumulators let it
 //                overlap the next tile's main loop.
 //   warp 6       (4-bit) TMA producer of packed slabs.
-//   warps 7..22  (4-bit) dequantisation.
+//   warps 7..18  (4-bit) dequantisation.
 //
 // Row bounds.  The host does not know how many rows A has (that is
 // a_offsets[G], on the device), so the token tensor maps are encoded with a
@@ -71,27 +71,44 @@ constexpr int kBK = 64;                       // K per stage: one 128-byte swizz
 constexpr int kMaxStages = 12;                // deepest W+T stage ring
 constexpr int kMaxGroups = 4096;
 constexpr int kThreads = 192;                 // bf16 kernel: producer, MMA, 4 epilogue warps
-constexpr int kDequantThreads = 512;          // 4-bit kernel: 16 dequantisation warps, one thread per row and K quarter
+// 4-bit kernel: 64-wide K sub-slabs per stage, and the dequantisation warps.  The
+// 12 warps form kDqGroups groups that take the stages in turn (stage s goes to group
+// s % kDqGroups), so each warp has kDqGroups stage-times for its loop of waits,
+// loads, arithmetic, TMEM store and arrive, whose fixed latency alone is longer
+// than a stage.  Within a group, each TMEM lane quadrant gets kDqWarpsPerStage / 4
+// warps with a thread per weight row, each covering kDqSubsPerWarp 64-K sub-slabs.
+constexpr int kSub4 = 2;
+constexpr int kDqGroups = 3;
+constexpr int kDequantThreads = 384;
+constexpr int kDqWarpsPerStage = kDequantThreads / 32 / kDqGroups;       // 4: one per quadrant
+constexpr int kDqSubsPerWarp = kSub4 * 4 / kDqWarpsPerStage;             // 2: the whole 128 of K
+static_assert(kDqWarpsPerStage % 4 == 0 && kDqSubsPerWarp >= 1, "every quadrant and sub-slab covered");
 constexpr int kInt4Threads = kThreads + 32 + kDequantThreads;   // + one packed-slab producer warp
 constexpr int kWBytes = kBlockN * kBK * 2;    // 16 KB bf16 weight slab
-constexpr int kQBytes = kBlockN * kBK / 2;    // 4 KB packed 4-bit slab (128 rows x 8 words)
-constexpr int kQStages = 8;                   // 4-bit kernel: depth of the packed ring (one 128-K stage per slot)
-constexpr int kQSlotBytes = 2 * kQBytes;
+// 4-bit kernel, packed ring: a slot holds a chunk of kQChunkStages stages, 128 bytes of
+// each weight row (one TMA box of 128 rows x 32 words, 128-byte swizzle).  Whole
+// 128-byte rows make full-line DRAM requests, a quarter as many as 32-byte rows.
+constexpr int kQChunkStages = 2;
+constexpr int kQRowBytes = kQChunkStages * kSub4 * kBK / 2;   // 128
+constexpr int kQSlotBytes = kBlockN * kQRowBytes;            // 16 KB
+constexpr int kQStages = 4;                                  // slots: 8 stages ahead
 constexpr int kQRingBytes = kQStages * kQSlotBytes;
+static_assert(kQRowBytes == 128, "the packed chunk is one 128-byte swizzle row per weight row");
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 // 4-bit kernel: dequantised weight slabs live in TMEM (128 lanes = weight rows, 32
 // columns = 64 bf16 of K per 64-wide slab) in the columns the accumulators leave
 // free: an accumulator holds at most 160 token columns (kMaxTok), so columns
-// 160..255 and 416..511 hold six slabs, three 128-K stages of two slabs each.  The
-// 4-bit kernel's stage ring is therefore three deep, and a stage is its token slab
-// and its TMEM weight slabs together: one barrier tells the MMA that both are ready,
-// one commit frees both (the MMA-issuing thread's cost per stage is what bounds this
-// kernel).  Three stages hide the token copies' latency from L2 in the CTA-pair
-// kernel, whose CTAs each load half of a stage's tokens.
-constexpr uint32_t kAStages = 3;
+// 160..255 and 416..511 hold six slabs.  The 4-bit kernel's stage ring is as deep as
+// the slabs allow (6 / kSub4 stages), and a stage is its token slab and its TMEM
+// weight slabs together: one barrier tells the MMA that both are ready, one commit
+// frees both.  128-K stages (a 3-deep ring) measured faster than 64-K stages (6
+// deep): the MMA thread's fixed cost per stage outweighs the deeper ring's better
+// cover of the token copies' latency from L2.
+constexpr uint32_t kASlabs = 6;
+constexpr uint32_t kAStages = kASlabs / kSub4;
 __device__ __forceinline__ uint32_t a_slab_col(uint32_t stage, uint32_t sub) {
-  const uint32_t i = 2 * stage + sub;   // 0..5
+  const uint32_t i = stage * kSub4 + sub;   // 0..5
   return i < 3 ? 160u + 32u * i : 416u + 32u * (i - 3u);
 }
 constexpr int kMapSlotBytes = 256;            // per-CTA workspace: two patched 128-byte tensor maps
@@ -121,10 +138,11 @@ struct Geom {
   static constexpr uint32_t kMaxTok = kInt4 ? 160 : 256;   // 4-bit: also bounded by the TMEM layout above
   static constexpr uint32_t kTSlot = (kPair ? kMaxTok / 2 : kMaxTok) * kBK * 2;   // token slab per CTA
   static_assert(kTSlot % 1024 == 0, "token slabs must keep the 1024-byte swizzle alignment");
-  // 64-wide K sub-slabs per pipeline stage.  The pair and 4-bit kernels take 128 of K
-  // per stage (8 MMAs per barrier wait and commit): the MMA thread's fixed cost per
-  // stage (wait, fence, commit, loop) is then spread over twice the tensor work.
-  static constexpr uint32_t kSub = (kPair || kInt4) ? 2 : 1;
+  // 64-wide K sub-slabs per pipeline stage.  The bf16 pair kernel takes 128 of K per
+  // stage (8 MMAs per barrier wait and commit): the MMA thread's fixed cost per stage
+  // (wait, fence, commit, loop) is then spread over twice the tensor work.  The 4-bit
+  // kernel's width is kSub4 (see the TMEM layout above).
+  static constexpr uint32_t kSub = kInt4 ? kSub4 : (kPair ? 2 : 1);
   // Shared memory of one stage of the W+T ring (the 4-bit kernel's weights are in TMEM).
   static constexpr uint32_t kStageBytes = kSub * ((kInt4 ? 0 : kWBytes) + kTSlot);
 };
@@ -167,8 +185,8 @@ struct __align__(8) Ctrl {
                                  // 4-bit: and its TMEM weight slabs written by every dequantisation
                                  // warp (pair: of both CTAs)
   uint64_t empty[kMaxStages];    // MMAs that read the stage completed
-  uint64_t qfull[kQStages];      // 4-bit: a packed stage landed
-  uint64_t qempty[kQStages];     // 4-bit: the dequantisation warps are done with a packed stage
+  uint64_t qfull[kQStages];      // 4-bit: a packed chunk landed
+  uint64_t qempty[kQStages];     // 4-bit: the dequantisation warps are done with a packed chunk
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t tq_full[kTileQueue];  // tile queue entry published
@@ -414,8 +432,9 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   constexpr uint32_t kEpiArrivals = (kPair ? 2 : 1) * 4;   // one per epilogue warp of each CTA
   constexpr uint32_t kDequantWarps = kDequantThreads / 32;
   // Arrivals per phase of a stage's `full` barrier: the token producer's (which also
-  // sets the expected bytes) and, 4-bit, one per dequantisation warp of each CTA.
-  constexpr uint32_t kFullArrivals = 1 + (kInt4 ? (kPair ? 2 : 1) * kDequantWarps : 0);
+  // sets the expected bytes) and, 4-bit, one per dequantisation warp of the stage's
+  // group in each CTA.
+  constexpr uint32_t kFullArrivals = 1 + (kInt4 ? (kPair ? 2 : 1) * kDqWarpsPerStage : 0);
   __shared__ Ctrl ctl;
   __shared__ uint32_t prefix[kMaxGroups + 1];
   extern __shared__ uint8_t dyn_smem[];
@@ -447,7 +466,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     }
     for (int s = 0; s < kQStages && kInt4; ++s) {
       mbar_init(smem_addr(&ctl.qfull[s]), 1);
-      mbar_init(smem_addr(&ctl.qempty[s]), kDequantWarps);
+      mbar_init(smem_addr(&ctl.qempty[s]), kQChunkStages * kDqWarpsPerStage);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_addr(&ctl.acc_full[a]), 1);
@@ -776,15 +795,13 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         const Tile ti = decode_tile<G>(tile, prefix, p);
         const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
         const uint64_t pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
-        for (int kb = 0; kb < KB; ++kb) {
+        const int KC = (KB + kQChunkStages - 1) / kQChunkStages;   // chunks of the tile
+        for (int kc = 0; kc < KC; ++kc) {
           if (!wait_phase(smem_addr(&ctl.qempty[rq.slot]), rq.phase ^ 1u, abort)) { ok = false; break; }
           const uint32_t qfull = smem_addr(&ctl.qfull[rq.slot]);
           mbar_arrive_expect_tx(qfull, kQSlotBytes);
-          // Two 64-K packed slabs per stage; one past K is zero-filled by TMA.
-#pragma unroll
-          for (uint32_t sub = 0; sub < 2; ++sub)
-            tma_load_3d_hint(q_ring + rq.slot * kQSlotBytes + sub * kQBytes, &p.w_map, qfull,
-                             (kb * 2 + static_cast<int32_t>(sub)) * (kBK / 8), w_row, ti.e, pol);
+          // One box of kQChunkStages stages; words past K are zero-filled by TMA.
+          tma_load_3d_hint(q_ring + rq.slot * kQSlotBytes, &p.w_map, qfull, kc * (kQRowBytes / 4), w_row, ti.e, pol);
           pending |= 1u << rq.slot;
           pend_phase = (pend_phase & ~(1u << rq.slot)) | (rq.phase << rq.slot);
           rq.next(kQStages);
@@ -799,24 +816,27 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     }
   } else if (kInt4) {
     // ------------------------------------------------------------ 4-bit dequantisation
-    // Warp w (7..22) may write the TMEM lanes of quadrant w % 4, so its thread `lane`
-    // owns weight row r = 32 (w % 4) + lane; the four warps of a quadrant split every
-    // 128-K stage into 32-wide K quarters (quarter x = (w - 7) / 4): 4 packed words in
-    // (16 bytes of the packed slab), 16 TMEM columns of bf16 pairs out.  Sixteen
-    // warps with short chains keep the dequantisation latency per stage below the
-    // MMAs' time.  A stage's packed slab is consumed as soon as it lands and the TMEM
-    // stage is free (the MMAs that last read it completed).  Scales are loaded four
-    // stages ahead.
+    // Warp w (7 .. 18) may write the TMEM lanes of quadrant w % 4, so its thread `lane`
+    // owns weight row r = 32 (w % 4) + lane.  The warp belongs to group
+    // (w - 7) / kDqWarpsPerStage, which handles every kDqGroups-th stage (counted
+    // across tiles); in a handled stage it converts kDqSubsPerWarp 64-K sub-slabs of
+    // its row (8 packed words each) into 32 TMEM columns of bf16 pairs each.  The
+    // arithmetic needs only the packed slab, so it runs as soon as the slab lands;
+    // only the TMEM store waits for the slot (the MMAs that last read it completed).
+    // Stages of other groups just advance the ring positions: a slot cannot move past
+    // a phase this warp still waits for, because releasing it needs this warp's
+    // arrival.
+    const uint32_t dw = static_cast<uint32_t>(warp - 7);
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
-    const uint32_t x = static_cast<uint32_t>(warp - 7) >> 2;   // K quarter of each stage
+    const uint32_t grp = dw / kDqWarpsPerStage;
+    const uint32_t sub0 = ((dw % kDqWarpsPerStage) >> 2) * kDqSubsPerWarp;   // first sub-slab of this warp
     const uint32_t r = quad * 32u + static_cast<uint32_t>(lane);
     const int spr = p.K / p.group_size;   // scales per weight row
-    const uint32_t gq = static_cast<uint32_t>(p.group_size) / 32u;   // K quarters per scale (>= 2)
     const unsigned short *sbits = reinterpret_cast<const unsigned short *>(p.scales);
     const uint32_t lane_field = (quad * 32u) << 16;
-    const uint32_t qoff = (x >> 1) * kQBytes + (x & 1u) * 16u + r * 32u;   // this thread's 16 packed bytes
-    const uint32_t col_off = (x & 1u) * 16u;                               // and its TMEM columns in the slab
-    Ring rs, rq;   // stage ring (token slab + TMEM weight slabs), packed ring
+    Ring rs;                  // stage ring (token slab + TMEM weight slabs)
+    uint32_t stage_no = 0;    // stages seen, across tiles
+    uint32_t chunk_base = 0;  // packed chunks of earlier tiles
     // The stage's `full` barrier lives in the leader CTA of a pair.
     const uint32_t full0 = kPair ? map_to_rank(smem_addr(&ctl.full[0]), 0) : smem_addr(&ctl.full[0]);
     bool ok = true;
@@ -831,59 +851,61 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const uint32_t n = ti.n0 + rank * kBlockN + r;
       const bool row_ok = n < static_cast<uint32_t>(p.N);
       const unsigned short *srow = sbits + (static_cast<size_t>(ti.e) * p.N + (row_ok ? n : 0)) * spr;
-      // The K quarter of stage kb is u = 4 kb + x (32 of K each); its scale is number
-      // u / gq, tracked incrementally (no division in the loop) for the prefetch
-      // position kb + 4.  Past K (the last stage's second half when K is an odd
-      // multiple of 64) or past N the scale is zero, so the weights there are zero,
-      // matching the zero-filled tokens.
-      const uint32_t quarters = static_cast<uint32_t>(p.K) / 32u;
-      uint32_t pu = x, pidx = x / gq, prem = x % gq;   // prefetch position: quarter, scale index, remainder
-      auto scale_next = [&]() -> unsigned short {
-        const unsigned short v =
-            (row_ok && pu < quarters) ? __ldg(srow + pidx) : static_cast<unsigned short>(0);
-        pu += 4u;
-        prem += 4u;
-        while (prem >= gq) {
-          prem -= gq;
-          ++pidx;
-        }
-        return v;
-      };
-      // Scale of stage kb sits in sq[kb % 4], loaded four stages before it is used
-      // (the loop is unrolled by four so each slot stays in its own register).
-      unsigned short sq[4];
+      for (int kb = 0; kb < KB && ok; ++kb) {
+        const bool mine = (stage_no % kDqGroups) == grp;
+        ++stage_no;
+        if (mine) {
+          // Scales of this thread's sub-slabs; zero past K (the last stage's second
+          // half when K is an odd multiple of 64) or past N, so the weights there are
+          // zero, matching the zero-filled tokens.  Loaded first: the waits below
+          // cover their latency.
+          unsigned short sv[kDqSubsPerWarp];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) sq[j] = scale_next();
-      for (int kb0 = 0; kb0 < KB && ok; kb0 += 4) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int kb = kb0 + j;
-          if (kb >= KB || !ok) continue;
-          const unsigned short s = sq[j];
-          sq[j] = scale_next();
-          // The arithmetic needs only the packed slab: dequantise into registers and
-          // release the packed slot first, and only then wait for the TMEM stage, so
-          // the loop from an MMA's completion to the next write of its TMEM stage is
-          // just the store.
-          if (!__all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.qfull[rq.slot]), rq.phase, abort))) {
-            ok = false;   // the warp aborts together
-            continue;
+          for (int i = 0; i < kDqSubsPerWarp; ++i) {
+            const int k0 = (kb * kSub4 + static_cast<int>(sub0) + i) * kBK;
+            sv[i] = (row_ok && k0 < p.K) ? __ldg(srow + k0 / p.group_size) : static_cast<unsigned short>(0);
           }
-          const uint4 q = *reinterpret_cast<const uint4 *>(dyn_smem + (q_ring - dyn_base) + rq.slot * kQSlotBytes + qoff);
-          const __nv_bfloat16 sb = __ushort_as_bfloat16(s);
-          const __nv_bfloat162 s2v = __halves2bfloat162(sb, sb);
-          const uint4 d0 = dequant_word(q.x, s2v), d1 = dequant_word(q.y, s2v);
-          const uint4 d2 = dequant_word(q.z, s2v), d3 = dequant_word(q.w, s2v);
-          const uint32_t cols[16] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w,
-                                     d2.x, d2.y, d2.z, d2.w, d3.x, d3.y, d3.z, d3.w};
+          // Packed chunk of this stage (slot and phase from the chunk count) and the
+          // stage's half of it; 16-byte piece c of row r sits at piece c ^ (r % 8).
+          const uint32_t chunk = chunk_base + static_cast<uint32_t>(kb) / kQChunkStages;
+          const uint32_t qslot = chunk % kQStages, qphase = (chunk / kQStages) & 1u;
+          const uint32_t piece0 = (static_cast<uint32_t>(kb) % kQChunkStages) * (kSub4 * 2);
+          if (!__all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.qfull[qslot]), qphase, abort))) {
+            ok = false;   // the warp aborts together
+            break;
+          }
+          const uint8_t *qrow = dyn_smem + (q_ring - dyn_base) + qslot * kQSlotBytes + r * kQRowBytes;
+          uint32_t cols[kDqSubsPerWarp][32];
+#pragma unroll
+          for (int i = 0; i < kDqSubsPerWarp; ++i) {
+            const uint32_t c = piece0 + (sub0 + i) * 2;
+            const uint4 qa = *reinterpret_cast<const uint4 *>(qrow + (((c + 0) ^ (r & 7u)) << 4));
+            const uint4 qb = *reinterpret_cast<const uint4 *>(qrow + (((c + 1) ^ (r & 7u)) << 4));
+            const __nv_bfloat16 sb = __ushort_as_bfloat16(sv[i]);
+            const __nv_bfloat162 s2v = __halves2bfloat162(sb, sb);
+            const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+            for (int j8 = 0; j8 < 8; ++j8) {
+              const uint4 d = dequant_word(words[j8], s2v);
+              cols[i][4 * j8 + 0] = d.x;
+              cols[i][4 * j8 + 1] = d.y;
+              cols[i][4 * j8 + 2] = d.z;
+              cols[i][4 * j8 + 3] = d.w;
+            }
+          }
           __syncwarp();
-          if (lane == 0) mbar_arrive(smem_addr(&ctl.qempty[rq.slot]));   // the loads above are done
+          if (lane == 0) {   // the loads above are done; a chunk holding one stage gets both arrivals
+            mbar_arrive(smem_addr(&ctl.qempty[qslot]));
+            if (kb == KB - 1 && (KB % kQChunkStages) != 0) mbar_arrive(smem_addr(&ctl.qempty[qslot]));
+          }
           if (!__all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.empty[rs.slot]), rs.phase ^ 1u, abort))) {
             ok = false;
-            continue;
+            break;
           }
           tc_fence_after_sync();   // the MMAs' reads of this TMEM stage precede the overwrite
-          tmem_st_x16(tmem_base + lane_field + a_slab_col(rs.slot, x >> 1) + col_off, cols);
+#pragma unroll
+          for (int i = 0; i < kDqSubsPerWarp; ++i)
+            tmem_st_x32(tmem_base + lane_field + a_slab_col(rs.slot, sub0 + i), cols[i]);
           tmem_st_wait();
           tc_fence_before_sync();
           __syncwarp();
@@ -891,11 +913,11 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
             const uint32_t full = full0 + rs.slot * static_cast<uint32_t>(sizeof(uint64_t));
             if constexpr (kPair) mbar_arrive_cluster(full); else mbar_arrive(full);
           }
-          rq.next(kQStages);
-          rs.next(ST);
         }
+        rs.next(ST);
       }
       if (!ok) break;
+      chunk_base += static_cast<uint32_t>((KB + kQChunkStages - 1) / kQChunkStages);
     }
     if (!ok) atomicOr(p.status, kStatusTimeout);
   }
