@@ -344,6 +344,10 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
   if (rc) return rc;
   fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K, max_tok(h, true));
   p.scales = static_cast<const __nv_bfloat16 *>(b_scales);
+  // Scale index of 64-K sub-slab j is j / (group_size / 64): a shift when that is a power of two.
+  p.scale_shift = -1;
+  for (int s = 0, g64 = group_size / gmm::kBK; (1 << s) <= g64; ++s)
+    if ((1 << s) == g64) p.scale_shift = s;
   p.group_size = group_size;
   return launch<true>(h, p, stream);
 }

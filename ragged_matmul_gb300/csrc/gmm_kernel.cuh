@@ -165,6 +165,7 @@ struct alignas(128) GmmParams {
   int num_stages;                // depth of the W+T stage ring
   const __nv_bfloat16 *scales;   // 4-bit path: [E, N, K / group_size]
   int group_size;                // 4-bit path: multiple of 64 dividing K
+  int scale_shift;               // 4-bit path: log2(group_size / 64) when that is a power of two, else -1
   int tok_band;                  // token blocks per band of the tile order (see decode_tile)
   uint32_t *tile_counter;        // workspace, 8-byte aligned, zero between launches: [0..1] one 64-bit claim
                                  // word (tiles claimed from the front | from the back << 32), [2] CTAs finished
@@ -353,23 +354,27 @@ __device__ __forceinline__ Tile decode_tile(uint32_t t, const uint32_t *prefix, 
 // into four bf16 pairs in K order (one TMEM column each): w_i = bf16((q_i - 8) * s).
 // 0x4300 | q is the bf16 encoding of 128 + q (q < 16 fits the 7-bit mantissa at
 // exponent 7), so subtracting 136 gives q - 8 exactly; the bf16x2 multiply then
-// rounds the exact product (q - 8) * s once, to nearest even.
+// rounds the exact product (q - 8) * s once, to nearest even.  The bytes are put in
+// place with byte permutes: the even nibbles (w & 0x0F0F0F0F) and the odd ones
+// ((w >> 4) & 0x0F0F0F0F, the shift done as a high multiply) are interleaved into
+// q0..q3 and q4..q7, and each pair then takes 0x43 as its high bytes.
 __device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
   const __nv_bfloat162 bias = __floats2bfloat162_rn(136.0f, 136.0f);
-  uint32_t pr[4];   // pr[i] = {w_i, w_{i+4}}
+  const uint32_t ev = w & 0x0F0F0F0Fu;                       // q0 q2 q4 q6
+  const uint32_t od = __umulhi(w, 1u << 28) & 0x0F0F0F0Fu;   // q1 q3 q5 q7
+  const uint32_t a = __byte_perm(ev, od, 0x5140);            // q0 q1 q2 q3
+  const uint32_t b = __byte_perm(ev, od, 0x7362);            // q4 q5 q6 q7
+  constexpr uint32_t kHi = 0x43434343u;
+  const uint32_t x[4] = {__byte_perm(a, kHi, 0x4140), __byte_perm(a, kHi, 0x4342),
+                         __byte_perm(b, kHi, 0x4140), __byte_perm(b, kHi, 0x4342)};
+  uint32_t out[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t x = ((w >> (4 * i)) & 0x000F000Fu) | 0x43004300u;
-    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&x);
+    __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&x[i]);
     v = __hmul2(__hsub2(v, bias), s2);
-    pr[i] = *reinterpret_cast<const uint32_t *>(&v);
+    out[i] = *reinterpret_cast<const uint32_t *>(&v);
   }
-  uint4 out;
-  out.x = __byte_perm(pr[0], pr[1], 0x5410);   // {w0, w1}
-  out.y = __byte_perm(pr[2], pr[3], 0x5410);   // {w2, w3}
-  out.z = __byte_perm(pr[0], pr[1], 0x7632);   // {w4, w5}
-  out.w = __byte_perm(pr[2], pr[3], 0x7632);   // {w6, w7}
-  return out;
+  return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // Reader of the tile queue (one thread).  Returns 1 with *tile set, 0 when the work
@@ -823,22 +828,26 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     // its row (8 packed words each) into 32 TMEM columns of bf16 pairs each.  The
     // arithmetic needs only the packed slab, so it runs as soon as the slab lands;
     // only the TMEM store waits for the slot (the MMAs that last read it completed).
-    // Stages of other groups just advance the ring positions: a slot cannot move past
-    // a phase this warp still waits for, because releasing it needs this warp's
-    // arrival.
+    // With as many groups as stage slots, group g always fills slot g, and its warps
+    // step straight from one of their stages to the next.  A slot cannot move past a
+    // phase this warp still waits for, because releasing it needs this warp's arrival.
+    static_assert(kDqGroups == static_cast<int>(kAStages), "group g always fills stage slot g");
     const uint32_t dw = static_cast<uint32_t>(warp - 7);
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
-    const uint32_t grp = dw / kDqWarpsPerStage;
+    const uint32_t grp = dw / kDqWarpsPerStage;   // also the stage slot this warp fills
     const uint32_t sub0 = ((dw % kDqWarpsPerStage) >> 2) * kDqSubsPerWarp;   // first sub-slab of this warp
     const uint32_t r = quad * 32u + static_cast<uint32_t>(lane);
     const int spr = p.K / p.group_size;   // scales per weight row
     const unsigned short *sbits = reinterpret_cast<const unsigned short *>(p.scales);
     const uint32_t lane_field = (quad * 32u) << 16;
-    Ring rs;                  // stage ring (token slab + TMEM weight slabs)
-    uint32_t stage_no = 0;    // stages seen, across tiles
+    const uint32_t kb_mod = static_cast<uint32_t>(KB) % kDqGroups;
+    uint32_t aphase = 0;      // phase of this warp's stage slot (flips on every use)
+    uint32_t base_mod = 0;    // stages of earlier tiles, modulo kDqGroups
     uint32_t chunk_base = 0;  // packed chunks of earlier tiles
-    // The stage's `full` barrier lives in the leader CTA of a pair.
-    const uint32_t full0 = kPair ? map_to_rank(smem_addr(&ctl.full[0]), 0) : smem_addr(&ctl.full[0]);
+    // The weight stage's `full` barrier lives in the leader CTA of a pair.
+    const uint32_t full_g = (kPair ? map_to_rank(smem_addr(&ctl.full[0]), 0) : smem_addr(&ctl.full[0])) +
+                            grp * static_cast<uint32_t>(sizeof(uint64_t));
+    const uint32_t empty_g = smem_addr(&ctl.empty[grp]);
     bool ok = true;
     TileSource reader(dynamic, unit0, units, total);
     for (;;) {
@@ -851,72 +860,71 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const uint32_t n = ti.n0 + rank * kBlockN + r;
       const bool row_ok = n < static_cast<uint32_t>(p.N);
       const unsigned short *srow = sbits + (static_cast<size_t>(ti.e) * p.N + (row_ok ? n : 0)) * spr;
-      for (int kb = 0; kb < KB && ok; ++kb) {
-        const bool mine = (stage_no % kDqGroups) == grp;
-        ++stage_no;
-        if (mine) {
-          // Scales of this thread's sub-slabs; zero past K (the last stage's second
-          // half when K is an odd multiple of 64) or past N, so the weights there are
-          // zero, matching the zero-filled tokens.  Loaded first: the waits below
-          // cover their latency.
-          unsigned short sv[kDqSubsPerWarp];
+      // This group's stages of the tile: kb = kb0, kb0 + kDqGroups, ...
+      const int kb0 = static_cast<int>((grp + kDqGroups - base_mod) % kDqGroups);
+      for (int kb = kb0; kb < KB && ok; kb += kDqGroups) {
+        // Scales of this thread's sub-slabs; zero past K (the last stage's second
+        // half when K is an odd multiple of 64) or past N, so the weights there are
+        // zero, matching the zero-filled tokens.  Loaded first: the waits below
+        // cover their latency.
+        unsigned short sv[kDqSubsPerWarp];
 #pragma unroll
-          for (int i = 0; i < kDqSubsPerWarp; ++i) {
-            const int k0 = (kb * kSub4 + static_cast<int>(sub0) + i) * kBK;
-            sv[i] = (row_ok && k0 < p.K) ? __ldg(srow + k0 / p.group_size) : static_cast<unsigned short>(0);
-          }
-          // Packed chunk of this stage (slot and phase from the chunk count) and the
-          // stage's half of it; 16-byte piece c of row r sits at piece c ^ (r % 8).
-          const uint32_t chunk = chunk_base + static_cast<uint32_t>(kb) / kQChunkStages;
-          const uint32_t qslot = chunk % kQStages, qphase = (chunk / kQStages) & 1u;
-          const uint32_t piece0 = (static_cast<uint32_t>(kb) % kQChunkStages) * (kSub4 * 2);
-          if (!__all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.qfull[qslot]), qphase, abort))) {
-            ok = false;   // the warp aborts together
-            break;
-          }
-          const uint8_t *qrow = dyn_smem + (q_ring - dyn_base) + qslot * kQSlotBytes + r * kQRowBytes;
-          uint32_t cols[kDqSubsPerWarp][32];
+        for (int i = 0; i < kDqSubsPerWarp; ++i) {
+          const int sub = kb * kSub4 + static_cast<int>(sub0) + i;   // 64-K sub-slab along K
+          const int idx = p.scale_shift >= 0 ? (sub >> p.scale_shift) : sub * kBK / p.group_size;
+          sv[i] = (row_ok && sub * kBK < p.K) ? __ldg(srow + idx) : static_cast<unsigned short>(0);
+        }
+        // Packed chunk of this stage (slot and phase from the chunk count) and the
+        // stage's half of it; 16-byte piece c of row r sits at piece c ^ (r % 8).
+        const uint32_t chunk = chunk_base + static_cast<uint32_t>(kb) / kQChunkStages;
+        const uint32_t qslot = chunk % kQStages, qphase = (chunk / kQStages) & 1u;
+        const uint32_t piece0 = (static_cast<uint32_t>(kb) % kQChunkStages) * (kSub4 * 2);
+        if (!__all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.qfull[qslot]), qphase, abort))) {
+          ok = false;   // the warp aborts together
+          break;
+        }
+        const uint8_t *qrow = dyn_smem + (q_ring - dyn_base) + qslot * kQSlotBytes + r * kQRowBytes;
+        uint32_t cols[kDqSubsPerWarp][32];
 #pragma unroll
-          for (int i = 0; i < kDqSubsPerWarp; ++i) {
-            const uint32_t c = piece0 + (sub0 + i) * 2;
-            const uint4 qa = *reinterpret_cast<const uint4 *>(qrow + (((c + 0) ^ (r & 7u)) << 4));
-            const uint4 qb = *reinterpret_cast<const uint4 *>(qrow + (((c + 1) ^ (r & 7u)) << 4));
-            const __nv_bfloat16 sb = __ushort_as_bfloat16(sv[i]);
-            const __nv_bfloat162 s2v = __halves2bfloat162(sb, sb);
-            const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+        for (int i = 0; i < kDqSubsPerWarp; ++i) {
+          const uint32_t c = piece0 + (sub0 + i) * 2;
+          const uint4 qa = *reinterpret_cast<const uint4 *>(qrow + (((c + 0) ^ (r & 7u)) << 4));
+          const uint4 qb = *reinterpret_cast<const uint4 *>(qrow + (((c + 1) ^ (r & 7u)) << 4));
+          const __nv_bfloat16 sb = __ushort_as_bfloat16(sv[i]);
+          const __nv_bfloat162 s2v = __halves2bfloat162(sb, sb);
+          const uint32_t words[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-            for (int j8 = 0; j8 < 8; ++j8) {
-              const uint4 d = dequant_word(words[j8], s2v);
-              cols[i][4 * j8 + 0] = d.x;
-              cols[i][4 * j8 + 1] = d.y;
-              cols[i][4 * j8 + 2] = d.z;
-              cols[i][4 * j8 + 3] = d.w;
-            }
-          }
-          __syncwarp();
-          if (lane == 0) {   // the loads above are done; a chunk holding one stage gets both arrivals
-            mbar_arrive(smem_addr(&ctl.qempty[qslot]));
-            if (kb == KB - 1 && (KB % kQChunkStages) != 0) mbar_arrive(smem_addr(&ctl.qempty[qslot]));
-          }
-          if (!__all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.empty[rs.slot]), rs.phase ^ 1u, abort))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();   // the MMAs' reads of this TMEM stage precede the overwrite
-#pragma unroll
-          for (int i = 0; i < kDqSubsPerWarp; ++i)
-            tmem_st_x32(tmem_base + lane_field + a_slab_col(rs.slot, sub0 + i), cols[i]);
-          tmem_st_wait();
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) {
-            const uint32_t full = full0 + rs.slot * static_cast<uint32_t>(sizeof(uint64_t));
-            if constexpr (kPair) mbar_arrive_cluster(full); else mbar_arrive(full);
+          for (int j8 = 0; j8 < 8; ++j8) {
+            const uint4 d = dequant_word(words[j8], s2v);
+            cols[i][4 * j8 + 0] = d.x;
+            cols[i][4 * j8 + 1] = d.y;
+            cols[i][4 * j8 + 2] = d.z;
+            cols[i][4 * j8 + 3] = d.w;
           }
         }
-        rs.next(ST);
+        __syncwarp();
+        if (lane == 0) {   // the loads above are done; a chunk holding one stage gets both arrivals
+          mbar_arrive(smem_addr(&ctl.qempty[qslot]));
+          if (kb == KB - 1 && (KB % kQChunkStages) != 0) mbar_arrive(smem_addr(&ctl.qempty[qslot]));
+        }
+        if (!__all_sync(0xffffffffu, wait_phase(empty_g, aphase ^ 1u, abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();   // the MMAs' reads of this TMEM stage precede the overwrite
+#pragma unroll
+        for (int i = 0; i < kDqSubsPerWarp; ++i)
+          tmem_st_x32(tmem_base + lane_field + a_slab_col(grp, sub0 + i), cols[i]);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          if constexpr (kPair) mbar_arrive_cluster(full_g); else mbar_arrive(full_g);
+        }
+        aphase ^= 1u;
       }
       if (!ok) break;
+      base_mod = (base_mod + kb_mod) % kDqGroups;
       chunk_base += static_cast<uint32_t>((KB + kQChunkStages - 1) / kQChunkStages);
     }
     if (!ok) atomicOr(p.status, kStatusTimeout);

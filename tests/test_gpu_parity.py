@@ -245,10 +245,11 @@ def test_int4_random(gs, variant):
     assert status == binding.GMM_OK
 
 
-@pytest.mark.parametrize("N,K,gs", [(136, 192, 64), (200, 320, 64), (128, 64, 64), (72, 1088, 64)])
+@pytest.mark.parametrize("N,K,gs", [(136, 192, 64), (200, 320, 64), (128, 64, 64), (72, 1088, 64), (136, 576, 192)])
 def test_int4_k_and_n_tails(N, K, gs):
-    """K an odd multiple of 64 (the last 128-wide K stage has one half past K) and N
-    not a multiple of 128 (rows past N in the last weight block)."""
+    """K an odd multiple of 64 (the last 128-wide K stage has one half past K), N not a
+    multiple of 128 (rows past N in the last weight block), and a group size that is
+    not a power-of-two multiple of 64."""
     r = routing(5, N, K, [1, 17, 160, 161, 40], [4, 0, 2, 3, -1], dist=("normal", 1.0), int4=True, gs=gs)
     v = wl.host_values(r, 15)
     _, _, status, _ = check_against_oracle(handle(5), r, v, where=f"int4 tails N={N} K={K}")
