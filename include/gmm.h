@@ -106,8 +106,8 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
  * It computes exactly what gmm_run computes, with the same kernel, on the CALLER'S
  * CURRENT DEVICE (all pointers must live there), and needs no handle: num_experts is
  * passed directly.  The caller still provides every input and output buffer.  The
- * kernel's scratch (a status word and one 256-byte tensor-map slot per CTA) comes from
- * a fixed array compiled into the library, 65,792 bytes on every GPU that loads it,
+ * kernel's scratch (a status word and one 2 KB slot of tensor maps per CTA) comes from
+ * a fixed array compiled into the library, 524,544 bytes on every GPU that loads it,
  * held until the process exits.  That array has slots for at most 256 CTAs; the grid
  * is one CTA per SM, so a device with more than 256 SMs gets GMM_ERR_UNSUPPORTED.
  *

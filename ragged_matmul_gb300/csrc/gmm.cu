@@ -71,17 +71,14 @@ int encode_map(gmm_ctx *h, CUtensorMap *m, CUtensorMapDataType type, uint32_t ra
   return r == CUDA_SUCCESS ? GMM_OK : GMM_ERR_CUDA;
 }
 
-// Token (A) maps: {K, rows} bf16 with 128-row and 16-row boxes.  The row extent
-// written here is a placeholder: the kernel patches it to a_offsets[G].
+// Token (A) map: {K, rows} bf16, 128-byte swizzle.  The row extent and the box height
+// written here are placeholders: each CTA derives one map per box height from it and
+// patches the extent to a_offsets[G].
 int encode_token_maps(gmm_ctx *h, GmmParams &p, const void *a, int K) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), 256};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  cuuint32_t box128[2] = {gmm::kBK, 128};
-  cuuint32_t box16[2] = {gmm::kBK, 16};
-  int rc = encode_map(h, &p.tok_map128, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, dims, strides, box128,
-                      CU_TENSOR_MAP_SWIZZLE_128B);
-  if (rc) return rc;
-  return encode_map(h, &p.tok_map16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, dims, strides, box16,
+  cuuint32_t box[2] = {gmm::kBK, 128};
+  return encode_map(h, &p.tok_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -391,7 +388,7 @@ constexpr int kNoAllocMaxCtas = 256;   // persistent grid = SM count; 152 on GB3
 constexpr size_t kNoAllocScratchBytes = kStatusBytes + static_cast<size_t>(kNoAllocMaxCtas) * gmm::kMapSlotBytes;
 constexpr int kNoAllocMaxDevices = 64;
 
-static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];   // 65,792 bytes
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];   // 524,544 bytes
 
 struct NoAllocDevice {
   bool ready = false;

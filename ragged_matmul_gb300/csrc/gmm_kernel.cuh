@@ -111,7 +111,8 @@ __device__ __forceinline__ uint32_t a_slab_col(uint32_t stage, uint32_t sub) {
   const uint32_t i = stage * kSub4 + sub;   // 0..5
   return i < 3 ? 160u + 32u * i : 416u + 32u * (i - 3u);
 }
-constexpr int kMapSlotBytes = 256;            // per-CTA workspace: two patched 128-byte tensor maps
+constexpr int kTokMaps = 16;                  // token maps per CTA: boxes of 16, 32, ..., 256 rows
+constexpr int kMapSlotBytes = kTokMaps * 128; // per-CTA workspace: the patched 128-byte token maps
 constexpr int kTileQueue = 4;                 // entries of the shared-memory tile queue
 constexpr uint32_t kDynamicTilesPerUnit = 16; // bf16: dynamic tile claiming from this many tiles per CTA (pair)
 constexpr uint32_t kDynamicTilesPerUnit4 = 8; // 4-bit: the same (its tiles are longer, measured better lower)
@@ -136,7 +137,9 @@ struct Geom {
   // deep: its MMA per stage is short (about 128 tokens), and the token copies come
   // from L2 with microsecond latency.
   static constexpr uint32_t kMaxTok = kInt4 ? 160 : 256;   // 4-bit: also bounded by the TMEM layout above
-  static constexpr uint32_t kTSlot = (kPair ? kMaxTok / 2 : kMaxTok) * kBK * 2;   // token slab per CTA
+  static constexpr uint32_t kCtaTok = kPair ? kMaxTok / 2 : kMaxTok;   // token rows one CTA loads, at most
+  static constexpr uint32_t kTSlot = kCtaTok * kBK * 2;                 // token slab per CTA
+  static_assert(kCtaTok % 16 == 0 && kCtaTok / 16 <= kTokMaps, "a token map per 16-row slab height");
   static_assert(kTSlot % 1024 == 0, "token slabs must keep the 1024-byte swizzle alignment");
   // 64-wide K sub-slabs per pipeline stage.  The bf16 pair kernel takes 128 of K per
   // stage (8 MMAs per barrier wait and commit): the MMA thread's fixed cost per stage
@@ -150,8 +153,8 @@ struct Geom {
 struct alignas(128) GmmParams {
   CUtensorMap w_map;       // bf16 path: B {K, N, E}, box {64, 128, 1}, 128 B swizzle
                            // 4-bit path: packed words {K/8, N, E}, box {8, 128, 1}, no swizzle
-  CUtensorMap tok_map128;  // A bf16 {K, rows}, box {64, 128} (rows patched on the device)
-  CUtensorMap tok_map16;   // A bf16 {K, rows}, box {64, 16}  (rows patched on the device)
+  CUtensorMap tok_map;     // A bf16 {K, rows}, box {64, 128}; each CTA derives from it one map per
+                           // box height (16, 32, ... rows) and patches the row extent on the device
   __nv_bfloat16 *c;
   const uint32_t *a_offsets;
   const int32_t *expert_ids;
@@ -521,23 +524,23 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ token (and bf16 weight) producer
-    if (lane == 0 && total > 0) {
-      uint8_t *slot = p.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlotBytes;
-      const uint4 *src128 = reinterpret_cast<const uint4 *>(&p.tok_map128);
-      const uint4 *src16 = reinterpret_cast<const uint4 *>(&p.tok_map16);
-      uint4 *dst = reinterpret_cast<uint4 *>(slot);
+    // Token maps: lane i builds the map whose copies are 16 (i + 1) rows high, so a
+    // tile's token slab (a multiple of 16 rows) is one copy per 64-K sub-slab.
+    constexpr int kMaps = static_cast<int>(G::kCtaTok / 16);
+    uint8_t *slot = p.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlotBytes;
+    if (total > 0 && lane < kMaps) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(&p.tok_map);
+      uint4 *dst = reinterpret_cast<uint4 *>(slot + lane * 128);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        dst[i] = src128[i];
-        dst[8 + i] = src16[i];
-      }
-      const uint32_t rows = __ldg(p.a_offsets + p.num_groups);
-      tensormap_set_dim1(slot, rows);
-      tensormap_set_dim1(slot + 128, rows);
-      tensormap_publish(slot);
-      tensormap_publish(slot + 128);
-      const CUtensorMap *tok128 = reinterpret_cast<const CUtensorMap *>(slot);
-      const CUtensorMap *tok16 = reinterpret_cast<const CUtensorMap *>(slot + 128);
+      for (int i = 0; i < 8; ++i) dst[i] = src[i];
+      tensormap_set_dim1(dst, __ldg(p.a_offsets + p.num_groups));
+      tensormap_set_box1(dst, 16u * static_cast<uint32_t>(lane + 1));
+      tensormap_release();
+    }
+    __syncwarp();
+    if (lane == 0 && total > 0) {
+      for (int i = 0; i < kMaps; ++i) tensormap_acquire(slot + i * 128);
+      const CUtensorMap *tok_maps = reinterpret_cast<const CUtensorMap *>(slot);
       prefetch_tensormap(&p.w_map);
       const uint64_t pol_first = l2_policy_evict_first();
       const uint64_t pol_last = l2_policy_evict_last();
@@ -624,22 +627,16 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
             // +sub*kTSlot.  A sub-slab past K is zero-filled by TMA and adds nothing.
             const int32_t k0 = (kb * static_cast<int32_t>(G::kSub) + static_cast<int32_t>(sub)) * kBK;
             const uint32_t dst_w = w_ring + (rt.slot * G::kSub + sub) * kWBytes;
-            uint32_t dst_t = t_ring + (rt.slot * G::kSub + sub) * G::kTSlot;
-            int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok);
-            uint32_t left = my_tok;
+            const uint32_t dst_t = t_ring + (rt.slot * G::kSub + sub) * G::kTSlot;
+            const int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok);
+            const CUtensorMap *tok = tok_maps + (my_tok / 16u - 1u);   // copies my_tok rows high
             if constexpr (kPair) {
               const uint32_t full_leader = map_to_rank(full_local, 0);
               if (!kInt4) tma_load_3d_pair(dst_w, &p.w_map, full_leader, k0, w_row, ti.e, w_pol);
-              for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
-                tma_load_2d_pair(dst_t, tok128, full_leader, k0, r, t_pol);
-              for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
-                tma_load_2d_pair(dst_t, tok16, full_leader, k0, r, t_pol);
+              tma_load_2d_pair(dst_t, tok, full_leader, k0, r, t_pol);
             } else {
               if (!kInt4) tma_load_3d_hint(dst_w, &p.w_map, full_local, k0, w_row, ti.e, w_pol);
-              for (; left >= 128; left -= 128, r += 128, dst_t += 128 * kBK * 2)
-                tma_load_2d_hint(dst_t, tok128, full_local, k0, r, t_pol);
-              for (; left > 0; left -= 16, r += 16, dst_t += 16 * kBK * 2)
-                tma_load_2d_hint(dst_t, tok16, full_local, k0, r, t_pol);
+              tma_load_2d_hint(dst_t, tok, full_local, k0, r, t_pol);
             }
           }
           pending |= 1u << rt.slot;

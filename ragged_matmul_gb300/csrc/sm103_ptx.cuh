@@ -144,10 +144,22 @@ __device__ __forceinline__ void tensormap_set_dim1(void *gmap, uint32_t extent) 
                : "memory");
 }
 
-// Publish generic-proxy writes of a global tensor map to the tensor-map proxy
-// used by this thread's later bulk tensor copies.
-__device__ __forceinline__ void tensormap_publish(const void *gmap) {
+// Rewrite the box size of dimension 1 (rows per copy) of a tensor map in global memory.
+__device__ __forceinline__ void tensormap_set_box1(void *gmap, uint32_t rows) {
+  asm volatile("tensormap.replace.tile.box_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(
+                   reinterpret_cast<uint64_t>(gmap)),
+               "r"(rows)
+               : "memory");
+}
+
+// Make generic-proxy writes of global tensor maps (this thread's) visible to the
+// tensor-map proxy, for any thread that acquires them afterwards.
+__device__ __forceinline__ void tensormap_release() {
   asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
+}
+
+// Acquire a global tensor map for this thread's later bulk tensor copies.
+__device__ __forceinline__ void tensormap_acquire(const void *gmap) {
   asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
                    reinterpret_cast<uint64_t>(gmap))
                : "memory");
