@@ -71,14 +71,25 @@ int encode_map(gmm_ctx *h, CUtensorMap *m, CUtensorMapDataType type, uint32_t ra
   return r == CUDA_SUCCESS ? GMM_OK : GMM_ERR_CUDA;
 }
 
-// Token (A) map: {K, rows} bf16, 128-byte swizzle.  The row extent and the box height
-// written here are placeholders: each CTA derives one map per box height from it and
-// patches the extent to a_offsets[G].
-int encode_token_maps(gmm_ctx *h, GmmParams &p, const void *a, int K) {
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), 256};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-  cuuint32_t box[2] = {gmm::kBK, 128};
-  return encode_map(h, &p.tok_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, dims, strides, box,
+// Token (A) map, 128-byte swizzle.  The row extent and the box height written here
+// are placeholders: each CTA derives one map per box height from it and patches the
+// extent to a_offsets[G].
+//   2-D {K, rows}, box {64, rows}: one 64-K sub-slab per copy (any K).
+//   3-D {64, rows, K / 64} (strides: a row, then 128 bytes to the next 64 of K), box
+//   {64, rows, sub}: `sub` sub-slabs of a stage in one copy, landing one after the
+//   other in shared memory.  Only when K is a multiple of 64 (the 4-bit path).
+int encode_token_maps(gmm_ctx *h, GmmParams &p, const void *a, int K, int sub_per_copy) {
+  if (sub_per_copy == 1) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), 256};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    cuuint32_t box[2] = {gmm::kBK, 128};
+    return encode_map(h, &p.tok_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, dims, strides, box,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(gmm::kBK), 256, static_cast<cuuint64_t>(K / gmm::kBK)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(gmm::kBK) * 2};
+  cuuint32_t box[3] = {gmm::kBK, 128, static_cast<cuuint32_t>(sub_per_copy)};
+  return encode_map(h, &p.tok_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -308,7 +319,7 @@ int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, c
                     CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
-  rc = encode_token_maps(h, p, a, K);
+  rc = encode_token_maps(h, p, a, K, 1);
   if (rc) return rc;
   fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K, max_tok(h, false));
   return launch<false>(h, p, stream);
@@ -337,7 +348,7 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
                     CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
-  rc = encode_token_maps(h, p, a, K);
+  rc = encode_token_maps(h, p, a, K, gmm::kSub4);
   if (rc) return rc;
   fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K, max_tok(h, true));
   p.scales = static_cast<const __nv_bfloat16 *>(b_scales);
@@ -471,7 +482,7 @@ extern "C" int gmm_run_noalloc(void *c, const void *a, const uint32_t *a_offsets
                     CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
-  rc = encode_token_maps(h, p, a, K);
+  rc = encode_token_maps(h, p, a, K, 1);
   if (rc) return rc;
   fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K, max_tok(h, false));
   p.num_experts = num_experts;

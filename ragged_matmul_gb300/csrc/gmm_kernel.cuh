@@ -224,6 +224,7 @@ struct Ring {
 // epilogue and MMA-issuing warps of its SM need; the abort flag and the clock are
 // checked after every test.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (mbar_test_wait(bar, parity)) return true;   // already complete: no potentially blocking test
   if (mbar_try_wait_hint(bar, parity, kSuspendNs)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
@@ -238,6 +239,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 
 // The same with cluster-scope acquire, for barriers the peer CTA arrives on.
 __device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, volatile int *abort) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
   if (mbar_try_wait_cluster_hint(bar, parity, kSuspendNs)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
@@ -621,21 +623,29 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           const uint32_t full_local = smem_addr(&ctl.full[rt.slot]);
           if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
           if (rank == 0) mbar_arrive_expect_tx(full_local, tx);
+          const int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok);
+          const CUtensorMap *tok = tok_maps + (my_tok / 16u - 1u);   // copies my_tok rows high
+          if constexpr (kInt4) {
+            // All kSub sub-slabs of the stage in one copy (3-D token map): sub-slab s
+            // lands at +s * my_tok rows; one past K is zero-filled by TMA.
+            const uint32_t dst_t = t_ring + rt.slot * G::kSub * G::kTSlot;
+            const int32_t s0 = kb * static_cast<int32_t>(G::kSub);
+            if constexpr (kPair) tma_load_3d_pair(dst_t, tok, map_to_rank(full_local, 0), 0, r, s0, t_pol);
+            else tma_load_3d_hint(dst_t, tok, full_local, 0, r, s0, t_pol);
+          }
 #pragma unroll
-          for (uint32_t sub = 0; sub < G::kSub; ++sub) {
+          for (uint32_t sub = 0; sub < G::kSub && !kInt4; ++sub) {
             // Sub-slab `sub` of the stage: K from k0, weights at +sub*16 KB, tokens at
             // +sub*kTSlot.  A sub-slab past K is zero-filled by TMA and adds nothing.
             const int32_t k0 = (kb * static_cast<int32_t>(G::kSub) + static_cast<int32_t>(sub)) * kBK;
             const uint32_t dst_w = w_ring + (rt.slot * G::kSub + sub) * kWBytes;
             const uint32_t dst_t = t_ring + (rt.slot * G::kSub + sub) * G::kTSlot;
-            const int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok);
-            const CUtensorMap *tok = tok_maps + (my_tok / 16u - 1u);   // copies my_tok rows high
             if constexpr (kPair) {
               const uint32_t full_leader = map_to_rank(full_local, 0);
-              if (!kInt4) tma_load_3d_pair(dst_w, &p.w_map, full_leader, k0, w_row, ti.e, w_pol);
+              tma_load_3d_pair(dst_w, &p.w_map, full_leader, k0, w_row, ti.e, w_pol);
               tma_load_2d_pair(dst_t, tok, full_leader, k0, r, t_pol);
             } else {
-              if (!kInt4) tma_load_3d_hint(dst_w, &p.w_map, full_local, k0, w_row, ti.e, w_pol);
+              tma_load_3d_hint(dst_w, &p.w_map, full_local, k0, w_row, ti.e, w_pol);
               tma_load_2d_hint(dst_t, tok, full_local, k0, r, t_pol);
             }
           }
@@ -698,7 +708,10 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           tc_fence_after_sync();
 #pragma unroll
           for (uint32_t sub = 0; sub < G::kSub; ++sub) {
-            const uint64_t b_desc = t_desc0 + (((rt.slot * G::kSub + sub) * G::kTSlot) >> 4);
+            // 4-bit: the stage's sub-slabs sit my_tok rows apart (one 3-D copy); bf16: kTSlot apart.
+            const uint32_t b_off = kInt4 ? rt.slot * G::kSub * G::kTSlot + sub * (kPair ? ti.ntok / 2 : ti.ntok) * (kBK * 2)
+                                         : (rt.slot * G::kSub + sub) * G::kTSlot;
+            const uint64_t b_desc = t_desc0 + (b_off >> 4);
             if constexpr (kInt4) {
               const uint32_t a_tmem = tmem_base + a_slab_col(rt.slot, sub);
 #pragma unroll
