@@ -113,7 +113,7 @@ __device__ __forceinline__ uint32_t a_slab_col(uint32_t stage, uint32_t sub) {
 }
 constexpr int kTokMaps = 16;                  // token maps per CTA: boxes of 16, 32, ..., 256 rows
 constexpr int kMapSlotBytes = kTokMaps * 128; // per-CTA workspace: the patched 128-byte token maps
-constexpr int kTileQueue = 4;                 // entries of the shared-memory tile queue
+constexpr int kTileQueue = 8;                 // entries of the shared-memory tile queue
 constexpr uint32_t kDynamicTilesPerUnit = 16; // bf16: dynamic tile claiming from this many tiles per CTA (pair)
 constexpr uint32_t kDynamicTilesPerUnit4 = 8; // 4-bit: the same (its tiles are longer, measured better lower)
 constexpr uint32_t kUnevenRatio = 4;          // groups this uneven get the two-ended claim order
@@ -196,6 +196,7 @@ struct __align__(8) Ctrl {
   uint64_t tq_full[kTileQueue];  // tile queue entry published
   uint64_t tq_empty[kTileQueue]; // every reader has taken the entry (pair: both CTAs', on the leader)
   uint32_t tq_tile[kTileQueue];
+  Tile tq_info[kTileQueue];      // the entry's tile, decoded once by the publisher
   uint32_t tmem_base;
   int abort;
   uint32_t total_tiles;
@@ -382,19 +383,30 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, __nv_bfloat162 s2) {
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-// Reader of the tile queue (one thread).  Returns 1 with *tile set, 0 when the work
-// is done, -1 when a wait gave up.  `empty0` is the address of the leader CTA's
-// tq_empty[0] (a cluster address in the pair's second CTA, which then arrives
-// remotely; that CTA's entries are published by the leader, so it waits with
-// cluster scope).
+// Reader of the tile queue (one thread).  Returns 1 with *tile and *info set (the
+// publisher decodes each tile once and stores it with the entry, so readers need no
+// global loads), 0 when the work is done, -1 when a wait gave up.  `empty0` is the
+// address of the leader CTA's tq_empty[0] (a cluster address in the pair's second
+// CTA, which then arrives remotely; that CTA's entries are published by the leader,
+// so it waits with cluster scope).  The entry is copied out before the arrive that
+// lets the publisher reuse it.
 struct TileQueueReader {
   uint32_t pos = 0;
   __device__ __forceinline__ int next(Ctrl &ctl, uint32_t empty0, bool remote, volatile int *abort,
-                                      uint32_t *tile) {
+                                      uint32_t *tile, Tile *info) {
     const uint32_t slot = pos % kTileQueue, parity = (pos / kTileQueue) & 1u;
     const uint32_t full = smem_addr(&ctl.tq_full[slot]);
     if (!(remote ? wait_phase_cluster(full, parity, abort) : wait_phase(full, parity, abort))) return -1;
     *tile = *reinterpret_cast<volatile uint32_t *>(&ctl.tq_tile[slot]);
+    if (*tile != kNoTile) {
+      const volatile Tile &src = ctl.tq_info[slot];
+      info->e = src.e;
+      info->single_block = src.single_block;
+      info->row0 = src.row0;
+      info->nrows = src.nrows;
+      info->ntok = src.ntok;
+      info->n0 = src.n0;
+    }
     const uint32_t empty = empty0 + slot * static_cast<uint32_t>(sizeof(uint64_t));
     if (remote) mbar_arrive_cluster(empty); else mbar_arrive(empty);
     ++pos;
@@ -403,34 +415,45 @@ struct TileQueueReader {
 };
 
 // Where a role gets its tiles: with few tiles per CTA the static round-robin share
-// (unit, unit + units, ...), computed by every role itself; with many, the queue.
+// (unit, unit + units, ...), computed and decoded by every role itself; with many,
+// the queue.
 struct TileSource {
   bool dynamic;
   uint32_t next_static, units, total;
   TileQueueReader q;
   __device__ __forceinline__ TileSource(bool dyn, uint32_t unit0, uint32_t units_, uint32_t total_)
       : dynamic(dyn), next_static(unit0), units(units_), total(total_) {}
+  template <class G>
   __device__ __forceinline__ int next(Ctrl &ctl, uint32_t empty0, bool remote, volatile int *abort,
-                                      uint32_t *tile) {
+                                      const uint32_t *prefix, const GmmParams &p, Tile *info) {
+    uint32_t tile;
     if (!dynamic) {
       if (next_static >= total) return 0;
-      *tile = next_static;
+      tile = next_static;
       next_static += units;
+      *info = decode_tile<G>(tile, prefix, p);
       return 1;
     }
-    return q.next(ctl, empty0, remote, abort, tile);
+    return q.next(ctl, empty0, remote, abort, &tile, info);
   }
 };
 
-// The same for a whole warp: lane 0 reads, the warp agrees.
+// The same for a whole warp: lane 0 reads the queue, the warp agrees.
+template <class G>
 __device__ __forceinline__ int next_tile_warp(TileSource &src, Ctrl &ctl, uint32_t empty0, bool remote,
-                                              volatile int *abort, uint32_t *tile) {
-  if (!src.dynamic) return src.next(ctl, empty0, remote, abort, tile);
+                                              volatile int *abort, const uint32_t *prefix, const GmmParams &p,
+                                              Tile *info) {
+  if (!src.dynamic) return src.next<G>(ctl, empty0, remote, abort, prefix, p, info);
   int r = 0;
-  uint32_t t = kNoTile;
-  if ((threadIdx.x & 31) == 0) r = src.next(ctl, empty0, remote, abort, &t);
+  Tile x{};
+  if ((threadIdx.x & 31) == 0) r = src.next<G>(ctl, empty0, remote, abort, prefix, p, &x);
   r = __shfl_sync(0xffffffffu, r, 0);
-  *tile = __shfl_sync(0xffffffffu, t, 0);
+  info->e = __shfl_sync(0xffffffffu, x.e, 0);
+  info->single_block = __shfl_sync(0xffffffffu, x.single_block, 0);
+  info->row0 = __shfl_sync(0xffffffffu, x.row0, 0);
+  info->nrows = __shfl_sync(0xffffffffu, x.nrows, 0);
+  info->ntok = __shfl_sync(0xffffffffu, x.ntok, 0);
+  info->n0 = __shfl_sync(0xffffffffu, x.n0, 0);
   return r;
 }
 
@@ -581,8 +604,14 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         if (!(kPair ? wait_phase_cluster(empty, parity ^ 1u, abort) : wait_phase(empty, parity ^ 1u, abort)))
           return false;
         ctl.tq_tile[slot] = t;
+        const Tile x = t == kNoTile ? Tile{} : decode_tile<G>(t, prefix, p);
+        ctl.tq_info[slot] = x;
         if constexpr (kPair) {   // the second CTA's copy of the entry, then its signal
           st_shared_cluster_u32(map_to_rank(smem_addr(&ctl.tq_tile[slot]), 1), t);
+          const uint32_t *xw = reinterpret_cast<const uint32_t *>(&x);
+          const uint32_t info1 = map_to_rank(smem_addr(&ctl.tq_info[slot]), 1);
+#pragma unroll
+          for (int i = 0; i < static_cast<int>(sizeof(Tile) / 4); ++i) st_shared_cluster_u32(info1 + 4u * i, xw[i]);
           mbar_arrive_cluster(map_to_rank(smem_addr(&ctl.tq_full[slot]), 1));
         }
         mbar_arrive(smem_addr(&ctl.tq_full[slot]));
@@ -598,18 +627,17 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         ok = publish(cur) && (cur == kNoTile || publish(nxt));
       }
       for (; ok;) {
-        uint32_t tile;
+        Tile ti;
         uint32_t after = kNoTile;   // claimed now, published when `nxt` starts
         if (publisher) {
-          tile = cur;
-          if (tile == kNoTile) break;
+          if (cur == kNoTile) break;
+          ti = decode_tile<G>(cur, prefix, p);
           if (nxt != kNoTile) after = claim();
         } else {
-          const int got = reader.next(ctl, q_empty0, q_remote, abort, &tile);
+          const int got = reader.next<G>(ctl, q_empty0, q_remote, abort, prefix, p, &ti);
           if (got < 0) ok = false;
           if (got <= 0) break;
         }
-        const Tile ti = decode_tile<G>(tile, prefix, p);
         const uint32_t my_tok = kPair ? ti.ntok / 2 : ti.ntok;     // token rows this CTA loads
         const uint32_t tx =
             (kPair ? 2u : 1u) * G::kSub * ((kInt4 ? 0u : static_cast<uint32_t>(kWBytes)) + my_tok * (kBK * 2));
@@ -686,11 +714,10 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const uint64_t t_desc0 = smem_desc_k_sw128(t_ring);
       const uint64_t w_desc0 = smem_desc_k_sw128(w_ring);
       for (;;) {
-        uint32_t tile;
-        const int got = next_tile_warp(reader, ctl, q_empty0, q_remote, abort, &tile);
+        Tile ti;
+        const int got = next_tile_warp<G>(reader, ctl, q_empty0, q_remote, abort, prefix, p, &ti);
         if (got < 0) ok = false;
         if (got <= 0) break;
-        const Tile ti = decode_tile<G>(tile, prefix, p);
         const bool acc_free = __all_sync(
             0xffffffffu, kPair ? wait_phase_cluster(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort)
                                : wait_phase(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort));
@@ -755,11 +782,10 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     TileSource reader(dynamic, unit0, units, total);
     for (;;) {
       if (total == 0) break;
-      uint32_t tile;
-      const int got = next_tile_warp(reader, ctl, q_empty0, q_remote, abort, &tile);
+      Tile ti;
+      const int got = next_tile_warp<G>(reader, ctl, q_empty0, q_remote, abort, prefix, p, &ti);
       if (got < 0 && lane == 0) atomicOr(p.status, kStatusTimeout);
       if (got <= 0) break;
-      const Tile ti = decode_tile<G>(tile, prefix, p);
       int ok = 1;
       if (lane == 0) ok = wait_phase(smem_addr(&ctl.acc_full[acc]), acc_phase, abort);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -803,11 +829,10 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       bool ok = true;
       TileSource reader(dynamic, unit0, units, total);
       for (;;) {
-        uint32_t tile;
-        const int got = reader.next(ctl, q_empty0, q_remote, abort, &tile);
+        Tile ti;
+        const int got = reader.next<G>(ctl, q_empty0, q_remote, abort, prefix, p, &ti);
         if (got < 0) ok = false;
         if (got <= 0) break;
-        const Tile ti = decode_tile<G>(tile, prefix, p);
         const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * kBlockN);
         const uint64_t pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
         const int KC = (KB + kQChunkStages - 1) / kQChunkStages;   // chunks of the tile
@@ -862,11 +887,10 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     TileSource reader(dynamic, unit0, units, total);
     for (;;) {
       if (total == 0) break;
-      uint32_t tile;
-      const int got = next_tile_warp(reader, ctl, q_empty0, q_remote, abort, &tile);
+      Tile ti;
+      const int got = next_tile_warp<G>(reader, ctl, q_empty0, q_remote, abort, prefix, p, &ti);
       if (got < 0) ok = false;
       if (got <= 0) break;
-      const Tile ti = decode_tile<G>(tile, prefix, p);
       const uint32_t n = ti.n0 + rank * kBlockN + r;
       const bool row_ok = n < static_cast<uint32_t>(p.N);
       const unsigned short *srow = sbits + (static_cast<size_t>(ti.e) * p.N + (row_ok ? n : 0)) * spr;
