@@ -591,14 +591,17 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       // every claim comes from the front, which keeps more reuse in L2.
       const bool two_ended = ctl.max_group_tiles >= kUnevenRatio * ctl.min_group_tiles;
       const bool from_back = two_ended && (unit0 & 1u);
-      auto claim = [&]() -> uint32_t {
-        const unsigned long long old =
-            atomicAdd(reinterpret_cast<unsigned long long *>(p.tile_counter), from_back ? (1ull << 32) : 1ull);
+      // A claim is the atomic on the claim word (issued as early as possible) and,
+      // once its old value is needed, the tile it names.
+      auto claim_issue = [&]() -> unsigned long long {
+        return atomicAdd(reinterpret_cast<unsigned long long *>(p.tile_counter), from_back ? (1ull << 32) : 1ull);
+      };
+      auto claim_tile = [&](unsigned long long old) -> uint32_t {
         const uint32_t front = static_cast<uint32_t>(old), back = static_cast<uint32_t>(old >> 32);
         if (static_cast<unsigned long long>(front) + back >= total) return kNoTile;
         return from_back ? total - 1u - back : front;
       };
-      auto publish = [&](uint32_t t) -> bool {
+      auto publish = [&](uint32_t t, Tile *info) -> bool {
         const uint32_t slot = qpos % kTileQueue, parity = (qpos / kTileQueue) & 1u;
         const uint32_t empty = smem_addr(&ctl.tq_empty[slot]);
         if (!(kPair ? wait_phase_cluster(empty, parity ^ 1u, abort) : wait_phase(empty, parity ^ 1u, abort)))
@@ -606,6 +609,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         ctl.tq_tile[slot] = t;
         const Tile x = t == kNoTile ? Tile{} : decode_tile<G>(t, prefix, p);
         ctl.tq_info[slot] = x;
+        *info = x;
         if constexpr (kPair) {   // the second CTA's copy of the entry, then its signal
           st_shared_cluster_u32(map_to_rank(smem_addr(&ctl.tq_tile[slot]), 1), t);
           const uint32_t *xw = reinterpret_cast<const uint32_t *>(&x);
@@ -618,21 +622,25 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         ++qpos;
         return true;
       };
-      auto valid = [](uint32_t t) -> uint32_t { return t; };   // claim() already returns kNoTile at the end
       const bool publisher = dynamic && rank == 0;
       uint32_t cur = kNoTile, nxt = kNoTile;   // tile being loaded; tile already published after it
+      Tile cur_info{}, nxt_info{};              // their decoded forms, kept from publishing
       if (publisher) {
-        cur = valid(claim());
-        nxt = cur == kNoTile ? kNoTile : valid(claim());
-        ok = publish(cur) && (cur == kNoTile || publish(nxt));
+        cur = claim_tile(claim_issue());
+        nxt = cur == kNoTile ? kNoTile : claim_tile(claim_issue());
+        ok = publish(cur, &cur_info) && (cur == kNoTile || publish(nxt, &nxt_info));
       }
       for (; ok;) {
         Tile ti;
-        uint32_t after = kNoTile;   // claimed now, published when `nxt` starts
+        // The publisher claims the tile after `nxt` once this tile's first stage is
+        // issued, and decodes and publishes it after the second: readers need it only a
+        // tile later, and the copies of a new tile start without that work in between.
+        uint32_t after = kNoTile;
+        Tile after_info{};
+        unsigned long long claim_old = 0;
         if (publisher) {
           if (cur == kNoTile) break;
-          ti = decode_tile<G>(cur, prefix, p);
-          if (nxt != kNoTile) after = claim();
+          ti = cur_info;
         } else {
           const int got = reader.next<G>(ctl, q_empty0, q_remote, abort, prefix, p, &ti);
           if (got < 0) ok = false;
@@ -680,13 +688,21 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           pending |= 1u << rt.slot;
           pend_phase = (pend_phase & ~(1u << rt.slot)) | (rt.phase << rt.slot);
           rt.next(ST);
+          if (publisher && nxt != kNoTile) {
+            if (kb == 0) claim_old = claim_issue();
+            if (kb == (KB > 1 ? 1 : 0)) {
+              after = claim_tile(claim_old);
+              if (!publish(after, &after_info)) { ok = false; break; }
+            }
+          }
         }
         if (!ok) break;
         if (publisher) {
           cur = nxt;
+          cur_info = nxt_info;
           if (cur != kNoTile) {
-            nxt = valid(after);
-            if (!publish(nxt)) { ok = false; break; }
+            nxt = after;
+            nxt_info = after_info;
           }
         }
       }
