@@ -175,13 +175,14 @@ struct alignas(128) GmmParams {
   int cache_hints;               // 1: L2 eviction priorities on the TMA loads (see the producer)
 };
 
-struct Tile {
+struct __align__(32) Tile {
   int32_t e;
   uint32_t single_block;   // the group fits one token block: its weight panels are read once
   uint32_t row0;           // first token row of the tile
   uint32_t nrows;          // token rows that belong to the group
   uint32_t ntok;           // nrows rounded up to the MMA granule: the MMA's N
   uint32_t n0;             // first weight row / C column of the tile
+  uint32_t pad[2];         // to 32 bytes: a queue entry is read with two 16-byte loads
 };
 
 struct __align__(8) Ctrl {
@@ -438,23 +439,39 @@ struct TileSource {
   }
 };
 
-// The same for a whole warp: lane 0 reads the queue, the warp agrees.
+// The same for a whole warp: lane 0 waits for the entry, every lane reads it (two
+// 16-byte loads of the same shared-memory words), then lane 0 releases it.
 template <class G>
 __device__ __forceinline__ int next_tile_warp(TileSource &src, Ctrl &ctl, uint32_t empty0, bool remote,
                                               volatile int *abort, const uint32_t *prefix, const GmmParams &p,
                                               Tile *info) {
   if (!src.dynamic) return src.next<G>(ctl, empty0, remote, abort, prefix, p, info);
-  int r = 0;
-  Tile x{};
-  if ((threadIdx.x & 31) == 0) r = src.next<G>(ctl, empty0, remote, abort, prefix, p, &x);
-  r = __shfl_sync(0xffffffffu, r, 0);
-  info->e = __shfl_sync(0xffffffffu, x.e, 0);
-  info->single_block = __shfl_sync(0xffffffffu, x.single_block, 0);
-  info->row0 = __shfl_sync(0xffffffffu, x.row0, 0);
-  info->nrows = __shfl_sync(0xffffffffu, x.nrows, 0);
-  info->ntok = __shfl_sync(0xffffffffu, x.ntok, 0);
-  info->n0 = __shfl_sync(0xffffffffu, x.n0, 0);
-  return r;
+  TileQueueReader &q = src.q;
+  const uint32_t slot = q.pos % kTileQueue, parity = (q.pos / kTileQueue) & 1u;
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    const uint32_t full = smem_addr(&ctl.tq_full[slot]);
+    ok = remote ? wait_phase_cluster(full, parity, abort) : wait_phase(full, parity, abort);
+  }
+  if (!__shfl_sync(0xffffffffu, ok, 0)) return -1;
+  __syncwarp();   // orders the other lanes' reads after lane 0's acquire
+  const uint32_t tile = *reinterpret_cast<volatile uint32_t *>(&ctl.tq_tile[slot]);
+  const uint4 w0 = ld_shared_v4(smem_addr(&ctl.tq_info[slot]));
+  const uint4 w1 = ld_shared_v4(smem_addr(&ctl.tq_info[slot]) + 16u);
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    const uint32_t empty = empty0 + slot * static_cast<uint32_t>(sizeof(uint64_t));
+    if (remote) mbar_arrive_cluster(empty); else mbar_arrive(empty);
+  }
+  ++q.pos;
+  if (tile == kNoTile) return 0;
+  info->e = static_cast<int32_t>(w0.x);
+  info->single_block = w0.y;
+  info->row0 = w0.z;
+  info->nrows = w0.w;
+  info->ntok = w1.x;
+  info->n0 = w1.y;
+  return 1;
 }
 
 template <bool kInt4, bool kPair>
