@@ -172,3 +172,56 @@ def gmm_int4(a_bits, a_offsets, packed, scales, expert_ids, *, group_size: int =
     if flags < 0:
         raise MemoryError("oracle allocation failed")
     return OracleResult(c, ref32, ref64, stats, flags)
+
+
+# ---------------------------------------------------------------- optional epilogue
+# The grouped and quantised GEMM pages both take an optional elementwise function of
+# the output (Modular "grouped_matmul_sm100_persistent" and "multistage_gemm_q",
+# section "Parameters", elementwise_lambda_fn).  The library offers the common MoE
+# steps instead of a function:  y = act(ref[r, n] + bias[e, n]) * row_scale[r], with e
+# the expert of row r's group; C = bf16(y).  Rows outside active groups are untouched.
+
+def activation_ref(name: str, y: np.ndarray) -> np.ndarray:
+    """The activations, written from their definitions (fp64)."""
+    y = np.asarray(y, dtype=np.float64)
+    if name == "none":
+        return y
+    if name == "relu":
+        return np.maximum(y, 0.0)
+    if name == "silu":                      # y * sigmoid(y)
+        return y / (1.0 + np.exp(-y))
+    if name == "gelu_tanh":                 # the tanh form of GELU (Hendrycks and Gimpel)
+        return 0.5 * y * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (y + 0.044715 * y ** 3)))
+    raise ValueError(f"unknown activation {name!r}")
+
+
+def apply_epilogue(res: OracleResult, a_offsets, expert_ids, num_experts: int, *, bias_bits=None,
+                   row_scale=None, activation: str = "none") -> OracleResult:
+    """The optional epilogue on an oracle result: returns C with it applied to the rows
+    of active groups, and `ref32` = y (fp32) there, for the comparison."""
+    off = np.asarray(a_offsets, dtype=np.int64)
+    ids = np.asarray(expert_ids, dtype=np.int64)
+    c = res.c.copy()
+    ref = res.ref32.copy()
+    if res.flags & BAD_OFFSETS:
+        return OracleResult(c, ref, res.ref64, res.stats, res.flags)
+    bias = None if bias_bits is None else bf16_bits_to_f32(bias_bits).astype(np.float64)
+    scale = None if row_scale is None else np.asarray(row_scale, dtype=np.float64)
+    for g, e in enumerate(ids):
+        if not (0 <= e < num_experts) or off[g + 1] <= off[g]:
+            continue
+        r0, r1 = off[g], off[g + 1]
+        y = res.ref32[r0:r1].astype(np.float64)
+        if bias is not None:
+            y = y + bias[e][None, :]
+        y = activation_ref(activation, y)
+        if scale is not None:
+            y = y * scale[r0:r1, None]
+        ref[r0:r1] = y.astype(np.float32)
+        c[r0:r1] = round_bf16(ref[r0:r1])
+    return OracleResult(c, ref, res.ref64, res.stats, res.flags)
+
+
+def bf16_bits_to_f32(bits) -> np.ndarray:
+    """bf16 bit patterns -> fp32 (exact: bf16 is the top half of an fp32)."""
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)

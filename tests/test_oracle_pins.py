@@ -345,3 +345,64 @@ def test_named_routings_have_the_stated_structure():
     assert f.rows == 32768 and int((f.expert_ids < 0).sum()) == 13 and (f.N, f.K) == (4096, 7168)
     q = wl.routing("int4")
     assert q.rows == 8192 and q.int4 and (q.N, q.K, q.group_size) == (4096, 4096, 128)
+
+
+# ------------------------------------------------------------------ optional epilogue
+
+def test_epilogue_activations_against_independent_forms():
+    """relu exactly; silu against scipy's logistic function; the tanh form of GELU against
+    the exact (erf) GELU within the approximation's error, and both fixed points."""
+    sp = pytest.importorskip("scipy.special")
+    y = np.concatenate([np.linspace(-12, 12, 2001), [0.0, -0.0, 30.0, -30.0]])
+    assert np.array_equal(oracle.activation_ref("relu", y), np.where(y > 0, y, 0.0))
+    assert np.allclose(oracle.activation_ref("silu", y), y * sp.expit(y), rtol=1e-12, atol=1e-300)
+    gelu_exact = 0.5 * y * (1.0 + sp.erf(y / np.sqrt(2.0)))
+    assert np.max(np.abs(oracle.activation_ref("gelu_tanh", y) - gelu_exact)) < 1e-3
+    for name in ("relu", "silu", "gelu_tanh"):
+        assert oracle.activation_ref(name, np.array([0.0]))[0] == 0.0
+        assert abs(oracle.activation_ref(name, np.array([30.0]))[0] - 30.0) < 1e-9   # identity far right
+    assert np.array_equal(oracle.activation_ref("none", y), y)
+
+
+def test_epilogue_small_integer_case_is_exact():
+    """Integer A, B and bias, row scales that are powers of two: every value is exact, so
+    C must equal bf16(act(A.B^T + bias) * scale) computed with int64 arithmetic."""
+    rng = np.random.default_rng(21)
+    E, N, K = 3, 40, 24
+    loads, ids = [5, 0, 9, 7], [2, 1, -1, 0]
+    r = wl.make_routing("t", E, N, K, loads, ids, a_dist=("int", -3, 3), b_dist=("int", -3, 3))
+    v = wl.host_values(r, 22)
+    bias = rng.integers(-20, 21, (E, N))
+    scale = rng.choice([0.5, 1.0, 2.0, 4.0], r.rows).astype(np.float32)
+    c0 = wl.sentinel_c(r.rows, N)
+    base = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, c_init=c0)
+    A = bits_to_f32(v["a"]).astype(np.int64)
+    B = bits_to_f32(v["b"]).astype(np.int64)
+    for act in ("none", "relu"):
+        got = oracle.apply_epilogue(base, r.a_offsets, r.expert_ids, E, bias_bits=bf16_bits(bias),
+                                    row_scale=scale, activation=act)
+        want = c0.copy()
+        off = r.a_offsets
+        for g, e in enumerate(ids):
+            if e < 0:
+                continue
+            y = A[off[g]:off[g + 1]] @ B[e].T + bias[e][None, :]
+            if act == "relu":
+                y = np.maximum(y, 0)
+            want[off[g]:off[g + 1]] = bf16_bits(y * scale[off[g]:off[g + 1], None].astype(np.float64))
+        assert np.array_equal(got.c, want), act
+
+
+def test_epilogue_leaves_rows_outside_active_groups():
+    r = wl.make_routing("t", 2, 16, 16, [3, 4, 2], [1, -1, 0], a_dist=("normal", 1.0), b_dist=("normal", 1.0))
+    v = wl.host_values(r, 23)
+    c0 = wl.sentinel_c(r.rows + 5, 16)
+    base = oracle.gmm_bf16(np.concatenate([v["a"], np.zeros((5, 16), np.uint16)]), r.a_offsets, v["b"],
+                           r.expert_ids, c_init=c0)
+    got = oracle.apply_epilogue(base, r.a_offsets, r.expert_ids, 2, activation="silu",
+                                row_scale=np.full(r.rows + 5, 3.0, np.float32))
+    skipped = np.zeros(r.rows + 5, bool)
+    skipped[3:7] = True
+    skipped[r.rows:] = True
+    assert np.all(got.c[skipped] == wl.SENTINEL_BF16)
+    assert not np.any(got.c[~skipped] == wl.SENTINEL_BF16)
