@@ -82,6 +82,40 @@ int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, c
             cudaStream_t stream);
 
 /*
+ * Optional elementwise epilogue, applied to each fp32 result before it is rounded
+ * to bf16 (the grouped and quantised GEMM pages both take an optional elementwise
+ * function on the output: Modular "grouped_matmul_sm100_persistent" and
+ * "multistage_gemm_q", section "Parameters", elementwise_lambda_fn; a C interface
+ * takes these common steps instead of a function):
+ *     y = act( acc[r, n] + bias[e, n] ) * row_scale[r]
+ * where e is the group's expert and r the row of A.  Each part is optional:
+ *   bias:       bf16 [num_experts, N] (2-byte aligned), or NULL for none;
+ *   row_scale:  fp32 [rows of A] (4-byte aligned, e.g. routing weights), or NULL;
+ *   activation: GMM_ACT_NONE, GMM_ACT_RELU (max(y, 0)), GMM_ACT_SILU (y / (1 + e^-y)),
+ *               GMM_ACT_GELU_TANH (y/2 (1 + tanh(sqrt(2/pi) (y + 0.044715 y^3)))).
+ * Rows that no active group covers stay untouched, as without the epilogue.
+ */
+#define GMM_ACT_NONE      0
+#define GMM_ACT_RELU      1
+#define GMM_ACT_SILU      2
+#define GMM_ACT_GELU_TANH 3
+
+typedef struct gmm_epilogue {
+  const void *bias;
+  const float *row_scale;
+  int activation;
+} gmm_epilogue;
+
+/*
+ * gmm_run with the optional epilogue (epilogue == NULL: exactly gmm_run).
+ * Errors: as gmm_run, plus GMM_ERR_INVALID_ARG for an unknown activation or a
+ * misaligned bias / row_scale.
+ */
+int gmm_run_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, const void *b,
+               const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
+               const gmm_epilogue *epilogue, cudaStream_t stream);
+
+/*
  * 4-bit grouped GEMM (the grouped path with the weights of Modular's
  * "multistage_gemm_q", section "Parameters": pack_factor 4-bit values per uint32 and
  * one scale per group_size K elements).  B[e, n, k] is replaced by
@@ -96,6 +130,12 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
                  const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
                  uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
                  cudaStream_t stream);
+
+/* gmm_run_int4 with the optional epilogue (epilogue == NULL: exactly gmm_run_int4). */
+int gmm_run_int4_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets,
+                    const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
+                    uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
+                    const gmm_epilogue *epilogue, cudaStream_t stream);
 
 /*
  * Allocation-free variant of gmm_run, for callers that cannot call cudaMalloc when

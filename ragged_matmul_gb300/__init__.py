@@ -7,5 +7,6 @@ first call does, and raises if the library is missing.
 """
 from .binding import (EXPORTED, GMM_ERR_BAD_INPUT, GMM_ERR_CUDA, GMM_ERR_DEVICE_TIMEOUT,  # noqa: F401
                       GMM_ERR_INVALID_ARG, GMM_ERR_NO_DEVICE, GMM_ERR_UNSUPPORTED, GMM_OK, GmmError,
+                      GMM_ACT_GELU_TANH, GMM_ACT_NONE, GMM_ACT_RELU, GMM_ACT_SILU,
                       Handle, gmm_create, gmm_destroy, gmm_error_string, gmm_query_status, gmm_run,
-                      gmm_run_int4, library_path, load_library)
+                      gmm_run_ex, gmm_run_int4, gmm_run_int4_ex, library_path, load_library)

@@ -31,8 +31,20 @@ GMM_ERR_DEVICE_TIMEOUT = -4
 GMM_ERR_BAD_INPUT = -5
 GMM_ERR_NO_DEVICE = -6
 
-EXPORTED = ("gmm_create", "gmm_run", "gmm_run_int4", "gmm_run_noalloc", "gmm_query_status",
-            "gmm_error_string", "gmm_destroy")
+EXPORTED = ("gmm_create", "gmm_run", "gmm_run_ex", "gmm_run_int4", "gmm_run_int4_ex", "gmm_run_noalloc",
+            "gmm_query_status", "gmm_error_string", "gmm_destroy")
+
+# Activations of the optional epilogue (GMM_ACT_* in gmm.h).
+GMM_ACT_NONE = 0
+GMM_ACT_RELU = 1
+GMM_ACT_SILU = 2
+GMM_ACT_GELU_TANH = 3
+ACTIVATIONS = {"none": GMM_ACT_NONE, "relu": GMM_ACT_RELU, "silu": GMM_ACT_SILU, "gelu_tanh": GMM_ACT_GELU_TANH}
+
+
+class GmmEpilogue(ctypes.Structure):
+    """gmm_epilogue: y = act(acc + bias[e, n]) * row_scale[r] before the bf16 store."""
+    _fields_ = [("bias", ctypes.c_void_p), ("row_scale", ctypes.c_void_p), ("activation", ctypes.c_int)]
 
 _lib = None
 
@@ -63,6 +75,11 @@ def load_library(path: str | None = None):
     lib.gmm_run.restype = I
     lib.gmm_run_int4.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, P]
     lib.gmm_run_int4.restype = I
+    EP = ctypes.POINTER(GmmEpilogue)
+    lib.gmm_run_ex.argtypes = [P, P, P, P, P, P, P, I, I, I, EP, P]
+    lib.gmm_run_ex.restype = I
+    lib.gmm_run_int4_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, EP, P]
+    lib.gmm_run_int4_ex.restype = I
     lib.gmm_run_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
     lib.gmm_run_noalloc.restype = I
     lib.gmm_query_status.argtypes = [P, P]
@@ -149,9 +166,32 @@ def _routing_args(h, a_offsets, expert_ids, stats):
             _check(stats, "expert_usage_stats", _i32_types(), h.device, 2), G)
 
 
+def _epilogue(h: Handle, rows: int, N: int, bias, row_scale, activation) -> GmmEpilogue:
+    """Marshal the optional epilogue's operands (checked like the others)."""
+    import torch
+    act = ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
+    pb = None
+    if bias is not None:
+        if tuple(bias.shape) != (h.num_experts, N):
+            raise ValueError(f"bias must be [E, N] = [{h.num_experts}, {N}], got {tuple(bias.shape)}")
+        pb = _check(bias, "bias", (torch.bfloat16,), h.device).value
+    ps = None
+    if row_scale is not None:
+        if row_scale.dim() != 1 or row_scale.numel() < rows:
+            raise ValueError(f"row_scale must be 1-D with at least {rows} entries")
+        ps = _check(row_scale, "row_scale", (torch.float32,), h.device).value
+    return GmmEpilogue(pb, ps, act)
+
+
 def gmm_run(h: Handle, c, a, a_offsets, b, expert_ids, expert_usage_stats, stream=None,
             check: bool = True) -> int:
     """C[r, :] = A[r, :] @ B[expert_ids[g]].T for rows of active groups (asynchronous)."""
+    return gmm_run_ex(h, c, a, a_offsets, b, expert_ids, expert_usage_stats, stream=stream, check=check)
+
+
+def gmm_run_ex(h: Handle, c, a, a_offsets, b, expert_ids, expert_usage_stats, bias=None, row_scale=None,
+               activation=GMM_ACT_NONE, stream=None, check: bool = True) -> int:
+    """gmm_run with the optional epilogue y = act(acc + bias[e, n]) * row_scale[r] (asynchronous)."""
     import torch
     if a.dim() != 2 or b.dim() != 3 or c.dim() != 2:
         raise ValueError("a must be [rows, K], b [E, N, K], c [rows, N]")
@@ -164,7 +204,13 @@ def gmm_run(h: Handle, c, a, a_offsets, b, expert_ids, expert_usage_stats, strea
     pa = _check(a, "a", bf, h.device)
     pb = _check(b, "b", bf, h.device)
     po, pi, ps, G = _routing_args(h, a_offsets, expert_ids, expert_usage_stats)
-    rc = load_library().gmm_run(h.ptr, pc, pa, po, pb, pi, ps, G, N, K, stream_handle(h.device, stream))
+    lib = load_library()
+    if bias is None and row_scale is None and not activation:
+        rc = lib.gmm_run(h.ptr, pc, pa, po, pb, pi, ps, G, N, K, stream_handle(h.device, stream))
+    else:
+        epi = _epilogue(h, a.shape[0], N, bias, row_scale, activation)
+        rc = lib.gmm_run_ex(h.ptr, pc, pa, po, pb, pi, ps, G, N, K, ctypes.byref(epi),
+                            stream_handle(h.device, stream))
     if check and rc != GMM_OK:
         raise GmmError(rc, "gmm_run")
     return rc
@@ -173,6 +219,14 @@ def gmm_run(h: Handle, c, a, a_offsets, b, expert_ids, expert_usage_stats, strea
 def gmm_run_int4(h: Handle, c, a, a_offsets, b_packed, b_scales, expert_ids, expert_usage_stats,
                  group_size: int = 128, stream=None, check: bool = True) -> int:
     """4-bit variant: b_packed [E, N, K/8] 32-bit words, b_scales [E, N, K/group_size] bf16."""
+    return gmm_run_int4_ex(h, c, a, a_offsets, b_packed, b_scales, expert_ids, expert_usage_stats,
+                           group_size=group_size, stream=stream, check=check)
+
+
+def gmm_run_int4_ex(h: Handle, c, a, a_offsets, b_packed, b_scales, expert_ids, expert_usage_stats,
+                    group_size: int = 128, bias=None, row_scale=None, activation=GMM_ACT_NONE, stream=None,
+                    check: bool = True) -> int:
+    """gmm_run_int4 with the optional epilogue y = act(acc + bias[e, n]) * row_scale[r]."""
     import torch
     if a.dim() != 2 or b_packed.dim() != 3 or c.dim() != 2 or b_scales.dim() != 3:
         raise ValueError("a must be [rows, K], b_packed [E, N, K/8], b_scales [E, N, K/gs], c [rows, N]")
@@ -187,8 +241,14 @@ def gmm_run_int4(h: Handle, c, a, a_offsets, b_packed, b_scales, expert_ids, exp
     pq = _check(b_packed, "b_packed", _i32_types(), h.device)
     psc = _check(b_scales, "b_scales", bf, h.device)
     po, pi, ps, G = _routing_args(h, a_offsets, expert_ids, expert_usage_stats)
-    rc = load_library().gmm_run_int4(h.ptr, pc, pa, po, pq, psc, pi, ps, G, N, K, int(group_size),
-                                     stream_handle(h.device, stream))
+    lib = load_library()
+    if bias is None and row_scale is None and not activation:
+        rc = lib.gmm_run_int4(h.ptr, pc, pa, po, pq, psc, pi, ps, G, N, K, int(group_size),
+                              stream_handle(h.device, stream))
+    else:
+        epi = _epilogue(h, a.shape[0], N, bias, row_scale, activation)
+        rc = lib.gmm_run_int4_ex(h.ptr, pc, pa, po, pq, psc, pi, ps, G, N, K, int(group_size), ctypes.byref(epi),
+                                 stream_handle(h.device, stream))
     if check and rc != GMM_OK:
         raise GmmError(rc, "gmm_run_int4")
     return rc

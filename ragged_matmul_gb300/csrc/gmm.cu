@@ -93,6 +93,24 @@ int encode_token_maps(gmm_ctx *h, GmmParams &p, const void *a, int K, int sub_pe
                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// The optional epilogue: a known activation, and operands aligned for their element type.
+int check_epilogue(const gmm_epilogue *e) {
+  if (!e) return GMM_OK;
+  if (e->activation < GMM_ACT_NONE || e->activation > GMM_ACT_GELU_TANH) return GMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(e->bias) & 1u) || (reinterpret_cast<uintptr_t>(e->row_scale) & 3u))
+    return GMM_ERR_INVALID_ARG;
+  return GMM_OK;
+}
+
+void set_epilogue(GmmParams &p, const gmm_epilogue *e) {
+  static_assert(GMM_ACT_NONE == gmm::kActNone && GMM_ACT_RELU == gmm::kActRelu && GMM_ACT_SILU == gmm::kActSilu &&
+                    GMM_ACT_GELU_TANH == gmm::kActGeluTanh,
+                "activation codes of the C ABI and the kernel agree");
+  p.epi_bias = e ? static_cast<const __nv_bfloat16 *>(e->bias) : nullptr;
+  p.epi_row_scale = e ? e->row_scale : nullptr;
+  p.epi_act = e ? e->activation : GMM_ACT_NONE;
+}
+
 int check_common(gmm_ctx *h, void *c, const void *a, const uint32_t *a_offsets, const int32_t *ids,
                  uint32_t *stats, int G, int N, int K) {
   if (!h || !c || !a || !a_offsets || !stats) return GMM_ERR_INVALID_ARG;
@@ -301,10 +319,12 @@ int gmm_destroy(gmm_handle_t h) {
   return rc;
 }
 
-int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, const void *b,
-            const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
-            cudaStream_t stream) {
+int gmm_run_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, const void *b,
+               const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
+               const gmm_epilogue *epilogue, cudaStream_t stream) {
   int rc = check_common(h, c, a, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  if (rc) return rc;
+  rc = check_epilogue(epilogue);
   if (rc) return rc;
   if (!b || !aligned16(b)) return GMM_ERR_INVALID_ARG;
 
@@ -322,14 +342,23 @@ int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, c
   rc = encode_token_maps(h, p, a, K, 1);
   if (rc) return rc;
   fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K, max_tok(h, false));
+  set_epilogue(p, epilogue);
   return launch<false>(h, p, stream);
 }
 
-int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets,
-                 const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
-                 uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
-                 cudaStream_t stream) {
+int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, const void *b,
+            const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
+            cudaStream_t stream) {
+  return gmm_run_ex(h, c, a, a_offsets, b, expert_ids, expert_usage_stats, num_groups, N, K, nullptr, stream);
+}
+
+int gmm_run_int4_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets,
+                    const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
+                    uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
+                    const gmm_epilogue *epilogue, cudaStream_t stream) {
   int rc = check_common(h, c, a, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  if (rc) return rc;
+  rc = check_epilogue(epilogue);
   if (rc) return rc;
   if (!b_packed || !b_scales) return GMM_ERR_INVALID_ARG;
   if (!aligned16(b_packed) || (reinterpret_cast<uintptr_t>(b_scales) & 1u)) return GMM_ERR_INVALID_ARG;
@@ -357,7 +386,16 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
   for (int s = 0, g64 = group_size / gmm::kBK; (1 << s) <= g64; ++s)
     if ((1 << s) == g64) p.scale_shift = s;
   p.group_size = group_size;
+  set_epilogue(p, epilogue);
   return launch<true>(h, p, stream);
+}
+
+int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets,
+                 const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
+                 uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
+                 cudaStream_t stream) {
+  return gmm_run_int4_ex(h, c, a, a_offsets, b_packed, b_scales, expert_ids, expert_usage_stats, num_groups, N,
+                         K, group_size, nullptr, stream);
 }
 
 int gmm_query_status(gmm_handle_t h, cudaStream_t stream) {

@@ -119,6 +119,11 @@ constexpr uint32_t kDynamicTilesPerUnit4 = 8; // 4-bit: the same (its tiles are 
 constexpr uint32_t kUnevenRatio = 4;          // groups this uneven get the two-ended claim order
 constexpr uint32_t kNoTile = 0xffffffffu;     // queue entry meaning "no more tiles"
 
+constexpr int kActNone = 0;       // activations of the optional epilogue (the C ABI's GMM_ACT_* values)
+constexpr int kActRelu = 1;
+constexpr int kActSilu = 2;
+constexpr int kActGeluTanh = 3;
+
 constexpr uint32_t kStatusBadOffsets = 1u;
 constexpr uint32_t kStatusBadExpert = 2u;
 constexpr uint32_t kStatusTimeout = 4u;
@@ -173,6 +178,11 @@ struct alignas(128) GmmParams {
   uint32_t *tile_counter;        // workspace, 8-byte aligned, zero between launches: [0..1] one 64-bit claim
                                  // word (tiles claimed from the front | from the back << 32), [2] CTAs finished
   int cache_hints;               // 1: L2 eviction priorities on the TMA loads (see the producer)
+  // Optional elementwise epilogue on the fp32 result before it is rounded to bf16:
+  //   y = act(acc + bias[e, n]) * row_scale[r]      (each part optional)
+  const __nv_bfloat16 *epi_bias;   // [E, N] or null
+  const float *epi_row_scale;      // [rows of A] or null
+  int epi_act;                     // kActNone, kActRelu, kActSilu, kActGeluTanh
 };
 
 struct __align__(32) Tile {
@@ -355,6 +365,22 @@ __device__ __forceinline__ Tile decode_tile(uint32_t t, const uint32_t *prefix, 
   x.ntok = (x.nrows + G::kTokAlign - 1) & ~(G::kTokAlign - 1);
   x.n0 = nb * G::kRows;
   return x;
+}
+
+// The optional epilogue of one output element: bias, then activation, then row scale.
+//   relu(y) = max(y, 0);  silu(y) = y / (1 + e^-y);
+//   gelu(y) = y/2 * (1 + tanh(sqrt(2/pi) * (y + 0.044715 y^3)))   (the tanh form of GELU)
+__device__ __forceinline__ float epilogue_op(float y, float bias, int act, float scale) {
+  y += bias;
+  if (act == kActRelu) {
+    y = fmaxf(y, 0.0f);
+  } else if (act == kActSilu) {
+    y = y / (1.0f + __expf(-y));
+  } else if (act == kActGeluTanh) {
+    const float kSqrt2OverPi = 0.7978845608028654f;
+    y = 0.5f * y * (1.0f + tanhf(kSqrt2OverPi * (y + 0.044715f * y * y * y)));
+  }
+  return y * scale;
 }
 
 // Dequantise one packed word (8 four-bit values, k = 8j .. 8j+7, low nibble first)
@@ -831,15 +857,35 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const bool col_ok = n < static_cast<uint32_t>(p.N);
       __nv_bfloat16 *cp = p.c + static_cast<size_t>(ti.row0) * p.N + n;
       const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * kAccCols;
-      for (uint32_t c0 = 0; c0 < ti.ntok; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld_x16(taddr + c0, v);
-        tmem_ld_wait();
-        if (col_ok) {
+      const bool fused = p.epi_bias != nullptr || p.epi_row_scale != nullptr || p.epi_act != kActNone;
+      if (!fused) {
+        for (uint32_t c0 = 0; c0 < ti.ntok; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld_x16(taddr + c0, v);
+          tmem_ld_wait();
+          if (col_ok) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < ti.nrows)
-              cp[static_cast<size_t>(c0 + j) * p.N] = __float2bfloat16_rn(__uint_as_float(v[j]));
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < ti.nrows)
+                cp[static_cast<size_t>(c0 + j) * p.N] = __float2bfloat16_rn(__uint_as_float(v[j]));
+          }
+        }
+      } else {
+        const float bias = (p.epi_bias != nullptr && col_ok)
+                               ? __bfloat162float(p.epi_bias[static_cast<size_t>(ti.e) * p.N + n]) : 0.0f;
+        for (uint32_t c0 = 0; c0 < ti.ntok; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld_x16(taddr + c0, v);
+          tmem_ld_wait();
+          if (col_ok) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < ti.nrows) {
+                const float s = p.epi_row_scale != nullptr ? __ldg(p.epi_row_scale + ti.row0 + c0 + j) : 1.0f;
+                cp[static_cast<size_t>(c0 + j) * p.N] =
+                    __float2bfloat16_rn(epilogue_op(__uint_as_float(v[j]), bias, p.epi_act, s));
+              }
+          }
         }
       }
       tc_fence_before_sync();

@@ -50,9 +50,17 @@ def sentinel_dev(rows, N, dev):
 
 
 def run_gpu(h, a_bits, off, ids, *, b_bits=None, packed=None, scales=None, group_size=128, N=None,
-            rows_alloc=None, stats_init=None, dev="cuda:0"):
-    """Upload host inputs, run the CUDA path, return (C bits, stats, status code)."""
+            rows_alloc=None, stats_init=None, epilogue=None, dev="cuda:0"):
+    """Upload host inputs, run the CUDA path, return (C bits, stats, status code).
+    `epilogue`: optional dict(bias_bits=[E, N] bf16 bits, row_scale=[rows] fp32, activation=name)."""
     torch = _torch()
+    epi = {}
+    if epilogue:
+        if epilogue.get("bias_bits") is not None:
+            epi["bias"] = to_dev_u16(epilogue["bias_bits"], dev)
+        if epilogue.get("row_scale") is not None:
+            epi["row_scale"] = torch.from_numpy(np.ascontiguousarray(epilogue["row_scale"], np.float32)).to(dev)
+        epi["activation"] = epilogue.get("activation", "none")
     rows = a_bits.shape[0] if rows_alloc is None else rows_alloc
     a = to_dev_u16(a_bits, dev)
     c = sentinel_dev(rows, N, dev)
@@ -61,11 +69,17 @@ def run_gpu(h, a_bits, off, ids, *, b_bits=None, packed=None, scales=None, group
     ids_d = to_dev_i32(ids, dev)
     if packed is None:
         b = to_dev_u16(b_bits, dev)
-        binding.gmm_run(h, c, a, off_d, b, ids_d, stats)
+        if epi:
+            binding.gmm_run_ex(h, c, a, off_d, b, ids_d, stats, **epi)
+        else:
+            binding.gmm_run(h, c, a, off_d, b, ids_d, stats)
     else:
         q = torch.from_numpy(np.ascontiguousarray(packed).view(np.int32)).to(dev)
         s = to_dev_u16(scales, dev)
-        binding.gmm_run_int4(h, c, a, off_d, q, s, ids_d, stats, group_size=group_size)
+        if epi:
+            binding.gmm_run_int4_ex(h, c, a, off_d, q, s, ids_d, stats, group_size=group_size, **epi)
+        else:
+            binding.gmm_run_int4(h, c, a, off_d, q, s, ids_d, stats, group_size=group_size)
     status = binding.gmm_query_status(h)
     return bits_of(c), stats.cpu().numpy().view(np.uint32), status
 
@@ -92,8 +106,9 @@ def live_row_mask(rows_alloc, off, ids, E):
     return live
 
 
-def check_against_oracle(h, r: wl.Routing, vals, *, rows_alloc=None, exact=False, where=""):
-    """Full-output comparison of the CUDA path with the oracle on host inputs."""
+def check_against_oracle(h, r: wl.Routing, vals, *, rows_alloc=None, exact=False, epilogue=None, where=""):
+    """Full-output comparison of the CUDA path with the oracle on host inputs (with the
+    optional epilogue, given as in run_gpu, applied on both sides)."""
     rows_alloc = r.rows if rows_alloc is None else rows_alloc
     c0 = wl.sentinel_c(rows_alloc, r.N)
     st0 = np.full(4, wl.SENTINEL_STATS, np.uint32)
@@ -102,11 +117,15 @@ def check_against_oracle(h, r: wl.Routing, vals, *, rows_alloc=None, exact=False
                               group_size=r.group_size, c_init=c0, stats_init=st0)
         got, stats, status = run_gpu(h, vals["a"], r.a_offsets, r.expert_ids, packed=vals["packed"],
                                      scales=vals["scales"], group_size=r.group_size, N=r.N,
-                                     rows_alloc=rows_alloc)
+                                     rows_alloc=rows_alloc, epilogue=epilogue)
     else:
         ref = oracle.gmm_bf16(vals["a"], r.a_offsets, vals["b"], r.expert_ids, c_init=c0, stats_init=st0)
         got, stats, status = run_gpu(h, vals["a"], r.a_offsets, r.expert_ids, b_bits=vals["b"], N=r.N,
-                                     rows_alloc=rows_alloc)
+                                     rows_alloc=rows_alloc, epilogue=epilogue)
+    if epilogue:
+        ref = oracle.apply_epilogue(ref, r.a_offsets, r.expert_ids, r.E, bias_bits=epilogue.get("bias_bits"),
+                                    row_scale=epilogue.get("row_scale"),
+                                    activation=epilogue.get("activation", "none"))
     live = live_row_mask(rows_alloc, r.a_offsets, r.expert_ids, r.E)
     if ref.flags & oracle.BAD_OFFSETS:
         live[:] = False

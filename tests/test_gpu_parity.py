@@ -307,3 +307,73 @@ def sampled_full_size(name, rows_per_group=2, ncols=96, seed=0):
 @pytest.mark.parametrize("name", ["decode", "prefill", "fine_grained", "int4"])
 def test_full_size_sampled(name):
     sampled_full_size(name)
+
+
+# ---------------------------------------------------------------- optional epilogue
+
+def _epilogue_case(r, seed, activation, bias=True, scale=True, rows_alloc=None):
+    rng = np.random.default_rng(seed)
+    rows = r.rows if rows_alloc is None else rows_alloc
+    epi = {"activation": activation}
+    if bias:
+        epi["bias_bits"] = wl._to_bf16_bits(rng.normal(0.0, 1.0, (r.E, r.N)).astype(np.float32))
+    if scale:
+        epi["row_scale"] = rng.uniform(0.1, 2.0, rows).astype(np.float32)
+    return epi
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("activation", ["none", "relu", "silu", "gelu_tanh"])
+def test_epilogue_bf16(activation, variant):
+    """act(acc + bias[e, n]) * row_scale[r] fused before the bf16 store, against the oracle."""
+    loads = [1, 17, 0, 130, 33, 257, 7]
+    ids = [2, 0, 1, 3, -1, 1, 0]
+    r = routing(4, 392, 200, loads, ids, dist=("normal", 0.5))
+    v = wl.host_values(r, 30)
+    epi = _epilogue_case(r, 31, activation)
+    _, _, status, _ = check_against_oracle(handle(4, variant), r, v, epilogue=epi,
+                                           where=f"epilogue {activation} {variant}")
+    assert status == binding.GMM_OK
+
+
+@pytest.mark.parametrize("parts", [(True, False), (False, True)])
+def test_epilogue_bias_only_and_scale_only(parts):
+    r = routing(3, 256, 128, [40, 0, 129], [1, 2, 0], dist=("normal", 1.0))
+    v = wl.host_values(r, 32)
+    epi = _epilogue_case(r, 33, "silu", bias=parts[0], scale=parts[1])
+    check_against_oracle(handle(3), r, v, epilogue=epi, where=f"epilogue parts {parts}")
+
+
+@pytest.mark.parametrize("activation", ["relu", "gelu_tanh"])
+def test_epilogue_int4(activation):
+    r = routing(5, 200, 320, [1, 17, 160, 161, 40], [4, 0, 2, 3, -1], dist=("normal", 1.0), int4=True, gs=64)
+    v = wl.host_values(r, 34)
+    epi = _epilogue_case(r, 35, activation)
+    _, _, status, _ = check_against_oracle(handle(5), r, v, epilogue=epi, where=f"int4 epilogue {activation}")
+    assert status == binding.GMM_OK
+
+
+def test_epilogue_exact_integer_case():
+    """Integer operands and bias, power-of-two row scales, relu: every value is exact."""
+    r = routing(5, 392, 24, [1, 17, 0, 130, 33, 256], [4, 0, 2, 3, -1, 1], dist=("int", -3, 3))
+    v = wl.host_values(r, 36)
+    rng = np.random.default_rng(37)
+    epi = {"bias_bits": wl._to_bf16_bits(rng.integers(-20, 21, (5, 392)).astype(np.float32)),
+           "row_scale": rng.choice([0.5, 1.0, 2.0], r.rows).astype(np.float32), "activation": "relu"}
+    check_against_oracle(handle(5), r, v, epilogue=epi, exact=True, where="epilogue exact")
+
+
+def test_epilogue_argument_errors():
+    import torch
+    h = handle(4)
+    r = routing(4, 128, 64, [8], [1])
+    v = wl.host_values(r, 38)
+    c = sentinel_dev(r.rows, 128, DEV)
+    av = torch.from_numpy(v["a"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    b = torch.from_numpy(v["b"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    off = to_dev_i32(r.a_offsets, DEV)
+    ids = to_dev_i32(r.expert_ids, DEV)
+    st = to_dev_i32(np.zeros(4), DEV)
+    rc = binding.gmm_run_ex(h, c, av, off, b, ids, st, activation=7, check=False)
+    assert rc == binding.GMM_ERR_INVALID_ARG      # unknown activation: nothing launched
+    assert np.all(bits_of(c) == wl.SENTINEL_BF16)
