@@ -289,6 +289,9 @@ def main():
                     help="profile-sized sub-workload: only the first G groups of the named routing")
     ap.add_argument("--group-range", default=None,
                     help="sub-workload lo:hi - groups lo .. hi-1 of the named routing")
+    ap.add_argument("--epilogue", default="none", choices=["none", "relu", "silu", "gelu_tanh"],
+                    help="time the fused epilogue act(acc + bias[e, n]) * row_scale[r] with this activation "
+                         "(seeded bias and per-row scales); 'none' is the plain GEMM")
     ap.add_argument("--variant", default=None, choices=["pair", "single"],
                     help="kernel variant (default: the library's choice, CTA pairs)")
     args = ap.parse_args()
@@ -314,6 +317,8 @@ def main():
               "useful_flops": flops, "algorithmic_bytes": nbytes,
               "l2": "flushed between steps (512 MiB written, then another 512 MiB read: cold, clean L2)",
               "weights": "int4" if r.int4 else "bf16"}
+    if args.epilogue != "none":
+        config["epilogue"] = f"{args.epilogue}(acc + bias[e, n]) * row_scale[r], fused before the bf16 store"
 
     if args.impl == "reference":
         # The CPU oracle, timed on this host's cores; under torchrun only rank 0 works.
@@ -371,12 +376,19 @@ def main():
         flush_r.sum()
     stream = torch.cuda.current_stream(dev)
 
+    epi = {}
+    if args.epilogue != "none":   # seeded epilogue operands, made on the device
+        gen = torch.Generator(device=dev).manual_seed(1000 + rank)
+        epi = {"bias": (0.1 * torch.randn((r.E, r.N), generator=gen, device=dev)).to(torch.bfloat16),
+               "row_scale": torch.rand((r.rows,), generator=gen, device=dev) * 0.9 + 0.1,
+               "activation": args.epilogue}
+
     def step(cc=c, aa=vals["a"], oo=off, ii=ids, ss=stats):
         if r.int4:
-            binding.gmm_run_int4(h, cc, aa, oo, vals["packed"], vals["scales"], ii, ss,
-                                 group_size=r.group_size, stream=stream)
+            binding.gmm_run_int4_ex(h, cc, aa, oo, vals["packed"], vals["scales"], ii, ss,
+                                    group_size=r.group_size, stream=stream, **epi)
         else:
-            binding.gmm_run(h, cc, aa, oo, vals["b"], ii, ss, stream=stream)
+            binding.gmm_run_ex(h, cc, aa, oo, vals["b"], ii, ss, stream=stream, **epi)
 
     for _ in range(args.warmup):
         flush_l2()

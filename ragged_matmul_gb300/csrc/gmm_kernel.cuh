@@ -375,7 +375,7 @@ __device__ __forceinline__ float epilogue_op(float y, float bias, int act, float
   if (act == kActRelu) {
     y = fmaxf(y, 0.0f);
   } else if (act == kActSilu) {
-    y = y / (1.0f + __expf(-y));
+    y = __fdividef(y, 1.0f + __expf(-y));   // a huge denominator gives 0, the limit
   } else if (act == kActGeluTanh) {
     const float kSqrt2OverPi = 0.7978845608028654f;
     y = 0.5f * y * (1.0f + tanhf(kSqrt2OverPi * (y + 0.044715f * y * y * y)));
@@ -874,17 +874,19 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         const float bias = (p.epi_bias != nullptr && col_ok)
                                ? __bfloat162float(p.epi_bias[static_cast<size_t>(ti.e) * p.N + n]) : 0.0f;
         for (uint32_t c0 = 0; c0 < ti.ntok; c0 += 16) {
+          // The chunk's 16 row scales: lane j loads row c0 + j, the warp shares them.
+          float s_lane = 1.0f;
+          if (p.epi_row_scale != nullptr && lane < 16 && c0 + lane < ti.nrows)
+            s_lane = __ldg(p.epi_row_scale + ti.row0 + c0 + lane);
           uint32_t v[16];
           tmem_ld_x16(taddr + c0, v);
           tmem_ld_wait();
-          if (col_ok) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < ti.nrows) {
-                const float s = p.epi_row_scale != nullptr ? __ldg(p.epi_row_scale + ti.row0 + c0 + j) : 1.0f;
-                cp[static_cast<size_t>(c0 + j) * p.N] =
-                    __float2bfloat16_rn(epilogue_op(__uint_as_float(v[j]), bias, p.epi_act, s));
-              }
+          for (int j = 0; j < 16; ++j) {
+            const float s = __shfl_sync(0xffffffffu, s_lane, j);
+            if (col_ok && c0 + j < ti.nrows)
+              cp[static_cast<size_t>(c0 + j) * p.N] =
+                  __float2bfloat16_rn(epilogue_op(__uint_as_float(v[j]), bias, p.epi_act, s));
           }
         }
       }
