@@ -31,8 +31,8 @@
  * they do not synchronise and allocate nothing.
  *
  * A handle owns a small device workspace (a status word, a 64-bit tile-claim
- * word and a finished-CTA counter that each launch returns to zero, and per-CTA
- * tensor-map slots) that
+ * word and a finished-CTA counter that each launch returns to zero, the routing of
+ * gmm_matmul_int4's single group, and per-CTA tensor-map slots) that
  * every launch made through it rewrites.  Launches made through the
  * same handle must therefore not overlap on the GPU: issue them on one stream, or
  * use one handle per stream.
@@ -130,6 +130,23 @@ int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offse
                  const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
                  uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
                  cudaStream_t stream);
+
+/*
+ * Dense rank-2 4-bit GEMM (Modular "multistage_gemm_q": C = A . B^T with B packed
+ * 4-bit and group-quantised, section "Parameters": pack_factor, group_size):
+ *     C[r, n] = sum_k A[r, k] * w[n, k],  w[n, k] = bf16( (q - 8) * scale[n, k / group_size] )
+ * for r < M, with the nibble layout of gmm_run_int4.  It is the grouped path with one
+ * group of M rows and one expert; the group's offsets and id are written into the
+ * handle's workspace (stream-ordered), so the caller passes none.
+ *   c: bf16 [M, N]; a: bf16 [M, K]; b_packed: uint32 [N, K/8]; b_scales: bf16 [N, K/group_size].
+ * The page's function raises when an operand is not rank-2; here the ranks are fixed
+ * by the signature (the Python binding raises for tensors of another rank).
+ * M == 0 launches nothing.  Requirements and errors: as gmm_run_int4_ex, plus
+ * GMM_ERR_INVALID_ARG for M < 0.  Calls through one handle share its workspace, so
+ * they must be stream-ordered, as for every call through a handle.
+ */
+int gmm_matmul_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *b_packed, const void *b_scales,
+                    int M, int N, int K, int group_size, const gmm_epilogue *epilogue, cudaStream_t stream);
 
 /* gmm_run_int4 with the optional epilogue (epilogue == NULL: exactly gmm_run_int4). */
 int gmm_run_int4_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets,

@@ -31,8 +31,8 @@ GMM_ERR_DEVICE_TIMEOUT = -4
 GMM_ERR_BAD_INPUT = -5
 GMM_ERR_NO_DEVICE = -6
 
-EXPORTED = ("gmm_create", "gmm_run", "gmm_run_ex", "gmm_run_int4", "gmm_run_int4_ex", "gmm_run_noalloc",
-            "gmm_query_status", "gmm_error_string", "gmm_destroy")
+EXPORTED = ("gmm_create", "gmm_run", "gmm_run_ex", "gmm_run_int4", "gmm_run_int4_ex", "gmm_matmul_int4",
+            "gmm_run_noalloc", "gmm_query_status", "gmm_error_string", "gmm_destroy")
 
 # Activations of the optional epilogue (GMM_ACT_* in gmm.h).
 GMM_ACT_NONE = 0
@@ -80,6 +80,8 @@ def load_library(path: str | None = None):
     lib.gmm_run_ex.restype = I
     lib.gmm_run_int4_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, EP, P]
     lib.gmm_run_int4_ex.restype = I
+    lib.gmm_matmul_int4.argtypes = [P, P, P, P, P, I, I, I, I, EP, P]
+    lib.gmm_matmul_int4.restype = I
     lib.gmm_run_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
     lib.gmm_run_noalloc.restype = I
     lib.gmm_query_status.argtypes = [P, P]
@@ -251,6 +253,47 @@ def gmm_run_int4_ex(h: Handle, c, a, a_offsets, b_packed, b_scales, expert_ids, 
                                  stream_handle(h.device, stream))
     if check and rc != GMM_OK:
         raise GmmError(rc, "gmm_run_int4")
+    return rc
+
+
+def gmm_matmul_int4(h: Handle, c, a, b_packed, b_scales, group_size: int = 128, bias=None, row_scale=None,
+                    activation=GMM_ACT_NONE, stream=None, check: bool = True) -> int:
+    """Dense 4-bit GEMM C = A . w^T (Modular "multistage_gemm_q"): a [M, K] bf16,
+    b_packed [N, K/8] 32-bit words, b_scales [N, K/group_size] bf16, c [M, N] bf16.
+    Raises ValueError when an operand is not rank-2, as the page's function does.
+    `bias` (if given) is [1, N] bf16: the single expert's row."""
+    import torch
+    for name, t_ in (("c", c), ("a", a), ("b_packed", b_packed), ("b_scales", b_scales)):
+        if t_.dim() != 2:
+            raise ValueError(f"{name} must be rank-2, got rank {t_.dim()}")
+    M, K = a.shape
+    N, KW = b_packed.shape
+    if KW * 8 != K or tuple(c.shape) != (M, N) or group_size <= 0 or tuple(b_scales.shape) != (N, K // group_size):
+        raise ValueError(f"shape mismatch: a {tuple(a.shape)}, b_packed {tuple(b_packed.shape)}, "
+                         f"b_scales {tuple(b_scales.shape)}, c {tuple(c.shape)}")
+    bf = (torch.bfloat16,)
+    pc = _check(c, "c", bf, h.device)
+    pa = _check(a, "a", bf, h.device)
+    pq = _check(b_packed, "b_packed", _i32_types(), h.device)
+    psc = _check(b_scales, "b_scales", bf, h.device)
+    epi = None
+    if bias is not None or row_scale is not None or activation:
+        pb = None
+        if bias is not None:
+            if tuple(bias.shape) != (1, N):
+                raise ValueError(f"bias must be [1, {N}]")
+            pb = _check(bias, "bias", bf, h.device).value
+        ps = None
+        if row_scale is not None:
+            if row_scale.dim() != 1 or row_scale.numel() < M:
+                raise ValueError(f"row_scale must be 1-D with at least {M} entries")
+            ps = _check(row_scale, "row_scale", (torch.float32,), h.device).value
+        act = ACTIVATIONS[activation] if isinstance(activation, str) else int(activation)
+        epi = ctypes.byref(GmmEpilogue(pb, ps, act))
+    rc = load_library().gmm_matmul_int4(h.ptr, pc, pa, pq, psc, M, N, K, int(group_size), epi,
+                                        stream_handle(h.device, stream))
+    if check and rc != GMM_OK:
+        raise GmmError(rc, "gmm_matmul_int4")
     return rc
 
 

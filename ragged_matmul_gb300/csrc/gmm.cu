@@ -21,9 +21,12 @@ using gmm::GmmParams;
 
 // Workspace layout: a 256-byte block with the status word at byte 0, the 64-bit
 // tile-claim word (front count | back count << 32) at byte 64 and the finished-CTA
-// counter at byte 72 (all zero between launches), then one tensor-map slot per CTA.
+// counter at byte 72 (all zero between launches), the dense call's routing at 128 and
+// its usage stats at 144; then one slot of tensor maps per CTA.
 constexpr size_t kStatusBytes = 256;
 constexpr size_t kTileCounterOffset = 64;
+constexpr size_t kDenseRoutingOffset = 128;   // gmm_matmul_int4: a_offsets {0, M} and expert id 0
+constexpr size_t kDenseStatsOffset = 144;     // and its usage stats (written, never read)
 
 struct DeviceGuard {
   int prev = -1;
@@ -352,10 +355,16 @@ int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, c
   return gmm_run_ex(h, c, a, a_offsets, b, expert_ids, expert_usage_stats, num_groups, N, K, nullptr, stream);
 }
 
-int gmm_run_int4_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets,
-                    const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
-                    uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
-                    const gmm_epilogue *epilogue, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// The 4-bit path for `num_experts` experts of packed weights (the handle's E for the
+// grouped calls, 1 for the dense one).
+int run_int4(gmm_handle_t h, int num_experts, void *c, const void *a, const uint32_t *a_offsets,
+             const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
+             uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
+             const gmm_epilogue *epilogue, cudaStream_t stream) {
   int rc = check_common(h, c, a, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
   if (rc) return rc;
   rc = check_epilogue(epilogue);
@@ -370,7 +379,7 @@ int gmm_run_int4_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_of
     // Packed weights as 32-bit words {K/8, N, E}; one box = 128 rows x 32 words (128 B,
     // two 128-K stages), 128-byte swizzle.
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(K / 8), static_cast<cuuint64_t>(N),
-                          static_cast<cuuint64_t>(h->num_experts)};
+                          static_cast<cuuint64_t>(num_experts)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(K / 8) * 4, static_cast<cuuint64_t>(N) * (K / 8) * 4};
     cuuint32_t box[3] = {gmm::kQRowBytes / 4, gmm::kBlockN, 1};
     rc = encode_map(h, &p.w_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, b_packed, dims, strides, box,
@@ -386,8 +395,41 @@ int gmm_run_int4_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_of
   for (int s = 0, g64 = group_size / gmm::kBK; (1 << s) <= g64; ++s)
     if ((1 << s) == g64) p.scale_shift = s;
   p.group_size = group_size;
+  p.num_experts = num_experts;
   set_epilogue(p, epilogue);
   return launch<true>(h, p, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gmm_run_int4_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets,
+                    const uint32_t *b_packed, const void *b_scales, const int32_t *expert_ids,
+                    uint32_t *expert_usage_stats, int num_groups, int N, int K, int group_size,
+                    const gmm_epilogue *epilogue, cudaStream_t stream) {
+  if (!h) return GMM_ERR_INVALID_ARG;
+  return run_int4(h, h->num_experts, c, a, a_offsets, b_packed, b_scales, expert_ids, expert_usage_stats,
+                  num_groups, N, K, group_size, epilogue, stream);
+}
+
+int gmm_matmul_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *b_packed, const void *b_scales,
+                    int M, int N, int K, int group_size, const gmm_epilogue *epilogue, cudaStream_t stream) {
+  if (!h || M < 0) return GMM_ERR_INVALID_ARG;
+  if (M == 0) return GMM_OK;
+  // One group of M rows with expert 0: its offsets, id and (unread) usage stats live
+  // in the handle's status block, written in stream order before the kernel.
+  DeviceGuard guard(h->device);
+  const uint32_t routing[3] = {0u, static_cast<uint32_t>(M), 0u};   // a_offsets[0..1], expert_ids[0]
+  if (cudaMemcpyAsync(h->ws + kDenseRoutingOffset, routing, sizeof(routing), cudaMemcpyHostToDevice, stream) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return GMM_ERR_CUDA;
+  }
+  const uint32_t *off = reinterpret_cast<const uint32_t *>(h->ws + kDenseRoutingOffset);
+  const int32_t *ids = reinterpret_cast<const int32_t *>(h->ws + kDenseRoutingOffset + 8);
+  uint32_t *stats = reinterpret_cast<uint32_t *>(h->ws + kDenseStatsOffset);
+  return run_int4(h, 1, c, a, off, b_packed, b_scales, ids, stats, 1, N, K, group_size, epilogue, stream);
 }
 
 int gmm_run_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets,

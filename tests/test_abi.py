@@ -70,3 +70,19 @@ def test_product_package_does_not_reach_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
                 assert "oracle.c" not in text and "liboracle" not in text, f
+
+
+def test_dense_int4_rejects_operands_of_another_rank():
+    """gmm_matmul_int4 raises for non-rank-2 operands (as the dense quantised GEMM's page
+    says its function does), before touching the library or a device."""
+    import torch
+    from ragged_matmul_gb300 import binding
+    a = torch.zeros(4, 64, dtype=torch.bfloat16)
+    c = torch.zeros(4, 16, dtype=torch.bfloat16)
+    q = torch.zeros(16, 8, dtype=torch.int32)
+    s = torch.zeros(16, 1, dtype=torch.bfloat16)
+    for bad in ("a", "c", "q", "s"):
+        args = {"a": a, "c": c, "q": q, "s": s}
+        args[bad] = args[bad].unsqueeze(0)
+        with pytest.raises(ValueError, match="rank-2"):
+            binding.gmm_matmul_int4(None, args["c"], args["a"], args["q"], args["s"], group_size=64)

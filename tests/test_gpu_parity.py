@@ -12,7 +12,7 @@ from ragged_matmul_gb300 import binding
 from ragged_matmul_gb300 import workloads as wl
 
 from gpu_util import (assert_close, bits_of, check_against_oracle, live_row_mask, run_gpu,
-                      sentinel_dev, to_dev_i32)
+                      sentinel_dev, to_dev_i32, to_dev_u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -377,3 +377,46 @@ def test_epilogue_argument_errors():
     rc = binding.gmm_run_ex(h, c, av, off, b, ids, st, activation=7, check=False)
     assert rc == binding.GMM_ERR_INVALID_ARG      # unknown activation: nothing launched
     assert np.all(bits_of(c) == wl.SENTINEL_BF16)
+
+
+# ---------------------------------------------------------------- dense rank-2 4-bit GEMM
+
+@pytest.mark.parametrize("M,N,K,gs", [(1, 128, 128, 128), (150, 200, 320, 64), (300, 256, 512, 128),
+                                      (33, 72, 1088, 64)])
+def test_dense_int4_matches_single_group_oracle(M, N, K, gs):
+    """gmm_matmul_int4 (the dense quantised GEMM) = the grouped 4-bit oracle with one group."""
+    import torch
+    r = routing(1, N, K, [M], [0], dist=("normal", 1.0), int4=True, gs=gs)
+    v = wl.host_values(r, 40)
+    ref = oracle.gmm_int4(v["a"], r.a_offsets, v["packed"], v["scales"], r.expert_ids, group_size=gs)
+    h = handle(3)
+    a = torch.from_numpy(v["a"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    q = torch.from_numpy(np.ascontiguousarray(v["packed"][0]).view(np.int32)).to(DEV)
+    s = torch.from_numpy(np.ascontiguousarray(v["scales"][0]).view(np.int16)).to(DEV).view(torch.bfloat16)
+    c = sentinel_dev(M, N, DEV)
+    binding.gmm_matmul_int4(h, c, a, q, s, group_size=gs)
+    assert binding.gmm_query_status(h) == binding.GMM_OK
+    assert_close(bits_of(c), ref.ref32, np.ones(M, bool), f"dense int4 M={M} N={N} K={K}")
+
+
+def test_dense_int4_zero_rows_and_epilogue():
+    import torch
+    h = handle(3)
+    N, K, gs, M = 128, 256, 128, 70
+    r = routing(1, N, K, [M], [0], dist=("normal", 1.0), int4=True, gs=gs)
+    v = wl.host_values(r, 41)
+    a = torch.from_numpy(v["a"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    q = torch.from_numpy(np.ascontiguousarray(v["packed"][0]).view(np.int32)).to(DEV)
+    s = torch.from_numpy(np.ascontiguousarray(v["scales"][0]).view(np.int16)).to(DEV).view(torch.bfloat16)
+    c0 = sentinel_dev(0, N, DEV)
+    assert binding.gmm_matmul_int4(h, c0, a[:0], q, s, group_size=gs) == binding.GMM_OK   # nothing launched
+    rng = np.random.default_rng(42)
+    bias = wl._to_bf16_bits(rng.normal(0, 1, (1, N)).astype(np.float32))
+    scale = rng.uniform(0.5, 1.5, M).astype(np.float32)
+    c = sentinel_dev(M, N, DEV)
+    binding.gmm_matmul_int4(h, c, a, q, s, group_size=gs, bias=to_dev_u16(bias, DEV),
+                            row_scale=torch.from_numpy(scale).to(DEV), activation="silu")
+    ref = oracle.apply_epilogue(oracle.gmm_int4(v["a"], r.a_offsets, v["packed"], v["scales"], r.expert_ids,
+                                                group_size=gs),
+                                r.a_offsets, r.expert_ids, 1, bias_bits=bias, row_scale=scale, activation="silu")
+    assert_close(bits_of(c), ref.ref32, np.ones(M, bool), "dense int4 epilogue")
