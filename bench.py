@@ -384,7 +384,10 @@ def main():
                "activation": args.epilogue}
 
     def step(cc=c, aa=vals["a"], oo=off, ii=ids, ss=stats):
-        if r.int4:
+        if r.name == "int4_dense":   # the dense quantised GEMM's own entry point
+            binding.gmm_matmul_int4(h, cc, aa, vals["packed"][0], vals["scales"][0], group_size=r.group_size,
+                                    stream=stream, **epi)
+        elif r.int4:
             binding.gmm_run_int4_ex(h, cc, aa, oo, vals["packed"], vals["scales"], ii, ss,
                                     group_size=r.group_size, stream=stream, **epi)
         else:

@@ -112,7 +112,7 @@ def _balanced_loads(rng, total, E, spread):
     return loads
 
 
-WORKLOAD_NAMES = ("tiny", "decode", "prefill", "fine_grained", "int4")
+WORKLOAD_NAMES = ("tiny", "decode", "prefill", "fine_grained", "int4", "int4_dense")
 WORKLOAD_SEEDS = {name: i for i, name in enumerate(WORKLOAD_NAMES)}
 
 
@@ -146,6 +146,12 @@ def routing(name: str, seed: int | None = None) -> Routing:
         E = 64
         loads = rng.multinomial(8192, np.full(E, 1.0 / E)).astype(np.int64)
         return make_routing("int4", E, 4096, 4096, loads, np.arange(E),
+                            a_dist=("normal", 1.0), b_dist=None, int4=True, group_size=128,
+                            scale_range=(0.005, 0.02))
+    if name == "int4_dense":
+        # The dense quantised GEMM (one expert, one group): the int4 workload's rows,
+        # shapes and value distributions as a single 8192 x 4096 x 4096 problem.
+        return make_routing("int4_dense", 1, 4096, 4096, [8192], [0],
                             a_dist=("normal", 1.0), b_dist=None, int4=True, group_size=128,
                             scale_range=(0.005, 0.02))
     raise KeyError(name)
