@@ -5,11 +5,14 @@ leg of ``bench.py`` may import this package.  The product path (the
 ``ragged_matmul_gb300`` package and its CUDA library) never does, and shares
 no code with it.
 
-The arithmetic lives in ``oracle.c`` (plain C, one thread per slice of output
-rows); this module only compiles it with gcc, loads it with ctypes and
-marshals numpy arrays.  See ``oracle.c`` for the definition it implements and
-the page sections it follows (Modular "grouped_matmul_sm100_persistent",
-section "Args"; Modular "multistage_gemm_q", section "Parameters").
+The bf16 and 4-bit grouped GEMMs live in ``oracle.c`` (plain C, one thread
+per slice of output rows); this module compiles it with gcc, loads it with
+ctypes and marshals numpy arrays.  See ``oracle.c`` for the definition it
+implements and the page sections it follows (Modular
+"grouped_matmul_sm100_persistent", section "Args"; Modular "multistage_gemm_q",
+section "Parameters").  The optional epilogue and the block-scaled e4m3
+variant (Modular "k_matmul_ragged_paged_scale", sections "Args" and the
+scales_granularity_mnk parameter) are written here in numpy, in fp64.
 """
 from __future__ import annotations
 
@@ -225,3 +228,74 @@ def apply_epilogue(res: OracleResult, a_offsets, expert_ids, num_experts: int, *
 def bf16_bits_to_f32(bits) -> np.ndarray:
     """bf16 bit patterns -> fp32 (exact: bf16 is the top half of an fp32)."""
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) scaled variant
+# The scaled ragged matmul page (Modular "k_matmul_ragged_paged_scale", section "Args":
+# input_scale and weight_scale are multiplied to the input and to the weight; template
+# parameter scales_granularity_mnk) scales both operands in blocks of a given (m, n, k)
+# granularity.  The page prints no formula; the reading taken here is the usual one for
+# block-scaled low-precision GEMMs: input_scale holds one value per gm rows and gk
+# columns of A, weight_scale one per gn rows and gk columns of each expert's weight, and
+#     ref[r, n] = sum_kb input_scale[r // gm, kb] * weight_scale[e, n // gn, kb]
+#                        * sum_{k in block kb} a8[r, k] * w8[e, n, k]
+# with kb = k // gk.  Offsets, expert ids, skipped groups, untouched rows and
+# expert_usage_stats follow the bf16 grouped GEMM exactly.
+
+def e4m3_to_f32(bits) -> np.ndarray:
+    """e4m3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no infinities,
+    S.1111.111 is NaN) bit patterns -> fp32, from the format's definition."""
+    b = np.asarray(bits, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    exp = (b >> 3) & 0xF
+    man = b & 0x7
+    normal = sign * (1.0 + man / 8.0) * np.power(2.0, exp - 7)
+    subnormal = sign * (man / 8.0) * 2.0 ** -6
+    out = np.where(exp == 0, subnormal, normal)
+    out = np.where((exp == 0xF) & (man == 0x7), np.nan, out)
+    return out.astype(np.float32)
+
+
+def gmm_fp8(a8, a_offsets, w8, expert_ids, input_scale, weight_scale, granularity, *,
+            c_init=None, stats_init=None) -> OracleResult:
+    """Block-scaled FP8 grouped GEMM.
+
+    a8 [rows, K] and w8 [E, N, K]: e4m3 bit patterns (uint8).  granularity = (gm, gn, gk).
+    input_scale fp32 [ceil(rows / gm), ceil(K / gk)]; weight_scale fp32
+    [E, ceil(N / gn), ceil(K / gk)].  Sums in fp64 (products of e4m3 values are exact)."""
+    gm, gn, gk = (int(x) for x in granularity)
+    a = e4m3_to_f32(a8).astype(np.float64)
+    w = e4m3_to_f32(w8).astype(np.float64)
+    E, N, K = w.shape
+    rows = a.shape[0]
+    assert a.shape[1] == K and min(gm, gn, gk) >= 1
+    nkb = -(-K // gk)
+    isc = np.asarray(input_scale, np.float64).reshape(-(-rows // gm) if rows else 0, nkb)
+    wsc = np.asarray(weight_scale, np.float64).reshape(E, -(-N // gn), nkb)
+    off = np.asarray(a_offsets, dtype=np.int64)
+    ids = np.asarray(expert_ids, dtype=np.int64)
+    flags, active = validate(a_offsets, expert_ids, E)
+    c = (np.zeros((rows, N), np.uint16) if c_init is None
+         else np.array(c_init, dtype=np.uint16, copy=True).reshape(rows, N))
+    ref32 = np.full((rows, N), np.nan, np.float32)
+    ref64 = np.full((rows, N), np.nan, np.float64)
+    stats = (np.zeros(4, np.uint32) if stats_init is None
+             else np.array(stats_init, dtype=np.uint32, copy=True))
+    stats[1] = active
+    if flags & BAD_OFFSETS:
+        return OracleResult(c, ref32, ref64, stats, flags)
+    ncol = np.arange(N) // gn
+    for g, e in enumerate(ids):
+        r0, r1 = int(off[g]), int(off[g + 1])
+        if not (0 <= e < E) or r1 <= r0:
+            continue
+        mrow = np.arange(r0, r1) // gm
+        y = np.zeros((r1 - r0, N), np.float64)
+        for kb in range(nkb):
+            ks = slice(kb * gk, min(K, (kb + 1) * gk))
+            part = a[r0:r1, ks] @ w[e][:, ks].T
+            y += part * isc[mrow, kb][:, None] * wsc[e][ncol, kb][None, :]
+        ref64[r0:r1] = y
+        ref32[r0:r1] = y.astype(np.float32)
+        c[r0:r1] = round_bf16(ref32[r0:r1])
+    return OracleResult(c, ref32, ref64, stats, flags)

@@ -23,6 +23,12 @@ shapes this library targets):
                 B packed 8 unsigned 4-bit values per uint32 along K (low
                 nibble first), zero point 8, one bf16 scale per 128 K elements,
                 scales ~ U[0.005, 0.02]; A ~ N(0, 1).
+  int4_dense    the int4 workload as one dense problem: E=1, one group of 8192
+                rows, K=N=4096.
+  fp8_prefill,  the prefill / decode routings and shapes with e4m3 operands:
+  fp8_decode    A, B ~ e4m3(N(0, 2)) (the fp32 draw cast to e4m3, round to
+                nearest even), fp32 scales at granularity (1, 128, K):
+                input_scale ~ U[0.25, 1], weight_scale ~ U[0.002, 0.008].
 
 Values are drawn in fp32 and rounded to bf16 (round to nearest even).  Host
 generation uses numpy's PCG64 (``default_rng``); device generation, used for
@@ -31,7 +37,7 @@ give different (equally distributed) values; each caller sticks to one.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 
 import numpy as np
 
@@ -112,7 +118,8 @@ def _balanced_loads(rng, total, E, spread):
     return loads
 
 
-WORKLOAD_NAMES = ("tiny", "decode", "prefill", "fine_grained", "int4", "int4_dense")
+WORKLOAD_NAMES = ("tiny", "decode", "prefill", "fine_grained", "int4", "int4_dense", "fp8_prefill",
+                  "fp8_decode")
 WORKLOAD_SEEDS = {name: i for i, name in enumerate(WORKLOAD_NAMES)}
 
 
@@ -154,6 +161,11 @@ def routing(name: str, seed: int | None = None) -> Routing:
         return make_routing("int4_dense", 1, 4096, 4096, [8192], [0],
                             a_dist=("normal", 1.0), b_dist=None, int4=True, group_size=128,
                             scale_range=(0.005, 0.02))
+    if name in ("fp8_prefill", "fp8_decode"):
+        # The scaled e4m3 variant on the prefill / decode routings and shapes; operand
+        # values come from fp8_host_values / fp8_device_values.
+        base = routing(name[4:], seed)
+        return replace(base, name=name, meta={"fp8": True})
     raise KeyError(name)
 
 
@@ -273,3 +285,64 @@ def device_values(r: Routing, seed: int = 0, device="cuda", chunk_elems: int = 1
     else:
         out["b"] = fill((r.E, r.N, r.K), r.b_dist)
     return out
+
+
+# ---------------------------------------------------------------- e4m3 operands and block scales
+
+FP8_STD = 2.0                       # e4m3 operands ~ e4m3(N(0, FP8_STD))
+FP8_IN_SCALE = (0.25, 1.0)          # input_scale ~ U[lo, hi]
+FP8_W_SCALE = (0.002, 0.008)        # weight_scale ~ U[lo, hi]
+
+
+def fp8_scale_shapes(rows: int, E: int, N: int, K: int, granularity) -> tuple:
+    """Shapes of input_scale and weight_scale for granularity (gm, gn, gk); gk None means K."""
+    gm, gn, gk = granularity
+    gk = K if gk is None else gk
+    nkb = -(-K // gk)
+    return (-(-rows // gm), nkb), (E, -(-N // gn), nkb)
+
+
+def _to_e4m3_bits(x) -> np.ndarray:
+    """fp32 -> e4m3 bit patterns (uint8), round to nearest even, via torch's CPU cast."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
+
+
+def fp8_host_values(r: Routing, seed: int = 0, granularity=(1, 128, None), rows: int | None = None) -> dict:
+    """e4m3 operands (uint8 bit patterns) and fp32 scales as numpy arrays:
+    a8 [rows, K], w8 [E, N, K], input_scale and weight_scale (fp8_scale_shapes)."""
+    rng = np.random.default_rng([seed, 2])
+    rows = r.rows if rows is None else rows
+    s_in, s_w = fp8_scale_shapes(rows, r.E, r.N, r.K, granularity)
+    return {
+        "a8": _to_e4m3_bits(rng.standard_normal((rows, r.K), dtype=np.float32) * np.float32(FP8_STD)),
+        "w8": _to_e4m3_bits(rng.standard_normal((r.E, r.N, r.K), dtype=np.float32) * np.float32(FP8_STD)),
+        "input_scale": rng.uniform(*FP8_IN_SCALE, s_in).astype(np.float32),
+        "weight_scale": rng.uniform(*FP8_W_SCALE, s_w).astype(np.float32),
+    }
+
+
+def fp8_device_values(r: Routing, seed: int = 0, granularity=(1, 128, None), device="cuda",
+                      chunk_elems: int = 1 << 27) -> dict:
+    """The same distributions drawn on the device with torch's seeded CUDA generator
+    (values differ from fp8_host_values).  Operands are uint8 tensors of e4m3 bits."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1000003 + 29)
+
+    def fill(shape):
+        out = torch.empty(shape, dtype=torch.uint8, device=device)
+        flat = out.view(-1)
+        for s in range(0, flat.numel(), chunk_elems):
+            n = min(chunk_elems, flat.numel() - s)
+            x = torch.randn(n, generator=g, device=device, dtype=torch.float32) * FP8_STD
+            flat[s:s + n] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+        return out
+
+    def uniform(shape, lo, hi):
+        return torch.rand(shape, generator=g, device=device, dtype=torch.float32) * (hi - lo) + lo
+
+    s_in, s_w = fp8_scale_shapes(r.rows, r.E, r.N, r.K, granularity)
+    return {"a8": fill((r.rows, r.K)), "w8": fill((r.E, r.N, r.K)),
+            "input_scale": uniform(s_in, *FP8_IN_SCALE), "weight_scale": uniform(s_w, *FP8_W_SCALE)}

@@ -406,3 +406,124 @@ def test_epilogue_leaves_rows_outside_active_groups():
     skipped[r.rows:] = True
     assert np.all(got.c[skipped] == wl.SENTINEL_BF16)
     assert not np.any(got.c[~skipped] == wl.SENTINEL_BF16)
+
+
+# ------------------------------------------------------------------ scaled e4m3 variant
+
+def test_e4m3_decode_matches_torch_and_format_values():
+    """All 256 patterns against torch's float8_e4m3fn, plus values the format fixes:
+    bias 7, 3 mantissa bits, subnormals at exponent 0, S.1111.111 the only NaN."""
+    bits = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_to_f32(bits)
+    ref = torch.from_numpy(bits).view(torch.float8_e4m3fn).to(torch.float32).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and nan.sum() == 2
+    assert np.array_equal(got[~nan], ref[~nan])
+    fixed = {0x38: 1.0, 0xB8: -1.0, 0x40: 2.0, 0x30: 0.5, 0x7E: 448.0, 0x08: 2.0**-6,
+             0x01: 2.0**-9, 0x07: 7 * 2.0**-9, 0x00: 0.0, 0x3C: 1.5}
+    for b, v in fixed.items():
+        assert got[b] == v, hex(b)
+    assert np.signbit(got[0x80]) and got[0x80] == 0.0
+
+
+def test_fp8_hand_worked_example():
+    """One row, one weight row, K=2: a = (1, 2), w = (0.5, -1.5), input scale 2,
+    weight scale 0.25: (1*0.5 + 2*(-1.5)) * 2 * 0.25 = -1.25."""
+    a8 = np.array([[0x38, 0x40]], np.uint8)
+    w8 = np.array([[[0x30, 0xBC]]], np.uint8)
+    res = oracle.gmm_fp8(a8, [0, 1], w8, [0], np.array([[2.0]], np.float32),
+                         np.array([[[0.25]]], np.float32), (1, 1, 2))
+    assert res.ref64[0, 0] == -1.25 and res.ref32[0, 0] == -1.25
+    assert res.c[0, 0] == bf16_bits([-1.25])[0]
+
+
+def _fp8_problem(seed, E, N, K, loads, ids, gran):
+    r = wl.make_routing("t", E, N, K, loads, ids)
+    v = wl.fp8_host_values(r, seed, gran)
+    return r, v
+
+
+def test_fp8_per_element_brute_force():
+    """Tiny problem, granularities that do not divide the sizes: every output against
+    a triple loop that scales each product by its own two block scales."""
+    gran = (2, 4, 5)
+    r, v = _fp8_problem(3, E=3, N=7, K=13, loads=[2, 1, 3, 0], ids=[2, -1, 0, 1], gran=gran)
+    c0 = wl.sentinel_c(r.rows, r.N)
+    res = oracle.gmm_fp8(v["a8"], r.a_offsets, v["w8"], r.expert_ids, v["input_scale"],
+                         v["weight_scale"], gran, c_init=c0)
+    a = oracle.e4m3_to_f32(v["a8"]).astype(np.float64)
+    w = oracle.e4m3_to_f32(v["w8"]).astype(np.float64)
+    gm, gn, gk = gran
+    for g in range(r.G):
+        e = int(r.expert_ids[g])
+        for row in range(int(r.a_offsets[g]), int(r.a_offsets[g + 1])):
+            if e < 0:
+                assert np.all(res.c[row] == wl.SENTINEL_BF16)
+                continue
+            for n in range(r.N):
+                acc = 0.0
+                for k in range(r.K):
+                    acc += (a[row, k] * w[e, n, k] * float(v["input_scale"][row // gm, k // gk])
+                            * float(v["weight_scale"][e, n // gn, k // gk]))
+                assert abs(res.ref64[row, n] - acc) <= 1e-12 * max(1.0, abs(acc))
+    assert res.stats[1] == 3 and res.flags == 0
+
+
+def test_fp8_unit_granularity_is_matmul_of_prescaled_operands():
+    """(1, 1, 1): every element has its own scale, so the result is the plain matmul of
+    (a * input_scale) and (w * weight_scale)."""
+    gran = (1, 1, 1)
+    r, v = _fp8_problem(5, E=2, N=24, K=40, loads=[9, 6], ids=[1, 0], gran=gran)
+    res = oracle.gmm_fp8(v["a8"], r.a_offsets, v["w8"], r.expert_ids, v["input_scale"],
+                         v["weight_scale"], gran)
+    a = oracle.e4m3_to_f32(v["a8"]).astype(np.float64) * v["input_scale"]
+    w = oracle.e4m3_to_f32(v["w8"]).astype(np.float64) * v["weight_scale"]
+    exact = np.concatenate([a[:9] @ w[1].T, a[9:] @ w[0].T])
+    assert np.allclose(res.ref64, exact, rtol=1e-12, atol=1e-300)
+
+
+def test_fp8_unit_scales_equal_the_bf16_oracle():
+    """Unit scales: the grouped GEMM of the decoded values (e4m3 values are bf16 values),
+    which the C oracle computes independently; the fp32 sums agree within their bound."""
+    gran = (1, 128, None)
+    r, v = _fp8_problem(7, E=4, N=40, K=96, loads=[5, 0, 11, 3], ids=[3, 1, 0, -1], gran=gran)
+    ones_in = np.ones_like(v["input_scale"])
+    ones_w = np.ones_like(v["weight_scale"])
+    res = oracle.gmm_fp8(v["a8"], r.a_offsets, v["w8"], r.expert_ids, ones_in, ones_w, (1, 128, 96))
+    a_bits = bf16_bits(oracle.e4m3_to_f32(v["a8"]))
+    w_bits = bf16_bits(oracle.e4m3_to_f32(v["w8"]))
+    ref = oracle.gmm_bf16(a_bits, r.a_offsets, w_bits, r.expert_ids, want64=True)
+    act = ~np.isnan(ref.ref64[:, 0])
+    assert np.array_equal(act, ~np.isnan(res.ref64[:, 0]))
+    assert np.allclose(res.ref64[act], ref.ref64[act], rtol=1e-12, atol=1e-300)
+    assert np.array_equal(res.stats, ref.stats) and res.flags == ref.flags
+
+
+def test_fp8_whole_k_scales_factorise():
+    """gk = K: the result is input_scale[r // gm] * weight_scale[e, n // gn] times the
+    unscaled sum (the form the CUDA path computes in its epilogue)."""
+    gran = (3, 16, None)
+    r, v = _fp8_problem(9, E=2, N=48, K=64, loads=[7, 10], ids=[0, 1], gran=gran)
+    res = oracle.gmm_fp8(v["a8"], r.a_offsets, v["w8"], r.expert_ids, v["input_scale"],
+                         v["weight_scale"], (3, 16, 64))
+    unit = oracle.gmm_fp8(v["a8"], r.a_offsets, v["w8"], r.expert_ids, np.ones_like(v["input_scale"]),
+                          np.ones_like(v["weight_scale"]), (3, 16, 64))
+    rows = np.arange(r.rows)
+    e_of_row = np.repeat(r.expert_ids, r.loads)
+    isc = v["input_scale"].astype(np.float64)
+    wsc = v["weight_scale"].astype(np.float64)
+    scale = isc[rows // 3, 0][:, None] * wsc[e_of_row][:, np.arange(48) // 16, 0]
+    assert np.allclose(res.ref64, unit.ref64 * scale, rtol=1e-12, atol=1e-300)
+
+
+def test_fp8_invalid_inputs_follow_the_grouped_rules():
+    r, v = _fp8_problem(11, E=2, N=8, K=16, loads=[2, 2], ids=[0, 1], gran=(1, 8, None))
+    c0 = wl.sentinel_c(4, 8)
+    bad = oracle.gmm_fp8(v["a8"], [0, 3, 2], v["w8"], [0, 1], v["input_scale"], v["weight_scale"],
+                         (1, 8, 16), c_init=c0, stats_init=np.full(4, 7, np.uint32))
+    assert bad.flags & oracle.BAD_OFFSETS and np.all(bad.c == wl.SENTINEL_BF16)
+    assert list(bad.stats) == [7, 2, 7, 7]
+    oob = oracle.gmm_fp8(v["a8"], r.a_offsets, v["w8"], [0, 5], v["input_scale"], v["weight_scale"],
+                         (1, 8, 16), c_init=c0)
+    assert oob.flags & oracle.BAD_EXPERT_ID and oob.stats[1] == 1
+    assert np.all(oob.c[2:] == wl.SENTINEL_BF16) and not np.any(oob.c[:2] == wl.SENTINEL_BF16)
