@@ -68,10 +68,20 @@ def work_counts(r: wl.Routing):
     experts = np.unique(r.expert_ids[act])
     if r.int4:
         wbytes = r.N * r.K // 2 + r.N * (r.K // r.group_size) * 2
+    elif is_fp8(r):   # e4m3 weights and their fp32 scales; e4m3 activations and their scales
+        wbytes = r.N * r.K + (-(-r.N // FP8_GRAN[1])) * 4
     else:
         wbytes = r.N * r.K * 2
-    nbytes = len(experts) * wbytes + rows * r.K * 2 + rows * r.N * 2 + 4 * (2 * r.G + 2)
+    abytes = rows * (r.K + 4) if is_fp8(r) else rows * r.K * 2
+    nbytes = len(experts) * wbytes + abytes + rows * r.N * 2 + 4 * (2 * r.G + 2)
     return flops, float(nbytes), rows
+
+
+FP8_GRAN = (1, 128, None)   # scale granularity (m, n, k) of the e4m3 workloads; k None: all of K
+
+
+def is_fp8(r: wl.Routing) -> bool:
+    return bool(r.meta.get("fp8", False))
 
 
 def kernel_source_hash():
@@ -207,6 +217,8 @@ def barrier(world):
 def host_values_as_tensors(r: wl.Routing, seed: int = 0):
     """Seeded host-generated operands as CPU torch tensors (for hosts without a GPU)."""
     import torch
+    if is_fp8(r):
+        return {k: torch.from_numpy(x) for k, x in wl.fp8_host_values(r, seed, FP8_GRAN).items()}
     v = wl.host_values(r, seed)
     out = {"a": torch.from_numpy(v["a"].view(np.int16)).view(torch.bfloat16)}
     if r.int4:
@@ -227,15 +239,22 @@ def oracle_sample(r: wl.Routing, vals_dev, n_groups: int):
         rows += range(lo, hi)
         loads.append(hi - lo)
         ids.append(int(r.expert_ids[g]))
-    idx = torch.tensor(rows, dtype=torch.int64, device=vals_dev["a"].device)
-    a = vals_dev["a"][idx].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    sample = {"a": a, "off": wl.offsets_from_loads(loads), "ids": np.asarray(ids, np.int32),
-              "groups": len(act), "rows": len(rows)}
+    akey = "a8" if is_fp8(r) else "a"
+    idx = torch.tensor(rows, dtype=torch.int64, device=vals_dev[akey].device)
+    sample = {"off": wl.offsets_from_loads(loads), "groups": len(act), "rows": len(rows)}
+    if is_fp8(r):
+        sample["a8"] = vals_dev["a8"][idx].cpu().numpy()
+        sample["input_scale"] = vals_dev["input_scale"][idx].cpu().numpy()   # one per row (m granularity 1)
+    else:
+        sample["a"] = vals_dev["a"][idx].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     used = sorted(set(ids))
     remap = {e: i for i, e in enumerate(used)}           # keep only the experts the sample uses
     sample["ids"] = np.asarray([remap[e] for e in ids], np.int32)
-    sel = torch.tensor(used, dtype=torch.int64, device=vals_dev["a"].device)
-    if r.int4:
+    sel = torch.tensor(used, dtype=torch.int64, device=vals_dev[akey].device)
+    if is_fp8(r):
+        sample["w8"] = vals_dev["w8"][sel].cpu().numpy()
+        sample["weight_scale"] = vals_dev["weight_scale"][sel].cpu().numpy()
+    elif r.int4:
         sample["packed"] = vals_dev["packed"][sel].cpu().numpy().view(np.uint32)
         sample["scales"] = vals_dev["scales"][sel].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     else:
@@ -247,7 +266,10 @@ def oracle_sample(r: wl.Routing, vals_dev, n_groups: int):
 def run_oracle(r: wl.Routing, s, nthreads):
     import oracle
     t0 = time.perf_counter()
-    if r.int4:
+    if is_fp8(r):
+        oracle.gmm_fp8(s["a8"], s["off"], s["w8"], s["ids"], s["input_scale"], s["weight_scale"],
+                       (FP8_GRAN[0], FP8_GRAN[1], r.K))
+    elif r.int4:
         oracle.gmm_int4(s["a"], s["off"], s["packed"], s["scales"], s["ids"], group_size=r.group_size,
                         nthreads=nthreads)
     else:
@@ -309,14 +331,20 @@ def main():
         r = wl.group_range(r, lo, hi)
     flops, nbytes, rows = work_counts(r)
     peaks, peaks_kind = load_peaks()
-    t_tensor = flops / (peaks["bf16_tflops"] * 1e12)
+    # e4m3 MMAs run at twice the bf16 rate (the nominal dense ratio 4.5 : 2.25 PFLOP/s):
+    # their tensor peak is the measured bf16 peak times 2.
+    tensor_peak = peaks["bf16_tflops"] * (2.0 if is_fp8(r) else 1.0)
+    t_tensor = flops / (tensor_peak * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if t_tensor >= t_hbm else "hbm"
     config = {"workload": r.name, "E": r.E, "N": r.N, "K": r.K, "groups": r.G,
               "active_groups": int(r.active_mask().sum()), "rows": rows,
               "useful_flops": flops, "algorithmic_bytes": nbytes,
               "l2": "flushed between steps (512 MiB written, then another 512 MiB read: cold, clean L2)",
-              "weights": "int4" if r.int4 else "bf16"}
+              "weights": "int4" if r.int4 else ("e4m3" if is_fp8(r) else "bf16")}
+    if is_fp8(r):
+        config["scales"] = ("fp32 input_scale per row, fp32 weight_scale per 128 weight rows of each expert "
+                            "(granularity (1, 128, K))")
     if args.epilogue != "none":
         config["epilogue"] = f"{args.epilogue}(acc + bias[e, n]) * row_scale[r], fused before the bf16 store"
 
@@ -325,7 +353,8 @@ def main():
         if rank != 0:
             return
         if torch.cuda.is_available():
-            vals = wl.device_values(r, 0, device=torch.device(f"cuda:{local}"))
+            vals = (wl.fp8_device_values(r, 0, FP8_GRAN, device=torch.device(f"cuda:{local}")) if is_fp8(r)
+                    else wl.device_values(r, 0, device=torch.device(f"cuda:{local}")))
         else:
             vals = host_values_as_tensors(r, 0)
         nthreads = len(os.sched_getaffinity(0))
@@ -340,7 +369,9 @@ def main():
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 inputs, fp32 accumulation (C, CPU)",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": ("e4m3 inputs, fp64 sums (numpy, CPU)" if is_fp8(r)
+                      else "bf16 inputs, fp32 accumulation (C, CPU)"),
             "data": "synthetic (seeded)", "config": config,
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
                              "sample": sample_desc(r, s)},
@@ -360,7 +391,8 @@ def main():
         gbuild.build()
     barrier(world)
 
-    vals = wl.device_values(r, rank, device=dev)
+    vals = wl.fp8_device_values(r, rank, FP8_GRAN, device=dev) if is_fp8(r) else wl.device_values(r, rank, device=dev)
+    akey = "a8" if is_fp8(r) else "a"
     if args.variant:
         os.environ["GMM_VARIANT"] = args.variant
     h = binding.gmm_create(r.E, local)
@@ -383,8 +415,11 @@ def main():
                "row_scale": torch.rand((r.rows,), generator=gen, device=dev) * 0.9 + 0.1,
                "activation": args.epilogue}
 
-    def step(cc=c, aa=vals["a"], oo=off, ii=ids, ss=stats):
-        if r.name == "int4_dense":   # the dense quantised GEMM's own entry point
+    def step(cc=c, aa=vals[akey], oo=off, ii=ids, ss=stats):
+        if is_fp8(r):
+            binding.gmm_run_fp8(h, cc, aa, oo, vals["w8"], ii, ss, vals["input_scale"], vals["weight_scale"],
+                                FP8_GRAN, stream=stream, **epi)
+        elif r.name == "int4_dense":   # the dense quantised GEMM's own entry point
             binding.gmm_matmul_int4(h, cc, aa, vals["packed"][0], vals["scales"][0], group_size=r.group_size,
                                     stream=stream, **epi)
         elif r.int4:
@@ -429,12 +464,12 @@ def main():
     # (activations, offsets, ids) from pinned memory, the kernel, D2H of C and stats.
     e2e = None
     if not args.no_e2e:
-        a_h = vals["a"].cpu().pin_memory()
+        a_h = vals[akey].cpu().pin_memory()
         off_h, ids_h = off.cpu().pin_memory(), ids.cpu().pin_memory()
         c_h = torch.empty_like(c, device="cpu").pin_memory()
         st_h = torch.empty_like(stats, device="cpu").pin_memory()
-        a_d, off_d, ids_d = torch.empty_like(vals["a"]), torch.empty_like(off), torch.empty_like(ids)
-        h2d = a_h.numel() * 2 + off_h.numel() * 4 + ids_h.numel() * 4
+        a_d, off_d, ids_d = torch.empty_like(vals[akey]), torch.empty_like(off), torch.empty_like(ids)
+        h2d = a_h.numel() * a_h.element_size() + off_h.numel() * 4 + ids_h.numel() * 4
         d2h = c_h.numel() * 2 + st_h.numel() * 4
 
         def e2e_step():
@@ -482,17 +517,21 @@ def main():
         if bound == "hbm":
             achieved, peak, unit = nbytes / t_s / 1e9, peaks["hbm_gbs"], "GB/s"
         else:
-            achieved, peak, unit = flops / t_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+            achieved, peak, unit = flops / t_s / 1e12, tensor_peak, "TFLOP/s"
         roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                    "traffic": profiled_traffic(args.workload), "peak_source": f"{peaks_kind} (burst)",
+                    "traffic": profiled_traffic(args.workload),
+                    "peak_source": f"{peaks_kind} (burst)" + (" bf16 x 2, the nominal e4m3 : bf16 ratio"
+                                                              if is_fp8(r) and bound == "tensor" else ""),
                     "roofline_time_ms": max(t_tensor, t_hbm) * 1e3,
-                    "kernel": "gmm_grouped_kernel<%s, %s>" % (
+                    "kernel": "gmm_grouped_kernel<%s, %s, %s>" % (
                         "true" if r.int4 else "false",
-                        "true" if (args.variant == "pair" or (args.variant is None and not r.int4)) else "false")}
+                        "true" if (args.variant == "pair" or (args.variant is None and not r.int4)) else "false",
+                        "true" if is_fp8(r) else "false")}
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16" if not r.int4 else "int4 weights, bf16 MMA",
+            "vs_baseline": None,
+            "dtype": "int4 weights, bf16 MMA" if r.int4 else ("e4m3" if is_fp8(r) else "bf16"),
             "data": "synthetic (seeded, generated on device)", "config": config,
             "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": args.steps,
             "clocks": sampler.summary(w0, w1), "region_wall_ms": (w1 - w0) * 1e3,

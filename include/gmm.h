@@ -155,6 +155,30 @@ int gmm_run_int4_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_of
                     const gmm_epilogue *epilogue, cudaStream_t stream);
 
 /*
+ * Block-scaled e4m3 grouped GEMM (Modular "k_matmul_ragged_paged_scale", section
+ * "Args": input_scale and weight_scale multiply the input and the weight; template
+ * parameter scales_granularity_mnk; without the page's paged KV-cache write, the
+ * result goes to C as in gmm_run).  With (gm, gn, gk) = scales_granularity_mnk:
+ *     C[r, n] = bf16( input_scale[r / gm] * weight_scale[e, n / gn]
+ *                     * sum_k a[r, k] * b[e, n, k] )
+ * for the rows and groups of gmm_run, a and b e4m3 (1 sign, 4 exponent bits with
+ * bias 7, 3 mantissa bits), the sum in fp32.  Then the optional epilogue.
+ *   a: e4m3 bytes [rows, K] (16-byte aligned); b: e4m3 bytes [num_experts, N, K]
+ *   (16-byte aligned); input_scale: fp32 [ceil(rows / gm)]; weight_scale: fp32
+ *   [num_experts, ceil(N / gn)] (both 4-byte aligned, read only for active groups);
+ *   c and the other arguments as gmm_run.
+ * Requirements: those of gmm_run with K a multiple of 16 (an e4m3 row is K bytes, a
+ * multiple of 16 for TMA), gm, gn >= 1, and gk >= K: one scale over the whole
+ * reduction.  gk < K (per-K-block scales) returns GMM_ERR_UNSUPPORTED.
+ * Errors: as gmm_run_ex, plus GMM_ERR_INVALID_ARG for NULL or misaligned scales,
+ * a NULL scales_granularity_mnk or a granularity below 1.
+ */
+int gmm_run_fp8(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, const void *b,
+                const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
+                const float *input_scale, const float *weight_scale, const int *scales_granularity_mnk,
+                const gmm_epilogue *epilogue, cudaStream_t stream);
+
+/*
  * Allocation-free variant of gmm_run, for callers that cannot call cudaMalloc when
  * they need the GEMM: code running inside an allocator or memory-pool callback, a
  * framework that has reserved all device memory for its own pool, or a runtime that

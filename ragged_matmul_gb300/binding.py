@@ -32,7 +32,7 @@ GMM_ERR_BAD_INPUT = -5
 GMM_ERR_NO_DEVICE = -6
 
 EXPORTED = ("gmm_create", "gmm_run", "gmm_run_ex", "gmm_run_int4", "gmm_run_int4_ex", "gmm_matmul_int4",
-            "gmm_run_noalloc", "gmm_query_status", "gmm_error_string", "gmm_destroy")
+            "gmm_run_fp8", "gmm_run_noalloc", "gmm_query_status", "gmm_error_string", "gmm_destroy")
 
 # Activations of the optional epilogue (GMM_ACT_* in gmm.h).
 GMM_ACT_NONE = 0
@@ -81,6 +81,8 @@ def load_library(path: str | None = None):
     lib.gmm_run_int4_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, EP, P]
     lib.gmm_run_int4_ex.restype = I
     lib.gmm_matmul_int4.argtypes = [P, P, P, P, P, I, I, I, I, EP, P]
+    lib.gmm_run_fp8.restype = I
+    lib.gmm_run_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, P, P, P, EP, P]
     lib.gmm_matmul_int4.restype = I
     lib.gmm_run_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, P]
     lib.gmm_run_noalloc.restype = I
@@ -253,6 +255,49 @@ def gmm_run_int4_ex(h: Handle, c, a, a_offsets, b_packed, b_scales, expert_ids, 
                                  stream_handle(h.device, stream))
     if check and rc != GMM_OK:
         raise GmmError(rc, "gmm_run_int4")
+    return rc
+
+
+def _fp8_types():
+    import torch
+    return (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+
+
+def gmm_run_fp8(h: Handle, c, a, a_offsets, b, expert_ids, expert_usage_stats, input_scale, weight_scale,
+                scales_granularity_mnk=(1, 128, None), bias=None, row_scale=None, activation=GMM_ACT_NONE,
+                stream=None, check: bool = True) -> int:
+    """Block-scaled e4m3 grouped GEMM: a [rows, K] and b [E, N, K] e4m3 (uint8 bit patterns or
+    float8_e4m3fn), input_scale fp32 [ceil(rows / gm), ...], weight_scale fp32 [E, ceil(N / gn), ...]
+    with (gm, gn, gk) = scales_granularity_mnk (gk None: K); then the optional epilogue."""
+    import torch
+    if a.dim() != 2 or b.dim() != 3 or c.dim() != 2:
+        raise ValueError("a must be [rows, K], b [E, N, K], c [rows, N]")
+    E, N, K = b.shape
+    rows = a.shape[0]
+    if a.shape[1] != K or c.shape[1] != N or c.shape[0] != rows or E != h.num_experts:
+        raise ValueError(f"shape mismatch: a {tuple(a.shape)}, b {tuple(b.shape)}, c {tuple(c.shape)}, "
+                         f"handle E={h.num_experts}")
+    gm, gn, gk = scales_granularity_mnk
+    gk = K if gk is None else gk
+    gran = (ctypes.c_int * 3)(int(gm), int(gn), int(gk))
+    nkb = -(-K // gk) if gk > 0 else 0
+    if gm > 0 and input_scale.numel() != -(-rows // gm) * nkb:
+        raise ValueError(f"input_scale needs ceil(rows / gm) * ceil(K / gk) = {-(-rows // gm) * nkb} entries")
+    if gn > 0 and (weight_scale.shape[0] != E or weight_scale.numel() != E * -(-N // gn) * nkb):
+        raise ValueError(f"weight_scale must be [E, ceil(N / gn), ceil(K / gk)] = [{E}, {-(-N // gn)}, {nkb}]")
+    pc = _check(c, "c", (torch.bfloat16,), h.device)
+    pa = _check(a, "a", _fp8_types(), h.device)
+    pb = _check(b, "b", _fp8_types(), h.device)
+    pis = _check(input_scale, "input_scale", (torch.float32,), h.device)
+    pws = _check(weight_scale, "weight_scale", (torch.float32,), h.device)
+    po, pi, ps, G = _routing_args(h, a_offsets, expert_ids, expert_usage_stats)
+    epi = None
+    if bias is not None or row_scale is not None or activation:
+        epi = ctypes.byref(_epilogue(h, rows, N, bias, row_scale, activation))
+    rc = load_library().gmm_run_fp8(h.ptr, pc, pa, po, pb, pi, ps, G, N, K, pis, pws, gran, epi,
+                                    stream_handle(h.device, stream))
+    if check and rc != GMM_OK:
+        raise GmmError(rc, "gmm_run_fp8")
     return rc
 
 

@@ -55,6 +55,7 @@ struct gmm_ctx {
   int num_experts = 0;
   int num_sms = 0;
   gmm_variant var[2][2];          // [4-bit][pair]
+  gmm_variant var_fp8[2];         // e4m3 kernels, [pair]
   int use_pairs = 1;              // bf16 path: 1 = CTA-pair kernels (cta_group::2), 0 = one CTA per tile
   int use_pairs_int4 = 0;         // 4-bit path: the same (default one CTA per tile)
   uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
@@ -156,21 +157,22 @@ void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, c
 // Ring depths from the device's shared-memory budget (the pages' launcher likewise
 // derives its pipeline depth from the shared memory available), and the grid: one
 // CTA per SM, or for pairs twice the number of clusters of two that fit at once.
-template <bool kInt4, bool kPair>
+template <bool kInt4, bool kPair, bool kFp8 = false>
 int configure(gmm_variant *v, int optin, int num_sms) {
   using G = gmm::Geom<kInt4, kPair>;
-  auto kernel = gmm::gmm_grouped_kernel<kInt4, kPair>;
+  auto kernel = gmm::gmm_grouped_kernel<kInt4, kPair, kFp8>;
   cudaFuncAttributes attr;
   if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(kernel)) != cudaSuccess) return GMM_ERR_CUDA;
   long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024;
   if (kInt4) budget -= gmm::kQRingBytes;   // the packed-slab ring (the weights themselves are in TMEM)
+  budget -= gmm::kEpiStageBytes;          // the epilogue warps' staging tiles
   v->stages = static_cast<int>(budget / static_cast<long>(G::kStageBytes));
   if (v->stages > gmm::kMaxStages) v->stages = gmm::kMaxStages;
   // The 4-bit stage ring also holds the TMEM weight slabs: exactly kAStages deep.
   if (kInt4) v->stages = v->stages >= static_cast<int>(gmm::kAStages) ? static_cast<int>(gmm::kAStages) : 0;
   if (v->stages < 2) return GMM_ERR_UNSUPPORTED;
   v->smem = static_cast<size_t>(v->stages) * G::kStageBytes +
-            (kInt4 ? gmm::kQRingBytes : 0) + 1024;
+            (kInt4 ? gmm::kQRingBytes : 0) + gmm::kEpiStageBytes + 1024;
   if (cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(v->smem)) != cudaSuccess)
     return GMM_ERR_CUDA;
@@ -196,11 +198,11 @@ int configure(gmm_variant *v, int optin, int num_sms) {
   return GMM_OK;
 }
 
-template <bool kInt4>
+template <bool kInt4, bool kFp8 = false>
 int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   DeviceGuard guard(h->device);
   const int pairs = kInt4 ? h->use_pairs_int4 : h->use_pairs;
-  const gmm_variant &v = h->var[kInt4][pairs];
+  const gmm_variant &v = kFp8 ? h->var_fp8[pairs] : h->var[kInt4][pairs];
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cudaLaunchAttribute attr[1];
@@ -217,9 +219,9 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, true>, p);
+    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, true, kFp8>, p);
   } else {
-    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, false>, p);
+    err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, false, kFp8>, p);
   }
   if (err != cudaSuccess) {
     cudaGetLastError();
@@ -285,11 +287,13 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
   h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
 
   const int single_ok = configure<false, false>(&h->var[0][0], optin, sms) == GMM_OK &&
-                        configure<true, false>(&h->var[1][0], optin, sms) == GMM_OK;
+                        configure<true, false>(&h->var[1][0], optin, sms) == GMM_OK &&
+                        configure<false, false, true>(&h->var_fp8[0], optin, sms) == GMM_OK;
   // Tuning override GMM_VARIANT: "single" forces the one-CTA kernels, "pair" the pairs.
   const char *variant = getenv("GMM_VARIANT");
   const bool pairs_ok = sms >= 2 && configure<false, true>(&h->var[0][1], optin, sms) == GMM_OK &&
-                        configure<true, true>(&h->var[1][1], optin, sms) == GMM_OK;
+                        configure<true, true>(&h->var[1][1], optin, sms) == GMM_OK &&
+                        configure<false, true, true>(&h->var_fp8[1], optin, sms) == GMM_OK;
   h->use_pairs = pairs_ok && !(variant && std::strcmp(variant, "single") == 0);
   // The 4-bit path runs one CTA per tile unless GMM_VARIANT=pair: its pair kernel's
   // cross-CTA signal that both halves of a weight stage are in TMEM costs more than
@@ -353,6 +357,51 @@ int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, c
             const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
             cudaStream_t stream) {
   return gmm_run_ex(h, c, a, a_offsets, b, expert_ids, expert_usage_stats, num_groups, N, K, nullptr, stream);
+}
+
+// The e4m3 operands go through the bf16 kernel's tensor maps unchanged, over their
+// bytes: a row of K e4m3 values is a row of K / 2 two-byte units, so the maps, the
+// stage ring and the swizzled layout are the bf16 ones and only the MMA kind and the
+// epilogue's scales differ (see the kernel's kFp8 variant).
+int gmm_run_fp8(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, const void *b,
+                const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
+                const float *input_scale, const float *weight_scale, const int *scales_granularity_mnk,
+                const gmm_epilogue *epilogue, cudaStream_t stream) {
+  if (K < 16 || K % 16) return GMM_ERR_INVALID_ARG;
+  const int KU = K / 2;   // two-byte units per row
+  int rc = check_common(h, c, a, a_offsets, expert_ids, expert_usage_stats, num_groups, N, KU);
+  if (rc) return rc;
+  rc = check_epilogue(epilogue);
+  if (rc) return rc;
+  if (!b || !aligned16(b)) return GMM_ERR_INVALID_ARG;
+  if (!scales_granularity_mnk || !input_scale || !weight_scale) return GMM_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(input_scale) & 3u) || (reinterpret_cast<uintptr_t>(weight_scale) & 3u))
+    return GMM_ERR_INVALID_ARG;
+  const int gm = scales_granularity_mnk[0], gn = scales_granularity_mnk[1], gk = scales_granularity_mnk[2];
+  if (gm < 1 || gn < 1 || gk < 1) return GMM_ERR_INVALID_ARG;
+  if (gk < K) return GMM_ERR_UNSUPPORTED;
+
+  GmmParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(KU), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(h->num_experts)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N) * K};
+    cuuint32_t box[3] = {gmm::kBK, gmm::kBlockN, 1};
+    rc = encode_map(h, &p.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  }
+  rc = encode_token_maps(h, p, a, KU, 1);
+  if (rc) return rc;
+  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, KU, max_tok(h, false));
+  set_epilogue(p, epilogue);
+  p.in_scale = input_scale;
+  p.w_scale = weight_scale;
+  p.scale_gm = gm;
+  p.scale_gn = gn;
+  p.w_scale_cols = (N + gn - 1) / gn;
+  return launch<false, true>(h, p, stream);
 }
 
 }  // extern "C"

@@ -36,12 +36,23 @@
 //                  weights never touch shared memory, so shared memory carries only
 //                  the token slabs and the packed slabs, and no proxy fence sits
 //                  between the dequantisation and the MMA.
+//   kFp8 = true    (with kInt4 = false) e4m3 operands, block-scaled (Modular
+//                  "k_matmul_ragged_paged_scale", section "Args": input_scale and
+//                  weight_scale; template parameter scales_granularity_mnk).  An
+//                  e4m3 row of K elements is K bytes, i.e. the bf16 kernel's rows
+//                  with K / 2 two-byte units: the host encodes the same tensor maps
+//                  over the bytes, every stage carries 128 of K in the same
+//                  128-byte swizzled rows, and the MMA is kind::f8f6f4 (K = 32 per
+//                  instruction: the same 32 bytes per step).  The scales of the
+//                  (gm, gn, K) granularity are applied in the epilogue:
+//                    y = acc * input_scale[r / gm] * weight_scale[e, n / gn].
 //
 // Roles:
 //   warp 0       TMA producer of token slabs (and of bf16 weight slabs).
 //   warp 1       TMEM allocation (512 columns: two fp32 accumulators, and in the
 //                4-bit kernel a ring of dequantised weight slabs between them) and
-//                the single MMA-issuing thread (tcgen05.mma kind::f16).
+//                the single MMA-issuing thread (tcgen05.mma kind::f16, or
+//                kind::f8f6f4 for e4m3).
 //   warps 2..5   epilogue: TMEM -> registers -> bf16 -> C, masking token rows past
 //                the group's end and columns past N; two accumulators let it
 //                overlap the next tile's main loop.
@@ -94,6 +105,13 @@ constexpr int kQSlotBytes = kBlockN * kQRowBytes;            // 16 KB
 constexpr int kQStages = 4;                                  // slots: 8 stages ahead
 constexpr int kQRingBytes = kQStages * kQSlotBytes;
 static_assert(kQRowBytes == 128, "the packed chunk is one 128-byte swizzle row per weight row");
+// Epilogue staging: each epilogue warp transposes its accumulator rows through a
+// 16-row x 32-column fp32 tile in shared memory (rows padded to 36 floats: the
+// column-wise writes and the 16-byte row reads are both free of bank conflicts), so
+// that every thread stores 8 consecutive columns of one C row with one 16-byte store.
+constexpr uint32_t kEpiRows = 16;
+constexpr uint32_t kEpiStride = 36;
+constexpr int kEpiStageBytes = 4 * kEpiRows * kEpiStride * 4;   // 4 epilogue warps
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 // 4-bit kernel: dequantised weight slabs live in TMEM (128 lanes = weight rows, 32
@@ -183,6 +201,13 @@ struct alignas(128) GmmParams {
   const __nv_bfloat16 *epi_bias;   // [E, N] or null
   const float *epi_row_scale;      // [rows of A] or null
   int epi_act;                     // kActNone, kActRelu, kActSilu, kActGeluTanh
+  // Block scales of the e4m3 path, applied first: acc * in_scale[r / scale_gm] *
+  // w_scale[e * w_scale_cols + n / scale_gn] (in_scale null: no scaling).
+  const float *in_scale;           // [ceil(rows / scale_gm)]
+  const float *w_scale;            // [E, w_scale_cols]
+  int scale_gm;
+  int scale_gn;
+  int w_scale_cols;                // ceil(N / scale_gn)
 };
 
 struct __align__(32) Tile {
@@ -195,7 +220,7 @@ struct __align__(32) Tile {
   uint32_t pad[2];         // to 32 bytes: a queue entry is read with two 16-byte loads
 };
 
-struct __align__(8) Ctrl {
+struct __align__(32) Ctrl {   // 32: the tile queue entries inside
   uint64_t full[kMaxStages];     // stage's TMA bytes landed (pair: both CTAs' bytes, on the leader);
                                  // 4-bit: and its TMEM weight slabs written by every dequantisation
                                  // warp (pair: of both CTAs)
@@ -367,6 +392,13 @@ __device__ __forceinline__ Tile decode_tile(uint32_t t, const uint32_t *prefix, 
   return x;
 }
 
+// Two fp32 values -> one 32-bit word of two bf16 (round to nearest even), the lower
+// column in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
 // The optional epilogue of one output element: bias, then activation, then row scale.
 //   relu(y) = max(y, 0);  silu(y) = y / (1 + e^-y);
 //   gelu(y) = y/2 * (1 + tanh(sqrt(2/pi) * (y + 0.044715 y^3)))   (the tanh form of GELU)
@@ -500,9 +532,10 @@ __device__ __forceinline__ int next_tile_warp(TileSource &src, Ctrl &ctl, uint32
   return 1;
 }
 
-template <bool kInt4, bool kPair>
+template <bool kInt4, bool kPair, bool kFp8 = false>
 __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     gmm_grouped_kernel(const __grid_constant__ GmmParams p) {
+  static_assert(!(kInt4 && kFp8), "the e4m3 path has its weights in shared memory");
   using G = Geom<kInt4, kPair>;
   constexpr int NT = kInt4 ? kInt4Threads : kThreads;
   constexpr uint32_t kEpiArrivals = (kPair ? 2 : 1) * 4;   // one per epilogue warp of each CTA
@@ -534,6 +567,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   const uint32_t w_ring = ring;
   const uint32_t t_ring = ring + SW * G::kSub * kWBytes;
   const uint32_t q_ring = t_ring + ST * G::kSub * G::kTSlot;   // 4-bit only
+  const uint32_t epi_ring = q_ring + (kInt4 ? kQRingBytes : 0);  // epilogue staging tiles
 
   if (tid == 0) {
     for (uint32_t s = 0; s < ST; ++s) {
@@ -783,7 +817,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         if (!acc_free) { ok = false; break; }
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
-        const uint32_t idesc = idesc_bf16_f32(G::kRows, ti.ntok);
+        const uint32_t idesc = kFp8 ? idesc_e4m3_f32(G::kRows, ti.ntok) : idesc_bf16_f32(G::kRows, ti.ntok);
         for (int kb = 0; kb < KB; ++kb) {
           // The 4-bit pair's stage is also signalled by the second CTA's dequantisation
           // warps (cluster-scope release), so it is acquired at cluster scope.
@@ -813,8 +847,12 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k) {   // +32 bytes along K per step: +2 in the >>4 address field
                 const uint32_t accumulate = (kb | static_cast<int>(sub) | k) != 0;
-                if constexpr (kPair)
+                if constexpr (kPair && kFp8)
+                  mma_f8_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
+                else if constexpr (kPair)
                   mma_bf16_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
+                else if constexpr (kFp8)
+                  mma_f8(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
                 else
                   mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
               }
@@ -845,6 +883,47 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const int got = next_tile_warp<G>(reader, ctl, q_empty0, q_remote, abort, prefix, p, &ti);
       if (got < 0 && lane == 0) atomicOr(p.status, kStatusTimeout);
       if (got <= 0) break;
+      // This thread's C columns after the transpose: 8 consecutive ones, n8 .. n8 + 7
+      // (N is a multiple of 8, so they are all in range or all past N); its row in
+      // each 8-row pass is rsub.
+      const uint32_t seg = static_cast<uint32_t>(lane) & 3u;
+      const uint32_t rsub = static_cast<uint32_t>(lane) >> 2;
+      const uint32_t n8 = ti.n0 + rank * kBlockN + quad * 32 + seg * 8;
+      const bool cols_ok = n8 < static_cast<uint32_t>(p.N);
+      __nv_bfloat16 *crow = p.c + static_cast<size_t>(ti.row0) * p.N + n8;
+      const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * kAccCols;
+      const bool scaled = kFp8 && p.in_scale != nullptr;
+      const bool fused = p.epi_bias != nullptr || p.epi_row_scale != nullptr || p.epi_act != kActNone || scaled;
+      // The fused epilogue's operands are loaded before the accumulator wait, so their
+      // latency hides behind the tile's MMAs: the 8 columns' bias and (e4m3) weight
+      // scale, and the tile's per-row factors, lane l holding rows l, l + 32, ...
+      // (row scale rs, e4m3 input scale sc).
+      constexpr int kRowRegs = static_cast<int>(G::kMaxTok / 32);
+      float rs[kRowRegs], sc[kRowRegs], bias8[8], wc8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        bias8[k] = 0.0f;
+        wc8[k] = 1.0f;
+      }
+      if (fused) {
+        if (p.epi_bias != nullptr && cols_ok) {
+          const __nv_bfloat16 *bp = p.epi_bias + static_cast<size_t>(ti.e) * p.N + n8;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) bias8[k] = __bfloat162float(bp[k]);
+        }
+        if (scaled && cols_ok) {
+          const float *wp = p.w_scale + static_cast<size_t>(ti.e) * p.w_scale_cols;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) wc8[k] = __ldg(wp + (n8 + k) / static_cast<uint32_t>(p.scale_gn));
+        }
+#pragma unroll
+        for (int q = 0; q < kRowRegs; ++q) {
+          const uint32_t t = static_cast<uint32_t>(q * 32 + lane);
+          const bool row_ok = t < ti.nrows;
+          rs[q] = (p.epi_row_scale != nullptr && row_ok) ? __ldg(p.epi_row_scale + ti.row0 + t) : 1.0f;
+          sc[q] = (scaled && row_ok) ? __ldg(p.in_scale + (ti.row0 + t) / static_cast<uint32_t>(p.scale_gm)) : 1.0f;
+        }
+      }
       int ok = 1;
       if (lane == 0) ok = wait_phase(smem_addr(&ctl.acc_full[acc]), acc_phase, abort);
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -853,41 +932,55 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      const uint32_t n = ti.n0 + rank * kBlockN + quad * 32 + static_cast<uint32_t>(lane);
-      const bool col_ok = n < static_cast<uint32_t>(p.N);
-      __nv_bfloat16 *cp = p.c + static_cast<size_t>(ti.row0) * p.N + n;
-      const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * kAccCols;
-      const bool fused = p.epi_bias != nullptr || p.epi_row_scale != nullptr || p.epi_act != kActNone;
-      if (!fused) {
-        for (uint32_t c0 = 0; c0 < ti.ntok; c0 += 16) {
-          uint32_t v[16];
-          tmem_ld_x16(taddr + c0, v);
-          tmem_ld_wait();
-          if (col_ok) {
+      // 32 token rows per TMEM wait; each 16-row half goes through the staging tile:
+      // thread l writes its column (TMEM lane quad * 32 + l) down the tile, then reads
+      // back 8 columns of one row per pass.  The row factors of rows c0 .. c0 + 31 are
+      // in rs[0] / sc[0] and move down one register every 32 rows.
+      float *stg = reinterpret_cast<float *>(dyn_smem + (epi_ring - dyn_base)) + (warp - 2) * kEpiRows * kEpiStride;
+      for (uint32_t c0 = 0; c0 < ti.ntok; c0 += 32) {
+        uint32_t va[16], vb[16];
+        const bool two = c0 + 16 < ti.ntok;
+        tmem_ld_x16(taddr + c0, va);
+        if (two) tmem_ld_x16(taddr + c0 + 16, vb);
+        tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < ti.nrows)
-                cp[static_cast<size_t>(c0 + j) * p.N] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        for (uint32_t h = 0; h < 2; ++h) {
+          if (h == 1 && !two) break;
+          __syncwarp();   // the previous half's reads of the tile are done
+#pragma unroll
+          for (uint32_t j = 0; j < kEpiRows; ++j) stg[j * kEpiStride + lane] = __uint_as_float(h ? vb[j] : va[j]);
+          __syncwarp();
+#pragma unroll
+          for (uint32_t pass = 0; pass < 2; ++pass) {
+            const uint32_t rl = pass * 8u + rsub;   // row within the half
+            const uint32_t row = c0 + h * 16u + rl; // row within the tile
+            const float4 x0 = *reinterpret_cast<const float4 *>(stg + rl * kEpiStride + seg * 8);
+            const float4 x1 = *reinterpret_cast<const float4 *>(stg + rl * kEpiStride + seg * 8 + 4);
+            float y[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            if (fused) {
+              const int src = static_cast<int>(row & 31u);
+              const float s_r = __shfl_sync(0xffffffffu, rs[0], src);
+              const float s_i = kFp8 ? __shfl_sync(0xffffffffu, sc[0], src) : 1.0f;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (kFp8) y[k] *= s_i * wc8[k];
+                y[k] = epilogue_op(y[k], bias8[k], p.epi_act, s_r);
+              }
+            }
+            if (cols_ok && row < ti.nrows) {
+              uint4 out;
+              out.x = pack_bf16x2(y[0], y[1]);
+              out.y = pack_bf16x2(y[2], y[3]);
+              out.z = pack_bf16x2(y[4], y[5]);
+              out.w = pack_bf16x2(y[6], y[7]);
+              *reinterpret_cast<uint4 *>(crow + static_cast<size_t>(row) * p.N) = out;
+            }
           }
         }
-      } else {
-        const float bias = (p.epi_bias != nullptr && col_ok)
-                               ? __bfloat162float(p.epi_bias[static_cast<size_t>(ti.e) * p.N + n]) : 0.0f;
-        for (uint32_t c0 = 0; c0 < ti.ntok; c0 += 16) {
-          // The chunk's 16 row scales: lane j loads row c0 + j, the warp shares them.
-          float s_lane = 1.0f;
-          if (p.epi_row_scale != nullptr && lane < 16 && c0 + lane < ti.nrows)
-            s_lane = __ldg(p.epi_row_scale + ti.row0 + c0 + lane);
-          uint32_t v[16];
-          tmem_ld_x16(taddr + c0, v);
-          tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float s = __shfl_sync(0xffffffffu, s_lane, j);
-            if (col_ok && c0 + j < ti.nrows)
-              cp[static_cast<size_t>(c0 + j) * p.N] =
-                  __float2bfloat16_rn(epilogue_op(__uint_as_float(v[j]), bias, p.epi_act, s));
-          }
+        for (int q = 0; q + 1 < kRowRegs; ++q) {
+          rs[q] = rs[q + 1];
+          sc[q] = sc[q + 1];
         }
       }
       tc_fence_before_sync();

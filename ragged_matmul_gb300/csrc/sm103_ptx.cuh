@@ -446,6 +446,32 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 
+// The same two forms for 8-bit operands (kind::f8f6f4): K = 32 elements, i.e. the
+// same 32 bytes of each 128-byte swizzled row as one bf16 MMA, so the descriptors and
+// their per-step advance are the bf16 ones; the formats are in the instruction
+// descriptor.
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t.reg .b32 l;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the mbarrier at `bar` in every CTA of `cta_mask` when the pair MMAs
 // issued so far have completed.
 __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask) {
@@ -479,6 +505,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
   return (1u << 4)              // D format: f32
          | (1u << 7)            // A format: bf16
          | (1u << 10)           // B format: bf16
+         | ((N >> 3) << 17)     // N / 8
+         | ((M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor, kind::f8f6f4: e4m3 A and B (format code 0, both K-major),
+// fp32 D, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4)              // D format: f32
+         | (0u << 7)            // A format: e4m3
+         | (0u << 10)           // B format: e4m3
          | ((N >> 3) << 17)     // N / 8
          | ((M >> 4) << 24);    // M / 16
 }

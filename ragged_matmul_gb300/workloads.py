@@ -174,7 +174,7 @@ def group_range(r: Routing, lo: int, hi: int) -> Routing:
     loads = r.loads[lo:hi].copy()
     ids = r.expert_ids[lo:hi].copy()
     return Routing(f"{r.name}[{lo}:{hi}]", r.E, r.N, r.K, loads, ids, offsets_from_loads(loads), r.a_dist,
-                   r.b_dist, r.int4, r.group_size, r.scale_range)
+                   r.b_dist, r.int4, r.group_size, r.scale_range, dict(r.meta))
 
 
 def first_groups(r: Routing, G: int) -> Routing:
@@ -185,7 +185,7 @@ def first_groups(r: Routing, G: int) -> Routing:
     E = int(valid.max()) + 1 if valid.size else 1
     return Routing(f"{r.name}[:{G}]", E, r.N, r.K, r.loads[:G].copy(), ids.copy(),
                    offsets_from_loads(r.loads[:G]), r.a_dist, r.b_dist, r.int4, r.group_size,
-                   r.scale_range)
+                   r.scale_range, dict(r.meta))
 
 
 # ---------------------------------------------------------------- host values (numpy)

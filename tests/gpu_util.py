@@ -137,3 +137,66 @@ def check_against_oracle(h, r: wl.Routing, vals, *, rows_alloc=None, exact=False
     else:
         err = assert_close(got, ref.ref32, live, where)
     return got, ref, status, err
+
+
+# ---------------------------------------------------------------- block-scaled e4m3 path
+
+def to_dev_u8(x, dev):
+    torch = _torch()
+    return torch.from_numpy(np.ascontiguousarray(x, np.uint8)).to(dev)
+
+
+def to_dev_f32(x, dev):
+    torch = _torch()
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
+
+
+def run_gpu_fp8(h, vals, off, ids, granularity, *, N, rows_alloc=None, stats_init=None, epilogue=None,
+                dev="cuda:0"):
+    """Upload e4m3 operands and fp32 scales, run gmm_run_fp8, return (C bits, stats, status)."""
+    torch = _torch()
+    epi = {}
+    if epilogue:
+        if epilogue.get("bias_bits") is not None:
+            epi["bias"] = to_dev_u16(epilogue["bias_bits"], dev)
+        if epilogue.get("row_scale") is not None:
+            epi["row_scale"] = to_dev_f32(epilogue["row_scale"], dev)
+        epi["activation"] = epilogue.get("activation", "none")
+    rows = vals["a8"].shape[0] if rows_alloc is None else rows_alloc
+    c = sentinel_dev(rows, N, dev)
+    stats = to_dev_i32(np.full(4, 0xFFFFFFFF, np.uint32) if stats_init is None else stats_init, dev)
+    binding.gmm_run_fp8(h, c, to_dev_u8(vals["a8"], dev), to_dev_i32(off, dev), to_dev_u8(vals["w8"], dev),
+                        to_dev_i32(ids, dev), stats, to_dev_f32(vals["input_scale"], dev),
+                        to_dev_f32(vals["weight_scale"], dev), granularity, **epi)
+    status = binding.gmm_query_status(h)
+    torch.cuda.synchronize()
+    return bits_of(c), stats.cpu().numpy().view(np.uint32), status
+
+
+def check_fp8_against_oracle(h, r: wl.Routing, vals, granularity, *, rows_alloc=None, exact=False,
+                             epilogue=None, where=""):
+    """Full-output comparison of gmm_run_fp8 with the oracle (scales, then the optional
+    epilogue, on both sides)."""
+    rows_alloc = r.rows if rows_alloc is None else rows_alloc
+    gm, gn, gk = granularity
+    gran = (gm, gn, r.K if gk is None else gk)
+    ref = oracle.gmm_fp8(vals["a8"], r.a_offsets, vals["w8"], r.expert_ids, vals["input_scale"],
+                         vals["weight_scale"], gran, c_init=wl.sentinel_c(rows_alloc, r.N),
+                         stats_init=np.full(4, wl.SENTINEL_STATS, np.uint32))
+    got, stats, status = run_gpu_fp8(h, vals, r.a_offsets, r.expert_ids, granularity, N=r.N,
+                                     rows_alloc=rows_alloc, epilogue=epilogue)
+    if epilogue:
+        ref = oracle.apply_epilogue(ref, r.a_offsets, r.expert_ids, r.E, bias_bits=epilogue.get("bias_bits"),
+                                    row_scale=epilogue.get("row_scale"),
+                                    activation=epilogue.get("activation", "none"))
+    live = live_row_mask(rows_alloc, r.a_offsets, r.expert_ids, r.E)
+    if ref.flags & oracle.BAD_OFFSETS:
+        live[:] = False
+    assert np.array_equal(got[~live], ref.c[~live]), f"{where}: rows outside active groups changed"
+    assert np.array_equal(stats, ref.stats), f"{where}: stats {stats} != {ref.stats}"
+    if exact:
+        assert np.array_equal(got[live], ref.c[live]), f"{where}: not bit-exact"
+        err = 0.0
+    else:
+        err = assert_close(got, ref.ref32, live, where)
+    return got, ref, status, err
