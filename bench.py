@@ -69,19 +69,24 @@ def work_counts(r: wl.Routing):
     if r.int4:
         wbytes = r.N * r.K // 2 + r.N * (r.K // r.group_size) * 2
     elif is_fp8(r):   # e4m3 weights and their fp32 scales; e4m3 activations and their scales
-        wbytes = r.N * r.K + (-(-r.N // FP8_GRAN[1])) * 4
+        gm, gn, gk = fp8_gran(r)
+        nkb = -(-r.K // gk)
+        wbytes = r.N * r.K + (-(-r.N // gn)) * nkb * 4
     else:
         wbytes = r.N * r.K * 2
-    abytes = rows * (r.K + 4) if is_fp8(r) else rows * r.K * 2
+    abytes = rows * (r.K + 4 * -(-r.K // fp8_gran(r)[2])) if is_fp8(r) else rows * r.K * 2
     nbytes = len(experts) * wbytes + abytes + rows * r.N * 2 + 4 * (2 * r.G + 2)
     return flops, float(nbytes), rows
 
 
-FP8_GRAN = (1, 128, None)   # scale granularity (m, n, k) of the e4m3 workloads; k None: all of K
-
-
 def is_fp8(r: wl.Routing) -> bool:
     return bool(r.meta.get("fp8", False))
+
+
+def fp8_gran(r: wl.Routing):
+    """Scale granularity (m, n, k) of an e4m3 workload, k resolved to K when it spans all of K."""
+    gm, gn, gk = r.meta.get("granularity", (1, 128, None))
+    return gm, gn, (r.K if gk is None else gk)
 
 
 def kernel_source_hash():
@@ -95,9 +100,11 @@ def kernel_source_hash():
 
 def profiled_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it matches the current kernel."""
-    path = os.path.join(ROOT, "profiles", f"gmm_grouped_kernel_{workload}.md")
-    if not os.path.exists(path):
+    paths = [os.path.join(ROOT, "profiles", f"{k}_{workload}.md") for k in ("gmm_grouped_kernel", "gmm_fp8_block_kernel")]
+    paths = [x for x in paths if os.path.exists(x)]
+    if not paths:
         return None
+    path = paths[0]
     text = open(path).read()
     m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     hm = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
@@ -218,7 +225,7 @@ def host_values_as_tensors(r: wl.Routing, seed: int = 0):
     """Seeded host-generated operands as CPU torch tensors (for hosts without a GPU)."""
     import torch
     if is_fp8(r):
-        return {k: torch.from_numpy(x) for k, x in wl.fp8_host_values(r, seed, FP8_GRAN).items()}
+        return {k: torch.from_numpy(x) for k, x in wl.fp8_host_values(r, seed, fp8_gran(r)).items()}
     v = wl.host_values(r, seed)
     out = {"a": torch.from_numpy(v["a"].view(np.int16)).view(torch.bfloat16)}
     if r.int4:
@@ -267,8 +274,7 @@ def run_oracle(r: wl.Routing, s, nthreads):
     import oracle
     t0 = time.perf_counter()
     if is_fp8(r):
-        oracle.gmm_fp8(s["a8"], s["off"], s["w8"], s["ids"], s["input_scale"], s["weight_scale"],
-                       (FP8_GRAN[0], FP8_GRAN[1], r.K))
+        oracle.gmm_fp8(s["a8"], s["off"], s["w8"], s["ids"], s["input_scale"], s["weight_scale"], fp8_gran(r))
     elif r.int4:
         oracle.gmm_int4(s["a"], s["off"], s["packed"], s["scales"], s["ids"], group_size=r.group_size,
                         nthreads=nthreads)
@@ -343,8 +349,10 @@ def main():
               "l2": "flushed between steps (512 MiB written, then another 512 MiB read: cold, clean L2)",
               "weights": "int4" if r.int4 else ("e4m3" if is_fp8(r) else "bf16")}
     if is_fp8(r):
-        config["scales"] = ("fp32 input_scale per row, fp32 weight_scale per 128 weight rows of each expert "
-                            "(granularity (1, 128, K))")
+        gm, gn, gk = fp8_gran(r)
+        config["scales"] = (f"fp32 input_scale per {gm} row(s) and weight_scale per {gn} weight rows of each "
+                            f"expert, " + ("over all of K" if gk >= r.K else f"per {gk} of K") +
+                            f" (granularity ({gm}, {gn}, {gk}))")
     if args.epilogue != "none":
         config["epilogue"] = f"{args.epilogue}(acc + bias[e, n]) * row_scale[r], fused before the bf16 store"
 
@@ -353,7 +361,7 @@ def main():
         if rank != 0:
             return
         if torch.cuda.is_available():
-            vals = (wl.fp8_device_values(r, 0, FP8_GRAN, device=torch.device(f"cuda:{local}")) if is_fp8(r)
+            vals = (wl.fp8_device_values(r, 0, fp8_gran(r), device=torch.device(f"cuda:{local}")) if is_fp8(r)
                     else wl.device_values(r, 0, device=torch.device(f"cuda:{local}")))
         else:
             vals = host_values_as_tensors(r, 0)
@@ -391,7 +399,7 @@ def main():
         gbuild.build()
     barrier(world)
 
-    vals = wl.fp8_device_values(r, rank, FP8_GRAN, device=dev) if is_fp8(r) else wl.device_values(r, rank, device=dev)
+    vals = wl.fp8_device_values(r, rank, fp8_gran(r), device=dev) if is_fp8(r) else wl.device_values(r, rank, device=dev)
     akey = "a8" if is_fp8(r) else "a"
     if args.variant:
         os.environ["GMM_VARIANT"] = args.variant
@@ -418,7 +426,7 @@ def main():
     def step(cc=c, aa=vals[akey], oo=off, ii=ids, ss=stats):
         if is_fp8(r):
             binding.gmm_run_fp8(h, cc, aa, oo, vals["w8"], ii, ss, vals["input_scale"], vals["weight_scale"],
-                                FP8_GRAN, stream=stream, **epi)
+                                fp8_gran(r), stream=stream, **epi)
         elif r.name == "int4_dense":   # the dense quantised GEMM's own entry point
             binding.gmm_matmul_int4(h, cc, aa, vals["packed"][0], vals["scales"][0], group_size=r.group_size,
                                     stream=stream, **epi)
@@ -523,10 +531,11 @@ def main():
                     "peak_source": f"{peaks_kind} (burst)" + (" bf16 x 2, the nominal e4m3 : bf16 ratio"
                                                               if is_fp8(r) and bound == "tensor" else ""),
                     "roofline_time_ms": max(t_tensor, t_hbm) * 1e3,
-                    "kernel": "gmm_grouped_kernel<%s, %s, %s>" % (
-                        "true" if r.int4 else "false",
-                        "true" if (args.variant == "pair" or (args.variant is None and not r.int4)) else "false",
-                        "true" if is_fp8(r) else "false")}
+                    "kernel": ("gmm_fp8_block_kernel" if is_fp8(r) and fp8_gran(r)[2] < r.K else
+                               "gmm_grouped_kernel<%s, %s, %s>" % (
+                                   "true" if r.int4 else "false",
+                                   "true" if (args.variant == "pair" or (args.variant is None and not r.int4)) else "false",
+                                   "true" if is_fp8(r) else "false"))}
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",

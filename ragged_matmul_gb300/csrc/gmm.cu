@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -14,6 +15,7 @@
 
 #include "gmm.h"
 #include "gmm_kernel.cuh"
+#include "gmm_fp8_block.cuh"
 
 namespace {
 
@@ -41,6 +43,12 @@ struct DeviceGuard {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// GMM_DEBUG=1: report the CUDA call behind a GMM_ERR_CUDA on stderr (diagnostics only).
+void debug_report(const char *what, int code, const char *msg) {
+  static const bool on = getenv("GMM_DEBUG") != nullptr;
+  if (on) fprintf(stderr, "gmm: %s failed: %d %s\n", what, code, msg ? msg : "");
+}
+
 }  // namespace
 
 // One launch configuration per kernel variant.
@@ -56,6 +64,7 @@ struct gmm_ctx {
   int num_sms = 0;
   gmm_variant var[2][2];          // [4-bit][pair]
   gmm_variant var_fp8[2];         // e4m3 kernels, [pair]
+  gmm_variant var_fp8_block;      // e4m3 with per-K-block scales
   int use_pairs = 1;              // bf16 path: 1 = CTA-pair kernels (cta_group::2), 0 = one CTA per tile
   int use_pairs_int4 = 0;         // 4-bit path: the same (default one CTA per tile)
   uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
@@ -72,6 +81,7 @@ int encode_map(gmm_ctx *h, CUtensorMap *m, CUtensorMapDataType type, uint32_t ra
   CUresult r = h->encode(m, type, rank, const_cast<void *>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) debug_report("cuTensorMapEncodeTiled", static_cast<int>(r), nullptr);
   return r == CUDA_SUCCESS ? GMM_OK : GMM_ERR_CUDA;
 }
 
@@ -198,6 +208,42 @@ int configure(gmm_variant *v, int optin, int num_sms) {
   return GMM_OK;
 }
 
+// The per-K-block e4m3 kernel: one CTA per SM, as many 48 KB stages as fit.
+int configure_fp8_block(gmm_variant *v, int optin, int num_sms) {
+  cudaFuncAttributes attr;
+  if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(gmm::gmm_fp8_block_kernel)) != cudaSuccess)
+    return GMM_ERR_CUDA;
+  const long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024 - gmm::kBwBiasBytes;
+  v->stages = static_cast<int>(budget / static_cast<long>(gmm::kBwStageBytes));
+  if (v->stages > gmm::kMaxStages) v->stages = gmm::kMaxStages;
+  if (v->stages < 2) return GMM_ERR_UNSUPPORTED;
+  v->smem = static_cast<size_t>(v->stages) * gmm::kBwStageBytes + gmm::kBwBiasBytes + 1024;
+  if (cudaFuncSetAttribute(reinterpret_cast<const void *>(gmm::gmm_fp8_block_kernel),
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(v->smem)) != cudaSuccess)
+    return GMM_ERR_CUDA;
+  v->grid = num_sms;
+  return GMM_OK;
+}
+
+int launch_fp8_block(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
+  DeviceGuard guard(h->device);
+  const gmm_variant &v = h->var_fp8_block;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.blockDim = dim3(gmm::kBwThreads);
+  cfg.gridDim = dim3(static_cast<unsigned>(v.grid));
+  cfg.dynamicSmemBytes = v.smem;
+  cfg.stream = stream;
+  p.num_stages = v.stages;
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, gmm::gmm_fp8_block_kernel, p);
+  if (err != cudaSuccess) {
+    debug_report("launch of the block-scaled kernel", static_cast<int>(err), cudaGetErrorString(err));
+    cudaGetLastError();
+    return GMM_ERR_CUDA;
+  }
+  return GMM_OK;
+}
+
 template <bool kInt4, bool kFp8 = false>
 int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   DeviceGuard guard(h->device);
@@ -224,6 +270,7 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
     err = cudaLaunchKernelEx(&cfg, gmm::gmm_grouped_kernel<kInt4, false, kFp8>, p);
   }
   if (err != cudaSuccess) {
+    debug_report("launch of the grouped kernel", static_cast<int>(err), cudaGetErrorString(err));
     cudaGetLastError();
     return GMM_ERR_CUDA;
   }
@@ -288,7 +335,8 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
 
   const int single_ok = configure<false, false>(&h->var[0][0], optin, sms) == GMM_OK &&
                         configure<true, false>(&h->var[1][0], optin, sms) == GMM_OK &&
-                        configure<false, false, true>(&h->var_fp8[0], optin, sms) == GMM_OK;
+                        configure<false, false, true>(&h->var_fp8[0], optin, sms) == GMM_OK &&
+                        configure_fp8_block(&h->var_fp8_block, optin, sms) == GMM_OK;
   // Tuning override GMM_VARIANT: "single" forces the one-CTA kernels, "pair" the pairs.
   const char *variant = getenv("GMM_VARIANT");
   const bool pairs_ok = sms >= 2 && configure<false, true>(&h->var[0][1], optin, sms) == GMM_OK &&
@@ -379,7 +427,10 @@ int gmm_run_fp8(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offset
     return GMM_ERR_INVALID_ARG;
   const int gm = scales_granularity_mnk[0], gn = scales_granularity_mnk[1], gk = scales_granularity_mnk[2];
   if (gm < 1 || gn < 1 || gk < 1) return GMM_ERR_INVALID_ARG;
-  if (gk < K) return GMM_ERR_UNSUPPORTED;
+  // Per-K-block scales run the block-scaled kernel: whole 128-K stages per block, and
+  // one weight scale per 32-column TMEM load.
+  const bool blockwise = gk < K;
+  if (blockwise && (gk % 128 || gn % 32)) return GMM_ERR_UNSUPPORTED;
 
   GmmParams p;
   std::memset(&p, 0, sizeof(p));
@@ -387,21 +438,25 @@ int gmm_run_fp8(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offset
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(KU), static_cast<cuuint64_t>(N),
                           static_cast<cuuint64_t>(h->num_experts)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N) * K};
-    cuuint32_t box[3] = {gmm::kBK, gmm::kBlockN, 1};
+    const cuuint32_t rows = blockwise ? gmm::kBwRows : static_cast<cuuint32_t>(gmm::kBlockN);
+    cuuint32_t box[3] = {gmm::kBK, rows, 1};
     rc = encode_map(h, &p.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc) return rc;
   }
   rc = encode_token_maps(h, p, a, KU, 1);
   if (rc) return rc;
-  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, KU, max_tok(h, false));
+  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, KU,
+              blockwise ? gmm::kBwTok : max_tok(h, false));
   set_epilogue(p, epilogue);
   p.in_scale = input_scale;
   p.w_scale = weight_scale;
   p.scale_gm = gm;
   p.scale_gn = gn;
   p.w_scale_cols = (N + gn - 1) / gn;
-  return launch<false, true>(h, p, stream);
+  p.scale_kb = (K + gk - 1) / gk;
+  p.kb_stages = gk / 128;
+  return blockwise ? launch_fp8_block(h, p, stream) : launch<false, true>(h, p, stream);
 }
 
 }  // extern "C"

@@ -1,0 +1,301 @@
+// Block-scaled e4m3 grouped GEMM with per-K-block scales, for sm_103a.
+//
+// Operation (Modular "k_matmul_ragged_paged_scale" API page, section "Args":
+// input_scale and weight_scale multiply the input and the weight; template
+// parameter scales_granularity_mnk = (gm, gn, gk)), for each active group g with
+// expert e and rows r of the group:
+//   C[r, n] = bf16( sum_kb input_scale[r / gm, kb] * weight_scale[e, n / gn, kb]
+//                          * sum_{k in block kb} a[r, k] * w[e, n, k] )
+// then the optional epilogue, as in the grouped kernel.
+//
+// Each K block's partial sum is scaled before it joins the others, so the tensor
+// core cannot accumulate over all of K.  The MMA writes each block's partial into
+// one of two TMEM buffers; eight promotion warps fold it into a running fp32 sum
+// held in their registers, while the MMA fills the other buffer with the next block.
+//
+// Orientation.  Tokens are the MMA's M (128 rows per tile) and weights its N (256
+// rows), unlike the grouped kernel: a TMEM lane is then a token row, so the input
+// scale of a block is one value per thread, and with gn a multiple of 32 the weight
+// scale is one value per 32-column TMEM load.  A promotion is one multiply-add per
+// element.  Small groups pay for a 128-row M, which an HBM-bound tile hides.
+//
+// Roles (320 threads):
+//   warp 0       TMA producer: per stage (128 of K) a 128-row token slab (16 KB) and a
+//                256-row weight slab (32 KB), both 128-byte swizzled.
+//   warp 1       TMEM allocation (512 columns: two 256-column partial buffers) and the
+//                MMA issue (kind::f8f6f4, M = 128, N = 256, 4 MMAs per stage).
+//   warps 2..9   promotion and epilogue: warp w reads TMEM lane quadrant w % 4 and
+//                weight columns 128 * ((w - 2) / 4) .. + 128 of each partial; every
+//                thread owns one token row and 128 running sums.  After a tile's last
+//                block they apply the epilogue and store their row's 128 columns.
+//
+// Scheduling is the grouped kernel's static one (the same group scan and tile decode,
+// with 128-token x 256-weight tiles); every wait is bounded as there.
+#pragma once
+
+#include "gmm_kernel.cuh"
+
+namespace gmm {
+
+// The promotion warps: four per TMEM lane quadrant's worth of columns would leave
+// 96 registers a thread (warps spread over the four SM sub-partitions, 16K registers
+// each); two per quadrant (128 columns each, 10 warps in all) leave 168.
+constexpr uint32_t kBwPromoWarps = 8;
+constexpr int kBwThreads = 32 * (2 + kBwPromoWarps);
+constexpr uint32_t kBwTok = 128;                  // token rows per tile (MMA M)
+constexpr uint32_t kBwRows = 256;                 // weight rows per tile (MMA N)
+constexpr uint32_t kBwTBytes = kBwTok * 128;      // token slab of a stage: 128 rows x 128 e4m3
+constexpr uint32_t kBwWBytes = kBwRows * 128;     // weight slab of a stage
+constexpr uint32_t kBwStageBytes = kBwTBytes + kBwWBytes;
+constexpr uint32_t kBwCols = kBwRows * 4 / kBwPromoWarps;   // weight columns per promotion warp
+constexpr uint32_t kBwPiece = 8;                              // columns per TMEM load
+constexpr int kBwBiasBytes = kBwPromoWarps * kBwCols * 2;   // each promotion warp's bias columns (bf16)
+
+struct BwGeom {
+  static constexpr uint32_t kRows = kBwRows;
+  static constexpr uint32_t kMaxTok = kBwTok;
+  static constexpr uint32_t kTokAlign = 16;
+};
+
+// Each promotion thread keeps kBwCols running sums and an 8-column piece of a
+// partial in registers.
+__global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __grid_constant__ GmmParams p) {
+  using G = BwGeom;
+  __shared__ Ctrl ctl;
+  __shared__ uint32_t prefix[kMaxGroups + 1];
+  extern __shared__ uint8_t dyn_smem[];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t ST = static_cast<uint32_t>(p.num_stages);
+  const int KS = (p.K + kBK - 1) / kBK;   // stages per tile: 64 two-byte units = 128 e4m3 of K each
+  const int SPB = p.kb_stages;            // stages per scale block (gk / 128)
+  const int NKB = (KS + SPB - 1) / SPB;   // scale blocks per tile
+
+  const uint32_t dyn_base = smem_addr(dyn_smem);
+  const uint32_t ring = (dyn_base + 1023u) & ~1023u;
+  const uint32_t t_ring = ring;
+  const uint32_t w_ring = ring + ST * kBwTBytes;
+  const uint32_t bias_stage = w_ring + ST * kBwWBytes;
+
+  if (tid == 0) {
+    for (uint32_t s = 0; s < ST; ++s) {
+      mbar_init(smem_addr(&ctl.full[s]), 1);
+      mbar_init(smem_addr(&ctl.empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_addr(&ctl.acc_full[a]), 1);
+      mbar_init(smem_addr(&ctl.acc_empty[a]), kBwPromoWarps);
+    }
+    ctl.abort = 0;
+    ctl.active = 0;
+    ctl.flags = 0;
+    ctl.max_group_tiles = 0;
+    ctl.min_group_tiles = 0xffffffffu;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(&ctl.tmem_base), kTmemCols);
+    tmem_relinquish();
+    tc_fence_before_sync();
+  }
+  __syncthreads();
+  build_schedule<kBwThreads, G>(p, ctl, prefix);
+  if (blockIdx.x == 0 && tid == 0) {
+    p.stats[1] = ctl.active;
+    const uint32_t f = ctl.flags & (kStatusBadOffsets | kStatusBadExpert | kStatusTooLarge);
+    if (f) atomicOr(p.status, f);
+  }
+  tc_fence_after_sync();
+  const uint32_t tmem_base = ctl.tmem_base;
+  const uint32_t total = ctl.total_tiles;
+  volatile int *abort = &ctl.abort;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    // The CTA's token map: the host's map with the row extent patched to a_offsets[G]
+    // (rows past the end of A are zero-filled) and 128-row boxes.
+    uint8_t *slot = p.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlotBytes;
+    if (total > 0 && lane == 0) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(&p.tok_map);
+      uint4 *dst = reinterpret_cast<uint4 *>(slot);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dst[i] = src[i];
+      tensormap_set_dim1(dst, __ldg(p.a_offsets + p.num_groups));
+      tensormap_set_box1(dst, kBwTok);
+      tensormap_release();
+      tensormap_acquire(slot);
+      const CUtensorMap *tok = reinterpret_cast<const CUtensorMap *>(slot);
+      prefetch_tensormap(&p.w_map);
+      const uint64_t pol_first = l2_policy_evict_first();
+      const uint64_t pol_last = l2_policy_evict_last();
+      const uint64_t pol_normal = l2_policy_evict_normal();
+      Ring rt;
+      uint32_t pending = 0, pend_phase = 0;
+      bool ok = true;
+      for (uint32_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        const Tile ti = decode_tile<G>(t, prefix, p);
+        const uint64_t w_pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
+        const uint64_t t_pol = p.cache_hints ? pol_last : pol_normal;
+        for (int s = 0; s < KS; ++s) {
+          const uint32_t full = smem_addr(&ctl.full[rt.slot]);
+          if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
+          mbar_arrive_expect_tx(full, kBwStageBytes);
+          const int32_t k0 = s * kBK;
+          tma_load_2d_hint(t_ring + rt.slot * kBwTBytes, tok, full, k0, static_cast<int32_t>(ti.row0), t_pol);
+          tma_load_3d_hint(w_ring + rt.slot * kBwWBytes, &p.w_map, full, k0, static_cast<int32_t>(ti.n0), ti.e,
+                           w_pol);
+          pending |= 1u << rt.slot;
+          pend_phase = (pend_phase & ~(1u << rt.slot)) | (rt.phase << rt.slot);
+          rt.next(ST);
+        }
+      }
+      if (!ok) {
+        for (uint32_t s = 0; s < ST; ++s)
+          if (pending & (1u << s)) wait_phase_for(smem_addr(&ctl.full[s]), (pend_phase >> s) & 1u, kDrainLimitNs);
+        atomicOr(p.status, kStatusTimeout);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issue (whole warp, one elected lane)
+    if (total > 0) {
+      Ring rt;
+      uint32_t pb = 0, pb_phase = 0;   // partial buffer of the current block, and its use parity
+      bool ok = true;
+      const uint64_t t_desc0 = smem_desc_k_sw128(t_ring);
+      const uint64_t w_desc0 = smem_desc_k_sw128(w_ring);
+      const uint32_t idesc = idesc_e4m3_f32(kBwTok, kBwRows);
+      for (uint32_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        for (int s = 0; s < KS; ++s) {
+          const int in_block = s % SPB;
+          if (in_block == 0) {   // a new block starts in a free partial buffer
+            const bool free_ = __all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.acc_empty[pb]), pb_phase ^ 1u, abort));
+            if (!free_) { ok = false; break; }
+          }
+          const bool staged = __all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort));
+          if (!staged) { ok = false; break; }
+          tc_fence_after_sync();
+          const uint64_t a_desc = t_desc0 + ((rt.slot * kBwTBytes) >> 4);
+          const uint64_t b_desc = w_desc0 + ((rt.slot * kBwWBytes) >> 4);
+          const uint32_t d_tmem = tmem_base + pb * kAccCols;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)   // K = 32 e4m3 (32 bytes) per MMA
+            mma_f8(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (in_block | k) != 0);
+          mma_commit(smem_addr(&ctl.empty[rt.slot]));
+          rt.next(ST);
+          if (in_block == SPB - 1 || s == KS - 1) {   // the block's partial is complete
+            mma_commit(smem_addr(&ctl.acc_full[pb]));
+            pb ^= 1u;
+            if (pb == 0) pb_phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && lane == 0) atomicOr(p.status, kStatusTimeout);
+    }
+  } else {
+    // ------------------------------------------------------------ promotion and epilogue
+    const uint32_t quad = static_cast<uint32_t>(warp & 3);
+    const uint32_t part = static_cast<uint32_t>(warp - 2) >> 2;   // which kBwCols of the tile's 256 columns
+    const uint32_t trow = quad * 32 + static_cast<uint32_t>(lane);   // this thread's token row in the tile
+    __nv_bfloat16 *bias_s = reinterpret_cast<__nv_bfloat16 *>(dyn_smem + (bias_stage - dyn_base)) + (warp - 2) * kBwCols;
+    const int wcols = p.w_scale_cols;
+    uint32_t pb = 0, pb_phase = 0;
+    bool ok = true;
+    for (uint32_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const Tile ti = decode_tile<G>(t, prefix, p);
+      const bool row_ok = trow < ti.nrows;
+      const uint32_t grow = ti.row0 + trow;
+      const uint32_t ncol0 = ti.n0 + part * kBwCols;   // first of this warp's weight columns
+      // Scale rows: this thread's input scales and the warp's 32-column weight scales
+      // (gn is a multiple of 32); a block's scales are loaded before its partial is
+      // waited for, so the wait covers their latency.
+      const float *is_row = p.in_scale + static_cast<size_t>(grow / static_cast<uint32_t>(p.scale_gm)) * p.scale_kb;
+      // Weight scale rows of the 32-column chunks, as offsets from the expert's first
+      // row (a column past N reads row 0 and is never stored).
+      constexpr int kChunks = static_cast<int>(kBwCols / 32);
+      const float *ws_e = p.w_scale + static_cast<size_t>(ti.e) * wcols * p.scale_kb;
+      uint32_t ws_off[kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const uint32_t n = ncol0 + 32u * c;
+        ws_off[c] = (n < static_cast<uint32_t>(p.N) ? n / static_cast<uint32_t>(p.scale_gn) : 0u) *
+                    static_cast<uint32_t>(p.scale_kb);
+      }
+      float acc[kBwCols];
+#pragma unroll
+      for (int j = 0; j < static_cast<int>(kBwCols); ++j) acc[j] = 0.0f;
+      for (int kb = 0; kb < NKB; ++kb) {
+        const float isv = row_ok ? __ldg(is_row + kb) : 0.0f;
+        float wsv[kChunks];
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) wsv[c] = __ldg(ws_e + ws_off[c] + kb);
+        int w_ok = 1;
+        if (lane == 0) w_ok = wait_phase(smem_addr(&ctl.acc_full[pb]), pb_phase, abort);
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) { ok = false; break; }
+        tc_fence_after_sync();
+        const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + pb * kAccCols + part * kBwCols;
+#pragma unroll
+        for (int c = 0; c < static_cast<int>(kBwCols / kBwPiece); ++c) {
+          uint32_t v[kBwPiece];
+          tmem_ld_x8(taddr + kBwPiece * c, v);
+          tmem_ld_wait();
+          const float f = isv * wsv[c * kBwPiece / 32];
+#pragma unroll
+          for (int j = 0; j < static_cast<int>(kBwPiece); ++j)
+            acc[kBwPiece * c + j] = fmaf(f, __uint_as_float(v[j]), acc[kBwPiece * c + j]);
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&ctl.acc_empty[pb]));
+        pb ^= 1u;
+        if (pb == 0) pb_phase ^= 1u;
+      }
+      if (!ok) break;
+      // Epilogue: act(y + bias[e, n]) * row_scale[r] on the finished sums, 8 columns
+      // per 16-byte store (N is a multiple of 8: a group of 8 is in or past N whole).
+      const bool fused = p.epi_bias != nullptr || p.epi_row_scale != nullptr || p.epi_act != kActNone;
+      if (p.epi_bias != nullptr) {   // the warp's bias columns, staged once per tile
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < static_cast<int>(kBwCols / 32); ++i) {
+          const uint32_t j = static_cast<uint32_t>(lane) * (kBwCols / 32) + i;
+          const uint32_t n = ncol0 + j;
+          bias_s[j] = n < static_cast<uint32_t>(p.N) ? p.epi_bias[static_cast<size_t>(ti.e) * p.N + n]
+                                                      : __float2bfloat16_rn(0.0f);
+        }
+        __syncwarp();
+      }
+      const float rs = (p.epi_row_scale != nullptr && row_ok) ? __ldg(p.epi_row_scale + grow) : 1.0f;
+      __nv_bfloat16 *crow = p.c + static_cast<size_t>(grow) * p.N + ncol0;
+#pragma unroll
+      for (int q = 0; q < static_cast<int>(kBwCols / 8); ++q) {
+        float y[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y[k] = acc[8 * q + k];
+        if (fused) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float b = p.epi_bias != nullptr ? __bfloat162float(bias_s[8 * q + k]) : 0.0f;
+            y[k] = epilogue_op(y[k], b, p.epi_act, rs);
+          }
+        }
+        if (row_ok && ncol0 + 8u * q < static_cast<uint32_t>(p.N)) {
+          uint4 out;
+          out.x = pack_bf16x2(y[0], y[1]);
+          out.y = pack_bf16x2(y[2], y[3]);
+          out.z = pack_bf16x2(y[4], y[5]);
+          out.w = pack_bf16x2(y[6], y[7]);
+          *reinterpret_cast<uint4 *>(crow + 8 * q) = out;
+        }
+      }
+    }
+    if (!ok && lane == 0) atomicOr(p.status, kStatusTimeout);
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace gmm

@@ -208,6 +208,10 @@ struct alignas(128) GmmParams {
   int scale_gm;
   int scale_gn;
   int w_scale_cols;                // ceil(N / scale_gn)
+  // Per-K-block scales (the block-scaled kernel): scale_kb = ceil(K / gk) values per
+  // scale row, kb_stages = gk / 128 pipeline stages per block.
+  int scale_kb;
+  int kb_stages;
 };
 
 struct __align__(32) Tile {

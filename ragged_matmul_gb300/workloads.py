@@ -29,6 +29,9 @@ shapes this library targets):
   fp8_decode    A, B ~ e4m3(N(0, 2)) (the fp32 draw cast to e4m3, round to
                 nearest even), fp32 scales at granularity (1, 128, K):
                 input_scale ~ U[0.25, 1], weight_scale ~ U[0.002, 0.008].
+  fp8_block_prefill,  the same with per-K-block scales: granularity
+  fp8_block_decode    (1, 128, 128), one scale per row (input) or per 128
+                weight rows (weight) and 128 of K.
 
 Values are drawn in fp32 and rounded to bf16 (round to nearest even).  Host
 generation uses numpy's PCG64 (``default_rng``); device generation, used for
@@ -119,7 +122,7 @@ def _balanced_loads(rng, total, E, spread):
 
 
 WORKLOAD_NAMES = ("tiny", "decode", "prefill", "fine_grained", "int4", "int4_dense", "fp8_prefill",
-                  "fp8_decode")
+                  "fp8_decode", "fp8_block_prefill", "fp8_block_decode")
 WORKLOAD_SEEDS = {name: i for i, name in enumerate(WORKLOAD_NAMES)}
 
 
@@ -165,7 +168,11 @@ def routing(name: str, seed: int | None = None) -> Routing:
         # The scaled e4m3 variant on the prefill / decode routings and shapes; operand
         # values come from fp8_host_values / fp8_device_values.
         base = routing(name[4:], seed)
-        return replace(base, name=name, meta={"fp8": True})
+        return replace(base, name=name, meta={"fp8": True, "granularity": (1, 128, None)})
+    if name in ("fp8_block_prefill", "fp8_block_decode"):
+        # The same with per-K-block scales: granularity (1, 128, 128).
+        base = routing(name[10:], seed)
+        return replace(base, name=name, meta={"fp8": True, "granularity": (1, 128, 128)})
     raise KeyError(name)
 
 

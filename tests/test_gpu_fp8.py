@@ -162,7 +162,8 @@ def test_fp8_argument_errors():
                                None if pin is None else P(pin.data_ptr()), None if pw is None else P(pw.data_ptr()),
                                g, None, stream)
     assert call(K=56) == binding.GMM_ERR_INVALID_ARG                  # K not a multiple of 16
-    assert call(gran=(1, 128, 32)) == binding.GMM_ERR_UNSUPPORTED     # per-K-block scales
+    assert call(gran=(1, 128, 32)) == binding.GMM_ERR_UNSUPPORTED     # K blocks of less than 128
+    assert call(K=256, gran=(1, 48, 128)) == binding.GMM_ERR_UNSUPPORTED   # per-K-block with gn % 32 != 0
     assert call(gran=(0, 128, 64)) == binding.GMM_ERR_INVALID_ARG
     assert call(gran=(1, 0, 64)) == binding.GMM_ERR_INVALID_ARG
     assert call(gran=None) == binding.GMM_ERR_INVALID_ARG
@@ -183,7 +184,7 @@ def _sampled_fp8(name, rows_per_group=2, ncols=96, seed=0):
     """The full fp8 workload on the GPU, checked on sampled rows and columns."""
     import torch
     r = wl.routing(name)
-    gran = (1, 128, None)
+    gran = tuple(r.meta.get("granularity", (1, 128, None)))
     v = wl.fp8_device_values(r, seed, gran, device=DEV)
     h = handle(r.E)
     c = sentinel_dev(r.rows, r.N, DEV)
@@ -208,8 +209,9 @@ def _sampled_fp8(name, rows_per_group=2, ncols=96, seed=0):
     # The sampled columns are weight rows of each expert; their scales keep their own
     # block: with one column per block (gn = 1) the scale is gathered per column.
     ws = v["weight_scale"][:, (cols_t // gran[1]), :].cpu().numpy()
+    gk = r.K if gran[2] is None else gran[2]
     ref = oracle.gmm_fp8(v["a8"][rows_t].cpu().numpy(), off_s, v["w8"][:, cols_t, :].cpu().numpy(),
-                         r.expert_ids, v["input_scale"][rows_t].cpu().numpy(), ws, (1, 1, r.K))
+                         r.expert_ids, v["input_scale"][rows_t].cpu().numpy(), ws, (1, 1, gk))
     got = bits_of(c[rows_t][:, cols_t])
     live_s = live_row_mask(len(rows), off_s, r.expert_ids, r.E)
     err = assert_close(got, ref.ref32, live_s, where=name)
@@ -217,6 +219,61 @@ def _sampled_fp8(name, rows_per_group=2, ncols=96, seed=0):
     return err
 
 
-@pytest.mark.parametrize("name", ["fp8_decode", "fp8_prefill"])
+@pytest.mark.parametrize("name", ["fp8_decode", "fp8_prefill", "fp8_block_decode", "fp8_block_prefill"])
 def test_fp8_full_size_sampled(name):
     _sampled_fp8(name)
+
+
+# ---------------------------------------------------------------- per-K-block scales (gk < K)
+
+@pytest.mark.parametrize("N,K,gran", [(384, 512, (1, 128, 128)), (264, 1104, (1, 32, 128)),
+                                      (512, 768, (3, 64, 256)), (1024, 1024, (2, 256, 384)),
+                                      (136, 256, (1, 32, 128)), (256, 4096, (1, 128, 128))])
+def test_fp8_block_scales_ragged(N, K, gran):
+    """Ragged groups (1 .. 513 rows, a skipped one), N and K tails (K = 1104: a partial last
+    block), granularities that divide nothing, against the oracle's per-block sums."""
+    loads = [1, 15, 16, 17, 127, 128, 129, 255, 257, 513, 0, 40]
+    ids = [3, 0, 5, 1, 7, 2, 6, 4, -1, 0, 1, 2]
+    r, v = case(8, N, K, loads, ids, 20, gran=gran)
+    _, _, status, _ = check_fp8_against_oracle(handle(8), r, v, gran, where=f"fp8 block N={N} K={K} {gran}")
+    assert status == binding.GMM_OK
+
+
+def test_fp8_block_scales_bit_exact():
+    """e4m3 integers in [-3, 3] and power-of-two block scales: every partial, scaled
+    partial, sum and rounding is exact."""
+    r = wl.make_routing("t", 3, 256, 512, [1, 40, 0, 200, 17], [2, 0, 1, 1, -1])
+    rng = np.random.default_rng(21)
+    to8 = wl._to_e4m3_bits
+    v = {"a8": to8(rng.integers(-3, 4, (r.rows, 512)).astype(np.float32)),
+         "w8": to8(rng.integers(-3, 4, (3, 256, 512)).astype(np.float32)),
+         "input_scale": rng.choice([0.25, 0.5, 1.0], (r.rows, 4)).astype(np.float32),
+         "weight_scale": rng.choice([0.125, 0.25, 0.5], (3, 2, 4)).astype(np.float32)}
+    check_fp8_against_oracle(handle(3), r, v, (1, 128, 128), exact=True, where="fp8 block exact")
+
+
+@pytest.mark.parametrize("activation", ["none", "gelu_tanh"])
+def test_fp8_block_scales_with_epilogue(activation):
+    r, v = case(4, 392, 640, [1, 17, 0, 130, 33, 257, 7], [2, 0, 1, 3, -1, 1, 0], 22, gran=(2, 64, 128))
+    rng = np.random.default_rng(23)
+    epi = {"bias_bits": wl._to_bf16_bits(rng.normal(0.0, 0.1, (4, 392)).astype(np.float32)),
+           "row_scale": rng.uniform(0.1, 2.0, r.rows).astype(np.float32), "activation": activation}
+    _, _, status, _ = check_fp8_against_oracle(handle(4), r, v, (2, 64, 128), epilogue=epi,
+                                               where=f"fp8 block epilogue {activation}")
+    assert status == binding.GMM_OK
+
+
+def test_fp8_block_scales_edge_cases():
+    """Offset base with trailing rows, bad offsets (nothing written), and no groups."""
+    r, v = case(4, 256, 384, [50, 300, 20, 64], [-1, 2, 3, 0], 24, gran=(1, 128, 128), base=37)
+    rows_alloc = r.rows + 19
+    v = wl.fp8_host_values(r, 24, (1, 128, 128), rows=rows_alloc)
+    check_fp8_against_oracle(handle(4), r, v, (1, 128, 128), rows_alloc=rows_alloc, where="fp8 block base")
+    off = np.array([0, 30, 20, 80], np.uint32)
+    r2, v2 = case(4, 128, 256, [30, 40, 10], [0, 1, 2], 25, gran=(1, 128, 128))
+    got, stats, status = run_gpu_fp8(handle(4), v2, off, r2.expert_ids, (1, 128, 128), N=128)
+    assert np.all(got == wl.SENTINEL_BF16) and status == binding.GMM_ERR_BAD_INPUT
+    r3, v3 = case(4, 128, 256, [], [], 26, gran=(1, 128, 128), rows=16)
+    got, stats, status = run_gpu_fp8(handle(4), v3, r3.a_offsets, r3.expert_ids, (1, 128, 128), N=128,
+                                     rows_alloc=16)
+    assert np.all(got == wl.SENTINEL_BF16) and stats[1] == 0 and status == binding.GMM_OK
