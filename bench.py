@@ -531,7 +531,8 @@ def main():
                     "peak_source": f"{peaks_kind} (burst)" + (" bf16 x 2, the nominal e4m3 : bf16 ratio"
                                                               if is_fp8(r) and bound == "tensor" else ""),
                     "roofline_time_ms": max(t_tensor, t_hbm) * 1e3,
-                    "kernel": ("gmm_fp8_block_kernel" if is_fp8(r) and fp8_gran(r)[2] < r.K else
+                    "kernel": ("gmm_fp8_block_kernel<%s>" % ("true" if args.variant == "pair" else "false")
+                               if is_fp8(r) and fp8_gran(r)[2] < r.K else
                                "gmm_grouped_kernel<%s, %s, %s>" % (
                                    "true" if r.int4 else "false",
                                    "true" if (args.variant == "pair" or (args.variant is None and not r.int4)) else "false",

@@ -10,59 +10,83 @@
 //
 // Each K block's partial sum is scaled before it joins the others, so the tensor
 // core cannot accumulate over all of K.  The MMA writes each block's partial into
-// one of two TMEM buffers; eight promotion warps fold it into a running fp32 sum
-// held in their registers, while the MMA fills the other buffer with the next block.
+// one of two TMEM buffers; eight promotion warps per CTA fold it into a running fp32
+// sum held in their registers, while the MMA fills the other buffer with the next
+// block.
 //
-// Orientation.  Tokens are the MMA's M (128 rows per tile) and weights its N (256
-// rows), unlike the grouped kernel: a TMEM lane is then a token row, so the input
-// scale of a block is one value per thread, and with gn a multiple of 32 the weight
-// scale is one value per 32-column TMEM load.  A promotion is one multiply-add per
-// element.  Small groups pay for a 128-row M, which an HBM-bound tile hides.
+// Orientation.  Tokens are the MMA's M and weights its N (256 rows), unlike the
+// grouped kernel: a TMEM lane is then a token row, so the input scale of a block is
+// one value per thread, and with gn a multiple of 32 the weight scale is one value per
+// 32-column TMEM load.  A promotion is one multiply-add per element.
 //
-// Roles (320 threads):
-//   warp 0       TMA producer: per stage (128 of K) a 128-row token slab (16 KB) and a
-//                256-row weight slab (32 KB), both 128-byte swizzled.
+// Variants: kShare = false (default) runs one CTA per tile of 128 token rows.
+// kShare = true runs a cluster of two CTAs per tile of 256 token rows: each CTA
+// computes its own 128 rows (its own MMAs, partial buffers and promotion), but a
+// stage's weight slab is loaded once for both, each CTA copying half of it with TMA
+// multicast into both CTAs' shared memory (32 KB per CTA and stage from L2 instead of
+// 48 KB).  It measured no faster, because neither form is bound by its
+// copies: a K block of 128 is one stage, and the MMA warp's own path through a stage
+// (the partial-buffer wait, the stage wait, four MMA issues, two commits; about 1,100
+// cycles under load) is longer than the stage's tensor work (335 to 670 cycles).
+// Tried and measured no better: 192- and 128-row tiles with 12 promotion warps or four
+// partial buffers, and a CTA-pair form (cta_group::2), whose every block crosses CTAs
+// twice.
+//
+// Roles (320 threads per CTA):
+//   warp 0       TMA producer: per stage (128 of K) a 128-row token slab (16 KB) and
+//                this CTA's weight rows (half of them, multicast to both CTAs, or all),
+//                128-byte swizzled.
 //   warp 1       TMEM allocation (512 columns: two 256-column partial buffers) and the
-//                MMA issue (kind::f8f6f4, M = 128, N = 256, 4 MMAs per stage).
+//                MMA issue (kind::f8f6f4, M = 128, N = 256, 4 MMAs per stage).  With
+//                kShare a stage slot is free once both CTAs' MMAs have read it: the
+//                commit that frees it arrives on both CTAs' barriers.
 //   warps 2..9   promotion and epilogue: warp w reads TMEM lane quadrant w % 4 and
 //                weight columns 128 * ((w - 2) / 4) .. + 128 of each partial; every
 //                thread owns one token row and 128 running sums.  After a tile's last
 //                block they apply the epilogue and store their row's 128 columns.
 //
-// Scheduling is the grouped kernel's static one (the same group scan and tile decode,
-// with 128-token x 256-weight tiles); every wait is bounded as there.
+// Registers: the warps of a CTA spread over the SM's four sub-partitions, 16K
+// registers each, so ten warps leave 168 registers a thread, of which 128 are running
+// sums; the partial is read 16 columns per TMEM wait.
+//
+// Scheduling is the grouped kernel's static one (the same group scan and tile decode);
+// every wait is bounded as there.
 #pragma once
 
 #include "gmm_kernel.cuh"
 
 namespace gmm {
 
-// The promotion warps: four per TMEM lane quadrant's worth of columns would leave
-// 96 registers a thread (warps spread over the four SM sub-partitions, 16K registers
-// each); two per quadrant (128 columns each, 10 warps in all) leave 168.
-constexpr uint32_t kBwPromoWarps = 8;
+constexpr uint32_t kBwPromoWarps = 8;              // two per TMEM lane quadrant
 constexpr int kBwThreads = 32 * (2 + kBwPromoWarps);
-constexpr uint32_t kBwTok = 128;                  // token rows per tile (MMA M)
-constexpr uint32_t kBwRows = 256;                 // weight rows per tile (MMA N)
-constexpr uint32_t kBwTBytes = kBwTok * 128;      // token slab of a stage: 128 rows x 128 e4m3
-constexpr uint32_t kBwWBytes = kBwRows * 128;     // weight slab of a stage
-constexpr uint32_t kBwStageBytes = kBwTBytes + kBwWBytes;
+constexpr uint32_t kBwCtaTok = 128;                // token rows per CTA (its TMEM lanes)
+constexpr uint32_t kBwRows = 256;                  // weight rows per tile (MMA N)
+constexpr uint32_t kBwBufs = kTmemCols / kBwRows;  // partial buffers in TMEM
+constexpr uint32_t kBwTBytes = kBwCtaTok * 128;    // token slab of a stage: 128 rows x 128 e4m3
 constexpr uint32_t kBwCols = kBwRows * 4 / kBwPromoWarps;   // weight columns per promotion warp
-constexpr uint32_t kBwPiece = 8;                              // columns per TMEM load
+constexpr uint32_t kBwPiece = 16;                  // columns per TMEM wait
 constexpr int kBwBiasBytes = kBwPromoWarps * kBwCols * 2;   // each promotion warp's bias columns (bf16)
 
+template <bool kShare>
 struct BwGeom {
   static constexpr uint32_t kRows = kBwRows;
-  static constexpr uint32_t kMaxTok = kBwTok;
+  static constexpr uint32_t kMaxTok = kShare ? 2 * kBwCtaTok : kBwCtaTok;   // token rows per tile
   static constexpr uint32_t kTokAlign = 16;
+  static constexpr uint32_t kCtaRows = kShare ? kBwRows / 2 : kBwRows;      // weight rows a CTA copies
+  static constexpr uint32_t kWBytes = kBwRows * 128;                        // a stage's weight slab
+  static constexpr uint32_t kStageBytes = kBwTBytes + kWBytes;              // shared memory per stage
+  static_assert((kCtaRows * 128) % 1024 == 0, "weight halves keep the 1024-byte swizzle alignment");
 };
 
-// Each promotion thread keeps kBwCols running sums and an 8-column piece of a
-// partial in registers.
+// Each promotion thread keeps kBwCols running sums and a 32-column piece of a partial
+// in registers.
+template <bool kShare>
 __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __grid_constant__ GmmParams p) {
-  using G = BwGeom;
+  using G = BwGeom<kShare>;
   __shared__ Ctrl ctl;
   __shared__ uint32_t prefix[kMaxGroups + 1];
+  __shared__ uint64_t part_full[kBwBufs];    // a block's partial is in the buffer (MMA commit)
+  __shared__ uint64_t part_empty[kBwBufs];   // every promotion warp has read it
   extern __shared__ uint8_t dyn_smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -70,21 +94,23 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   const int KS = (p.K + kBK - 1) / kBK;   // stages per tile: 64 two-byte units = 128 e4m3 of K each
   const int SPB = p.kb_stages;            // stages per scale block (gk / 128)
   const int NKB = (KS + SPB - 1) / SPB;   // scale blocks per tile
+  const uint32_t rank = kShare ? cluster_ctarank() : 0u;
 
+  // 1024-byte aligned rings, at identical offsets in both CTAs of a cluster.
   const uint32_t dyn_base = smem_addr(dyn_smem);
   const uint32_t ring = (dyn_base + 1023u) & ~1023u;
   const uint32_t t_ring = ring;
   const uint32_t w_ring = ring + ST * kBwTBytes;
-  const uint32_t bias_stage = w_ring + ST * kBwWBytes;
+  const uint32_t bias_stage = w_ring + ST * G::kWBytes;
 
   if (tid == 0) {
     for (uint32_t s = 0; s < ST; ++s) {
       mbar_init(smem_addr(&ctl.full[s]), 1);
-      mbar_init(smem_addr(&ctl.empty[s]), 1);
+      mbar_init(smem_addr(&ctl.empty[s]), kShare ? 2 : 1);   // both CTAs' MMAs read the slot
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(smem_addr(&ctl.acc_full[a]), 1);
-      mbar_init(smem_addr(&ctl.acc_empty[a]), kBwPromoWarps);
+    for (uint32_t a = 0; a < kBwBufs; ++a) {
+      mbar_init(smem_addr(&part_full[a]), 1);
+      mbar_init(smem_addr(&part_empty[a]), kBwPromoWarps);
     }
     ctl.abort = 0;
     ctl.active = 0;
@@ -100,6 +126,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   }
   __syncthreads();
   build_schedule<kBwThreads, G>(p, ctl, prefix);
+  if constexpr (kShare) cluster_sync();   // the peer's barriers are initialised before anyone signals them
   if (blockIdx.x == 0 && tid == 0) {
     p.stats[1] = ctl.active;
     const uint32_t f = ctl.flags & (kStatusBadOffsets | kStatusBadExpert | kStatusTooLarge);
@@ -109,6 +136,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   const uint32_t tmem_base = ctl.tmem_base;
   const uint32_t total = ctl.total_tiles;
   volatile int *abort = &ctl.abort;
+  const uint32_t unit0 = kShare ? cluster_id_x() : blockIdx.x;   // static share: tiles unit0, unit0 + units, ...
+  const uint32_t units = kShare ? cluster_count_x() : gridDim.x;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -121,7 +150,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
 #pragma unroll
       for (int i = 0; i < 8; ++i) dst[i] = src[i];
       tensormap_set_dim1(dst, __ldg(p.a_offsets + p.num_groups));
-      tensormap_set_box1(dst, kBwTok);
+      tensormap_set_box1(dst, kBwCtaTok);
       tensormap_release();
       tensormap_acquire(slot);
       const CUtensorMap *tok = reinterpret_cast<const CUtensorMap *>(slot);
@@ -132,24 +161,30 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
       Ring rt;
       uint32_t pending = 0, pend_phase = 0;
       bool ok = true;
-      for (uint32_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (uint32_t t = unit0; t < total && ok; t += units) {
         const Tile ti = decode_tile<G>(t, prefix, p);
         const uint64_t w_pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
         const uint64_t t_pol = p.cache_hints ? pol_last : pol_normal;
+        const int32_t t_row = static_cast<int32_t>(ti.row0 + rank * kBwCtaTok);
+        const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * G::kCtaRows);
         for (int s = 0; s < KS; ++s) {
           const uint32_t full = smem_addr(&ctl.full[rt.slot]);
           if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
-          mbar_arrive_expect_tx(full, kBwStageBytes);
+          // This CTA's token slab and the whole weight slab (its own half plus, shared,
+          // the peer's multicast half) land in this CTA's slot.
+          mbar_arrive_expect_tx(full, G::kStageBytes);
           const int32_t k0 = s * kBK;
-          tma_load_2d_hint(t_ring + rt.slot * kBwTBytes, tok, full, k0, static_cast<int32_t>(ti.row0), t_pol);
-          tma_load_3d_hint(w_ring + rt.slot * kBwWBytes, &p.w_map, full, k0, static_cast<int32_t>(ti.n0), ti.e,
-                           w_pol);
+          tma_load_2d_hint(t_ring + rt.slot * kBwTBytes, tok, full, k0, t_row, t_pol);
+          const uint32_t w_dst = w_ring + rt.slot * G::kWBytes + rank * (G::kCtaRows * 128);
+          if constexpr (kShare) tma_load_3d_mc(w_dst, &p.w_map, full, k0, w_row, ti.e, 0x3, w_pol);
+          else tma_load_3d_hint(w_dst, &p.w_map, full, k0, w_row, ti.e, w_pol);
           pending |= 1u << rt.slot;
           pend_phase = (pend_phase & ~(1u << rt.slot)) | (rt.phase << rt.slot);
           rt.next(ST);
         }
       }
       if (!ok) {
+        // Let the copies already issued land before the CTA can exit.
         for (uint32_t s = 0; s < ST; ++s)
           if (pending & (1u << s)) wait_phase_for(smem_addr(&ctl.full[s]), (pend_phase >> s) & 1u, kDrainLimitNs);
         atomicOr(p.status, kStatusTimeout);
@@ -163,29 +198,33 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
       bool ok = true;
       const uint64_t t_desc0 = smem_desc_k_sw128(t_ring);
       const uint64_t w_desc0 = smem_desc_k_sw128(w_ring);
-      const uint32_t idesc = idesc_e4m3_f32(kBwTok, kBwRows);
-      for (uint32_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      const uint32_t idesc = idesc_e4m3_f32(kBwCtaTok, kBwRows);
+      for (uint32_t t = unit0; t < total && ok; t += units) {
         for (int s = 0; s < KS; ++s) {
           const int in_block = s % SPB;
           if (in_block == 0) {   // a new block starts in a free partial buffer
-            const bool free_ = __all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.acc_empty[pb]), pb_phase ^ 1u, abort));
+            const bool free_ =
+                __all_sync(0xffffffffu, wait_phase(smem_addr(&part_empty[pb]), pb_phase ^ 1u, abort));
             if (!free_) { ok = false; break; }
           }
           const bool staged = __all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort));
           if (!staged) { ok = false; break; }
           tc_fence_after_sync();
           const uint64_t a_desc = t_desc0 + ((rt.slot * kBwTBytes) >> 4);
-          const uint64_t b_desc = w_desc0 + ((rt.slot * kBwWBytes) >> 4);
-          const uint32_t d_tmem = tmem_base + pb * kAccCols;
+          const uint64_t b_desc = w_desc0 + ((rt.slot * G::kWBytes) >> 4);
+          const uint32_t d_tmem = tmem_base + pb * kBwRows;
 #pragma unroll
           for (int k = 0; k < 4; ++k)   // K = 32 e4m3 (32 bytes) per MMA
             mma_f8(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (in_block | k) != 0);
-          mma_commit(smem_addr(&ctl.empty[rt.slot]));
+          if constexpr (kShare) mma_commit_mc(smem_addr(&ctl.empty[rt.slot]), 0x3);   // frees the slot in both CTAs
+          else mma_commit(smem_addr(&ctl.empty[rt.slot]));
           rt.next(ST);
           if (in_block == SPB - 1 || s == KS - 1) {   // the block's partial is complete
-            mma_commit(smem_addr(&ctl.acc_full[pb]));
-            pb ^= 1u;
-            if (pb == 0) pb_phase ^= 1u;
+            mma_commit(smem_addr(&part_full[pb]));
+            if (++pb == kBwBufs) {
+              pb = 0;
+              pb_phase ^= 1u;
+            }
           }
         }
       }
@@ -194,20 +233,21 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   } else {
     // ------------------------------------------------------------ promotion and epilogue
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
-    const uint32_t part = static_cast<uint32_t>(warp - 2) >> 2;   // which kBwCols of the tile's 256 columns
-    const uint32_t trow = quad * 32 + static_cast<uint32_t>(lane);   // this thread's token row in the tile
+    const uint32_t part = static_cast<uint32_t>(warp - 2) >> 2;   // which kBwCols of the tile's columns
+    // This thread's token row in the tile (a cluster's second CTA holds rows 128 .. 255).
+    const uint32_t trow = rank * kBwCtaTok + quad * 32 + static_cast<uint32_t>(lane);
     __nv_bfloat16 *bias_s = reinterpret_cast<__nv_bfloat16 *>(dyn_smem + (bias_stage - dyn_base)) + (warp - 2) * kBwCols;
     const int wcols = p.w_scale_cols;
     uint32_t pb = 0, pb_phase = 0;
     bool ok = true;
-    for (uint32_t t = blockIdx.x; t < total && ok; t += gridDim.x) {
+    for (uint32_t t = unit0; t < total && ok; t += units) {
       const Tile ti = decode_tile<G>(t, prefix, p);
       const bool row_ok = trow < ti.nrows;
       const uint32_t grow = ti.row0 + trow;
       const uint32_t ncol0 = ti.n0 + part * kBwCols;   // first of this warp's weight columns
       // Scale rows: this thread's input scales and the warp's 32-column weight scales
-      // (gn is a multiple of 32); a block's scales are loaded before its partial is
-      // waited for, so the wait covers their latency.
+      // (gn is a multiple of 32), loaded one block ahead of their use (loaded in the
+      // same block, their latency was exposed once per block).
       const float *is_row = p.in_scale + static_cast<size_t>(grow / static_cast<uint32_t>(p.scale_gm)) * p.scale_kb;
       // Weight scale rows of the 32-column chunks, as offsets from the expert's first
       // row (a column past N reads row 0 and is never stored).
@@ -223,31 +263,40 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
       float acc[kBwCols];
 #pragma unroll
       for (int j = 0; j < static_cast<int>(kBwCols); ++j) acc[j] = 0.0f;
+      float isn = row_ok ? __ldg(is_row) : 0.0f, wsn[kChunks];
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) wsn[c] = __ldg(ws_e + ws_off[c]);
       for (int kb = 0; kb < NKB; ++kb) {
-        const float isv = row_ok ? __ldg(is_row + kb) : 0.0f;
+        const float isv = isn;
         float wsv[kChunks];
 #pragma unroll
-        for (int c = 0; c < kChunks; ++c) wsv[c] = __ldg(ws_e + ws_off[c] + kb);
+        for (int c = 0; c < kChunks; ++c) wsv[c] = wsn[c];
+        if (kb + 1 < NKB) {
+          if (row_ok) isn = __ldg(is_row + kb + 1);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) wsn[c] = __ldg(ws_e + ws_off[c] + kb + 1);
+        }
         int w_ok = 1;
-        if (lane == 0) w_ok = wait_phase(smem_addr(&ctl.acc_full[pb]), pb_phase, abort);
+        if (lane == 0) w_ok = wait_phase(smem_addr(&part_full[pb]), pb_phase, abort);
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) { ok = false; break; }
         tc_fence_after_sync();
-        const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + pb * kAccCols + part * kBwCols;
+        const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + pb * kBwRows + part * kBwCols;
 #pragma unroll
         for (int c = 0; c < static_cast<int>(kBwCols / kBwPiece); ++c) {
-          uint32_t v[kBwPiece];
-          tmem_ld_x8(taddr + kBwPiece * c, v);
+          uint32_t v[16];
+          tmem_ld_x16(taddr + kBwPiece * c, v);
           tmem_ld_wait();
           const float f = isv * wsv[c * kBwPiece / 32];
 #pragma unroll
-          for (int j = 0; j < static_cast<int>(kBwPiece); ++j)
-            acc[kBwPiece * c + j] = fmaf(f, __uint_as_float(v[j]), acc[kBwPiece * c + j]);
+          for (int j = 0; j < 16; ++j) acc[kBwPiece * c + j] = fmaf(f, __uint_as_float(v[j]), acc[kBwPiece * c + j]);
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&ctl.acc_empty[pb]));
-        pb ^= 1u;
-        if (pb == 0) pb_phase ^= 1u;
+        if (lane == 0) mbar_arrive(smem_addr(&part_empty[pb]));
+        if (++pb == kBwBufs) {
+          pb = 0;
+          pb_phase ^= 1u;
+        }
       }
       if (!ok) break;
       // Epilogue: act(y + bias[e, n]) * row_scale[r] on the finished sums, 8 columns
@@ -292,6 +341,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   }
 
   __syncthreads();
+  if constexpr (kShare) cluster_sync();   // no CTA leaves while its peer may still write or signal it
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
