@@ -200,8 +200,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
       const uint64_t w_desc0 = smem_desc_k_sw128(w_ring);
       const uint32_t idesc = idesc_e4m3_f32(kBwCtaTok, kBwRows);
       for (uint32_t t = unit0; t < total && ok; t += units) {
-        for (int s = 0; s < KS; ++s) {
-          const int in_block = s % SPB;
+        int in_block = 0;   // stage within its scale block (s % SPB, counted)
+        for (int s = 0; s < KS; ++s, in_block = (in_block + 1 == SPB) ? 0 : in_block + 1) {
           if (in_block == 0) {   // a new block starts in a free partial buffer
             const bool free_ =
                 __all_sync(0xffffffffu, wait_phase(smem_addr(&part_empty[pb]), pb_phase ^ 1u, abort));
