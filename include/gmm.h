@@ -158,18 +158,21 @@ int gmm_run_int4_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_of
  * Block-scaled e4m3 grouped GEMM (Modular "k_matmul_ragged_paged_scale", section
  * "Args": input_scale and weight_scale multiply the input and the weight; template
  * parameter scales_granularity_mnk; without the page's paged KV-cache write, the
- * result goes to C as in gmm_run).  With (gm, gn, gk) = scales_granularity_mnk:
- *     C[r, n] = bf16( input_scale[r / gm] * weight_scale[e, n / gn]
- *                     * sum_k a[r, k] * b[e, n, k] )
+ * result goes to C as in gmm_run).  With (gm, gn, gk) = scales_granularity_mnk and
+ * kb = k / gk the K block of k:
+ *     C[r, n] = bf16( sum_kb input_scale[r / gm, kb] * weight_scale[e, n / gn, kb]
+ *                            * sum_{k in block kb} a[r, k] * b[e, n, k] )
  * for the rows and groups of gmm_run, a and b e4m3 (1 sign, 4 exponent bits with
- * bias 7, 3 mantissa bits), the sum in fp32.  Then the optional epilogue.
+ * bias 7, 3 mantissa bits), sums in fp32.  Then the optional epilogue.
  *   a: e4m3 bytes [rows, K] (16-byte aligned); b: e4m3 bytes [num_experts, N, K]
- *   (16-byte aligned); input_scale: fp32 [ceil(rows / gm)]; weight_scale: fp32
- *   [num_experts, ceil(N / gn)] (both 4-byte aligned, read only for active groups);
- *   c and the other arguments as gmm_run.
+ *   (16-byte aligned); input_scale: fp32 [ceil(rows / gm), ceil(K / gk)];
+ *   weight_scale: fp32 [num_experts, ceil(N / gn), ceil(K / gk)] (both row-major,
+ *   4-byte aligned, read only for active groups); c and the rest as gmm_run.
  * Requirements: those of gmm_run with K a multiple of 16 (an e4m3 row is K bytes, a
- * multiple of 16 for TMA), gm, gn >= 1, and gk >= K: one scale over the whole
- * reduction.  gk < K (per-K-block scales) returns GMM_ERR_UNSUPPORTED.
+ * multiple of 16 for TMA), gm, gn, gk >= 1, and either gk >= K (one scale over the
+ * whole reduction, applied to the finished sum) or gk a multiple of 128 with gn a
+ * multiple of 32 (per-K-block scales, a kernel of their own); other granularities
+ * return GMM_ERR_UNSUPPORTED.
  * Errors: as gmm_run_ex, plus GMM_ERR_INVALID_ARG for NULL or misaligned scales,
  * a NULL scales_granularity_mnk or a granularity below 1.
  */
