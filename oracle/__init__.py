@@ -121,7 +121,7 @@ def gmm_bf16(a_bits, a_offsets, b_bits, expert_ids, *, c_init=None, stats_init=N
     G = ids.size
     assert off.size == G + 1
     c = (np.zeros((rows, N), np.uint16) if c_init is None
-         else np.array(c_init, dtype=np.uint16, copy=True).reshape(rows, N))
+         else np.array(c_init, dtype=np.uint16, copy=True, order="C").reshape(rows, N))
     ref32 = np.full((rows, N), np.nan, np.float32)
     ref64 = np.full((rows, N), np.nan, np.float64) if want64 else None
     stats = (np.zeros(4, np.uint32) if stats_init is None
@@ -162,7 +162,7 @@ def gmm_int4(a_bits, a_offsets, packed, scales, expert_ids, *, group_size: int =
     G = ids.size
     assert off.size == G + 1
     c = (np.zeros((rows, N), np.uint16) if c_init is None
-         else np.array(c_init, dtype=np.uint16, copy=True).reshape(rows, N))
+         else np.array(c_init, dtype=np.uint16, copy=True, order="C").reshape(rows, N))
     ref32 = np.full((rows, N), np.nan, np.float32)
     ref64 = np.full((rows, N), np.nan, np.float64) if want64 else None
     stats = (np.zeros(4, np.uint32) if stats_init is None
@@ -276,7 +276,7 @@ def gmm_fp8(a8, a_offsets, w8, expert_ids, input_scale, weight_scale, granularit
     ids = np.asarray(expert_ids, dtype=np.int64)
     flags, active = validate(a_offsets, expert_ids, E)
     c = (np.zeros((rows, N), np.uint16) if c_init is None
-         else np.array(c_init, dtype=np.uint16, copy=True).reshape(rows, N))
+         else np.array(c_init, dtype=np.uint16, copy=True, order="C").reshape(rows, N))
     ref32 = np.full((rows, N), np.nan, np.float32)
     ref64 = np.full((rows, N), np.nan, np.float64)
     stats = (np.zeros(4, np.uint32) if stats_init is None
@@ -299,3 +299,56 @@ def gmm_fp8(a8, a_offsets, w8, expert_ids, input_scale, weight_scale, granularit
         ref32[r0:r1] = y.astype(np.float32)
         c[r0:r1] = round_bf16(ref32[r0:r1])
     return OracleResult(c, ref32, ref64, stats, flags)
+
+
+# ---------------------------------------------------------------- A-plane row offsetting
+# The grouped GEMM page's a_plane_splits parameter (Modular "grouped_matmul_sm100_persistent",
+# section "Parameters": per-plane split sizes for fused LoRA QKV A-plane row offsetting;
+# (0, 0) disables it).  The reading taken: A holds three planes of M = a_offsets[G] rows
+# stacked along its rows (the q, k and v inputs of a fused QKV projection), the split
+# sizes (s0, s1) cut the N columns of C and B into the q, k and v parts, and column n
+# reads the plane p(n) its part belongs to:
+#     ref[r, n] = sum_k A[p(n) * M + r, k] * B[e, n, k],
+#     p(n) = 0 for n < s0, 1 for s0 <= n < s0 + s1, 2 otherwise.
+
+def plane_of_columns(N: int, splits) -> np.ndarray:
+    """p(n) for n in [0, N): the plane each output column reads (all 0 when splits = (0, 0))."""
+    s0, s1 = (int(x) for x in splits)
+    n = np.arange(N)
+    if s0 == 0 and s1 == 0:
+        return np.zeros(N, np.int64)
+    return (n >= s0).astype(np.int64) + (n >= s0 + s1).astype(np.int64)
+
+
+def gmm_bf16_planes(a_bits, a_offsets, b_bits, expert_ids, splits, *, c_init=None,
+                    stats_init=None, nthreads: int | None = None) -> OracleResult:
+    """The grouped GEMM with A-plane row offsetting: the bf16 oracle run once per plane on
+    that plane's rows of A and its columns of B, the results put in their columns of C."""
+    a = np.asarray(a_bits, np.uint16)
+    b = np.asarray(b_bits, np.uint16)
+    E, N, K = b.shape
+    off = np.asarray(a_offsets, np.uint32)
+    M = int(off[-1]) if off.size else 0
+    planes = plane_of_columns(N, splits)
+    first = gmm_bf16(a[:M] if M else a, a_offsets, b[:, :0, :] if N == 0 else b[:, :1, :], expert_ids,
+                     stats_init=stats_init, nthreads=nthreads)   # flags and stats only
+    rows = M
+    c = (np.zeros((rows, N), np.uint16) if c_init is None
+         else np.array(c_init, dtype=np.uint16, copy=True)[:rows].reshape(rows, N))
+    ref32 = np.full((rows, N), np.nan, np.float32)
+    for p in range(3):
+        cols = np.flatnonzero(planes == p)
+        if cols.size == 0:
+            continue
+        part = gmm_bf16(a[p * M:(p + 1) * M], a_offsets, b[:, cols, :], expert_ids,
+                        c_init=c[:, cols], nthreads=nthreads)
+        c[:, cols] = part.c
+        ref32[:, cols] = part.ref32
+    if c_init is not None:
+        full = np.array(c_init, dtype=np.uint16, copy=True)
+        full[:rows] = c
+        c = full
+        r32 = np.full(full.shape, np.nan, np.float32)
+        r32[:rows] = ref32
+        ref32 = r32
+    return OracleResult(c, ref32, None, first.stats, first.flags)

@@ -527,3 +527,64 @@ def test_fp8_invalid_inputs_follow_the_grouped_rules():
                          (1, 8, 16), c_init=c0)
     assert oob.flags & oracle.BAD_EXPERT_ID and oob.stats[1] == 1
     assert np.all(oob.c[2:] == wl.SENTINEL_BF16) and not np.any(oob.c[:2] == wl.SENTINEL_BF16)
+
+
+# ------------------------------------------------------------------ A-plane row offsetting
+
+def _plane_problem(seed, E, N, K, loads, ids, planes=3):
+    r = wl.make_routing("t", E, N, K, loads, ids, a_dist=("normal", 1.0), b_dist=("normal", 1.0))
+    rng = np.random.default_rng(seed)
+    a = bf16_bits(rng.standard_normal((planes * r.rows, K)).astype(np.float32))
+    b = bf16_bits(rng.standard_normal((E, N, K)).astype(np.float32))
+    return r, a, b
+
+
+def test_planes_disabled_is_the_grouped_gemm():
+    r, a, b = _plane_problem(1, 3, 40, 24, [5, 0, 9], [2, 1, 0])
+    got = oracle.gmm_bf16_planes(a, r.a_offsets, b, r.expert_ids, (0, 0))
+    ref = oracle.gmm_bf16(a[:r.rows], r.a_offsets, b, r.expert_ids)
+    assert np.array_equal(got.c, ref.c) and np.array_equal(got.stats, ref.stats)
+
+
+def test_planes_brute_force():
+    """Every output against a loop that reads row p(n) * M + r of A."""
+    r, a, b = _plane_problem(2, 2, 12, 8, [3, 2, 4], [1, -1, 0])
+    splits = (5, 4)
+    got = oracle.gmm_bf16_planes(a, r.a_offsets, b, r.expert_ids, splits)
+    A, B = bits_to_f32(a).astype(np.float64), bits_to_f32(b).astype(np.float64)
+    M = r.rows
+    for g in range(r.G):
+        e = int(r.expert_ids[g])
+        for row in range(int(r.a_offsets[g]), int(r.a_offsets[g + 1])):
+            for n in range(12):
+                if e < 0:
+                    assert np.isnan(got.ref32[row, n])
+                    continue
+                p = 0 if n < 5 else (1 if n < 9 else 2)
+                exact = sum(A[p * M + row, k] * B[e, n, k] for k in range(8))
+                assert abs(got.ref32[row, n] - exact) <= 8 * 2.0**-24 * sum(abs(A[p * M + row, k] * B[e, n, k]) for k in range(8)) + 1e-30
+
+
+def test_planes_identical_planes_and_whole_plane_splits():
+    """Three copies of one plane give the grouped GEMM; (0, N) sends every column to plane 1."""
+    r, a, b = _plane_problem(3, 2, 32, 16, [7, 6], [0, 1])
+    M = r.rows
+    same = np.concatenate([a[:M]] * 3)
+    got = oracle.gmm_bf16_planes(same, r.a_offsets, b, r.expert_ids, (8, 16))
+    ref = oracle.gmm_bf16(a[:M], r.a_offsets, b, r.expert_ids)
+    assert np.array_equal(got.c, ref.c)
+    got1 = oracle.gmm_bf16_planes(a, r.a_offsets, b, r.expert_ids, (0, 32))
+    ref1 = oracle.gmm_bf16(a[M:2 * M], r.a_offsets, b, r.expert_ids)
+    assert np.array_equal(got1.c, ref1.c)
+    assert list(oracle.plane_of_columns(6, (2, 3))) == [0, 0, 1, 1, 1, 2]
+
+
+def test_c_init_memory_order_does_not_matter():
+    """A non-contiguous c_init (a column slice) gives the same result as a contiguous copy."""
+    r, v = _rand_problem(41, E=2, N=24, K=16, loads=[5, 4], ids=[1, 0])
+    wide = wl.sentinel_c(r.rows, 48)
+    view = wide[:, ::2]
+    assert not view.flags["C_CONTIGUOUS"]
+    a = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, c_init=view)
+    b = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, c_init=np.ascontiguousarray(view))
+    assert np.array_equal(a.c, b.c)
