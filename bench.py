@@ -75,6 +75,8 @@ def work_counts(r: wl.Routing):
     else:
         wbytes = r.N * r.K * 2
     abytes = rows * (r.K + 4 * -(-r.K // fp8_gran(r)[2])) if is_fp8(r) else rows * r.K * 2
+    if r.meta.get("planes"):   # each of the three planes of A is read once
+        abytes *= 3
     nbytes = len(experts) * wbytes + abytes + rows * r.N * 2 + 4 * (2 * r.G + 2)
     return flops, float(nbytes), rows
 
@@ -252,6 +254,10 @@ def oracle_sample(r: wl.Routing, vals_dev, n_groups: int):
     if is_fp8(r):
         sample["a8"] = vals_dev["a8"][idx].cpu().numpy()
         sample["input_scale"] = vals_dev["input_scale"][idx].cpu().numpy()   # one per row (m granularity 1)
+    elif r.meta.get("planes"):   # the sampled rows of each plane, the planes len(rows) apart
+        M = r.rows
+        sample["a"] = np.concatenate([vals_dev["a"][idx + p * M].contiguous().view(torch.int16).cpu().numpy()
+                                      .view(np.uint16) for p in range(3)])
     else:
         sample["a"] = vals_dev["a"][idx].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     used = sorted(set(ids))
@@ -275,6 +281,8 @@ def run_oracle(r: wl.Routing, s, nthreads):
     t0 = time.perf_counter()
     if is_fp8(r):
         oracle.gmm_fp8(s["a8"], s["off"], s["w8"], s["ids"], s["input_scale"], s["weight_scale"], fp8_gran(r))
+    elif r.meta.get("planes"):
+        oracle.gmm_bf16_planes(s["a"], s["off"], s["b"], s["ids"], r.meta["planes"], nthreads=nthreads)
     elif r.int4:
         oracle.gmm_int4(s["a"], s["off"], s["packed"], s["scales"], s["ids"], group_size=r.group_size,
                         nthreads=nthreads)
@@ -427,6 +435,8 @@ def main():
         if is_fp8(r):
             binding.gmm_run_fp8(h, cc, aa, oo, vals["w8"], ii, ss, vals["input_scale"], vals["weight_scale"],
                                 fp8_gran(r), stream=stream, **epi)
+        elif r.meta.get("planes"):
+            binding.gmm_run_planes(h, cc, aa, oo, vals["b"], ii, ss, r.meta["planes"], stream=stream, **epi)
         elif r.name == "int4_dense":   # the dense quantised GEMM's own entry point
             binding.gmm_matmul_int4(h, cc, aa, vals["packed"][0], vals["scales"][0], group_size=r.group_size,
                                     stream=stream, **epi)

@@ -155,6 +155,25 @@ int gmm_run_int4_ex(gmm_handle_t h, void *c, const void *a, const uint32_t *a_of
                     const gmm_epilogue *epilogue, cudaStream_t stream);
 
 /*
+ * The bf16 grouped GEMM with A-plane row offsetting (Modular
+ * "grouped_matmul_sm100_persistent", section "Parameters": a_plane_splits, per-plane
+ * split sizes for fused LoRA QKV A-plane row offsetting, (0, 0) disabling it).  The
+ * reading taken: a holds three planes of M = a_offsets[G] rows, stacked along its rows
+ * ([3 M, K], e.g. the q, k and v inputs of a fused QKV projection), and
+ * (s0, s1) = a_plane_splits cut the N columns into three parts:
+ *     C[r, n] = bf16( sum_k a[p(n) * M + r, k] * b[e, n, k] ),
+ *     p(n) = 0 for n < s0, 1 for s0 <= n < s0 + s1, 2 otherwise,
+ * for the rows and groups of gmm_run, then the optional epilogue.  (0, 0) is gmm_run_ex.
+ * a must hold 3 * a_offsets[G] rows (any a_offsets[G] rows when the splits are (0, 0)).
+ * Requirements: those of gmm_run, s0 and s1 multiples of 256 (a tile's 256 weight rows
+ * lie in one plane; else GMM_ERR_UNSUPPORTED), 0 <= s0, 0 <= s1, s0 + s1 <= N (else
+ * GMM_ERR_INVALID_ARG, also for a NULL a_plane_splits).  Errors: as gmm_run_ex.
+ */
+int gmm_run_planes(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, const void *b,
+                   const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
+                   const int *a_plane_splits, const gmm_epilogue *epilogue, cudaStream_t stream);
+
+/*
  * Block-scaled e4m3 grouped GEMM (Modular "k_matmul_ragged_paged_scale", section
  * "Args": input_scale and weight_scale multiply the input and the weight; template
  * parameter scales_granularity_mnk; without the page's paged KV-cache write, the

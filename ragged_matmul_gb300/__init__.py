@@ -9,5 +9,5 @@ from .binding import (EXPORTED, GMM_ERR_BAD_INPUT, GMM_ERR_CUDA, GMM_ERR_DEVICE_
                       GMM_ERR_INVALID_ARG, GMM_ERR_NO_DEVICE, GMM_ERR_UNSUPPORTED, GMM_OK, GmmError,
                       GMM_ACT_GELU_TANH, GMM_ACT_NONE, GMM_ACT_RELU, GMM_ACT_SILU,
                       Handle, gmm_create, gmm_destroy, gmm_error_string, gmm_query_status, gmm_run,
-                      gmm_matmul_int4, gmm_run_ex, gmm_run_fp8, gmm_run_int4, gmm_run_int4_ex, library_path,
+                      gmm_matmul_int4, gmm_run_ex, gmm_run_fp8, gmm_run_int4, gmm_run_planes, gmm_run_int4_ex, library_path,
                       load_library)

@@ -32,7 +32,7 @@ GMM_ERR_BAD_INPUT = -5
 GMM_ERR_NO_DEVICE = -6
 
 EXPORTED = ("gmm_create", "gmm_run", "gmm_run_ex", "gmm_run_int4", "gmm_run_int4_ex", "gmm_matmul_int4",
-            "gmm_run_fp8", "gmm_run_noalloc", "gmm_query_status", "gmm_error_string", "gmm_destroy")
+            "gmm_run_fp8", "gmm_run_planes", "gmm_run_noalloc", "gmm_query_status", "gmm_error_string", "gmm_destroy")
 
 # Activations of the optional epilogue (GMM_ACT_* in gmm.h).
 GMM_ACT_NONE = 0
@@ -81,6 +81,8 @@ def load_library(path: str | None = None):
     lib.gmm_run_int4_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, EP, P]
     lib.gmm_run_int4_ex.restype = I
     lib.gmm_matmul_int4.argtypes = [P, P, P, P, P, I, I, I, I, EP, P]
+    lib.gmm_run_planes.restype = I
+    lib.gmm_run_planes.argtypes = [P, P, P, P, P, P, P, I, I, I, P, EP, P]
     lib.gmm_run_fp8.restype = I
     lib.gmm_run_fp8.argtypes = [P, P, P, P, P, P, P, I, I, I, P, P, P, EP, P]
     lib.gmm_matmul_int4.restype = I
@@ -255,6 +257,36 @@ def gmm_run_int4_ex(h: Handle, c, a, a_offsets, b_packed, b_scales, expert_ids, 
                                  stream_handle(h.device, stream))
     if check and rc != GMM_OK:
         raise GmmError(rc, "gmm_run_int4")
+    return rc
+
+
+def gmm_run_planes(h: Handle, c, a, a_offsets, b, expert_ids, expert_usage_stats, a_plane_splits=(0, 0),
+                   bias=None, row_scale=None, activation=GMM_ACT_NONE, stream=None, check: bool = True) -> int:
+    """bf16 grouped GEMM with A-plane row offsetting: a holds three planes of a_offsets[G] rows
+    ([3 * rows, K] with rows = c.shape[0]); output columns n < s0 read plane 0, n < s0 + s1
+    plane 1, the rest plane 2 (s0, s1 multiples of 256); then the optional epilogue."""
+    import torch
+    if a.dim() != 2 or b.dim() != 3 or c.dim() != 2:
+        raise ValueError("a must be [3 * rows, K], b [E, N, K], c [rows, N]")
+    E, N, K = b.shape
+    s0, s1 = (int(x) for x in a_plane_splits)
+    planes = 1 if (s0, s1) == (0, 0) else 3
+    if a.shape[1] != K or c.shape[1] != N or a.shape[0] < planes * c.shape[0] or E != h.num_experts:
+        raise ValueError(f"shape mismatch: a {tuple(a.shape)} (needs {planes} planes of {c.shape[0]} rows), "
+                         f"b {tuple(b.shape)}, c {tuple(c.shape)}, handle E={h.num_experts}")
+    bf = (torch.bfloat16,)
+    pc = _check(c, "c", bf, h.device)
+    pa = _check(a, "a", bf, h.device)
+    pb = _check(b, "b", bf, h.device)
+    po, pi, ps, G = _routing_args(h, a_offsets, expert_ids, expert_usage_stats)
+    splits = (ctypes.c_int * 2)(s0, s1)
+    epi = None
+    if bias is not None or row_scale is not None or activation:
+        epi = ctypes.byref(_epilogue(h, c.shape[0], N, bias, row_scale, activation))
+    rc = load_library().gmm_run_planes(h.ptr, pc, pa, po, pb, pi, ps, G, N, K, splits, epi,
+                                       stream_handle(h.device, stream))
+    if check and rc != GMM_OK:
+        raise GmmError(rc, "gmm_run_planes")
     return rc
 
 

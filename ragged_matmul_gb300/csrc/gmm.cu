@@ -454,6 +454,40 @@ int gmm_run(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, c
   return gmm_run_ex(h, c, a, a_offsets, b, expert_ids, expert_usage_stats, num_groups, N, K, nullptr, stream);
 }
 
+// A-plane row offsetting: the bf16 grouped kernel with the tile's token rows read from
+// the plane its weight rows belong to (the producer adds plane * a_offsets[G]).
+int gmm_run_planes(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offsets, const void *b,
+                   const int32_t *expert_ids, uint32_t *expert_usage_stats, int num_groups, int N, int K,
+                   const int *a_plane_splits, const gmm_epilogue *epilogue, cudaStream_t stream) {
+  if (!a_plane_splits) return GMM_ERR_INVALID_ARG;
+  const int s0 = a_plane_splits[0], s1 = a_plane_splits[1];
+  if (s0 < 0 || s1 < 0 || s0 > N || s1 > N - s0) return GMM_ERR_INVALID_ARG;
+  if (s0 % 256 || s1 % 256) return GMM_ERR_UNSUPPORTED;   // a tile's 256 weight rows in one plane
+  int rc = check_common(h, c, a, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K);
+  if (rc) return rc;
+  rc = check_epilogue(epilogue);
+  if (rc) return rc;
+  if (!b || !aligned16(b)) return GMM_ERR_INVALID_ARG;
+  GmmParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                          static_cast<cuuint64_t>(h->num_experts)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(N) * K * 2};
+    cuuint32_t box[3] = {gmm::kBK, gmm::kBlockN, 1};
+    rc = encode_map(h, &p.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, strides, box,
+                    CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  }
+  rc = encode_token_maps(h, p, a, K, 1);
+  if (rc) return rc;
+  fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, K, max_tok(h, false));
+  set_epilogue(p, epilogue);
+  p.plane_s0 = s0;
+  p.plane_s1 = s1;
+  return launch<false>(h, p, stream);
+}
+
 // The e4m3 operands go through the bf16 kernel's tensor maps unchanged, over their
 // bytes: a row of K e4m3 values is a row of K / 2 two-byte units, so the maps, the
 // stage ring and the swizzled layout are the bf16 ones and only the MMA kind and the

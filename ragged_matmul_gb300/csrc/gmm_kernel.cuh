@@ -212,6 +212,11 @@ struct alignas(128) GmmParams {
   // scale row, kb_stages = gk / 128 pipeline stages per block.
   int scale_kb;
   int kb_stages;
+  // A-plane row offsetting (both 0: off): A holds three planes of M = a_offsets[G] rows;
+  // C columns n < plane_s0 read plane 0, n < plane_s0 + plane_s1 plane 1, the rest plane 2.
+  // Both are multiples of 256, so a tile's weight rows lie in one plane.
+  int plane_s0;
+  int plane_s1;
 };
 
 struct __align__(32) Tile {
@@ -394,6 +399,15 @@ __device__ __forceinline__ Tile decode_tile(uint32_t t, const uint32_t *prefix, 
   x.ntok = (x.nrows + G::kTokAlign - 1) & ~(G::kTokAlign - 1);
   x.n0 = nb * G::kRows;
   return x;
+}
+
+// First A row of the plane that the tile's weight rows n0 .. read (A-plane row
+// offsetting; 0 when it is off).
+__device__ __forceinline__ uint32_t plane_row0(const GmmParams &p, uint32_t n0, uint32_t m_rows) {
+  if ((p.plane_s0 | p.plane_s1) == 0) return 0u;
+  const uint32_t plane = (n0 >= static_cast<uint32_t>(p.plane_s0) ? 1u : 0u) +
+                         (n0 >= static_cast<uint32_t>(p.plane_s0 + p.plane_s1) ? 1u : 0u);
+  return plane * m_rows;
 }
 
 // Two fp32 values -> one 32-bit word of two bf16 (round to nearest even), the lower
@@ -639,7 +653,8 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       uint4 *dst = reinterpret_cast<uint4 *>(slot + lane * 128);
 #pragma unroll
       for (int i = 0; i < 8; ++i) dst[i] = src[i];
-      tensormap_set_dim1(dst, __ldg(p.a_offsets + p.num_groups));
+      const uint32_t planes = (p.plane_s0 | p.plane_s1) ? 3u : 1u;   // A-plane row offsetting: 3 planes of rows
+      tensormap_set_dim1(dst, planes * __ldg(p.a_offsets + p.num_groups));
       tensormap_set_box1(dst, 16u * static_cast<uint32_t>(lane + 1));
       tensormap_release();
     }
@@ -652,6 +667,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const uint64_t pol_last = l2_policy_evict_last();
       const uint64_t pol_normal = l2_policy_evict_normal();
 
+      const uint32_t m_rows = __ldg(p.a_offsets + p.num_groups);   // rows of one A plane
       Ring rt;
       uint32_t pending = 0;     // bit s: stage s has copies whose completion this thread has not seen
       uint32_t pend_phase = 0;  // bit s: the phase in which they complete
@@ -740,7 +756,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
           const uint32_t full_local = smem_addr(&ctl.full[rt.slot]);
           if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
           if (rank == 0) mbar_arrive_expect_tx(full_local, tx);
-          const int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok);
+          const int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok + plane_row0(p, ti.n0, m_rows));
           const CUtensorMap *tok = tok_maps + (my_tok / 16u - 1u);   // copies my_tok rows high
           if constexpr (kInt4) {
             // All kSub sub-slabs of the stage in one copy (3-D token map): sub-slab s

@@ -29,6 +29,9 @@ shapes this library targets):
   fp8_decode    A, B ~ e4m3(N(0, 2)) (the fp32 draw cast to e4m3, round to
                 nearest even), fp32 scales at granularity (1, 128, K):
                 input_scale ~ U[0.25, 1], weight_scale ~ U[0.002, 0.008].
+  lora_qkv      a fused LoRA QKV expand with A-plane row offsetting: 8192 tokens
+                over E=8 adapters (uniform Multinomial), K=64, N=6144 with splits
+                (4096, 1024); A [3 x 8192, 64] ~ N(0, 1), B ~ N(0, 0.02).
   fp8_block_prefill,  the same with per-K-block scales: granularity
   fp8_block_decode    (1, 128, 128), one scale per row (input) or per 128
                 weight rows (weight) and 128 of K.
@@ -122,7 +125,7 @@ def _balanced_loads(rng, total, E, spread):
 
 
 WORKLOAD_NAMES = ("tiny", "decode", "prefill", "fine_grained", "int4", "int4_dense", "fp8_prefill",
-                  "fp8_decode", "fp8_block_prefill", "fp8_block_decode")
+                  "fp8_decode", "fp8_block_prefill", "fp8_block_decode", "lora_qkv")
 WORKLOAD_SEEDS = {name: i for i, name in enumerate(WORKLOAD_NAMES)}
 
 
@@ -173,7 +176,23 @@ def routing(name: str, seed: int | None = None) -> Routing:
         # The same with per-K-block scales: granularity (1, 128, 128).
         base = routing(name[10:], seed)
         return replace(base, name=name, meta={"fp8": True, "granularity": (1, 128, 128)})
+    if name == "lora_qkv":
+        # A fused LoRA QKV expand: 8192 tokens over 8 adapters (Multinomial, uniform), rank
+        # K = 64, N = 4096 (q) + 1024 (k) + 1024 (v) columns; A holds the three planes of
+        # the shrink outputs (A-plane row offsetting with splits (4096, 1024)).
+        E = 8
+        loads = rng.multinomial(8192, np.full(E, 1.0 / E)).astype(np.int64)
+        r = make_routing("lora_qkv", E, 6144, 64, loads, np.arange(E),
+                         a_dist=("normal", 1.0), b_dist=("normal", 0.02))
+        return replace(r, meta={"planes": (4096, 1024)})
     raise KeyError(name)
+
+
+def a_rows(r: Routing, rows: int | None = None) -> int:
+    """Rows of A to allocate: one plane of `rows` (default the end of the last group), or
+    three with A-plane row offsetting."""
+    rows = r.rows if rows is None else rows
+    return 3 * rows if r.meta.get("planes") else rows
 
 
 def group_range(r: Routing, lo: int, hi: int) -> Routing:
@@ -220,7 +239,7 @@ def host_values(r: Routing, seed: int = 0, rows: int | None = None) -> dict:
     rows: rows of A to allocate (defaults to the end of the last group).
     """
     rng = np.random.default_rng([seed, 1])
-    rows = r.rows if rows is None else rows
+    rows = a_rows(r, rows)
     out = {"a": _to_bf16_bits(_draw(rng, r.a_dist, (rows, r.K)))}
     if r.int4:
         q = rng.integers(0, 16, size=(r.E, r.N, r.K), dtype=np.uint32)
@@ -274,7 +293,7 @@ def device_values(r: Routing, seed: int = 0, device="cuda", chunk_elems: int = 1
             flat[s:s + n] = x.to(torch.bfloat16)
         return out
 
-    out = {"a": fill((r.rows, r.K), r.a_dist)}
+    out = {"a": fill((a_rows(r), r.K), r.a_dist)}
     if r.int4:
         words = torch.empty((r.E, r.N, r.K // 8), dtype=torch.int32, device=device)
         flat = words.view(-1)

@@ -420,3 +420,109 @@ def test_dense_int4_zero_rows_and_epilogue():
                                                 group_size=gs),
                                 r.a_offsets, r.expert_ids, 1, bias_bits=bias, row_scale=scale, activation="silu")
     assert_close(bits_of(c), ref.ref32, np.ones(M, bool), "dense int4 epilogue")
+
+
+# ---------------------------------------------------------------- A-plane row offsetting
+
+def _planes_case(h, r, splits, seed, rows_alloc=None, epilogue=None, where=""):
+    rows_alloc = r.rows if rows_alloc is None else rows_alloc
+    rng = np.random.default_rng(seed)
+    a = wl._to_bf16_bits(rng.standard_normal((3 * rows_alloc, r.K)).astype(np.float32))
+    b = wl._to_bf16_bits((0.1 * rng.standard_normal((r.E, r.N, r.K))).astype(np.float32))
+    c0 = wl.sentinel_c(rows_alloc, r.N)
+    # The planes are a_offsets[G] rows apart: lay A out with that stride.
+    M = r.rows
+    a_dev_rows = np.concatenate([a[p * rows_alloc:p * rows_alloc + M] for p in range(3)] +
+                                [np.zeros((3 * rows_alloc - 3 * M, r.K), np.uint16)])
+    ref = oracle.gmm_bf16_planes(a_dev_rows, r.a_offsets, b, r.expert_ids, splits, c_init=c0,
+                                 stats_init=np.full(4, wl.SENTINEL_STATS, np.uint32))
+    if epilogue:
+        ref = oracle.apply_epilogue(ref, r.a_offsets, r.expert_ids, r.E, bias_bits=epilogue.get("bias_bits"),
+                                    row_scale=epilogue.get("row_scale"), activation=epilogue.get("activation", "none"))
+    import torch
+    c = sentinel_dev(rows_alloc, r.N, DEV)
+    st = to_dev_i32(np.full(4, 0xFFFFFFFF, np.uint32), DEV)
+    epi = {}
+    if epilogue:
+        epi = {"bias": to_dev_u16(epilogue["bias_bits"], DEV),
+               "row_scale": torch.from_numpy(epilogue["row_scale"]).to(DEV), "activation": epilogue["activation"]}
+    binding.gmm_run_planes(h, c, to_dev_u16(a_dev_rows, DEV), to_dev_i32(r.a_offsets, DEV), to_dev_u16(b, DEV),
+                           to_dev_i32(r.expert_ids, DEV), st, splits, **epi)
+    assert binding.gmm_query_status(h) == binding.GMM_OK
+    got = bits_of(c)
+    live = live_row_mask(rows_alloc, r.a_offsets, r.expert_ids, r.E)
+    assert np.array_equal(got[~live], ref.c[~live]), where
+    assert np.array_equal(st.cpu().numpy().view(np.uint32), ref.stats), where
+    assert_close(got, ref.ref32, live, where)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("N,splits", [(768, (256, 256)), (1280, (512, 256)), (512, (0, 512)), (512, (512, 0)),
+                                      (1024, (0, 0)), (1536, (1024, 256))])
+def test_a_plane_splits(N, splits, variant):
+    """Each output column reads its plane of A (rows p * a_offsets[G] + r); ragged groups,
+    a skipped group, N tails inside the last plane."""
+    r = routing(4, N, 192, [1, 17, 0, 130, 33, 257, 7], [2, 0, 1, 3, -1, 1, 0])
+    _planes_case(handle(4, variant), r, splits, 50, where=f"planes N={N} {splits} {variant}")
+
+
+def test_a_plane_splits_with_epilogue_and_trailing_rows():
+    r = routing(3, 1040, 128, [40, 300, 9], [2, 0, 1])
+    rng = np.random.default_rng(52)
+    epi = {"bias_bits": wl._to_bf16_bits(rng.normal(0, 0.5, (3, 1040)).astype(np.float32)),
+           "row_scale": rng.uniform(0.5, 2.0, r.rows + 13).astype(np.float32), "activation": "silu"}
+    _planes_case(handle(3), r, (512, 256), 51, rows_alloc=r.rows + 13, epilogue=epi, where="planes epilogue")
+
+
+def test_a_plane_splits_argument_errors():
+    import ctypes
+    h = handle(2)
+    r = routing(2, 512, 64, [8], [1])
+    c = sentinel_dev(r.rows, 512, DEV)
+    a = to_dev_u16(np.zeros((3 * r.rows, 64), np.uint16), DEV)
+    b = to_dev_u16(np.zeros((2, 512, 64), np.uint16), DEV)
+    off, ids, st = to_dev_i32(r.a_offsets, DEV), to_dev_i32(r.expert_ids, DEV), to_dev_i32(np.zeros(4), DEV)
+    lib = binding.load_library()
+    P = ctypes.c_void_p
+
+    def call(splits):
+        sp = None if splits is None else (ctypes.c_int * 2)(*splits)
+        return lib.gmm_run_planes(h.ptr, P(c.data_ptr()), P(a.data_ptr()), P(off.data_ptr()), P(b.data_ptr()),
+                                  P(ids.data_ptr()), P(st.data_ptr()), 1, 512, 64, sp, None, binding.stream_handle(0))
+    assert call((128, 256)) == binding.GMM_ERR_UNSUPPORTED      # not a multiple of 256
+    assert call((256, 512)) == binding.GMM_ERR_INVALID_ARG      # past N
+    assert call((-256, 0)) == binding.GMM_ERR_INVALID_ARG
+    assert call(None) == binding.GMM_ERR_INVALID_ARG
+    assert np.all(bits_of(c) == wl.SENTINEL_BF16)
+
+
+def test_lora_qkv_full_size_sampled():
+    """The full lora_qkv workload (A-plane row offsetting) on sampled rows and columns."""
+    import torch
+    r = wl.routing("lora_qkv")
+    v = wl.device_values(r, 0, device=DEV)
+    h = handle(r.E)
+    c = sentinel_dev(r.rows, r.N, DEV)
+    st = to_dev_i32(np.full(4, 0xFFFFFFFF, np.uint32), DEV)
+    binding.gmm_run_planes(h, c, v["a"], to_dev_i32(r.a_offsets, DEV), v["b"], to_dev_i32(r.expert_ids, DEV), st,
+                           r.meta["planes"])
+    assert binding.gmm_query_status(h) == binding.GMM_OK
+    rng = np.random.default_rng(7)
+    rows, loads = [], []
+    for g in range(r.G):
+        lo, hi = int(r.a_offsets[g]), int(r.a_offsets[g + 1])
+        pick = sorted(set([lo, hi - 1] + rng.integers(lo, hi, 3).tolist())) if hi > lo else []
+        rows += pick
+        loads.append(len(pick))
+    rows = np.asarray(rows, np.int64)
+    cols = np.unique(np.concatenate([[0, 4095, 4096, 5119, 5120, r.N - 1], rng.choice(r.N, 90, replace=False)]))
+    M = r.rows
+    a_s = np.concatenate([bits_of(v["a"][torch.from_numpy(rows + p * M).to(DEV)]) for p in range(3)])
+    b_s = bits_of(v["b"][:, torch.from_numpy(cols).to(DEV), :])
+    off_s = wl.offsets_from_loads(loads)
+    # The sampled columns keep their planes: recompute the split sizes in the sample.
+    planes = oracle.plane_of_columns(r.N, r.meta["planes"])[cols]
+    s0, s1 = int((planes == 0).sum()), int((planes == 1).sum())
+    ref = oracle.gmm_bf16_planes(a_s, off_s, b_s, r.expert_ids, (s0, s1) if (s0, s1) != (0, 0) else (0, len(cols)))
+    got = bits_of(c[torch.from_numpy(rows).to(DEV)][:, torch.from_numpy(cols).to(DEV)])
+    assert_close(got, ref.ref32, np.ones(len(rows), bool), "lora_qkv sampled")
