@@ -280,3 +280,13 @@ def test_fp8_block_scales_edge_cases():
     got, stats, status = run_gpu_fp8(handle(4), v3, r3.a_offsets, r3.expert_ids, (1, 128, 128), N=128,
                                      rows_alloc=16)
     assert np.all(got == wl.SENTINEL_BF16) and stats[1] == 0 and status == binding.GMM_OK
+
+
+@pytest.mark.parametrize("gran", [(1, 128, None), (1, 128, 128)])
+def test_fp8_max_groups(gran):
+    """4096 groups (the largest supported count) of 0..3 rows over 64 experts, both kernels."""
+    rng = np.random.default_rng(70)
+    G = 4096
+    r, v = case(64, 256, 256, rng.integers(0, 4, G), rng.integers(-1, 64, G).astype(np.int32), 71, gran=gran)
+    _, _, status, _ = check_fp8_against_oracle(handle(64), r, v, gran, where=f"fp8 max groups {gran}")
+    assert status == binding.GMM_OK

@@ -526,3 +526,36 @@ def test_lora_qkv_full_size_sampled():
     ref = oracle.gmm_bf16_planes(a_s, off_s, b_s, r.expert_ids, (s0, s1) if (s0, s1) != (0, 0) else (0, len(cols)))
     got = bits_of(c[torch.from_numpy(rows).to(DEV)][:, torch.from_numpy(cols).to(DEV)])
     assert_close(got, ref.ref32, np.ones(len(rows), bool), "lora_qkv sampled")
+
+
+# ---------------------------------------------------------------- maximum sizes
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_max_groups(variant):
+    """The largest supported group count (4096): rows 0..3 per group, ids over 64 experts with
+    skipped ones, every group in the scan, the schedule and the tile decode."""
+    rng = np.random.default_rng(60)
+    G = 4096
+    loads = rng.integers(0, 4, G)
+    ids = rng.integers(-1, 64, G).astype(np.int32)
+    r = routing(64, 264, 128, loads, ids, dist=("normal", 1.0))
+    v = wl.host_values(r, 61)
+    _, _, status, _ = check_against_oracle(handle(64, variant), r, v, where=f"max groups {variant}")
+    assert status == binding.GMM_OK
+
+
+def test_long_k():
+    """K = 16384 (128 pipeline stages per tile) with ragged groups and an N tail."""
+    r = routing(3, 264, 16384, [1, 130, 257], [2, 0, 1], dist=("normal", 0.5))
+    v = wl.host_values(r, 62)
+    check_against_oracle(handle(3), r, v, where="long K")
+
+
+def test_max_groups_int4():
+    rng = np.random.default_rng(63)
+    G = 4096
+    r = routing(32, 256, 256, rng.integers(0, 3, G), rng.integers(-1, 32, G).astype(np.int32),
+                dist=("normal", 1.0), int4=True, gs=128)
+    v = wl.host_values(r, 64)
+    _, _, status, _ = check_against_oracle(handle(32), r, v, where="max groups int4")
+    assert status == binding.GMM_OK
