@@ -92,11 +92,17 @@ def fp8_gran(r: wl.Routing):
 
 
 def kernel_source_hash():
+    """Hash of the CUDA sources with comments and whitespace removed: it changes when the
+    code the profiles were captured on changes, not when a comment does."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ragged_matmul_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        text = re.sub(r"\s+", " ", text)
+        h.update(f.encode() + text.encode())
     return h.hexdigest()[:16]
 
 

@@ -51,11 +51,13 @@
 //   warp 0       TMA producer of token slabs (and of bf16 weight slabs).
 //   warp 1       TMEM allocation (512 columns: two fp32 accumulators, and in the
 //                4-bit kernel a ring of dequantised weight slabs between them) and
-//                the single MMA-issuing thread (tcgen05.mma kind::f16, or
-//                kind::f8f6f4 for e4m3).
-//   warps 2..5   epilogue: TMEM -> registers -> bf16 -> C, masking token rows past
-//                the group's end and columns past N; two accumulators let it
-//                overlap the next tile's main loop.
+//                the MMA issue (the whole warp runs the loop, one elected lane
+//                issues tcgen05.mma kind::f16, or kind::f8f6f4 for e4m3).
+//   warps 2..5   epilogue: TMEM -> registers -> a shared-memory staging tile (the
+//                transpose from weight-row lanes to C rows) -> scales, optional
+//                bias / activation / row scale -> bf16 -> 16-byte stores to C,
+//                masking token rows past the group's end and columns past N; two
+//                accumulators let it overlap the next tile's main loop.
 //   warp 6       (4-bit) TMA producer of packed slabs.
 //   warps 7..18  (4-bit) dequantisation.
 //
