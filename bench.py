@@ -256,7 +256,7 @@ def oracle_sample(r: wl.Routing, vals_dev, n_groups: int):
         ids.append(int(r.expert_ids[g]))
     akey = "a8" if is_fp8(r) else "a"
     idx = torch.tensor(rows, dtype=torch.int64, device=vals_dev[akey].device)
-    sample = {"off": wl.offsets_from_loads(loads), "groups": len(act), "rows": len(rows)}
+    sample = {"off": wl.offsets_from_loads(loads), "groups": len(act), "rows": len(rows), "row_idx": list(rows)}
     if is_fp8(r):
         sample["a8"] = vals_dev["a8"][idx].cpu().numpy()
         sample["input_scale"] = vals_dev["input_scale"][idx].cpu().numpy()   # one per row (m granularity 1)
@@ -283,18 +283,36 @@ def oracle_sample(r: wl.Routing, vals_dev, n_groups: int):
 
 
 def run_oracle(r: wl.Routing, s, nthreads):
+    """One oracle pass over the sample; returns its wall time and keeps its fp32 sums in s["ref32"]."""
     import oracle
     t0 = time.perf_counter()
     if is_fp8(r):
-        oracle.gmm_fp8(s["a8"], s["off"], s["w8"], s["ids"], s["input_scale"], s["weight_scale"], fp8_gran(r))
+        res = oracle.gmm_fp8(s["a8"], s["off"], s["w8"], s["ids"], s["input_scale"], s["weight_scale"],
+                             fp8_gran(r))
     elif r.meta.get("planes"):
-        oracle.gmm_bf16_planes(s["a"], s["off"], s["b"], s["ids"], r.meta["planes"], nthreads=nthreads)
+        res = oracle.gmm_bf16_planes(s["a"], s["off"], s["b"], s["ids"], r.meta["planes"], nthreads=nthreads)
     elif r.int4:
-        oracle.gmm_int4(s["a"], s["off"], s["packed"], s["scales"], s["ids"], group_size=r.group_size,
-                        nthreads=nthreads)
+        res = oracle.gmm_int4(s["a"], s["off"], s["packed"], s["scales"], s["ids"], group_size=r.group_size,
+                              nthreads=nthreads)
     else:
-        oracle.gmm_bf16(s["a"], s["off"], s["b"], s["ids"], nthreads=nthreads)
-    return time.perf_counter() - t0
+        res = oracle.gmm_bf16(s["a"], s["off"], s["b"], s["ids"], nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    s["ref32"] = res.ref32
+    return dt
+
+
+def sample_parity(s, c_dev):
+    """The timed run's output rows of the oracle sample against the oracle (per element
+    |gpu - ref| <= 1e-2 + 1e-2 |ref|): the largest error as a fraction of its bound."""
+    import torch
+    idx = torch.tensor(s["row_idx"], dtype=torch.int64, device=c_dev.device)
+    got = c_dev[idx].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    got32 = (got.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ref = s["ref32"].astype(np.float64)
+    ratio = np.abs(got32 - ref) / (1e-2 + 1e-2 * np.abs(ref))
+    worst = float(np.nanmax(ratio)) if ratio.size else 0.0
+    return {"rows": int(len(s["row_idx"])), "elements": int(ratio.size), "max_err_over_bound": worst,
+            "ok": bool(worst <= 1.0 and not np.isnan(ratio).any())}
 
 
 def pick_oracle_sample(r, vals_dev, nthreads, target_s):
@@ -334,6 +352,9 @@ def main():
     ap.add_argument("--epilogue", default="none", choices=["none", "relu", "silu", "gelu_tanh"],
                     help="time the fused epilogue act(acc + bias[e, n]) * row_scale[r] with this activation "
                          "(seeded bias and per-row scales); 'none' is the plain GEMM")
+    ap.add_argument("--yardstick", action="store_true",
+                    help="also time torch.matmul per active group (cuBLAS, bf16 workloads) on the same data, "
+                         "for context")
     ap.add_argument("--variant", default=None, choices=["pair", "single"],
                     help="kernel variant (default: the library's choice, CTA pairs)")
     args = ap.parse_args()
@@ -522,6 +543,34 @@ def main():
         e2e = {"value": aggregate_tflops(world, flops, e2e_max), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_max}
 
+    # A library yardstick for context (never a reference for results): cuBLAS through
+    # torch.matmul, one GEMM per active group, on the same resident operands.
+    yardstick = None
+    if args.yardstick and rank == 0 and not (r.int4 or is_fp8(r) or r.meta.get("planes")):
+        segs = [(int(r.a_offsets[g]), int(r.a_offsets[g + 1]), int(r.expert_ids[g]))
+                for g in np.flatnonzero(r.active_mask()) if r.a_offsets[g + 1] > r.a_offsets[g]]
+        cy = torch.empty_like(c)
+
+        def ystep():
+            for r0, r1, e in segs:
+                torch.matmul(vals["a"][r0:r1], vals["b"][e].t(), out=cy[r0:r1])
+        for _ in range(args.warmup):
+            flush_l2()
+            ystep()
+        y_ms = []
+        for _ in range(min(args.steps, 50)):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            ystep()
+            e1.record(stream)
+            e1.synchronize()
+            y_ms.append(e0.elapsed_time(e1))
+        y = statistics.mean(y_ms)
+        yardstick = {"kind": "torch.matmul per active group (cuBLAS, bf16), context only", "ms_per_step": y,
+                     "value": flops / (y * 1e-3) / 1e12, "unit": "TFLOP/s", "launches_per_step": len(segs)}
+        del cy
+
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nthreads = len(os.sched_getaffinity(0))
@@ -535,6 +584,8 @@ def main():
         cpu_baseline = {"value": passes * s["flops"] / total / 1e12, "unit": "TFLOP/s", "cores": nthreads,
                         "kind": "oracle",
                         "sample": sample_desc(r, s) + f"; {passes} pass(es), {total:.2f} s"}
+        if args.epilogue == "none":   # the timed run's output on the sample, after timing
+            cpu_baseline["parity_after_timing"] = sample_parity(s, c)
 
     if rank == 0:
         t_s = mean_ms * 1e-3
@@ -560,6 +611,7 @@ def main():
             "dtype": "int4 weights, bf16 MMA" if r.int4 else ("e4m3" if is_fp8(r) else "bf16"),
             "data": "synthetic (seeded, generated on device)", "config": config,
             "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": args.steps,
+            **({"yardstick": yardstick} if yardstick else {}),
             "clocks": sampler.summary(w0, w1), "region_wall_ms": (w1 - w0) * 1e3,
             "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
         }
