@@ -28,7 +28,10 @@
  * All pointers passed to the run calls are DEVICE pointers on the handle's device
  * and are owned by the caller.  The run calls are asynchronous on `stream`: they
  * validate the arguments on the host, launch one persistent kernel and return;
- * they do not synchronise and allocate nothing.
+ * they do not synchronise and allocate nothing.  They can be captured in a CUDA
+ * graph and replayed (every device write they make before the kernel is a value
+ * write, not a copy from host memory); gmm_query_status synchronises and must not
+ * be called during a capture.
  *
  * A handle owns a small device workspace (a status word, a 64-bit tile-claim
  * word and a finished-CTA counter that each launch returns to zero, the routing of

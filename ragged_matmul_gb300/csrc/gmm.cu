@@ -71,6 +71,7 @@ struct gmm_ctx {
   uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
   size_t ws_bytes = 0;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  PFN_cuMemsetD32Async_v3020 memset32 = nullptr;   // value writes that a captured CUDA graph replays as such
 };
 
 namespace {
@@ -366,6 +367,14 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
     return GMM_ERR_CUDA;
   }
   h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuMemsetD32Async", &fn, 3020, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    cudaGetLastError();
+    delete h;
+    return GMM_ERR_CUDA;
+  }
+  h->memset32 = reinterpret_cast<PFN_cuMemsetD32Async_v3020>(fn);
 
   const int single_ok = configure<false, false>(&h->var[0][0], optin, sms) == GMM_OK &&
                         configure<true, false>(&h->var[1][0], optin, sms) == GMM_OK &&
@@ -605,11 +614,12 @@ int gmm_matmul_int4(gmm_handle_t h, void *c, const void *a, const uint32_t *b_pa
   if (!h || M < 0) return GMM_ERR_INVALID_ARG;
   if (M == 0) return GMM_OK;
   // One group of M rows with expert 0: its offsets, id and (unread) usage stats live
-  // in the handle's status block, written in stream order before the kernel.
+  // in the handle's status block, written in stream order before the kernel by value
+  // writes (memset nodes in a captured CUDA graph, so a replay needs no host memory).
   DeviceGuard guard(h->device);
-  const uint32_t routing[3] = {0u, static_cast<uint32_t>(M), 0u};   // a_offsets[0..1], expert_ids[0]
-  if (cudaMemcpyAsync(h->ws + kDenseRoutingOffset, routing, sizeof(routing), cudaMemcpyHostToDevice, stream) !=
-      cudaSuccess) {
+  const CUdeviceptr routing = reinterpret_cast<CUdeviceptr>(h->ws + kDenseRoutingOffset);   // a_offsets[0..1], expert_ids[0]
+  if (h->memset32(routing, 0u, 3, reinterpret_cast<CUstream>(stream)) != CUDA_SUCCESS ||
+      h->memset32(routing + 4, static_cast<unsigned int>(M), 1, reinterpret_cast<CUstream>(stream)) != CUDA_SUCCESS) {
     cudaGetLastError();
     return GMM_ERR_CUDA;
   }

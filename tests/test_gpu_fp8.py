@@ -290,3 +290,42 @@ def test_fp8_max_groups(gran):
     r, v = case(64, 256, 256, rng.integers(0, 4, G), rng.integers(-1, 64, G).astype(np.int32), 71, gran=gran)
     _, _, status, _ = check_fp8_against_oracle(handle(64), r, v, gran, where=f"fp8 max groups {gran}")
     assert status == binding.GMM_OK
+
+
+@pytest.mark.parametrize("gran", [(1, 128, None), (1, 128, 128)])
+def test_fp8_cuda_graph_replay(gran):
+    """Both e4m3 kernels captured in a CUDA graph once and replayed on new inputs."""
+    import torch
+    h = handle(4)
+    r = wl.make_routing("t", 4, 256, 512, [5, 130, 0, 77], [2, 0, -1, 3])
+    v0 = wl.fp8_host_values(r, 90, gran)
+    a8 = torch.empty(v0["a8"].shape, dtype=torch.uint8, device=DEV)
+    w8 = torch.empty(v0["w8"].shape, dtype=torch.uint8, device=DEV)
+    s_in = torch.empty(v0["input_scale"].shape, dtype=torch.float32, device=DEV)
+    s_w = torch.empty(v0["weight_scale"].shape, dtype=torch.float32, device=DEV)
+    c = sentinel_dev(r.rows, r.N, DEV)
+    off, ids = to_dev_i32(r.a_offsets, DEV), to_dev_i32(r.expert_ids, DEV)
+    st = to_dev_i32(np.zeros(4), DEV)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    call = lambda: binding.gmm_run_fp8(h, c, a8, off, w8, ids, st, s_in, s_w, gran)
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    live = live_row_mask(r.rows, r.a_offsets, r.expert_ids, r.E)
+    gk = r.K if gran[2] is None else gran[2]
+    for seed in (91, 92):
+        v = wl.fp8_host_values(r, seed, gran)
+        a8.copy_(to_dev_u8(v["a8"], DEV))
+        w8.copy_(to_dev_u8(v["w8"], DEV))
+        s_in.copy_(to_dev_f32(v["input_scale"], DEV))
+        s_w.copy_(to_dev_f32(v["weight_scale"], DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        assert binding.gmm_query_status(h) == binding.GMM_OK
+        ref = oracle.gmm_fp8(v["a8"], r.a_offsets, v["w8"], r.expert_ids, v["input_scale"], v["weight_scale"],
+                             (gran[0], gran[1], gk))
+        assert_close(bits_of(c), ref.ref32, live, f"graph replay fp8 {gran} seed {seed}")

@@ -559,3 +559,65 @@ def test_max_groups_int4():
     v = wl.host_values(r, 64)
     _, _, status, _ = check_against_oracle(handle(32), r, v, where="max groups int4")
     assert status == binding.GMM_OK
+
+
+# ---------------------------------------------------------------- CUDA graph capture
+
+def _capture(fn):
+    """Capture fn() (one library call on the current stream) in a CUDA graph."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()                      # once outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def test_cuda_graph_replay_bf16_and_dense_int4():
+    """gmm_run and gmm_matmul_int4 (whose routing words are written by value nodes) captured
+    once and replayed on new inputs written into the same buffers."""
+    import torch
+    h = handle(4)
+    r = routing(4, 384, 512, [5, 130, 0, 77], [2, 0, -1, 3], dist=("normal", 1.0))
+    a = torch.empty((r.rows, r.K), dtype=torch.bfloat16, device=DEV)
+    b = torch.empty((4, r.N, r.K), dtype=torch.bfloat16, device=DEV)
+    c = sentinel_dev(r.rows, r.N, DEV)
+    off, ids = to_dev_i32(r.a_offsets, DEV), to_dev_i32(r.expert_ids, DEV)
+    st = to_dev_i32(np.full(4, 0xFFFFFFFF, np.uint32), DEV)
+    g = _capture(lambda: binding.gmm_run(h, c, a, off, b, ids, st))
+    live = live_row_mask(r.rows, r.a_offsets, r.expert_ids, r.E)
+    for seed in (80, 81):
+        v = wl.host_values(r, seed)
+        a.copy_(to_dev_u16(v["a"], DEV))
+        b.copy_(to_dev_u16(v["b"], DEV))
+        c.copy_(sentinel_dev(r.rows, r.N, DEV))
+        g.replay()
+        torch.cuda.synchronize()
+        assert binding.gmm_query_status(h) == binding.GMM_OK
+        ref = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, c_init=wl.sentinel_c(r.rows, r.N))
+        got = bits_of(c)
+        assert np.array_equal(got[~live], ref.c[~live])
+        assert_close(got, ref.ref32, live, f"graph replay bf16 seed {seed}")
+
+    h1 = handle(1)
+    M, N, K, gs = 150, 256, 512, 128
+    rd = routing(1, N, K, [M], [0], dist=("normal", 1.0), int4=True, gs=gs)
+    a4 = torch.empty((M, K), dtype=torch.bfloat16, device=DEV)
+    q = torch.empty((N, K // 8), dtype=torch.int32, device=DEV)
+    sc = torch.empty((N, K // gs), dtype=torch.bfloat16, device=DEV)
+    c4 = sentinel_dev(M, N, DEV)
+    g4 = _capture(lambda: binding.gmm_matmul_int4(h1, c4, a4, q, sc, group_size=gs))
+    for seed in (82, 83):
+        v = wl.host_values(rd, seed)
+        a4.copy_(to_dev_u16(v["a"], DEV))
+        q.copy_(torch.from_numpy(np.ascontiguousarray(v["packed"][0]).view(np.int32)).to(DEV))
+        sc.copy_(to_dev_u16(v["scales"][0], DEV))
+        g4.replay()
+        torch.cuda.synchronize()
+        ref = oracle.gmm_int4(v["a"], rd.a_offsets, v["packed"], v["scales"], rd.expert_ids, group_size=gs)
+        assert_close(bits_of(c4), ref.ref32, np.ones(M, bool), f"graph replay dense int4 seed {seed}")
