@@ -65,7 +65,7 @@ def work_counts(r: wl.Routing):
     act = r.active_mask()
     rows = int(r.loads[act].sum())
     flops = 2.0 * r.N * r.K * rows
-    experts = np.unique(r.expert_ids[act])
+    experts = np.unique(r.expert_ids[act & (r.loads > 0)])   # an empty group reads no weights
     if r.int4:
         wbytes = r.N * r.K // 2 + r.N * (r.K // r.group_size) * 2
     elif is_fp8(r):   # e4m3 weights and their fp32 scales; e4m3 activations and their scales
@@ -347,6 +347,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--groups", type=int, default=0,
                     help="profile-sized sub-workload: only the first G groups of the named routing")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="redraw the named routing for this many rows (same groups and proportions)")
     ap.add_argument("--group-range", default=None,
                     help="sub-workload lo:hi - groups lo .. hi-1 of the named routing")
     ap.add_argument("--epilogue", default="none", choices=["none", "relu", "silu", "gelu_tanh"],
@@ -370,6 +372,8 @@ def main():
     if args.group_range:
         lo, hi = (int(x) for x in args.group_range.split(":"))
         r = wl.group_range(r, lo, hi)
+    if args.rows:
+        r = wl.with_rows(r, args.rows)
     flops, nbytes, rows = work_counts(r)
     peaks, peaks_kind = load_peaks()
     # e4m3 MMAs run at twice the bf16 rate (the nominal dense ratio 4.5 : 2.25 PFLOP/s):

@@ -195,6 +195,17 @@ def a_rows(r: Routing, rows: int | None = None) -> int:
     return 3 * rows if r.meta.get("planes") else rows
 
 
+def with_rows(r: Routing, total: int, seed: int = 0) -> Routing:
+    """The routing redrawn for `total` rows: Multinomial(total, p) over its groups with p
+    proportional to its loads (sizes, ids and value distributions kept)."""
+    rng = np.random.default_rng([seed, 3])
+    p = np.asarray(r.loads, np.float64)
+    p = p / p.sum() if p.sum() > 0 else np.full(p.size, 1.0 / p.size)
+    loads = rng.multinomial(int(total), p).astype(np.int64)
+    return Routing(f"{r.name}@{total}", r.E, r.N, r.K, loads, r.expert_ids.copy(), offsets_from_loads(loads),
+                   r.a_dist, r.b_dist, r.int4, r.group_size, r.scale_range, dict(r.meta))
+
+
 def group_range(r: Routing, lo: int, hi: int) -> Routing:
     """The sub-workload made of groups lo .. hi-1 of r (rows renumbered from 0, E kept)."""
     loads = r.loads[lo:hi].copy()
