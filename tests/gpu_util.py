@@ -200,3 +200,27 @@ def check_fp8_against_oracle(h, r: wl.Routing, vals, granularity, *, rows_alloc=
     else:
         err = assert_close(got, ref.ref32, live, where)
     return got, ref, status, err
+
+
+# ---------------------------------------------------------------- handles
+
+VARIANTS = ("pair", "single")   # CTA-pair kernels (default) and one CTA per tile
+_handles = {}
+
+
+def handle(E, variant="pair"):
+    """A handle per (E, kernel variant), shared by the test modules; the variant is fixed
+    when the handle is created (GMM_VARIANT)."""
+    import os
+    key = (E, variant)
+    if key not in _handles:
+        old = os.environ.get("GMM_VARIANT")
+        os.environ["GMM_VARIANT"] = variant
+        try:
+            _handles[key] = binding.gmm_create(E, 0)
+        finally:
+            if old is None:
+                del os.environ["GMM_VARIANT"]
+            else:
+                os.environ["GMM_VARIANT"] = old
+    return _handles[key]

@@ -9,14 +9,12 @@ import oracle
 from ragged_matmul_gb300 import binding
 from ragged_matmul_gb300 import workloads as wl
 
-from gpu_util import (assert_close, bits_of, check_fp8_against_oracle, live_row_mask, run_gpu_fp8,
-                      sentinel_dev, to_dev_f32, to_dev_i32, to_dev_u8)
+from gpu_util import (VARIANTS, assert_close, bits_of, check_fp8_against_oracle, handle, live_row_mask,
+                      run_gpu_fp8, sentinel_dev, to_dev_f32, to_dev_i32, to_dev_u8)
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-VARIANTS = ("pair", "single")
-_handles = {}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -27,22 +25,6 @@ def _built():
     from ragged_matmul_gb300 import build
     build.build()
     torch.cuda.set_device(0)
-
-
-def handle(E, variant="pair"):
-    import os
-    key = (E, variant)
-    if key not in _handles:
-        old = os.environ.get("GMM_VARIANT")
-        os.environ["GMM_VARIANT"] = variant
-        try:
-            _handles[key] = binding.gmm_create(E, 0)
-        finally:
-            if old is None:
-                del os.environ["GMM_VARIANT"]
-            else:
-                os.environ["GMM_VARIANT"] = old
-    return _handles[key]
 
 
 def case(E, N, K, loads, ids, seed, gran=(1, 128, None), base=0, rows=None):

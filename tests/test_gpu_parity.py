@@ -11,7 +11,7 @@ import oracle
 from ragged_matmul_gb300 import binding
 from ragged_matmul_gb300 import workloads as wl
 
-from gpu_util import (assert_close, bits_of, check_against_oracle, live_row_mask, run_gpu,
+from gpu_util import (VARIANTS, assert_close, bits_of, check_against_oracle, handle, live_row_mask, run_gpu,
                       sentinel_dev, to_dev_i32, to_dev_u16)
 
 pytestmark = pytest.mark.gpu
@@ -27,28 +27,6 @@ def _built():
     from ragged_matmul_gb300 import build
     build.build()
     torch.cuda.set_device(0)
-
-
-_handles = {}
-
-VARIANTS = ("pair", "single")   # CTA-pair kernels (default) and one CTA per tile
-
-
-def handle(E, variant="pair"):
-    """A handle per (E, kernel variant); the variant is fixed when the handle is created."""
-    import os
-    key = (E, variant)
-    if key not in _handles:
-        old = os.environ.get("GMM_VARIANT")
-        os.environ["GMM_VARIANT"] = variant
-        try:
-            _handles[key] = binding.gmm_create(E, 0)
-        finally:
-            if old is None:
-                del os.environ["GMM_VARIANT"]
-            else:
-                os.environ["GMM_VARIANT"] = old
-    return _handles[key]
 
 
 def routing(E, N, K, loads, ids, dist=("uniform", -1.0, 1.0), base=0, int4=False, gs=128):
