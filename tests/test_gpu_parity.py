@@ -599,3 +599,40 @@ def test_cuda_graph_replay_bf16_and_dense_int4():
         torch.cuda.synchronize()
         ref = oracle.gmm_int4(v["a"], rd.a_offsets, v["packed"], v["scales"], rd.expert_ids, group_size=gs)
         assert_close(bits_of(c4), ref.ref32, np.ones(M, bool), f"graph replay dense int4 seed {seed}")
+
+
+def test_two_handles_on_two_streams_concurrently():
+    """Handles share no device state: two handles, each launching on its own stream with
+    no ordering between them, both match the oracle."""
+    import torch
+    ha = binding.gmm_create(4, 0)
+    hb = binding.gmm_create(6, 0)
+    try:
+        ra = routing(4, 512, 1024, [100, 7, 300, 0], [1, 3, 0, 2], dist=("normal", 1.0))
+        rb = routing(6, 768, 512, [50, 250, 1, 90, 33], [5, 0, 2, -1, 4], dist=("normal", 1.0))
+        va, vb = wl.host_values(ra, 100), wl.host_values(rb, 101)
+        sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+        outs = []
+        for h, r, v, s in ((ha, ra, va, sa), (hb, rb, vb, sb)):
+            c = sentinel_dev(r.rows, r.N, DEV)
+            st = to_dev_i32(np.full(4, 0xFFFFFFFF, np.uint32), DEV)
+            args = (to_dev_u16(v["a"], DEV), to_dev_i32(r.a_offsets, DEV), to_dev_u16(v["b"], DEV),
+                    to_dev_i32(r.expert_ids, DEV))
+            outs.append((h, r, v, s, c, st, args))
+        torch.cuda.synchronize()
+        for _ in range(5):                     # interleave launches on the two streams
+            for h, r, v, s, c, st, (a, off, b, ids) in outs:
+                binding.gmm_run(h, c, a, off, b, ids, st, stream=s)
+        torch.cuda.synchronize()
+        for h, r, v, s, c, st, _ in outs:
+            assert binding.gmm_query_status(h) == binding.GMM_OK
+            ref = oracle.gmm_bf16(v["a"], r.a_offsets, v["b"], r.expert_ids, c_init=wl.sentinel_c(r.rows, r.N),
+                                  stats_init=np.full(4, 0xFFFFFFFF, np.uint32))
+            got = bits_of(c)
+            live = live_row_mask(r.rows, r.a_offsets, r.expert_ids, r.E)
+            assert np.array_equal(got[~live], ref.c[~live])
+            assert np.array_equal(st.cpu().numpy().view(np.uint32), ref.stats)
+            assert_close(got, ref.ref32, live, f"concurrent handle E={r.E}")
+    finally:
+        binding.gmm_destroy(ha)
+        binding.gmm_destroy(hb)
