@@ -240,6 +240,7 @@ struct __align__(32) Ctrl {   // 32: the tile queue entries inside
   uint64_t qempty[kQStages];     // 4-bit: the dequantisation warps are done with a packed chunk
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
+  uint64_t maps_ready;           // epilogue warp 2 has written this CTA's token maps
   uint64_t tq_full[kTileQueue];  // tile queue entry published
   uint64_t tq_empty[kTileQueue]; // every reader has taken the entry (pair: both CTAs', on the leader)
   uint32_t tq_tile[kTileQueue];
@@ -602,6 +603,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       mbar_init(smem_addr(&ctl.acc_full[a]), 1);
       mbar_init(smem_addr(&ctl.acc_empty[a]), kEpiArrivals);
     }
+    mbar_init(smem_addr(&ctl.maps_ready), 1);
     for (int q = 0; q < kTileQueue; ++q) {
       mbar_init(smem_addr(&ctl.tq_full[q]), 1);
       mbar_init(smem_addr(&ctl.tq_empty[q]), kQueueArrivals);
@@ -646,23 +648,12 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ token (and bf16 weight) producer
-    // Token maps: lane i builds the map whose copies are 16 (i + 1) rows high, so a
-    // tile's token slab (a multiple of 16 rows) is one copy per 64-K sub-slab.
+    // The token maps (one per copy height) are written by epilogue warp 2 while this
+    // thread decodes its first tile; they are acquired before the first copy.
     constexpr int kMaps = static_cast<int>(G::kCtaTok / 16);
     uint8_t *slot = p.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlotBytes;
-    if (total > 0 && lane < kMaps) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(&p.tok_map);
-      uint4 *dst = reinterpret_cast<uint4 *>(slot + lane * 128);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dst[i] = src[i];
-      const uint32_t planes = (p.plane_s0 | p.plane_s1) ? 3u : 1u;   // A-plane row offsetting: 3 planes of rows
-      tensormap_set_dim1(dst, planes * __ldg(p.a_offsets + p.num_groups));
-      tensormap_set_box1(dst, 16u * static_cast<uint32_t>(lane + 1));
-      tensormap_release();
-    }
-    __syncwarp();
     if (lane == 0 && total > 0) {
-      for (int i = 0; i < kMaps; ++i) tensormap_acquire(slot + i * 128);
+      bool maps_acquired = false;
       const CUtensorMap *tok_maps = reinterpret_cast<const CUtensorMap *>(slot);
       prefetch_tensormap(&p.w_map);
       const uint64_t pol_first = l2_policy_evict_first();
@@ -754,6 +745,11 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         // group (evict last), so streaming weights do not wash them out of L2.
         const uint64_t w_pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
         const uint64_t t_pol = p.cache_hints ? pol_last : pol_normal;
+        if (!maps_acquired) {
+          if (!wait_phase(smem_addr(&ctl.maps_ready), 0, abort)) { ok = false; break; }
+          for (int i = 0; i < kMaps; ++i) tensormap_acquire(slot + i * 128);
+          maps_acquired = true;
+        }
         for (int kb = 0; kb < KB; ++kb) {
           const uint32_t full_local = smem_addr(&ctl.full[rt.slot]);
           if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
@@ -894,6 +890,27 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue
+    if (warp == 2) {
+      // First, the producer's token maps: lane i builds the map whose copies are
+      // 16 (i + 1) rows high (a tile's token slab, a multiple of 16 rows, is then one copy
+      // per 64-K sub-slab), from the host's map with the row extent patched to
+      // a_offsets[G] (three planes of it with A-plane row offsetting).  Done here, not in
+      // the producer, so that it overlaps the producer's decode of its first tile.
+      constexpr int kMaps = static_cast<int>(G::kCtaTok / 16);
+      uint8_t *slot = p.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlotBytes;
+      if (total > 0 && lane < kMaps) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(&p.tok_map);
+        uint4 *dst = reinterpret_cast<uint4 *>(slot + lane * 128);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = src[i];
+        const uint32_t planes = (p.plane_s0 | p.plane_s1) ? 3u : 1u;
+        tensormap_set_dim1(dst, planes * __ldg(p.a_offsets + p.num_groups));
+        tensormap_set_box1(dst, 16u * static_cast<uint32_t>(lane + 1));
+        tensormap_release();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&ctl.maps_ready));
+    }
     const uint32_t quad = static_cast<uint32_t>(warp & 3);   // TMEM lanes this warp may read
     const uint32_t acc_empty0 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[0]), 0) : smem_addr(&ctl.acc_empty[0]);
     const uint32_t acc_empty1 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[1]), 0) : smem_addr(&ctl.acc_empty[1]);
