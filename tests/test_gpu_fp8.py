@@ -311,3 +311,23 @@ def test_fp8_cuda_graph_replay(gran):
         ref = oracle.gmm_fp8(v["a8"], r.a_offsets, v["w8"], r.expert_ids, v["input_scale"], v["weight_scale"],
                              (gran[0], gran[1], gk))
         assert_close(bits_of(c), ref.ref32, live, f"graph replay fp8 {gran} seed {seed}")
+
+
+@pytest.mark.parametrize("gran", [(1, 128, None), (1, 128, 128)])
+def test_fp8_nan_codes_propagate_like_the_oracle(gran):
+    """e4m3 NaN codes (S.1111.111) in A turn exactly the oracle's outputs into NaN."""
+    r, v = case(3, 256, 256, [9, 40, 0, 17], [2, 0, 1, -1], 111, gran=gran)
+    a8 = v["a8"].copy()
+    a8[3, 5] = 0x7F
+    a8[30, 200] = 0xFF
+    v = dict(v, a8=a8)
+    got, stats, status = run_gpu_fp8(handle(3), v, r.a_offsets, r.expert_ids, gran, N=r.N)
+    gk = r.K if gran[2] is None else gran[2]
+    ref = oracle.gmm_fp8(a8, r.a_offsets, v["w8"], r.expert_ids, v["input_scale"], v["weight_scale"],
+                         (gran[0], gran[1], gk))
+    live = live_row_mask(r.rows, r.a_offsets, r.expert_ids, r.E)
+    gf = (got.astype(np.uint32) << 16).view(np.float32)
+    assert np.array_equal(np.isnan(gf[live]), np.isnan(ref.ref32[live]))
+    assert np.isnan(ref.ref32[3]).all() and np.isnan(ref.ref32[30]).all()
+    finite_rows = live & np.isfinite(ref.ref32).all(axis=1)   # rows without a NaN input
+    assert_close(got, ref.ref32, finite_rows, f"fp8 finite rows {gran}")

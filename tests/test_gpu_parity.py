@@ -636,3 +636,36 @@ def test_two_handles_on_two_streams_concurrently():
     finally:
         binding.gmm_destroy(ha)
         binding.gmm_destroy(hb)
+
+
+def _nonfinite_compare(got_bits, ref, live, where):
+    got = (np.asarray(got_bits, np.uint16).astype(np.uint32) << 16).view(np.float32)[live]
+    r32 = ref.ref32[live]
+    assert np.array_equal(np.isnan(got), np.isnan(r32)), f"{where}: NaN positions differ"
+    inf = np.isinf(r32)
+    assert np.array_equal(np.isinf(got), inf) and np.array_equal(np.sign(got[inf]), np.sign(r32[inf])), \
+        f"{where}: Inf positions or signs differ"
+    fin = np.isfinite(r32)
+    err = np.abs(got[fin].astype(np.float64) - r32[fin])
+    assert np.all(err <= 1e-2 + 1e-2 * np.abs(r32[fin])), where
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_nonfinite_inputs_propagate_like_the_oracle(variant):
+    """NaN and +-Inf in A reach exactly the outputs the oracle says they reach (its row, all
+    columns; with Inf, NaN where products of opposite infinities meet)."""
+    r = routing(3, 264, 192, [9, 40, 0, 17], [2, 0, 1, -1], dist=("normal", 1.0))
+    v = wl.host_values(r, 110)
+    a = v["a"].copy()
+    a[3, 5] = 0x7FC0          # NaN
+    a[12, 0] = 0x7F80         # +Inf
+    a[20, 7] = 0xFF80         # -Inf
+    a[20, 9] = 0x7F80         # +Inf in the same row: that row's sums see +Inf and -Inf
+    v = dict(v, a=a)
+    got, stats, status = run_gpu(handle(3, variant), a, r.a_offsets, r.expert_ids, b_bits=v["b"], N=r.N)
+    ref = oracle.gmm_bf16(a, r.a_offsets, v["b"], r.expert_ids, c_init=wl.sentinel_c(r.rows, r.N),
+                          stats_init=np.full(4, 0xFFFFFFFF, np.uint32))
+    live = live_row_mask(r.rows, r.a_offsets, r.expert_ids, r.E)
+    assert np.isnan(ref.ref32[3]).all() and np.isinf(ref.ref32[12]).any()
+    assert np.array_equal(got[~live], ref.c[~live]) and np.array_equal(stats, ref.stats)
+    _nonfinite_compare(got, ref, live, f"non-finite {variant}")
