@@ -292,7 +292,9 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
         }
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_addr(&part_empty[pb]));
+        // Relaxed: the partials' loads are complete, and the next block's scale loads
+        // just issued stay in flight instead of being waited for.
+        if (lane == 0) mbar_arrive_relaxed(smem_addr(&part_empty[pb]));
         if (++pb == kBwBufs) {
           pb = 0;
           pb_phase ^= 1u;

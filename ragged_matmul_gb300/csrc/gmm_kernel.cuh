@@ -286,10 +286,19 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   }
 }
 
-// The same with cluster-scope acquire, for barriers the peer CTA arrives on.
+// The same at cluster scope, for barriers the peer CTA arrives on: with acquire
+// semantics, or relaxed (kRelaxed) where the phase publishes no generic-proxy writes.
+template <bool kRelaxed = false>
 __device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity, volatile int *abort) {
-  if (mbar_test_wait_cluster(bar, parity)) return true;
-  if (mbar_try_wait_cluster_hint(bar, parity, kSuspendNs)) return true;
+  auto test = [&]() {
+    return kRelaxed ? mbar_test_wait_cluster_relaxed(bar, parity) : mbar_test_wait_cluster(bar, parity);
+  };
+  auto try_wait = [&]() {
+    return kRelaxed ? mbar_try_wait_cluster_relaxed_hint(bar, parity, kSuspendNs)
+                    : mbar_try_wait_cluster_hint(bar, parity, kSuspendNs);
+  };
+  if (test()) return true;
+  if (try_wait()) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (*abort) return false;
@@ -297,7 +306,7 @@ __device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity
       *abort = 1;
       return false;
     }
-    if (mbar_try_wait_cluster_hint(bar, parity, kSuspendNs)) return true;
+    if (try_wait()) return true;
   }
 }
 
@@ -830,7 +839,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         if (got < 0) ok = false;
         if (got <= 0) break;
         const bool acc_free = __all_sync(
-            0xffffffffu, kPair ? wait_phase_cluster(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort)
+            0xffffffffu, kPair ? wait_phase_cluster<true>(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort)
                                : wait_phase(smem_addr(&ctl.acc_empty[acc]), acc_phase ^ 1u, abort));
         if (!acc_free) { ok = false; break; }
         tc_fence_after_sync();
@@ -838,9 +847,10 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         const uint32_t idesc = kFp8 ? idesc_e4m3_f32(G::kRows, ti.ntok) : idesc_bf16_f32(G::kRows, ti.ntok);
         for (int kb = 0; kb < KB; ++kb) {
           // The 4-bit pair's stage is also signalled by the second CTA's dequantisation
-          // warps (cluster-scope release), so it is acquired at cluster scope.
+          // warps, so it is waited for at cluster scope; relaxed, since their TMEM
+          // stores are ordered by tcgen05 fences and the token bytes by the barrier.
           const bool staged = __all_sync(
-              0xffffffffu, (kInt4 && kPair) ? wait_phase_cluster(smem_addr(&ctl.full[rt.slot]), rt.phase, abort)
+              0xffffffffu, (kInt4 && kPair) ? wait_phase_cluster<true>(smem_addr(&ctl.full[rt.slot]), rt.phase, abort)
                                             : wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort));
           if (!staged) { ok = false; break; }
           tc_fence_after_sync();
@@ -1025,8 +1035,10 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) {
-        if constexpr (kPair) mbar_arrive_cluster(acc ? acc_empty1 : acc_empty0);
-        else mbar_arrive(acc ? acc_empty1 : acc_empty0);
+        // Relaxed: the accumulator's loads are complete; the C stores need not be
+        // visible to the MMA issuer.
+        if constexpr (kPair) mbar_arrive_cluster_relaxed(acc ? acc_empty1 : acc_empty0);
+        else mbar_arrive_relaxed(acc ? acc_empty1 : acc_empty0);
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
@@ -1166,7 +1178,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) {
-          if constexpr (kPair) mbar_arrive_cluster(full_g); else mbar_arrive(full_g);
+          if constexpr (kPair) mbar_arrive_cluster_relaxed(full_g); else mbar_arrive_relaxed(full_g);   // TMEM stores done
         }
         aphase ^= 1u;
       }
