@@ -107,13 +107,15 @@ constexpr int kQSlotBytes = kBlockN * kQRowBytes;            // 16 KB
 constexpr int kQStages = 4;                                  // slots: 8 stages ahead
 constexpr int kQRingBytes = kQStages * kQSlotBytes;
 static_assert(kQRowBytes == 128, "the packed chunk is one 128-byte swizzle row per weight row");
-// Epilogue staging: each epilogue warp transposes its accumulator rows through a
-// 16-row x 32-column fp32 tile in shared memory (rows padded to 36 floats: the
-// column-wise writes and the 16-byte row reads are both free of bank conflicts), so
-// that every thread stores 8 consecutive columns of one C row with one 16-byte store.
-constexpr uint32_t kEpiRows = 16;
-constexpr uint32_t kEpiStride = 36;
-constexpr int kEpiStageBytes = 4 * kEpiRows * kEpiStride * 4;   // 4 epilogue warps
+// Epilogue staging: each epilogue warp transposes 32 token rows x its 32 C columns
+// at a time through a bf16 tile in shared memory (stmatrix in, 16-byte row reads out),
+// so that every thread stores 8 consecutive columns of one C row with one 16-byte
+// store.  A tile row is 64 bytes (four 16-byte blocks); block b of row r sits at
+// b ^ ((r >> 1) & 3), which keeps both the 8-row matrix writes and the row reads free
+// of bank conflicts.
+constexpr uint32_t kEpiRows = 32;
+constexpr uint32_t kEpiRowBytes = 64;
+constexpr int kEpiStageBytes = 4 * kEpiRows * kEpiRowBytes;   // 4 epilogue warps
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 // 4-bit kernel: dequantised weight slabs live in TMEM (128 lanes = weight rows, 32
@@ -932,38 +934,39 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const int got = next_tile_warp<G>(reader, ctl, q_empty0, q_remote, abort, prefix, p, &ti);
       if (got < 0 && lane == 0) atomicOr(p.status, kStatusTimeout);
       if (got <= 0) break;
-      // This thread's C columns after the transpose: 8 consecutive ones, n8 .. n8 + 7
-      // (N is a multiple of 8, so they are all in range or all past N); its row in
-      // each 8-row pass is rsub.
+      // Two views of a 32-row chunk.  Read from TMEM (16x256b shape, the stmatrix
+      // fragment): thread l holds columns quad * 32 + 8i + l / 4 (i = 0 .. 3) of rows
+      // 8g + 2(l % 4) + {0, 1} (g = 0 .. 3).  Stored to C: thread l writes 8
+      // consecutive columns n8 .. n8 + 7 of row 8 pass + rsub (N is a multiple of 8, so
+      // they are all in range or all past N).
       const uint32_t seg = static_cast<uint32_t>(lane) & 3u;
       const uint32_t rsub = static_cast<uint32_t>(lane) >> 2;
-      const uint32_t n8 = ti.n0 + rank * kBlockN + quad * 32 + seg * 8;
+      const uint32_t ncta = ti.n0 + rank * kBlockN + quad * 32;   // this warp's first C column
+      const uint32_t n8 = ncta + seg * 8;
       const bool cols_ok = n8 < static_cast<uint32_t>(p.N);
       __nv_bfloat16 *crow = p.c + static_cast<size_t>(ti.row0) * p.N + n8;
       const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + acc * kAccCols;
       const bool scaled = kFp8 && p.in_scale != nullptr;
       const bool fused = p.epi_bias != nullptr || p.epi_row_scale != nullptr || p.epi_act != kActNone || scaled;
       // The fused epilogue's operands are loaded before the accumulator wait, so their
-      // latency hides behind the tile's MMAs: the 8 columns' bias and (e4m3) weight
-      // scale, and the tile's per-row factors, lane l holding rows l, l + 32, ...
-      // (row scale rs, e4m3 input scale sc).
+      // latency hides behind the tile's MMAs: the bias and (e4m3) weight scale of the
+      // thread's 4 fragment columns, and the tile's per-row factors, lane l holding rows
+      // l, l + 32, ... (row scale rs, e4m3 input scale sc).
       constexpr int kRowRegs = static_cast<int>(G::kMaxTok / 32);
-      float rs[kRowRegs], sc[kRowRegs], bias8[8], wc8[8];
+      float rs[kRowRegs], sc[kRowRegs], bias4[4], wc4[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        bias8[k] = 0.0f;
-        wc8[k] = 1.0f;
+      for (int i = 0; i < 4; ++i) {
+        bias4[i] = 0.0f;
+        wc4[i] = 1.0f;
       }
       if (fused) {
-        if (p.epi_bias != nullptr && cols_ok) {
-          const __nv_bfloat16 *bp = p.epi_bias + static_cast<size_t>(ti.e) * p.N + n8;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) bias8[k] = __bfloat162float(bp[k]);
-        }
-        if (scaled && cols_ok) {
-          const float *wp = p.w_scale + static_cast<size_t>(ti.e) * p.w_scale_cols;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) wc8[k] = __ldg(wp + (n8 + k) / static_cast<uint32_t>(p.scale_gn));
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t n = ncta + 8u * i + (static_cast<uint32_t>(lane) >> 2);
+          if (ncta + 8u * i < static_cast<uint32_t>(p.N)) {
+            if (p.epi_bias != nullptr) bias4[i] = __bfloat162float(p.epi_bias[static_cast<size_t>(ti.e) * p.N + n]);
+            if (scaled) wc4[i] = __ldg(p.w_scale + static_cast<size_t>(ti.e) * p.w_scale_cols + n / static_cast<uint32_t>(p.scale_gn));
+          }
         }
 #pragma unroll
         for (int q = 0; q < kRowRegs; ++q) {
@@ -981,50 +984,62 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      // 32 token rows per TMEM wait; each 16-row half goes through the staging tile:
-      // thread l writes its column (TMEM lane quad * 32 + l) down the tile, then reads
-      // back 8 columns of one row per pass.  The row factors of rows c0 .. c0 + 31 are
-      // in rs[0] / sc[0] and move down one register every 32 rows.
-      float *stg = reinterpret_cast<float *>(dyn_smem + (epi_ring - dyn_base)) + (warp - 2) * kEpiRows * kEpiStride;
+      // Per chunk: two TMEM loads (lanes +0 .. 15 and +16 .. 31), one wait; per 8-row
+      // group g the four 8 x 8 matrices (fragment column blocks i) go to the staging
+      // tile transposed, one stmatrix; then four row reads and 16-byte stores.  A chunk
+      // may read TMEM columns past ntok (inside the accumulator); those rows are not
+      // stored.  The row factors of rows c0 .. c0 + 31 are in rs[0] / sc[0] and move
+      // down one register every 32 rows.
+      const uint32_t stg = epi_ring + static_cast<uint32_t>(warp - 2) * (kEpiRows * kEpiRowBytes);
+      // stmatrix: thread l addresses row 8g + (l % 8) of matrix i = l / 8 (block i).
+      const uint32_t st_row = static_cast<uint32_t>(lane) & 7u, st_blk = static_cast<uint32_t>(lane) >> 3;
+      const uint8_t *stg_ptr = dyn_smem + (stg - dyn_base);
       for (uint32_t c0 = 0; c0 < ti.ntok; c0 += 32) {
         uint32_t va[16], vb[16];
-        const bool two = c0 + 16 < ti.ntok;
-        tmem_ld_x16(taddr + c0, va);
-        if (two) tmem_ld_x16(taddr + c0 + 16, vb);
+        tmem_ld_16x256b_x4(taddr + c0, va);
+        tmem_ld_16x256b_x4(taddr + (16u << 16) + c0, vb);
         tmem_ld_wait();
+        __syncwarp();   // the previous chunk's row reads of the tile are done
 #pragma unroll
-        for (uint32_t h = 0; h < 2; ++h) {
-          if (h == 1 && !two) break;
-          __syncwarp();   // the previous half's reads of the tile are done
-#pragma unroll
-          for (uint32_t j = 0; j < kEpiRows; ++j) stg[j * kEpiStride + lane] = __uint_as_float(h ? vb[j] : va[j]);
-          __syncwarp();
-#pragma unroll
-          for (uint32_t pass = 0; pass < 2; ++pass) {
-            const uint32_t rl = pass * 8u + rsub;   // row within the half
-            const uint32_t row = c0 + h * 16u + rl; // row within the tile
-            const float4 x0 = *reinterpret_cast<const float4 *>(stg + rl * kEpiStride + seg * 8);
-            const float4 x1 = *reinterpret_cast<const float4 *>(stg + rl * kEpiStride + seg * 8 + 4);
-            float y[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            if (fused) {
-              const int src = static_cast<int>(row & 31u);
-              const float s_r = __shfl_sync(0xffffffffu, rs[0], src);
-              const float s_i = kFp8 ? __shfl_sync(0xffffffffu, sc[0], src) : 1.0f;
-#pragma unroll
-              for (int k = 0; k < 8; ++k) {
-                if (kFp8) y[k] *= s_i * wc8[k];
-                y[k] = epilogue_op(y[k], bias8[k], p.epi_act, s_r);
-              }
-            }
-            if (cols_ok && row < ti.nrows) {
-              uint4 out;
-              out.x = pack_bf16x2(y[0], y[1]);
-              out.y = pack_bf16x2(y[2], y[3]);
-              out.z = pack_bf16x2(y[4], y[5]);
-              out.w = pack_bf16x2(y[6], y[7]);
-              *reinterpret_cast<uint4 *>(crow + static_cast<size_t>(row) * p.N) = out;
+        for (uint32_t g = 0; g < 4; ++g) {
+          // Row factors of this thread's two rows of the group.
+          float s0 = 1.0f, s1 = 1.0f, q0 = 1.0f, q1 = 1.0f;
+          if (fused) {
+            const int r0 = static_cast<int>(8 * g + 2 * seg);
+            s0 = __shfl_sync(0xffffffffu, rs[0], r0);
+            s1 = __shfl_sync(0xffffffffu, rs[0], r0 + 1);
+            if (kFp8) {
+              q0 = __shfl_sync(0xffffffffu, sc[0], r0);
+              q1 = __shfl_sync(0xffffffffu, sc[0], r0 + 1);
             }
           }
+          uint32_t w[4];
+#pragma unroll
+          for (uint32_t i = 0; i < 4; ++i) {
+            const uint32_t *v = (i >> 1) ? vb : va;
+            float y0 = __uint_as_float(v[4 * g + 2 * (i & 1)]);
+            float y1 = __uint_as_float(v[4 * g + 2 * (i & 1) + 1]);
+            if (fused) {
+              if (kFp8) {
+                y0 *= q0 * wc4[i];
+                y1 *= q1 * wc4[i];
+              }
+              y0 = epilogue_op(y0, bias4[i], p.epi_act, s0);
+              y1 = epilogue_op(y1, bias4[i], p.epi_act, s1);
+            }
+            w[i] = pack_bf16x2(y0, y1);
+          }
+          const uint32_t row = 8 * g + st_row;
+          stmatrix_x4_trans(stg + row * kEpiRowBytes + ((st_blk ^ ((row >> 1) & 3u)) << 4), w[0], w[1], w[2], w[3]);
+        }
+        __syncwarp();
+#pragma unroll
+        for (uint32_t pass = 0; pass < 4; ++pass) {
+          const uint32_t rl = pass * 8u + rsub;   // row within the chunk
+          const uint32_t row = c0 + rl;           // row within the tile
+          const uint4 out =
+              *reinterpret_cast<const uint4 *>(stg_ptr + rl * kEpiRowBytes + ((seg ^ ((rl >> 1) & 3u)) << 4));
+          if (cols_ok && row < ti.nrows) *reinterpret_cast<uint4 *>(crow + static_cast<size_t>(row) * p.N) = out;
         }
 #pragma unroll
         for (int q = 0; q + 1 < kRowRegs; ++q) {

@@ -279,6 +279,31 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&v)[16]) {
       : "r"(taddr));
 }
 
+// 16 TMEM lanes x 32 columns in the 16x256b shape (four repeats of 16 lanes x 8
+// columns).  In repeat j (v[4j] .. v[4j + 3]) thread t holds lane t/4, columns
+// 8j + 2(t%4) and 8j + 2(t%4) + 1 (v[4j], v[4j + 1]), and the same two columns of
+// lane t/4 + 8 (v[4j + 2], v[4j + 3]), lanes counted from the lane of taddr.
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+
+// Four 8x8 matrices of 16-bit values to shared memory, each transposed: thread t's
+// word m (two values, row t/4 and columns 2(t%4), 2(t%4) + 1 of matrix m, the lower
+// column in the low half) lands in rows 2(t%4) and 2(t%4) + 1, column t/4, of the
+// stored matrix m, whose row r is the 16 bytes at the address of thread 8m + r.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2,
+                                                  uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r0),
+               "r"(r1), "r"(r2), "r"(r3)
+               : "memory");
+}
+
 // Each thread of the warp reads 8 consecutive 32-bit columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, uint32_t (&v)[8]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
