@@ -198,7 +198,7 @@ int configure(gmm_variant *v, int optin, int num_sms) {
     la[0].val.clusterDim.y = 1;
     la[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
-    cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : gmm::kThreads);
+    cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : gmm::kThreadsWide);   // the larger launch
     cfg.dynamicSmemBytes = v->smem;
     cfg.attrs = la;
     cfg.numAttrs = 1;
@@ -287,7 +287,8 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : gmm::kThreads);
+  // Short K: 8 epilogue warps (the bf16 / e4m3 kernel reads its warp count from blockDim).
+  cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : (p.K <= gmm::kWideEpilogueMaxK ? gmm::kThreadsWide : gmm::kThreads));
   cfg.gridDim = dim3(static_cast<unsigned>(v.grid));
   cfg.dynamicSmemBytes = v.smem;
   cfg.stream = stream;

@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
     tc_fence_before_sync();
   }
   __syncthreads();
-  build_schedule<kBwThreads, G>(p, ctl, prefix);
+  build_schedule<G>(p, ctl, prefix, kBwThreads);
   if constexpr (kShare) cluster_sync();   // the peer's barriers are initialised before anyone signals them
   if (blockIdx.x == 0 && tid == 0) {
     p.stats[1] = ctl.active;

@@ -84,6 +84,11 @@ constexpr int kBK = 64;                       // K per stage: one 128-byte swizz
 constexpr int kMaxStages = 12;                // deepest W+T stage ring
 constexpr int kMaxGroups = 4096;
 constexpr int kThreads = 192;                 // bf16 kernel: producer, MMA, 4 epilogue warps
+// With short K a tile is a few stages, and storing its accumulator takes longer than
+// computing it: the bf16 / e4m3 kernel then runs 8 epilogue warps, two per TMEM lane
+// quadrant, taking alternate 32-row chunks.
+constexpr int kThreadsWide = 320;
+constexpr int kWideEpilogueMaxK = 512;
 // 4-bit kernel: 64-wide K sub-slabs per stage, and the dequantisation warps.  The
 // 12 warps form kDqGroups groups that take the stages in turn (stage s goes to group
 // s % kDqGroups), so each warp has kDqGroups stage-times for its loop of waits,
@@ -115,7 +120,7 @@ static_assert(kQRowBytes == 128, "the packed chunk is one 128-byte swizzle row p
 // of bank conflicts.
 constexpr uint32_t kEpiRows = 32;
 constexpr uint32_t kEpiRowBytes = 64;
-constexpr int kEpiStageBytes = 4 * kEpiRows * kEpiRowBytes;   // 4 epilogue warps
+constexpr int kEpiStageBytes = 8 * kEpiRows * kEpiRowBytes;   // up to 8 epilogue warps
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 // 4-bit kernel: dequantised weight slabs live in TMEM (128 lanes = weight rows, 32
@@ -319,13 +324,13 @@ __device__ __forceinline__ bool wait_phase_for(uint32_t bar, uint32_t parity, ui
   return true;
 }
 
-// Scan a_offsets / expert_ids into prefix[g] = first tile of group g (all NT threads).
-template <int NT, class G>
-__device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix) {
+// Scan a_offsets / expert_ids into prefix[g] = first tile of group g (all nt threads).
+template <class G>
+__device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix, int nt) {
   const int Gn = p.num_groups;
   const uint32_t n_blocks = static_cast<uint32_t>((p.N + G::kRows - 1) / G::kRows);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int chunk = (Gn + NT - 1) / NT;
+  const int chunk = (Gn + nt - 1) / nt;
   const int g_begin = min(Gn, tid * chunk), g_end = min(Gn, g_begin + chunk);
 
   unsigned long long mine = 0;
@@ -362,7 +367,7 @@ __device__ void build_schedule(const GmmParams &p, Ctrl &ctl, uint32_t *prefix) 
   if (lane == 31) ctl.warp_tiles[warp] = incl;
   __syncthreads();
   unsigned long long base = 0, total = 0;
-  for (int w = 0; w < NT / 32; ++w) {
+  for (int w = 0; w < nt / 32; ++w) {
     if (w < warp) base += ctl.warp_tiles[w];
     total += ctl.warp_tiles[w];
   }
@@ -565,12 +570,13 @@ __device__ __forceinline__ int next_tile_warp(TileSource &src, Ctrl &ctl, uint32
 }
 
 template <bool kInt4, bool kPair, bool kFp8 = false>
-__global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
+__global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
     gmm_grouped_kernel(const __grid_constant__ GmmParams p) {
   static_assert(!(kInt4 && kFp8), "the e4m3 path has its weights in shared memory");
   using G = Geom<kInt4, kPair>;
-  constexpr int NT = kInt4 ? kInt4Threads : kThreads;
-  constexpr uint32_t kEpiArrivals = (kPair ? 2 : 1) * 4;   // one per epilogue warp of each CTA
+  // Epilogue warps 2 .. 2 + n_epi - 1: 4, or 8 in a wide launch (bf16 / e4m3 only).
+  const uint32_t n_epi = kInt4 ? 4u : blockDim.x / 32u - 2u;
+  const uint32_t epi_arrivals = (kPair ? 2u : 1u) * n_epi;   // one per epilogue warp of each CTA
   constexpr uint32_t kDequantWarps = kDequantThreads / 32;
   // Arrivals per phase of a stage's `full` barrier: the token producer's (which also
   // sets the expected bytes) and, 4-bit, one per dequantisation warp of the stage's
@@ -585,12 +591,12 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
   const uint32_t SW = kInt4 ? 0u : ST;                         // weight slabs in shared memory
   const int KB = (p.K + static_cast<int>(G::kSub * kBK) - 1) / static_cast<int>(G::kSub * kBK);   // stages per tile
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
-  // Readers of each tile-queue entry: per CTA the MMA thread (leader only), the four
+  // Readers of each tile-queue entry: per CTA the MMA thread (leader only), the
   // epilogue warps and (4-bit) the packed-slab producer and the dequantisation
   // warps; in the pair's second CTA also its token producer.
-  constexpr uint32_t kLeaderReaders = 1 + 4 + (kInt4 ? 1 + kDequantWarps : 0);
-  constexpr uint32_t kPeerReaders = 1 + 4 + (kInt4 ? 1 + kDequantWarps : 0);
-  constexpr uint32_t kQueueArrivals = kLeaderReaders + (kPair ? kPeerReaders : 0);
+  const uint32_t leader_readers = 1 + n_epi + (kInt4 ? 1 + kDequantWarps : 0);
+  const uint32_t peer_readers = 1 + n_epi + (kInt4 ? 1 + kDequantWarps : 0);
+  const uint32_t queue_arrivals = leader_readers + (kPair ? peer_readers : 0);
 
   // 1024-byte aligned rings, at identical offsets in both CTAs of a pair:
   // SW weight slabs (bf16), ST token slabs, then (4-bit) kQStages packed slabs.
@@ -612,12 +618,12 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_addr(&ctl.acc_full[a]), 1);
-      mbar_init(smem_addr(&ctl.acc_empty[a]), kEpiArrivals);
+      mbar_init(smem_addr(&ctl.acc_empty[a]), epi_arrivals);
     }
     mbar_init(smem_addr(&ctl.maps_ready), 1);
     for (int q = 0; q < kTileQueue; ++q) {
       mbar_init(smem_addr(&ctl.tq_full[q]), 1);
-      mbar_init(smem_addr(&ctl.tq_empty[q]), kQueueArrivals);
+      mbar_init(smem_addr(&ctl.tq_empty[q]), queue_arrivals);
     }
     ctl.abort = 0;
     ctl.active = 0;
@@ -637,7 +643,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
     tc_fence_before_sync();
   }
   __syncthreads();
-  build_schedule<NT, G>(p, ctl, prefix);
+  build_schedule<G>(p, ctl, prefix, static_cast<int>(blockDim.x));
   if constexpr (kPair) cluster_sync();   // the peer's barriers are initialised before anyone signals them
 
   if (blockIdx.x == 0 && tid == 0) {
@@ -900,7 +906,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       }
       if (!ok && lane == 0) atomicOr(p.status, kStatusTimeout);
     }
-  } else if (warp < 6) {
+  } else if (warp < 2 + static_cast<int>(n_epi)) {
     // ------------------------------------------------------------ epilogue
     if (warp == 2) {
       // First, the producer's token maps: lane i builds the map whose copies are
@@ -924,6 +930,9 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       if (lane == 0) mbar_arrive(smem_addr(&ctl.maps_ready));
     }
     const uint32_t quad = static_cast<uint32_t>(warp & 3);   // TMEM lanes this warp may read
+    // With 8 epilogue warps, warps 2 .. 5 take the even 32-row chunks of a tile and
+    // warps 6 .. 9 the odd ones.
+    const uint32_t esub = static_cast<uint32_t>(warp - 2) >> 2, nsub = n_epi >> 2;
     const uint32_t acc_empty0 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[0]), 0) : smem_addr(&ctl.acc_empty[0]);
     const uint32_t acc_empty1 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[1]), 0) : smem_addr(&ctl.acc_empty[1]);
     uint32_t acc = 0, acc_phase = 0;
@@ -950,8 +959,8 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       const bool fused = p.epi_bias != nullptr || p.epi_row_scale != nullptr || p.epi_act != kActNone || scaled;
       // The fused epilogue's operands are loaded before the accumulator wait, so their
       // latency hides behind the tile's MMAs: the bias and (e4m3) weight scale of the
-      // thread's 4 fragment columns, and the tile's per-row factors, lane l holding rows
-      // l, l + 32, ... (row scale rs, e4m3 input scale sc).
+      // thread's 4 fragment columns, and the per-row factors of this warp's chunks, lane
+      // l holding row l of each (row scale rs, e4m3 input scale sc).
       constexpr int kRowRegs = static_cast<int>(G::kMaxTok / 32);
       float rs[kRowRegs], sc[kRowRegs], bias4[4], wc4[4];
 #pragma unroll
@@ -970,7 +979,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
         }
 #pragma unroll
         for (int q = 0; q < kRowRegs; ++q) {
-          const uint32_t t = static_cast<uint32_t>(q * 32 + lane);
+          const uint32_t t = (static_cast<uint32_t>(q) * nsub + esub) * 32u + static_cast<uint32_t>(lane);
           const bool row_ok = t < ti.nrows;
           rs[q] = (p.epi_row_scale != nullptr && row_ok) ? __ldg(p.epi_row_scale + ti.row0 + t) : 1.0f;
           sc[q] = (scaled && row_ok) ? __ldg(p.in_scale + (ti.row0 + t) / static_cast<uint32_t>(p.scale_gm)) : 1.0f;
@@ -989,12 +998,12 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreads, 1)
       // tile transposed, one stmatrix; then four row reads and 16-byte stores.  A chunk
       // may read TMEM columns past ntok (inside the accumulator); those rows are not
       // stored.  The row factors of rows c0 .. c0 + 31 are in rs[0] / sc[0] and move
-      // down one register every 32 rows.
+      // down one register every chunk.
       const uint32_t stg = epi_ring + static_cast<uint32_t>(warp - 2) * (kEpiRows * kEpiRowBytes);
       // stmatrix: thread l addresses row 8g + (l % 8) of matrix i = l / 8 (block i).
       const uint32_t st_row = static_cast<uint32_t>(lane) & 7u, st_blk = static_cast<uint32_t>(lane) >> 3;
       const uint8_t *stg_ptr = dyn_smem + (stg - dyn_base);
-      for (uint32_t c0 = 0; c0 < ti.ntok; c0 += 32) {
+      for (uint32_t c0 = esub * 32u; c0 < ti.ntok; c0 += 32u * nsub) {
         uint32_t va[16], vb[16];
         tmem_ld_16x256b_x4(taddr + c0, va);
         tmem_ld_16x256b_x4(taddr + (16u << 16) + c0, vb);
