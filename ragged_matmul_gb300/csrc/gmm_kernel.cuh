@@ -30,7 +30,7 @@
 //                  both CTAs' barriers; each CTA stores its own 128 columns of C.
 //   kInt4 = false  bf16 weights, loaded by TMA into the stage together with tokens.
 //   kInt4 = true   packed 4-bit weights: a dedicated TMA warp
-//                  streams packed slabs through their own ring, and eight warps
+//                  streams packed slabs through their own ring, and twelve warps
 //                  dequantise them straight into tensor memory, where the MMA takes
 //                  its A operand from (tcgen05.mma with A in TMEM).  The dequantised
 //                  weights never touch shared memory, so shared memory carries only
@@ -53,11 +53,13 @@
 //                4-bit kernel a ring of dequantised weight slabs between them) and
 //                the MMA issue (the whole warp runs the loop, one elected lane
 //                issues tcgen05.mma kind::f16, or kind::f8f6f4 for e4m3).
-//   warps 2..5   epilogue: TMEM -> registers -> a shared-memory staging tile (the
-//                transpose from weight-row lanes to C rows) -> scales, optional
-//                bias / activation / row scale -> bf16 -> 16-byte stores to C,
-//                masking token rows past the group's end and columns past N; two
-//                accumulators let it overlap the next tile's main loop.
+//   warps 2..5   epilogue: TMEM (16x256b loads) -> scales, optional bias /
+//                activation / row scale -> bf16 -> stmatrix.trans into a
+//                shared-memory staging tile (the transpose from weight-row lanes
+//                to C rows) -> 16-byte stores to C, masking token rows past the
+//                group's end and columns past N; two accumulators let it overlap
+//                the next tile's main loop.  A 320-thread launch (bf16 / e4m3 with
+//                short K) adds warps 6..9, which take alternate 32-row chunks.
 //   warp 6       (4-bit) TMA producer of packed slabs.
 //   warps 7..18  (4-bit) dequantisation.
 //
