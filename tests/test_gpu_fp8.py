@@ -108,6 +108,18 @@ def test_fp8_with_epilogue(activation, variant):
     assert status == binding.GMM_OK
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+def test_fp8_with_epilogue_long_k(variant):
+    """The same with K = 2080 e4m3 values (1040 two-byte units): the 4-epilogue-warp launch."""
+    r, v = case(4, 392, 2080, [1, 17, 0, 130, 33, 257, 7], [2, 0, 1, 3, -1, 1, 0], 12, gran=(2, 64, None))
+    rng = np.random.default_rng(13)
+    epi = {"bias_bits": wl._to_bf16_bits(rng.normal(0.0, 0.1, (4, 392)).astype(np.float32)),
+           "row_scale": rng.uniform(0.1, 2.0, r.rows).astype(np.float32), "activation": "gelu_tanh"}
+    _, _, status, _ = check_fp8_against_oracle(handle(4, variant), r, v, (2, 64, None), epilogue=epi,
+                                               where=f"fp8 epilogue long K {variant}")
+    assert status == binding.GMM_OK
+
+
 def test_fp8_accepts_float8_tensors():
     """The binding takes torch.float8_e4m3fn tensors as well as their uint8 bit patterns."""
     import torch

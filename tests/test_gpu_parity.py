@@ -314,6 +314,20 @@ def test_epilogue_bf16(activation, variant):
     assert status == binding.GMM_OK
 
 
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("K", [520, 1096])
+def test_epilogue_bf16_long_k(K, variant):
+    """The fused epilogue with K above 512, where the kernel runs 4 epilogue warps (8 below)."""
+    loads = [1, 17, 0, 130, 33, 257, 7]
+    ids = [2, 0, 1, 3, -1, 1, 0]
+    r = routing(4, 392, K, loads, ids, dist=("normal", 0.5))
+    v = wl.host_values(r, 32)
+    epi = _epilogue_case(r, 33, "silu")
+    _, _, status, _ = check_against_oracle(handle(4, variant), r, v, epilogue=epi,
+                                           where=f"epilogue K={K} {variant}")
+    assert status == binding.GMM_OK
+
+
 @pytest.mark.parametrize("parts", [(True, False), (False, True)])
 def test_epilogue_bias_only_and_scale_only(parts):
     r = routing(3, 256, 128, [40, 0, 129], [1, 2, 0], dist=("normal", 1.0))
