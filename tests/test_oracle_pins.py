@@ -69,6 +69,39 @@ def _parse_golden_bf16():
     return d
 
 
+def test_bf16_bits_to_f32_matches_torch_on_every_pattern():
+    """All 65,536 bf16 bit patterns widen to the fp32 torch gives (NaNs compared as NaN)."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    got = oracle.bf16_bits_to_f32(bits)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))   # signed zeros too
+
+
+def test_validate_flags_and_active_count_hand_worked():
+    """grouped_matmul_sm100_persistent, Args (expert_ids, a_offsets): a negative id skips its
+    group and the stats count the active groups.  Where the page is silent the reading taken
+    is that an id of E or more is skipped, not counted and flagged, and that decreasing offsets
+    are flagged."""
+    E = 4
+    # ids 3, -1, 0, 2: three active; offsets non-decreasing (an empty group included)
+    assert oracle.validate([0, 5, 5, 9, 12], [3, -1, 0, 2], E) == (0, 3)
+    # all skipped: no flags, no active group
+    assert oracle.validate([0, 1, 2], [-1, -7], E) == (0, 0)
+    # id == E is out of range: flagged and not counted
+    flags, active = oracle.validate([0, 2, 4], [4, 1], E)
+    assert flags == oracle.BAD_EXPERT_ID and active == 1
+    # a decreasing offset is flagged whatever the ids
+    flags, active = oracle.validate([0, 6, 3], [0, -1], E)
+    assert flags == oracle.BAD_OFFSETS and active == 1
+    # both problems at once
+    flags, _ = oracle.validate([4, 2], [9], E)
+    assert flags == oracle.BAD_OFFSETS | oracle.BAD_EXPERT_ID
+    # no groups at all
+    assert oracle.validate([0], np.zeros(0, np.int32), E) == (0, 0)
+
+
 def test_hand_worked_bf16_example():
     d = _parse_golden_bf16()
     A = np.array([[float(v) for v in r] for r in d["A"]], np.float32)
