@@ -1,9 +1,18 @@
-"""Benchmark of the ragged grouped GEMM on GB300: useful TFLOP/s and fraction of roofline.
+"""Benchmark of the ragged grouped GEMM on GB300: useful TFLOP/s and fraction of roofline, per config.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode|prefill|fine_grained|int4|tiny]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload all|decode|prefill|...]
                     [--impl ours|reference]
 
-One step = one gmm_run (gmm_run_int4 for the int4 workload) over the whole
+With no --workload (or --workload all) one run measures the five configurations
+of the mixture-of-experts shapes in turn: tiny (E=4, 60 rows, N=K=256), decode
+(2048 rows over 64 experts, K=2048, N=2816), prefill (32768 rows over 8 experts,
+K=4096, N=14336), fine_grained (32768 rows over 128 experts with 13 skipped,
+K=7168, N=4096) and int4 (8192 rows over 64 experts of packed 4-bit weights,
+K=N=4096).  Each gets its own timed region, roofline, end-to-end number, CPU
+oracle baseline with a parity check of the timed output, and clock record, under
+"configs".  The top-level line repeats the entry of prefill, the largest of them.
+
+One step = one gmm_run (gmm_run_int4 for the 4-bit workload) over the whole
 workload: every group, every row, all N columns.  Inputs are seeded synthetic
 tensors already resident in HBM.  Between steps, outside the timed events, L2
 is flushed: a 512 MiB buffer is written, then a different 512 MiB buffer is
@@ -12,15 +21,14 @@ read, the timed kernel would also pay for writing the flush's dirty lines back
 to HBM).  Each step is timed with CUDA events on the launching stream; `value`
 is useful FLOPs / mean step time.
 
-The default workload is decode (256 tokens top-8 over 64 experts: 2048 rows,
-K=2048, N=2816).  Under torchrun each rank runs its own replica of the workload
-(the groups are independent problems and need no exchange), so scaling is weak
-and `value` = FLOPs of all ranks / the slowest rank's time.
+Under torchrun each rank runs its own replica of the workload (the groups are
+independent problems and need no exchange), so scaling is weak and `value` =
+FLOPs of all ranks / the slowest rank's time.
 
 --impl reference times the CPU oracle (oracle/, plain C, all host cores of this
-process) on a bounded sample of the same workload: the first whole groups in
-routing order, all N columns, grown until one pass takes a few seconds.  It is
-a baseline for context, not the target.
+process) on a bounded sample of each workload: the first rows of its active
+groups in routing order, all N columns, grown until one pass takes about a
+second.  It is a baseline for context, not the target.
 """
 from __future__ import annotations
 
@@ -244,19 +252,24 @@ def host_values_as_tensors(r: wl.Routing, seed: int = 0):
     return out
 
 
-def oracle_sample(r: wl.Routing, vals_dev, n_groups: int):
-    """The first n_groups active groups, all of their rows, all N columns, as host arrays."""
+def oracle_sample(r: wl.Routing, vals_dev, n_rows: int):
+    """The first n_rows rows of the active groups in routing order (the last group
+    touched may be cut short), all N columns, as host arrays."""
     import torch
-    act = np.flatnonzero(r.active_mask())[:n_groups]
     rows, loads, ids = [], [], []
-    for g in act:
+    for g in np.flatnonzero(r.active_mask()):
+        if len(rows) >= n_rows:
+            break
         lo, hi = int(r.a_offsets[g]), int(r.a_offsets[g + 1])
+        hi = min(hi, lo + n_rows - len(rows))
+        if hi <= lo:
+            continue
         rows += range(lo, hi)
         loads.append(hi - lo)
         ids.append(int(r.expert_ids[g]))
     akey = "a8" if is_fp8(r) else "a"
     idx = torch.tensor(rows, dtype=torch.int64, device=vals_dev[akey].device)
-    sample = {"off": wl.offsets_from_loads(loads), "groups": len(act), "rows": len(rows), "row_idx": list(rows)}
+    sample = {"off": wl.offsets_from_loads(loads), "groups": len(loads), "rows": len(rows), "row_idx": list(rows)}
     if is_fp8(r):
         sample["a8"] = vals_dev["a8"][idx].cpu().numpy()
         sample["input_scale"] = vals_dev["input_scale"][idx].cpu().numpy()   # one per row (m granularity 1)
@@ -316,64 +329,34 @@ def sample_parity(s, c_dev):
 
 
 def pick_oracle_sample(r, vals_dev, nthreads, target_s):
-    """Grow the number of whole groups (doubling) until one oracle pass takes about target_s."""
-    n_active = int(r.active_mask().sum())
-    n = 1
+    """Grow the sample's row count until one oracle pass takes about target_s (or the
+    whole workload is taken)."""
+    total_rows = int(r.loads[r.active_mask()].sum())
+    n = min(total_rows, 16)
     while True:
         s = oracle_sample(r, vals_dev, n)
         dt = run_oracle(r, s, nthreads)
-        if dt >= 0.5 * target_s or n >= n_active:
+        if dt >= 0.5 * target_s or n >= total_rows:
             return s, dt
-        n = min(n_active, n * 2 if dt <= 0 else max(n + 1, int(n * min(4.0, target_s / dt))))
+        grow = 4.0 if dt <= 0 else min(8.0, max(1.25, target_s / dt))
+        n = min(total_rows, max(n + 1, int(n * grow)))
 
 
 def sample_desc(r, s):
-    return (f"first {s['groups']} active groups in routing order ({s['rows']} rows), "
-            f"all N={r.N} columns, K={r.K}")
+    return (f"first {s['rows']} rows of the active groups in routing order ({s['groups']} group(s), "
+            f"the last possibly cut short), all N={r.N} columns, K={r.K}")
 
 
 # ------------------------------------------------------------------ main
 
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode", choices=[n for n in wl.WORKLOAD_NAMES])
-    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--oracle-seconds", type=float, default=10.0,
-                    help="CPU oracle work per step of the reference arm / per cpu_baseline pass")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--groups", type=int, default=0,
-                    help="profile-sized sub-workload: only the first G groups of the named routing")
-    ap.add_argument("--rows", type=int, default=0,
-                    help="redraw the named routing for this many rows (same groups and proportions)")
-    ap.add_argument("--group-range", default=None,
-                    help="sub-workload lo:hi - groups lo .. hi-1 of the named routing")
-    ap.add_argument("--epilogue", default="none", choices=["none", "relu", "silu", "gelu_tanh"],
-                    help="time the fused epilogue act(acc + bias[e, n]) * row_scale[r] with this activation "
-                         "(seeded bias and per-row scales); 'none' is the plain GEMM")
-    ap.add_argument("--yardstick", action="store_true",
-                    help="also time torch.matmul per active group (cuBLAS, bf16 workloads) on the same data, "
-                         "for context")
-    ap.add_argument("--variant", default=None, choices=["pair", "single"],
-                    help="kernel variant (default: the library's choice, CTA pairs)")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
+# The configurations of the default run, in order; the headline of the JSON line is the
+# largest of them.
+DEFAULT_CONFIGS = ("tiny", "decode", "prefill", "fine_grained", "int4")
+HEADLINE = "prefill"
 
-    world, rank, local = dist_env()
-    import torch
 
-    r = wl.routing(args.workload)
-    if args.groups:
-        r = wl.first_groups(r, args.groups)
-    if args.group_range:
-        lo, hi = (int(x) for x in args.group_range.split(":"))
-        r = wl.group_range(r, lo, hi)
-    if args.rows:
-        r = wl.with_rows(r, args.rows)
+def describe(r: wl.Routing, args):
+    """Work counts, roofline terms and the `config` object of one workload."""
     flops, nbytes, rows = work_counts(r)
     peaks, peaks_kind = load_peaks()
     # e4m3 MMAs run at twice the bf16 rate (the nominal dense ratio 4.5 : 2.25 PFLOP/s):
@@ -381,7 +364,6 @@ def main():
     tensor_peak = peaks["bf16_tflops"] * (2.0 if is_fp8(r) else 1.0)
     t_tensor = flops / (tensor_peak * 1e12)
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
-    bound = "tensor" if t_tensor >= t_hbm else "hbm"
     config = {"workload": r.name, "E": r.E, "N": r.N, "K": r.K, "groups": r.G,
               "active_groups": int(r.active_mask().sum()), "rows": rows,
               "useful_flops": flops, "algorithmic_bytes": nbytes,
@@ -394,54 +376,74 @@ def main():
                             f" (granularity ({gm}, {gn}, {gk}))")
     if args.epilogue != "none":
         config["epilogue"] = f"{args.epilogue}(acc + bias[e, n]) * row_scale[r], fused before the bf16 store"
+    return {"flops": flops, "nbytes": nbytes, "rows": rows, "peaks": peaks, "peaks_kind": peaks_kind,
+            "tensor_peak": tensor_peak, "t_tensor": t_tensor, "t_hbm": t_hbm,
+            "bound": "tensor" if t_tensor >= t_hbm else "hbm", "config": config}
 
-    if args.impl == "reference":
-        # The CPU oracle, timed on this host's cores; under torchrun only rank 0 works.
-        if rank != 0:
-            return
-        if torch.cuda.is_available():
-            vals = (wl.fp8_device_values(r, 0, fp8_gran(r), device=torch.device(f"cuda:{local}")) if is_fp8(r)
-                    else wl.device_values(r, 0, device=torch.device(f"cuda:{local}")))
-        else:
-            vals = host_values_as_tensors(r, 0)
-        nthreads = len(os.sched_getaffinity(0))
-        per_step = max(0.2, min(args.oracle_seconds, 150.0 / (args.steps + 1)))   # whole run: minutes
-        s, _ = pick_oracle_sample(r, vals, nthreads, per_step)
-        del vals
-        for _ in range(min(args.warmup, 1)):
-            run_oracle(r, s, nthreads)
-        times = [run_oracle(r, s, nthreads) for _ in range(args.steps)]
-        t = statistics.mean(times)
-        value = s["flops"] / t / 1e12
-        print(json.dumps({
-            "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None,
+
+def dtype_name(r):
+    return "int4 weights, bf16 MMA" if r.int4 else ("e4m3" if is_fp8(r) else "bf16")
+
+
+def kernel_name(r, variant):
+    if is_fp8(r) and fp8_gran(r)[2] < r.K:
+        return "gmm_fp8_block_kernel"
+    pair = variant == "pair" or (variant is None and not r.int4)
+    return "gmm_grouped_kernel<%s, %s, %s>" % ("true" if r.int4 else "false", "true" if pair else "false",
+                                               "true" if is_fp8(r) else "false")
+
+
+def select_routing(name, args):
+    r = wl.routing(name)
+    if args.groups:
+        r = wl.first_groups(r, args.groups)
+    if args.group_range:
+        lo, hi = (int(x) for x in args.group_range.split(":"))
+        r = wl.group_range(r, lo, hi)
+    if args.rows:
+        r = wl.with_rows(r, args.rows)
+    return r
+
+
+def reference_config(r, args, n_configs):
+    """The reference arm on one workload: the CPU oracle, timed as it stands."""
+    import torch
+    d = describe(r, args)
+    local = dist_env()[2]
+    if torch.cuda.is_available():
+        vals = (wl.fp8_device_values(r, 0, fp8_gran(r), device=torch.device(f"cuda:{local}")) if is_fp8(r)
+                else wl.device_values(r, 0, device=torch.device(f"cuda:{local}")))
+    else:
+        vals = host_values_as_tensors(r, 0)
+    nthreads = len(os.sched_getaffinity(0))
+    # The whole run (every config, warm-up and timed passes) takes a couple of minutes.
+    per_step = max(0.1, min(args.oracle_seconds, 100.0 / ((args.steps + 1) * n_configs)))
+    s, _ = pick_oracle_sample(r, vals, nthreads, per_step)
+    del vals
+    if torch.cuda.is_available():
+        torch.cuda.empty_cache()
+    for _ in range(min(args.warmup, 1)):
+        run_oracle(r, s, nthreads)
+    times = [run_oracle(r, s, nthreads) for _ in range(args.steps)]
+    t = statistics.mean(times)
+    value = s["flops"] / t / 1e12
+    return {"value": value, "unit": "TFLOP/s", "ms_per_step": t * 1e3, "config": d["config"],
             "dtype": ("e4m3 inputs, fp64 sums (numpy, CPU)" if is_fp8(r)
                       else "bf16 inputs, fp32 accumulation (C, CPU)"),
-            "data": "synthetic (seeded)", "config": config,
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": nthreads, "kind": "oracle",
                              "sample": sample_desc(r, s)},
-            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        }), flush=True)
-        return
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
-    torch.cuda.set_device(local)
-    dev = torch.device(f"cuda:{local}")
 
+def measure_config(r, args, world, rank, local, dev):
+    """Our arm on one workload: the timed region, the end-to-end run through host buffers,
+    the yardstick, the CPU oracle baseline and the parity of the timed output."""
+    import torch
     from ragged_matmul_gb300 import binding
-    from ragged_matmul_gb300 import build as gbuild
-    if rank == 0:
-        gbuild.build()
-    barrier(world)
-
+    d = describe(r, args)
+    flops, nbytes = d["flops"], d["nbytes"]
     vals = wl.fp8_device_values(r, rank, fp8_gran(r), device=dev) if is_fp8(r) else wl.device_values(r, rank, device=dev)
     akey = "a8" if is_fp8(r) else "a"
-    if args.variant:
-        os.environ["GMM_VARIANT"] = args.variant
     h = binding.gmm_create(r.E, local)
     c = torch.full((r.rows, r.N), wl.SENTINEL_BF16, dtype=torch.int16, device=dev).view(torch.bfloat16)
     off = torch.from_numpy(r.a_offsets.view(np.int32)).to(dev)
@@ -483,7 +485,7 @@ def main():
     torch.cuda.synchronize()
     status = binding.gmm_query_status(h)
     if status != binding.GMM_OK:
-        raise RuntimeError(f"device status after warm-up: {binding.gmm_error_string(status)}")
+        raise RuntimeError(f"{r.name}: device status after warm-up: {binding.gmm_error_string(status)}")
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -505,7 +507,7 @@ def main():
     mean_ms = statistics.mean(step_ms)
     status = binding.gmm_query_status(h)
     if status != binding.GMM_OK:
-        raise RuntimeError(f"device status after timing: {binding.gmm_error_string(status)}")
+        raise RuntimeError(f"{r.name}: device status after timing: {binding.gmm_error_string(status)}")
     max_ms = reduce_max(mean_ms, world, dev)
     value = aggregate_tflops(world, flops, max_ms)
 
@@ -546,6 +548,7 @@ def main():
         e2e_max = reduce_max(statistics.mean(e_ms), world, dev)
         e2e = {"value": aggregate_tflops(world, flops, e2e_max), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": e2e_max}
+        del a_h, c_h, a_d
 
     # A library yardstick for context (never a reference for results): cuBLAS through
     # torch.matmul, one GEMM per active group, on the same resident operands.
@@ -591,36 +594,116 @@ def main():
         if args.epilogue == "none":   # the timed run's output on the sample, after timing
             cpu_baseline["parity_after_timing"] = sample_parity(s, c)
 
-    if rank == 0:
-        t_s = mean_ms * 1e-3
-        if bound == "hbm":
-            achieved, peak, unit = nbytes / t_s / 1e9, peaks["hbm_gbs"], "GB/s"
-        else:
-            achieved, peak, unit = flops / t_s / 1e12, tensor_peak, "TFLOP/s"
-        roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                    "traffic": profiled_traffic(args.workload),
-                    "peak_source": f"{peaks_kind} (burst)" + (" bf16 x 2, the nominal e4m3 : bf16 ratio"
-                                                              if is_fp8(r) and bound == "tensor" else ""),
-                    "roofline_time_ms": max(t_tensor, t_hbm) * 1e3,
-                    "kernel": ("gmm_fp8_block_kernel<%s>" % ("true" if args.variant == "pair" else "false")
-                               if is_fp8(r) and fp8_gran(r)[2] < r.K else
-                               "gmm_grouped_kernel<%s, %s, %s>" % (
-                                   "true" if r.int4 else "false",
-                                   "true" if (args.variant == "pair" or (args.variant is None and not r.int4)) else "false",
-                                   "true" if is_fp8(r) else "false"))}
-        line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": max_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": "int4 weights, bf16 MMA" if r.int4 else ("e4m3" if is_fp8(r) else "bf16"),
-            "data": "synthetic (seeded, generated on device)", "config": config,
-            "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e, "gpu_launches": args.steps,
-            **({"yardstick": yardstick} if yardstick else {}),
-            "clocks": sampler.summary(w0, w1), "region_wall_ms": (w1 - w0) * 1e3,
-            "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
-        }
-        print(json.dumps(line), flush=True)
+    t_s = mean_ms * 1e-3
+    peaks = d["peaks"]
+    if d["bound"] == "hbm":
+        achieved, peak, unit = nbytes / t_s / 1e9, peaks["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = flops / t_s / 1e12, d["tensor_peak"], "TFLOP/s"
+    roofline = {"bound": d["bound"], "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                "traffic": profiled_traffic(r.name),
+                "peak_source": f"{d['peaks_kind']} (burst)" + (" bf16 x 2, the nominal e4m3 : bf16 ratio"
+                                                              if is_fp8(r) and d["bound"] == "tensor" else ""),
+                "roofline_time_ms": max(d["t_tensor"], d["t_hbm"]) * 1e3,
+                "frac_of_roofline_time": max(d["t_tensor"], d["t_hbm"]) / t_s,
+                "kernel": kernel_name(r, args.variant)}
+    out = {"value": value, "unit": "TFLOP/s", "ms_per_step": max_ms, "dtype": dtype_name(r),
+           "config": d["config"], "roofline": roofline, "cpu_baseline": cpu_baseline, "e2e": e2e,
+           "gpu_launches": args.steps, **({"yardstick": yardstick} if yardstick else {}),
+           "clocks": sampler.summary(w0, w1), "region_wall_ms": (w1 - w0) * 1e3,
+           "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms)}
     binding.gmm_destroy(h)
+    del vals, c, flush_w, flush_r
+    torch.cuda.empty_cache()
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="all", choices=["all", *wl.WORKLOAD_NAMES],
+                    help="'all' (default): the five configurations tiny, decode, prefill, fine_grained "
+                         "and int4, each timed in turn, prefill as the headline")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--oracle-seconds", type=float, default=3.0,
+                    help="CPU oracle work per step of the reference arm / per cpu_baseline pass")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--groups", type=int, default=0,
+                    help="profile-sized sub-workload: only the first G groups of the named routing")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="redraw the named routing for this many rows (same groups and proportions)")
+    ap.add_argument("--group-range", default=None,
+                    help="sub-workload lo:hi - groups lo .. hi-1 of the named routing")
+    ap.add_argument("--epilogue", default="none", choices=["none", "relu", "silu", "gelu_tanh"],
+                    help="time the fused epilogue act(acc + bias[e, n]) * row_scale[r] with this activation "
+                         "(seeded bias and per-row scales); 'none' is the plain GEMM")
+    ap.add_argument("--yardstick", action="store_true",
+                    help="also time torch.matmul per active group (cuBLAS, bf16 workloads) on the same data, "
+                         "for context")
+    ap.add_argument("--variant", default=None, choices=["pair", "single"],
+                    help="kernel variant (default: the library's choice, CTA pairs)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    names = list(DEFAULT_CONFIGS) if args.workload == "all" else [args.workload]
+    headline = HEADLINE if args.workload == "all" else args.workload
+
+    world, rank, local = dist_env()
+    import torch
+
+    common = {"metric": METRIC, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+              "higher_is_better": True, "scaling": "weak", "vs_baseline": None}
+
+    if args.impl == "reference":
+        # The CPU oracle, timed on this host's cores; under torchrun only rank 0 works.
+        if rank != 0:
+            return
+        per = {}
+        for name in names:
+            per[name] = reference_config(select_routing(name, args), args, len(names))
+        head = per[headline]
+        line = {"impl": "reference", **common, "n_gpus": 1, "value": head["value"], "unit": "TFLOP/s",
+                "ms_per_step": head["ms_per_step"], "dtype": head["dtype"], "data": "synthetic (seeded)",
+                "config": head["config"], "cpu_baseline": head["cpu_baseline"], "e2e": head["e2e"]}
+        if len(names) > 1:
+            line["headline"] = f"{headline}: the largest of the configurations in `configs`"
+            line["configs"] = per
+        print(json.dumps(line), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    torch.cuda.set_device(local)
+    dev = torch.device(f"cuda:{local}")
+
+    from ragged_matmul_gb300 import build as gbuild
+    if rank == 0:
+        gbuild.build()
+    barrier(world)
+    if args.variant:
+        os.environ["GMM_VARIANT"] = args.variant
+
+    per = {}
+    for name in names:
+        per[name] = measure_config(select_routing(name, args), args, world, rank, local, dev)
+    if rank == 0:
+        head = per[headline]
+        line = {**common, "value": head["value"], "unit": "TFLOP/s", "ms_per_step": head["ms_per_step"],
+                "dtype": head["dtype"], "data": "synthetic (seeded, generated on device)",
+                "config": head["config"], "roofline": head["roofline"], "cpu_baseline": head["cpu_baseline"],
+                "e2e": head["e2e"], "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+                **({"yardstick": head["yardstick"]} if "yardstick" in head else {}),
+                "region_wall_ms": head["region_wall_ms"], "step_ms_min": head["step_ms_min"],
+                "step_ms_median": head["step_ms_median"]}
+        if len(names) > 1:
+            line["headline"] = f"{headline}: the largest of the configurations in `configs`"
+            line["configs"] = per
+            line["gpu_launches_all_configs"] = sum(x["gpu_launches"] for x in per.values())
+        print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

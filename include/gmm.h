@@ -63,7 +63,12 @@ typedef struct gmm_ctx *gmm_handle_t;
 
 /*
  * Create a handle for `device` and `num_experts` experts (E, the leading
- * dimension of B; used for the id bounds check and the B tensor map).
+ * dimension of B; used for the id bounds check and the B tensor map).  This is
+ * the host-side set-up that the grouped GEMM page's launcher does before its
+ * persistent kernel (Modular "grouped_matmul_sm100_persistent", description: it
+ * builds the TMA descriptors and picks the pipeline depth from the shared memory
+ * available): here the ring depths of every kernel are sized from the device's
+ * opt-in shared memory once, and the tensor maps are built per call.
  * Allocates the handle's device workspace on `device` (cudaMalloc).  The
  * caller's current device is left unchanged.
  * Errors: GMM_ERR_INVALID_ARG (out == NULL, num_experts < 1),
@@ -219,7 +224,13 @@ int gmm_run_fp8(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offset
  *
  * The first call on a device does a one-time set-up (looks up the array's device
  * address, the tensor-map encoder, and the kernel's shared-memory setting); make that
- * first call before any stream capture.  No call allocates or frees device memory.
+ * first call before any stream capture.  A set-up that fails is not remembered: the
+ * next call tries it again.  No call allocates or frees device memory itself, but
+ * note that CUDA loads a library's device code lazily by default: the array is
+ * reserved on a device when the library's module is first loaded there, which is
+ * the first call into this library on that device (this one or any other).  A
+ * caller that later hands all free device memory to its own pool should make one
+ * call at start-up, before it does so.
  *
  * Every call shares the one array and finds the previous call's contents in it; the
  * call clears the status word itself (stream-ordered on `stream`), rewrites the
@@ -237,6 +248,10 @@ int gmm_run_noalloc(void *c, const void *a, const uint32_t *a_offsets, const voi
                     int num_groups, int N, int K, cudaStream_t stream);
 
 /*
+ * The error report of the quantised GEMM page (Modular "multistage_gemm_q", section
+ * "Raises": the function raises an error on invalid input) for the conditions that
+ * only the device sees: decreasing offsets and out-of-range expert ids, and a
+ * kernel that gave up on a pipeline wait.
  * Synchronise `stream`, then read and clear the device status that the kernels of
  * this handle accumulated since the last query.  Returns GMM_OK,
  * GMM_ERR_BAD_INPUT or GMM_ERR_DEVICE_TIMEOUT (timeout wins when both are set),

@@ -64,8 +64,7 @@ struct gmm_ctx {
   int num_sms = 0;
   gmm_variant var[2][2];          // [4-bit][pair]
   gmm_variant var_fp8[2];         // e4m3 kernels, [pair]
-  gmm_variant var_fp8_block[2];   // e4m3 with per-K-block scales, [cluster sharing the weight slab]
-  int use_share_block = 0;        // per-K-block e4m3: 1 = the weight-sharing cluster form
+  gmm_variant var_fp8_block;      // e4m3 with per-K-block scales (one CTA per tile)
   int use_pairs = 1;              // bf16 path: 1 = CTA-pair kernels (cta_group::2), 0 = one CTA per tile
   int use_pairs_int4 = 0;         // 4-bit path: the same (default one CTA per tile)
   uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
@@ -210,12 +209,10 @@ int configure(gmm_variant *v, int optin, int num_sms) {
   return GMM_OK;
 }
 
-// The per-K-block e4m3 kernel: as many stages as fit, one CTA per SM or (pairs)
-// twice the number of co-resident clusters of two.
-template <bool kPair>
+// The per-K-block e4m3 kernel: as many stages as fit, one CTA per SM.
 int configure_fp8_block(gmm_variant *v, int optin, int num_sms) {
-  using G = gmm::BwGeom<kPair>;
-  auto kernel = gmm::gmm_fp8_block_kernel<kPair>;
+  using G = gmm::BwGeom;
+  auto kernel = gmm::gmm_fp8_block_kernel;
   cudaFuncAttributes attr;
   if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(kernel)) != cudaSuccess) return GMM_ERR_CUDA;
   const long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024 - gmm::kBwBiasBytes;
@@ -227,53 +224,17 @@ int configure_fp8_block(gmm_variant *v, int optin, int num_sms) {
                            static_cast<int>(v->smem)) != cudaSuccess)
     return GMM_ERR_CUDA;
   v->grid = num_sms;
-  if (kPair) {
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute la[1];
-    la[0].id = cudaLaunchAttributeClusterDimension;
-    la[0].val.clusterDim.x = 2;
-    la[0].val.clusterDim.y = 1;
-    la[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
-    cfg.blockDim = dim3(gmm::kBwThreads);
-    cfg.dynamicSmemBytes = v->smem;
-    cfg.attrs = la;
-    cfg.numAttrs = 1;
-    int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess || clusters < 1) return GMM_ERR_CUDA;
-    v->grid = 2 * clusters < (num_sms & ~1) ? 2 * clusters : (num_sms & ~1);
-  }
   return GMM_OK;
 }
 
 int launch_fp8_block(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   DeviceGuard guard(h->device);
-  const int pairs = h->use_share_block;
-  const gmm_variant &v = h->var_fp8_block[pairs];
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cudaLaunchAttribute attr[1];
-  cfg.blockDim = dim3(gmm::kBwThreads);
-  cfg.gridDim = dim3(static_cast<unsigned>(v.grid));
-  cfg.dynamicSmemBytes = v.smem;
-  cfg.stream = stream;
+  const gmm_variant &v = h->var_fp8_block;
   p.num_stages = v.stages;
-  cudaError_t err;
-  if (pairs) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, gmm::gmm_fp8_block_kernel<true>, p);
-  } else {
-    err = cudaLaunchKernelEx(&cfg, gmm::gmm_fp8_block_kernel<false>, p);
-  }
+  gmm::gmm_fp8_block_kernel<<<v.grid, gmm::kBwThreads, v.smem, stream>>>(p);
+  const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) {
     debug_report("launch of the block-scaled kernel", static_cast<int>(err), cudaGetErrorString(err));
-    cudaGetLastError();
     return GMM_ERR_CUDA;
   }
   return GMM_OK;
@@ -380,22 +341,17 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
   const int single_ok = configure<false, false>(&h->var[0][0], optin, sms) == GMM_OK &&
                         configure<true, false>(&h->var[1][0], optin, sms) == GMM_OK &&
                         configure<false, false, true>(&h->var_fp8[0], optin, sms) == GMM_OK &&
-                        configure_fp8_block<false>(&h->var_fp8_block[0], optin, sms) == GMM_OK;
+                        configure_fp8_block(&h->var_fp8_block, optin, sms) == GMM_OK;
   // Tuning override GMM_VARIANT: "single" forces the one-CTA kernels, "pair" the pairs.
   const char *variant = getenv("GMM_VARIANT");
   const bool pairs_ok = sms >= 2 && configure<false, true>(&h->var[0][1], optin, sms) == GMM_OK &&
                         configure<true, true>(&h->var[1][1], optin, sms) == GMM_OK &&
-                        configure<false, true, true>(&h->var_fp8[1], optin, sms) == GMM_OK &&
-                        configure_fp8_block<true>(&h->var_fp8_block[1], optin, sms) == GMM_OK;
+                        configure<false, true, true>(&h->var_fp8[1], optin, sms) == GMM_OK;
   h->use_pairs = pairs_ok && !(variant && std::strcmp(variant, "single") == 0);
   // The 4-bit path runs one CTA per tile unless GMM_VARIANT=pair: its pair kernel's
   // cross-CTA signal that both halves of a weight stage are in TMEM costs more than
   // the halved token traffic saves.
   h->use_pairs_int4 = pairs_ok && variant && std::strcmp(variant, "pair") == 0;
-  // The per-K-block e4m3 kernel runs one CTA per tile unless GMM_VARIANT=pair: sharing
-  // the weight slab across a cluster of two measured no faster on prefill and slower on
-  // decode.
-  h->use_share_block = h->use_pairs_int4;
   if (!single_ok) {
     cudaGetLastError();
     delete h;
@@ -403,11 +359,10 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
   }
 
   if (getenv("GMM_DEBUG")) {
-    const gmm_variant *vs[8] = {&h->var[0][0], &h->var[0][1], &h->var[1][0], &h->var[1][1],
-                                &h->var_fp8[0], &h->var_fp8[1], &h->var_fp8_block[0], &h->var_fp8_block[1]};
-    const char *names[8] = {"bf16", "bf16 pair", "int4", "int4 pair", "e4m3", "e4m3 pair", "e4m3 block",
-                            "e4m3 block pair"};
-    for (int i = 0; i < 8; ++i)
+    const gmm_variant *vs[7] = {&h->var[0][0], &h->var[0][1], &h->var[1][0], &h->var[1][1],
+                                &h->var_fp8[0], &h->var_fp8[1], &h->var_fp8_block};
+    const char *names[7] = {"bf16", "bf16 pair", "int4", "int4 pair", "e4m3", "e4m3 pair", "e4m3 block"};
+    for (int i = 0; i < 7; ++i)
       fprintf(stderr, "gmm: %-16s stages %d smem %zu grid %d\n", names[i], vs[i]->stages, vs[i]->smem, vs[i]->grid);
   }
   h->ws_bytes = kStatusBytes + static_cast<size_t>(sms) * gmm::kMapSlotBytes;
@@ -529,8 +484,7 @@ int gmm_run_fp8(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offset
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(KU), static_cast<cuuint64_t>(N),
                           static_cast<cuuint64_t>(h->num_experts)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N) * K};
-    const cuuint32_t rows = !blockwise ? static_cast<cuuint32_t>(gmm::kBlockN)
-                                       : (h->use_share_block ? gmm::BwGeom<true>::kCtaRows : gmm::BwGeom<false>::kCtaRows);
+    const cuuint32_t rows = !blockwise ? static_cast<cuuint32_t>(gmm::kBlockN) : gmm::BwGeom::kRows;
     cuuint32_t box[3] = {gmm::kBK, rows, 1};
     rc = encode_map(h, &p.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, b, dims, strides, box,
                     CU_TENSOR_MAP_SWIZZLE_128B);
@@ -539,8 +493,7 @@ int gmm_run_fp8(gmm_handle_t h, void *c, const void *a, const uint32_t *a_offset
   rc = encode_token_maps(h, p, a, KU, 1);
   if (rc) return rc;
   fill_common(h, p, c, a_offsets, expert_ids, expert_usage_stats, num_groups, N, KU,
-              !blockwise ? max_tok(h, false)
-                         : (h->use_share_block ? gmm::BwGeom<true>::kMaxTok : gmm::BwGeom<false>::kMaxTok));
+              !blockwise ? max_tok(h, false) : gmm::BwGeom::kMaxTok);
   set_epilogue(p, epilogue);
   p.in_scale = input_scale;
   p.w_scale = weight_scale;
@@ -680,22 +633,25 @@ constexpr int kNoAllocMaxDevices = 64;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];   // 524,544 bytes
 
 struct NoAllocDevice {
-  bool ready = false;
-  int rc = GMM_OK;    // outcome of the one-time set-up
-  gmm_ctx ctx;        // static storage; ctx.ws points into g_noalloc_scratch on this device
+  bool ready = false;   // set-up succeeded; a failed set-up is retried by the next call
+  gmm_ctx ctx;          // static storage; ctx.ws points into g_noalloc_scratch on this device
 };
 
 NoAllocDevice g_noalloc_devices[kNoAllocMaxDevices];
 std::mutex g_noalloc_mutex;
 
 // One-time set-up for the current device: resolve the scratch array's device
-// address, the tensor-map encoder and the kernel's shared-memory configuration.
+// address (which loads the library's module on this device, and with it the array,
+// if that has not happened yet), the tensor-map encoder and the kernel's
+// shared-memory configuration.  Only a successful set-up is kept: one that failed
+// (for instance because it was attempted during a stream capture, where some of
+// these calls are refused) is attempted again by the next call.
 int noalloc_setup(int device, gmm_ctx **out) {
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   NoAllocDevice &d = g_noalloc_devices[device];
   if (d.ready) {
     *out = &d.ctx;
-    return d.rc;
+    return GMM_OK;
   }
   int major = 0, minor = 0, sms = 0, optin = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
@@ -723,11 +679,13 @@ int noalloc_setup(int device, gmm_ctx **out) {
     d.ctx.ws = static_cast<uint8_t *>(scratch);
     d.ctx.ws_bytes = kNoAllocScratchBytes;
   }
-  if (rc != GMM_OK) cudaGetLastError();
-  d.rc = rc;
+  if (rc != GMM_OK) {
+    cudaGetLastError();
+    return rc;
+  }
   d.ready = true;
   *out = &d.ctx;
-  return rc;
+  return GMM_OK;
 }
 
 }  // namespace

@@ -19,27 +19,19 @@
 // one value per thread, and with gn a multiple of 32 the weight scale is one value per
 // 32-column TMEM load.  A promotion is one multiply-add per element.
 //
-// Variants: kShare = false (default) runs one CTA per tile of 128 token rows.
-// kShare = true runs a cluster of two CTAs per tile of 256 token rows: each CTA
-// computes its own 128 rows (its own MMAs, partial buffers and promotion), but a
-// stage's weight slab is loaded once for both, each CTA copying half of it with TMA
-// multicast into both CTAs' shared memory (32 KB per CTA and stage from L2 instead of
-// 48 KB).  It measured no faster, because neither form is bound by its
-// copies: a K block of 128 is one stage, and the MMA warp's own path through a stage
-// (the partial-buffer wait, the stage wait, four MMA issues, two commits; about 1,100
-// cycles under load) is longer than the stage's tensor work (335 to 670 cycles).
-// Tried and measured no better: 192- and 128-row tiles with 12 promotion warps or four
-// partial buffers, and a CTA-pair form (cta_group::2), whose every block crosses CTAs
-// twice.
+// One CTA per tile of 128 token rows.  A K block of 128 is one stage, and the MMA
+// warp's own path through a stage (the partial-buffer wait, the stage wait, four
+// MMA issues, two commits; about 1,100 cycles under load) is longer than the
+// stage's tensor work (335 to 670 cycles), so the copies are not what bounds it.
+// Tried and measured no better: 192- and 128-row tiles with 12 promotion warps or
+// four partial buffers, and a CTA-pair form (cta_group::2), whose every block
+// crosses CTAs twice.
 //
 // Roles (320 threads per CTA):
 //   warp 0       TMA producer: per stage (128 of K) a 128-row token slab (16 KB) and
-//                this CTA's weight rows (half of them, multicast to both CTAs, or all),
-//                128-byte swizzled.
+//                the tile's 256 weight rows (32 KB), 128-byte swizzled.
 //   warp 1       TMEM allocation (512 columns: two 256-column partial buffers) and the
-//                MMA issue (kind::f8f6f4, M = 128, N = 256, 4 MMAs per stage).  With
-//                kShare a stage slot is free once both CTAs' MMAs have read it: the
-//                commit that frees it arrives on both CTAs' barriers.
+//                MMA issue (kind::f8f6f4, M = 128, N = 256, 4 MMAs per stage).
 //   warps 2..9   promotion and epilogue: warp w reads TMEM lane quadrant w % 4 and
 //                weight columns 128 * ((w - 2) / 4) .. + 128 of each partial; every
 //                thread owns one token row and 128 running sums.  After a tile's last
@@ -67,22 +59,18 @@ constexpr uint32_t kBwCols = kBwRows * 4 / kBwPromoWarps;   // weight columns pe
 constexpr uint32_t kBwPiece = 16;                  // columns per TMEM wait
 constexpr int kBwBiasBytes = kBwPromoWarps * kBwCols * 2;   // each promotion warp's bias columns (bf16)
 
-template <bool kShare>
 struct BwGeom {
   static constexpr uint32_t kRows = kBwRows;
-  static constexpr uint32_t kMaxTok = kShare ? 2 * kBwCtaTok : kBwCtaTok;   // token rows per tile
+  static constexpr uint32_t kMaxTok = kBwCtaTok;                 // token rows per tile
   static constexpr uint32_t kTokAlign = 16;
-  static constexpr uint32_t kCtaRows = kShare ? kBwRows / 2 : kBwRows;      // weight rows a CTA copies
-  static constexpr uint32_t kWBytes = kBwRows * 128;                        // a stage's weight slab
-  static constexpr uint32_t kStageBytes = kBwTBytes + kWBytes;              // shared memory per stage
-  static_assert((kCtaRows * 128) % 1024 == 0, "weight halves keep the 1024-byte swizzle alignment");
+  static constexpr uint32_t kWBytes = kBwRows * 128;             // a stage's weight slab
+  static constexpr uint32_t kStageBytes = kBwTBytes + kWBytes;   // shared memory per stage
 };
 
 // Each promotion thread keeps kBwCols running sums and a 32-column piece of a partial
 // in registers.
-template <bool kShare>
 __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __grid_constant__ GmmParams p) {
-  using G = BwGeom<kShare>;
+  using G = BwGeom;
   __shared__ Ctrl ctl;
   __shared__ uint32_t prefix[kMaxGroups + 1];
   __shared__ uint64_t part_full[kBwBufs];    // a block's partial is in the buffer (MMA commit)
@@ -94,9 +82,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   const int KS = (p.K + kBK - 1) / kBK;   // stages per tile: 64 two-byte units = 128 e4m3 of K each
   const int SPB = p.kb_stages;            // stages per scale block (gk / 128)
   const int NKB = (KS + SPB - 1) / SPB;   // scale blocks per tile
-  const uint32_t rank = kShare ? cluster_ctarank() : 0u;
 
-  // 1024-byte aligned rings, at identical offsets in both CTAs of a cluster.
+  // 1024-byte aligned rings.
   const uint32_t dyn_base = smem_addr(dyn_smem);
   const uint32_t ring = (dyn_base + 1023u) & ~1023u;
   const uint32_t t_ring = ring;
@@ -106,7 +93,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   if (tid == 0) {
     for (uint32_t s = 0; s < ST; ++s) {
       mbar_init(smem_addr(&ctl.full[s]), 1);
-      mbar_init(smem_addr(&ctl.empty[s]), kShare ? 2 : 1);   // both CTAs' MMAs read the slot
+      mbar_init(smem_addr(&ctl.empty[s]), 1);
     }
     for (uint32_t a = 0; a < kBwBufs; ++a) {
       mbar_init(smem_addr(&part_full[a]), 1);
@@ -126,7 +113,6 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   }
   __syncthreads();
   build_schedule<G>(p, ctl, prefix, kBwThreads);
-  if constexpr (kShare) cluster_sync();   // the peer's barriers are initialised before anyone signals them
   if (blockIdx.x == 0 && tid == 0) {
     p.stats[1] = ctl.active;
     const uint32_t f = ctl.flags & (kStatusBadOffsets | kStatusBadExpert | kStatusTooLarge);
@@ -136,8 +122,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   const uint32_t tmem_base = ctl.tmem_base;
   const uint32_t total = ctl.total_tiles;
   volatile int *abort = &ctl.abort;
-  const uint32_t unit0 = kShare ? cluster_id_x() : blockIdx.x;   // static share: tiles unit0, unit0 + units, ...
-  const uint32_t units = kShare ? cluster_count_x() : gridDim.x;
+  const uint32_t unit0 = blockIdx.x;   // static share: tiles unit0, unit0 + units, ...
+  const uint32_t units = gridDim.x;
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -165,19 +151,15 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
         const Tile ti = decode_tile<G>(t, prefix, p);
         const uint64_t w_pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
         const uint64_t t_pol = p.cache_hints ? pol_last : pol_normal;
-        const int32_t t_row = static_cast<int32_t>(ti.row0 + rank * kBwCtaTok);
-        const int32_t w_row = static_cast<int32_t>(ti.n0 + rank * G::kCtaRows);
+        const int32_t t_row = static_cast<int32_t>(ti.row0);
+        const int32_t w_row = static_cast<int32_t>(ti.n0);
         for (int s = 0; s < KS; ++s) {
           const uint32_t full = smem_addr(&ctl.full[rt.slot]);
           if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
-          // This CTA's token slab and the whole weight slab (its own half plus, shared,
-          // the peer's multicast half) land in this CTA's slot.
           mbar_arrive_expect_tx(full, G::kStageBytes);
           const int32_t k0 = s * kBK;
           tma_load_2d_hint(t_ring + rt.slot * kBwTBytes, tok, full, k0, t_row, t_pol);
-          const uint32_t w_dst = w_ring + rt.slot * G::kWBytes + rank * (G::kCtaRows * 128);
-          if constexpr (kShare) tma_load_3d_mc(w_dst, &p.w_map, full, k0, w_row, ti.e, 0x3, w_pol);
-          else tma_load_3d_hint(w_dst, &p.w_map, full, k0, w_row, ti.e, w_pol);
+          tma_load_3d_hint(w_ring + rt.slot * G::kWBytes, &p.w_map, full, k0, w_row, ti.e, w_pol);
           pending |= 1u << rt.slot;
           pend_phase = (pend_phase & ~(1u << rt.slot)) | (rt.phase << rt.slot);
           rt.next(ST);
@@ -216,8 +198,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
 #pragma unroll
           for (int k = 0; k < 4; ++k)   // K = 32 e4m3 (32 bytes) per MMA
             mma_f8(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (in_block | k) != 0);
-          if constexpr (kShare) mma_commit_mc(smem_addr(&ctl.empty[rt.slot]), 0x3);   // frees the slot in both CTAs
-          else mma_commit(smem_addr(&ctl.empty[rt.slot]));
+          mma_commit(smem_addr(&ctl.empty[rt.slot]));
           rt.next(ST);
           if (in_block == SPB - 1 || s == KS - 1) {   // the block's partial is complete
             mma_commit(smem_addr(&part_full[pb]));
@@ -234,8 +215,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
     // ------------------------------------------------------------ promotion and epilogue
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
     const uint32_t part = static_cast<uint32_t>(warp - 2) >> 2;   // which kBwCols of the tile's columns
-    // This thread's token row in the tile (a cluster's second CTA holds rows 128 .. 255).
-    const uint32_t trow = rank * kBwCtaTok + quad * 32 + static_cast<uint32_t>(lane);
+    // This thread's token row in the tile.
+    const uint32_t trow = quad * 32 + static_cast<uint32_t>(lane);
     __nv_bfloat16 *bias_s = reinterpret_cast<__nv_bfloat16 *>(dyn_smem + (bias_stage - dyn_base)) + (warp - 2) * kBwCols;
     const int wcols = p.w_scale_cols;
     uint32_t pb = 0, pb_phase = 0;
@@ -343,7 +324,6 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   }
 
   __syncthreads();
-  if constexpr (kShare) cluster_sync();   // no CTA leaves while its peer may still write or signal it
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);

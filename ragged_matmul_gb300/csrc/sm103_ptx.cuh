@@ -489,29 +489,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
-// A TMA load multicast to the CTAs of `cta_mask`: the box lands at `dst` in each of
-// them, and each one's mbarrier at `bar` (the same offset) counts the bytes it got.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap *map, uint32_t bar, int32_t x,
-                                               int32_t y, int32_t z, uint16_t cta_mask, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "h"(cta_mask), "l"(pol)
-      : "memory");
-}
-
-// Arrive once on the mbarrier at `bar` in every CTA of `cta_mask` when this CTA's
-// cta_group::1 MMAs issued so far have completed.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "{\n\t.reg .pred e;\n\t.reg .b32 l;\n\t"
-      "elect.sync l|e, 0xffffffff;\n\t"
-      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n\t}" ::"r"(bar),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // TMEM allocation for a CTA pair: one warp of EACH CTA of the pair executes it.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),

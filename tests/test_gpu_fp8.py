@@ -220,25 +220,22 @@ def test_fp8_full_size_sampled(name):
 
 # ---------------------------------------------------------------- per-K-block scales (gk < K)
 
-@pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("N,K,gran", [(384, 512, (1, 128, 128)), (264, 1104, (1, 32, 128)),
                                       (512, 768, (3, 64, 256)), (1024, 1024, (2, 256, 384)),
                                       (136, 256, (1, 32, 128)), (256, 4096, (1, 128, 128))])
-def test_fp8_block_scales_ragged(N, K, gran, variant):
+def test_fp8_block_scales_ragged(N, K, gran):
     """Ragged groups (1 .. 513 rows, a skipped one), N and K tails (K = 1104: a partial last
     block), granularities that divide nothing, against the oracle's per-block sums."""
     loads = [1, 15, 16, 17, 127, 128, 129, 255, 257, 513, 0, 40]
     ids = [3, 0, 5, 1, 7, 2, 6, 4, -1, 0, 1, 2]
     r, v = case(8, N, K, loads, ids, 20, gran=gran)
-    _, _, status, _ = check_fp8_against_oracle(handle(8, variant), r, v, gran,
-                                               where=f"fp8 block N={N} K={K} {gran} {variant}")
+    _, _, status, _ = check_fp8_against_oracle(handle(8), r, v, gran, where=f"fp8 block N={N} K={K} {gran}")
     assert status == binding.GMM_OK
 
 
-@pytest.mark.parametrize("variant", VARIANTS)
-def test_fp8_block_scales_bit_exact(variant):
+def test_fp8_block_scales_bit_exact():
     """e4m3 integers in [-3, 3] and power-of-two block scales: every partial, scaled
-    partial, sum and rounding is exact (CTA-pair and one-CTA kernels)."""
+    partial, sum and rounding is exact."""
     r = wl.make_routing("t", 3, 256, 512, [1, 40, 0, 200, 17], [2, 0, 1, 1, -1])
     rng = np.random.default_rng(21)
     to8 = wl._to_e4m3_bits
@@ -246,7 +243,7 @@ def test_fp8_block_scales_bit_exact(variant):
          "w8": to8(rng.integers(-3, 4, (3, 256, 512)).astype(np.float32)),
          "input_scale": rng.choice([0.25, 0.5, 1.0], (r.rows, 4)).astype(np.float32),
          "weight_scale": rng.choice([0.125, 0.25, 0.5], (3, 2, 4)).astype(np.float32)}
-    check_fp8_against_oracle(handle(3, variant), r, v, (1, 128, 128), exact=True, where=f"fp8 block exact {variant}")
+    check_fp8_against_oracle(handle(3), r, v, (1, 128, 128), exact=True, where="fp8 block exact")
 
 
 @pytest.mark.parametrize("activation", ["none", "gelu_tanh"])
