@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
@@ -51,11 +52,19 @@ void debug_report(const char *what, int code, const char *msg) {
 
 }  // namespace
 
-// One launch configuration per kernel variant.
+// One launch configuration per kernel variant.  The grouped kernel keeps its group
+// prefix (G + 1 words) in dynamic shared memory after the rings, so its ring depth is
+// set per launch: as many stages as the rest of the budget holds for that G.
 struct gmm_variant {
-  int stages = 0;     // depth of the W+T stage ring
-  size_t smem = 0;    // dynamic shared memory
-  int grid = 0;       // CTAs: the SM count, or (pairs) twice the co-resident clusters of two
+  int stages = 0;           // depth of the W+T stage ring (the grouped kernel: at the largest G)
+  size_t smem = 0;          // dynamic shared memory of every launch
+  size_t budget = 0;        // of which the kernel may use (the rest only keeps one CTA per SM)
+  size_t fixed = 0;         // grouped kernel: everything but the stage ring and the prefix
+  size_t stage_bytes = 0;   // grouped kernel: one stage of the ring
+  int stage_mult = 1;       // grouped kernel: the ring depth is a multiple of this (4-bit: kAStages)
+  int min_stages = 2;       // grouped kernel: the shallowest ring it runs with
+  int q_stages = 0;         // 4-bit kernel: packed-ring slots
+  int grid = 0;             // CTAs: the SM count, or (pairs) twice the co-resident clusters of two
 };
 
 struct gmm_ctx {
@@ -65,6 +74,7 @@ struct gmm_ctx {
   gmm_variant var[2][2];          // [4-bit][pair]
   gmm_variant var_fp8[2];         // e4m3 kernels, [pair]
   gmm_variant var_fp8_block;      // e4m3 with per-K-block scales (one CTA per tile)
+  int smem_per_sm = 0;            // shared memory of one SM (a launch reserves more than half: one CTA per SM)
   int use_pairs = 1;              // bf16 path: 1 = CTA-pair kernels (cta_group::2), 0 = one CTA per tile
   int use_pairs_int4 = 0;         // 4-bit path: the same (default one CTA per tile)
   uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
@@ -165,25 +175,54 @@ void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, c
   if (const char *env = getenv("GMM_CACHE_HINTS")) p.cache_hints = atoi(env) != 0;   // tuning override
 }
 
-// Ring depths from the device's shared-memory budget (the pages' launcher likewise
-// derives its pipeline depth from the shared memory available), and the grid: one
-// CTA per SM, or for pairs twice the number of clusters of two that fit at once.
+// Stage-ring depth of a grouped-kernel launch with G groups: what the budget holds after
+// the fixed parts and the prefix, capped at kMaxStages, a multiple of stage_mult.
+int stages_for(const gmm_variant &v, int G) {
+  const size_t prefix = (static_cast<size_t>(G + 1) * 4 + 15) & ~static_cast<size_t>(15);
+  if (v.budget < v.fixed + prefix) return 0;
+  long st = static_cast<long>((v.budget - v.fixed - prefix) / v.stage_bytes);
+  if (st > gmm::kMaxStages) st = gmm::kMaxStages;
+  st -= st % v.stage_mult;
+  return static_cast<int>(st);
+}
+
+// Ring depths from the shared-memory budget (the pages' launchers likewise derive their
+// pipeline depth from the shared memory available, and the quantised GEMM's launcher
+// reduces stages or warp partitions when the budget is exceeded): as many stages as fit,
+// and for the 4-bit kernel, if even its minimum ring does not fit with the full packed
+// ring, a packed ring of half the slots.  The grid: one CTA per SM, or for pairs twice
+// the number of clusters of two that fit at once.  `optin` is the budget (the device's
+// opt-in shared memory per block, or less when capped for testing), `sm_smem` the SM's
+// shared memory: a launch always reserves more than half of it, so one CTA runs per SM.
 template <bool kInt4, bool kPair, bool kFp8 = false>
-int configure(gmm_variant *v, int optin, int num_sms) {
+int configure(gmm_variant *v, int optin, int sm_smem, int device_optin, int num_sms) {
   using G = gmm::Geom<kInt4, kPair>;
   auto kernel = gmm::gmm_grouped_kernel<kInt4, kPair, kFp8>;
   cudaFuncAttributes attr;
   if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(kernel)) != cudaSuccess) return GMM_ERR_CUDA;
-  long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024;
-  if (kInt4) budget -= gmm::kQRingBytes;   // the packed-slab ring (the weights themselves are in TMEM)
-  budget -= gmm::kEpiStageBytes;          // the epilogue warps' staging tiles
-  v->stages = static_cast<int>(budget / static_cast<long>(G::kStageBytes));
-  if (v->stages > gmm::kMaxStages) v->stages = gmm::kMaxStages;
-  // The 4-bit stage ring also holds the TMEM weight slabs: exactly kAStages deep.
-  if (kInt4) v->stages = v->stages >= static_cast<int>(gmm::kAStages) ? static_cast<int>(gmm::kAStages) : 0;
-  if (v->stages < 2) return GMM_ERR_UNSUPPORTED;
-  v->smem = static_cast<size_t>(v->stages) * G::kStageBytes +
-            (kInt4 ? gmm::kQRingBytes : 0) + gmm::kEpiStageBytes + 1024;
+  const long avail = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes);
+  if (avail <= 0) return GMM_ERR_UNSUPPORTED;
+  v->budget = static_cast<size_t>(avail);
+  v->stage_bytes = G::kStageBytes;
+  v->stage_mult = kInt4 ? static_cast<int>(gmm::kAStages) : 1;
+  // The deepest configuration that fits with the largest prefix (kMaxGroups), else the
+  // deepest that fits with a one-group prefix (a launch with more groups than its budget
+  // holds then returns GMM_ERR_UNSUPPORTED).
+  v->min_stages = kInt4 ? static_cast<int>(gmm::kAStages) : 2;
+  v->stages = 0;
+  for (int groups : {gmm::kMaxGroups, 1}) {
+    for (int qs = gmm::kQStages; qs >= 2; qs /= 2) {   // 4-bit: full packed ring, then half of it
+      v->q_stages = kInt4 ? qs : 0;
+      v->fixed = 1024 + gmm::kEpiBytes<kInt4> + static_cast<size_t>(v->q_stages) * gmm::kQSlotBytes;
+      v->stages = stages_for(*v, groups);
+      if (v->stages >= v->min_stages || !kInt4) break;
+    }
+    if (v->stages >= v->min_stages) break;
+  }
+  if (v->stages < v->min_stages) return GMM_ERR_UNSUPPORTED;
+  const long reserve = static_cast<long>(sm_smem) / 2 + 1024;   // more than half an SM: one CTA per SM
+  const long cap = static_cast<long>(device_optin) - static_cast<long>(attr.sharedSizeBytes);
+  v->smem = static_cast<size_t>(std::min(cap, std::max(avail, reserve)));
   if (cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(v->smem)) != cudaSuccess)
     return GMM_ERR_CUDA;
@@ -210,7 +249,7 @@ int configure(gmm_variant *v, int optin, int num_sms) {
 }
 
 // The per-K-block e4m3 kernel: as many stages as fit, one CTA per SM.
-int configure_fp8_block(gmm_variant *v, int optin, int num_sms) {
+int configure_fp8_block(gmm_variant *v, int optin, int sm_smem, int device_optin, int num_sms) {
   using G = gmm::BwGeom;
   auto kernel = gmm::gmm_fp8_block_kernel;
   cudaFuncAttributes attr;
@@ -219,7 +258,9 @@ int configure_fp8_block(gmm_variant *v, int optin, int num_sms) {
   v->stages = static_cast<int>(budget / static_cast<long>(G::kStageBytes));
   if (v->stages > gmm::kMaxStages) v->stages = gmm::kMaxStages;
   if (v->stages < 2) return GMM_ERR_UNSUPPORTED;
-  v->smem = static_cast<size_t>(v->stages) * G::kStageBytes + gmm::kBwBiasBytes + 1024;
+  const long used = static_cast<long>(v->stages) * G::kStageBytes + gmm::kBwBiasBytes + 1024;
+  const long cap = static_cast<long>(device_optin) - static_cast<long>(attr.sharedSizeBytes);
+  v->smem = static_cast<size_t>(std::min(cap, std::max(used, static_cast<long>(sm_smem) / 2 + 1024)));
   if (cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(v->smem)) != cudaSuccess)
     return GMM_ERR_CUDA;
@@ -253,7 +294,9 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   cfg.gridDim = dim3(static_cast<unsigned>(v.grid));
   cfg.dynamicSmemBytes = v.smem;
   cfg.stream = stream;
-  p.num_stages = v.stages;
+  p.num_stages = stages_for(v, p.num_groups);
+  p.q_stages = v.q_stages;
+  if (p.num_stages < v.min_stages) return GMM_ERR_UNSUPPORTED;   // the prefix of this many groups does not fit
   cudaError_t err;
   if (pairs) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -305,12 +348,20 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
     cudaGetLastError();
     return GMM_ERR_NO_DEVICE;
   }
-  int major = 0, minor = 0, sms = 0, optin = 0;
+  int major = 0, minor = 0, sms = 0, optin = 0, sm_smem = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
   if (major != 10 || minor != 3 || sms < 1) return GMM_ERR_NO_DEVICE;
+  const int device_optin = optin;
+  // Test override GMM_SMEM_BUDGET (bytes): size the rings as if a block could opt in to
+  // no more shared memory than this, which exercises the reduced configurations.
+  if (const char *env = getenv("GMM_SMEM_BUDGET")) {
+    const int cap = atoi(env);
+    if (cap > 0 && cap < optin) optin = cap;
+  }
 
   gmm_ctx *h = new (std::nothrow) gmm_ctx;
   if (!h) return GMM_ERR_CUDA;
@@ -338,15 +389,16 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
   }
   h->memset32 = reinterpret_cast<PFN_cuMemsetD32Async_v3020>(fn);
 
-  const int single_ok = configure<false, false>(&h->var[0][0], optin, sms) == GMM_OK &&
-                        configure<true, false>(&h->var[1][0], optin, sms) == GMM_OK &&
-                        configure<false, false, true>(&h->var_fp8[0], optin, sms) == GMM_OK &&
-                        configure_fp8_block(&h->var_fp8_block, optin, sms) == GMM_OK;
+  h->smem_per_sm = sm_smem;
+  const int single_ok = configure<false, false>(&h->var[0][0], optin, sm_smem, device_optin, sms) == GMM_OK &&
+                        configure<true, false>(&h->var[1][0], optin, sm_smem, device_optin, sms) == GMM_OK &&
+                        configure<false, false, true>(&h->var_fp8[0], optin, sm_smem, device_optin, sms) == GMM_OK &&
+                        configure_fp8_block(&h->var_fp8_block, optin, sm_smem, device_optin, sms) == GMM_OK;
   // Tuning override GMM_VARIANT: "single" forces the one-CTA kernels, "pair" the pairs.
   const char *variant = getenv("GMM_VARIANT");
-  const bool pairs_ok = sms >= 2 && configure<false, true>(&h->var[0][1], optin, sms) == GMM_OK &&
-                        configure<true, true>(&h->var[1][1], optin, sms) == GMM_OK &&
-                        configure<false, true, true>(&h->var_fp8[1], optin, sms) == GMM_OK;
+  const bool pairs_ok = sms >= 2 && configure<false, true>(&h->var[0][1], optin, sm_smem, device_optin, sms) == GMM_OK &&
+                        configure<true, true>(&h->var[1][1], optin, sm_smem, device_optin, sms) == GMM_OK &&
+                        configure<false, true, true>(&h->var_fp8[1], optin, sm_smem, device_optin, sms) == GMM_OK;
   h->use_pairs = pairs_ok && !(variant && std::strcmp(variant, "single") == 0);
   // The 4-bit path runs one CTA per tile unless GMM_VARIANT=pair: its pair kernel's
   // cross-CTA signal that both halves of a weight stage are in TMEM costs more than
@@ -363,7 +415,8 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
                                 &h->var_fp8[0], &h->var_fp8[1], &h->var_fp8_block};
     const char *names[7] = {"bf16", "bf16 pair", "int4", "int4 pair", "e4m3", "e4m3 pair", "e4m3 block"};
     for (int i = 0; i < 7; ++i)
-      fprintf(stderr, "gmm: %-16s stages %d smem %zu grid %d\n", names[i], vs[i]->stages, vs[i]->smem, vs[i]->grid);
+      fprintf(stderr, "gmm: %-16s stages %d packed slots %d smem %zu grid %d\n", names[i], vs[i]->stages,
+              vs[i]->q_stages, vs[i]->smem, vs[i]->grid);
   }
   h->ws_bytes = kStatusBytes + static_cast<size_t>(sms) * gmm::kMapSlotBytes;
   if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess ||
@@ -675,7 +728,9 @@ int noalloc_setup(int device, gmm_ctx **out) {
     d.ctx.num_sms = sms;
     d.ctx.encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     d.ctx.use_pairs = 0;   // one CTA per tile: the grid is the SM count, one scratch slot per CTA
-    if (configure<false, false>(&d.ctx.var[0][0], optin, sms) != GMM_OK) rc = GMM_ERR_CUDA;
+    int sm_smem = 0;
+    cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device);
+    if (configure<false, false>(&d.ctx.var[0][0], optin, sm_smem, optin, sms) != GMM_OK) rc = GMM_ERR_CUDA;
     d.ctx.ws = static_cast<uint8_t *>(scratch);
     d.ctx.ws_bytes = kNoAllocScratchBytes;
   }

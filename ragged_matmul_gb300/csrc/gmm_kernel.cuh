@@ -111,7 +111,7 @@ constexpr int kWBytes = kBlockN * kBK * 2;    // 16 KB bf16 weight slab
 constexpr int kQChunkStages = 2;
 constexpr int kQRowBytes = kQChunkStages * kSub4 * kBK / 2;   // 128
 constexpr int kQSlotBytes = kBlockN * kQRowBytes;            // 16 KB
-constexpr int kQStages = 4;                                  // slots: 8 stages ahead
+constexpr int kQStages = 4;                                  // slots (at most): 8 stages ahead
 constexpr int kQRingBytes = kQStages * kQSlotBytes;
 static_assert(kQRowBytes == 128, "the packed chunk is one 128-byte swizzle row per weight row");
 // Epilogue staging: each epilogue warp transposes 32 token rows x its 32 C columns
@@ -123,22 +123,28 @@ static_assert(kQRowBytes == 128, "the packed chunk is one 128-byte swizzle row p
 constexpr uint32_t kEpiRows = 32;
 constexpr uint32_t kEpiRowBytes = 64;
 constexpr int kEpiStageBytes = 8 * kEpiRows * kEpiRowBytes;   // up to 8 epilogue warps
+template <bool kInt4>
+constexpr uint32_t kEpiBytes = kInt4 ? kEpiStageBytes / 2 : kEpiStageBytes;   // the 4-bit kernel has 4
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 // 4-bit kernel: dequantised weight slabs live in TMEM (128 lanes = weight rows, 32
 // columns = 64 bf16 of K per 64-wide slab) in the columns the accumulators leave
 // free: an accumulator holds at most 160 token columns (kMaxTok), so columns
-// 160..255 and 416..511 hold six slabs.  The 4-bit kernel's stage ring is as deep as
-// the slabs allow (6 / kSub4 stages), and a stage is its token slab and its TMEM
-// weight slabs together: one barrier tells the MMA that both are ready, one commit
-// frees both.  128-K stages (a 3-deep ring) measured faster than 64-K stages (6
-// deep): the MMA thread's fixed cost per stage outweighs the deeper ring's better
-// cover of the token copies' latency from L2.
+// 160..255 and 416..511 hold six slabs, kAStages = 6 / kSub4 stages of them: set s
+// has its first 64 of K at column 160 + 32 s and its second at 256 columns further.  A
+// stage is its token slab and its TMEM weight slabs together: one barrier tells the
+// MMA that both are ready, one commit frees both.  The token ring is deeper than the
+// slab ring (a multiple of kAStages, as deep as shared memory allows): stage s uses
+// barriers and token slot s % depth, and TMEM slab set s % kAStages.  A token copy
+// comes from L2 with about 1,900 cycles of latency under load, longer than the
+// tensor work of two stages, so a ring of three token slots left the MMAs waiting for
+// tokens at every stage.  128-K stages measured faster than 64-K stages: the MMA
+// thread's fixed cost per stage outweighs a finer ring.
 constexpr uint32_t kASlabs = 6;
 constexpr uint32_t kAStages = kASlabs / kSub4;
-__device__ __forceinline__ uint32_t a_slab_col(uint32_t stage, uint32_t sub) {
-  const uint32_t i = stage * kSub4 + sub;   // 0..5
-  return i < 3 ? 160u + 32u * i : 416u + 32u * (i - 3u);
+constexpr uint32_t kASlab0 = 160;    // column of slab set 0's first 64 of K
+__device__ __forceinline__ uint32_t a_slab_col(uint32_t set, uint32_t sub) {
+  return kASlab0 + 32u * set + kAccCols * sub;
 }
 constexpr int kTokMaps = 16;                  // token maps per CTA: boxes of 16, 32, ..., 256 rows
 constexpr int kMapSlotBytes = kTokMaps * 128; // per-CTA workspace: the patched 128-byte token maps
@@ -200,6 +206,7 @@ struct alignas(128) GmmParams {
   int N;
   int K;
   int num_stages;                // depth of the W+T stage ring
+  int q_stages;                  // 4-bit path: slots of the packed ring (kQStages, or 2 when shared memory is short)
   const __nv_bfloat16 *scales;   // 4-bit path: [E, N, K / group_size]
   int group_size;                // 4-bit path: multiple of 64 dividing K
   int scale_shift;               // 4-bit path: log2(group_size / 64) when that is a power of two, else -1
@@ -585,11 +592,12 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
   // group in each CTA.
   constexpr uint32_t kFullArrivals = 1 + (kInt4 ? (kPair ? 2 : 1) * kDqWarpsPerStage : 0);
   __shared__ Ctrl ctl;
-  __shared__ uint32_t prefix[kMaxGroups + 1];
   extern __shared__ uint8_t dyn_smem[];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t ST = static_cast<uint32_t>(p.num_stages);   // W+T stage ring (4-bit: tokens only)
+  const int QS = kInt4 ? p.q_stages : 0;   // packed ring: 2 or 4 slots
+  const uint32_t q_shift = QS == 4 ? 2u : 1u;
   const uint32_t SW = kInt4 ? 0u : ST;                         // weight slabs in shared memory
   const int KB = (p.K + static_cast<int>(G::kSub * kBK) - 1) / static_cast<int>(G::kSub * kBK);   // stages per tile
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
@@ -601,20 +609,22 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
   const uint32_t queue_arrivals = leader_readers + (kPair ? peer_readers : 0);
 
   // 1024-byte aligned rings, at identical offsets in both CTAs of a pair:
-  // SW weight slabs (bf16), ST token slabs, then (4-bit) kQStages packed slabs.
+  // SW weight slabs (bf16), ST token slabs, then (4-bit) QS packed slabs, the epilogue
+  // staging tiles, and the group prefix (as many entries as groups, G + 1).
   const uint32_t dyn_base = smem_addr(dyn_smem);
   const uint32_t ring = (dyn_base + 1023u) & ~1023u;
   const uint32_t w_ring = ring;
   const uint32_t t_ring = ring + SW * G::kSub * kWBytes;
   const uint32_t q_ring = t_ring + ST * G::kSub * G::kTSlot;   // 4-bit only
-  const uint32_t epi_ring = q_ring + (kInt4 ? kQRingBytes : 0);  // epilogue staging tiles
+  const uint32_t epi_ring = q_ring + static_cast<uint32_t>(QS) * kQSlotBytes;   // epilogue staging tiles
+  uint32_t *prefix = reinterpret_cast<uint32_t *>(dyn_smem + (epi_ring + kEpiBytes<kInt4> - dyn_base));
 
   if (tid == 0) {
     for (uint32_t s = 0; s < ST; ++s) {
       mbar_init(smem_addr(&ctl.full[s]), kFullArrivals);
       mbar_init(smem_addr(&ctl.empty[s]), 1);
     }
-    for (int s = 0; s < kQStages && kInt4; ++s) {
+    for (int s = 0; s < QS; ++s) {
       mbar_init(smem_addr(&ctl.qfull[s]), 1);
       mbar_init(smem_addr(&ctl.qempty[s]), kQChunkStages * kDqWarpsPerStage);
     }
@@ -839,9 +849,12 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
       // (shared-memory addresses stay below 256 KB, so the 14-bit field never carries).
       Ring rt;
       uint32_t acc = 0, acc_phase = 0;
+      uint32_t aset = 0;   // 4-bit: TMEM weight-slab set of the next stage (stage % kAStages)
       bool ok = true;
       TileSource reader(dynamic, unit0, units, total);
       const uint64_t t_desc0 = smem_desc_k_sw128(t_ring);
+      const uint32_t t_lo = static_cast<uint32_t>(t_desc0), t_hi = static_cast<uint32_t>(t_desc0 >> 32);
+      const uint32_t full0 = smem_addr(&ctl.full[0]), empty0 = smem_addr(&ctl.empty[0]);
       const uint64_t w_desc0 = smem_desc_k_sw128(w_ring);
       for (;;) {
         Tile ti;
@@ -855,32 +868,47 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + acc * kAccCols;
         const uint32_t idesc = kFp8 ? idesc_e4m3_f32(G::kRows, ti.ntok) : idesc_bf16_f32(G::kRows, ti.ntok);
+        if constexpr (kInt4) {
+          // One instruction stream per stage (mma_stage_ts_x8): the wait for the stage,
+          // its eight MMAs and the commit.  The pair's stage is also signalled by the
+          // second CTA's dequantisation warps, so it is tested at cluster scope, relaxed:
+          // their TMEM stores are ordered by tcgen05 fences and the token bytes by the
+          // barrier.  The stage's two token sub-slabs sit my_tok rows apart (one 3-D
+          // copy); its weight slabs are TMEM slab set `aset` (stage % kAStages).
+          const uint32_t tok_step = ((kPair ? ti.ntok / 2 : ti.ntok) * (kBK * 2)) >> 4;
+          for (int kb = 0; kb < KB; ++kb) {
+            const uint32_t b0 = t_lo + rt.slot * ((G::kSub * G::kTSlot) >> 4);
+            const uint32_t a0 = tmem_base + kASlab0 + 32u * aset;
+            const uint32_t full = full0 + rt.slot * 8u, empty = empty0 + rt.slot * 8u;
+            if (!mma_stage_ts_x8<kPair>(full, rt.phase, 4u, d_tmem, a0, a0 + kAccCols, b0, b0 + tok_step, t_hi, idesc,
+                                        kb != 0, empty)) {
+              // Not staged after a few suspended tests: check the clock and the abort
+              // flag between further attempts, as every bounded wait does.
+              const uint64_t t0 = global_timer_ns();
+              bool issued = false;
+              while (!issued) {
+                if (*abort || global_timer_ns() - t0 > kWaitLimitNs) break;
+                issued = mma_stage_ts_x8<kPair>(full, rt.phase, 4u, d_tmem, a0, a0 + kAccCols, b0, b0 + tok_step,
+                                                t_hi, idesc, kb != 0, empty);
+              }
+              if (!__all_sync(0xffffffffu, issued)) {
+                *abort = 1;
+                ok = false;
+                break;
+              }
+            }
+            if (++aset == kAStages) aset = 0;
+            rt.next(ST);
+          }
+        } else {
         for (int kb = 0; kb < KB; ++kb) {
-          // The 4-bit pair's stage is also signalled by the second CTA's dequantisation
-          // warps, so it is waited for at cluster scope; relaxed, since their TMEM
-          // stores are ordered by tcgen05 fences and the token bytes by the barrier.
-          const bool staged = __all_sync(
-              0xffffffffu, (kInt4 && kPair) ? wait_phase_cluster<true>(smem_addr(&ctl.full[rt.slot]), rt.phase, abort)
-                                            : wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort));
+          const bool staged = __all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort));
           if (!staged) { ok = false; break; }
           tc_fence_after_sync();
+          {
 #pragma unroll
-          for (uint32_t sub = 0; sub < G::kSub; ++sub) {
-            // 4-bit: the stage's sub-slabs sit my_tok rows apart (one 3-D copy); bf16: kTSlot apart.
-            const uint32_t b_off = kInt4 ? rt.slot * G::kSub * G::kTSlot + sub * (kPair ? ti.ntok / 2 : ti.ntok) * (kBK * 2)
-                                         : (rt.slot * G::kSub + sub) * G::kTSlot;
-            const uint64_t b_desc = t_desc0 + (b_off >> 4);
-            if constexpr (kInt4) {
-              const uint32_t a_tmem = tmem_base + a_slab_col(rt.slot, sub);
-#pragma unroll
-              for (int k = 0; k < kBK / 16; ++k) {   // A: +8 TMEM columns per K step; B: +32 bytes
-                const uint32_t accumulate = (kb | static_cast<int>(sub) | k) != 0;
-                if constexpr (kPair)
-                  mma_bf16_ts_pair(d_tmem, a_tmem + 8u * k, b_desc + 2u * k, idesc, accumulate);
-                else
-                  mma_bf16_ts(d_tmem, a_tmem + 8u * k, b_desc + 2u * k, idesc, accumulate);
-              }
-            } else {
+            for (uint32_t sub = 0; sub < G::kSub; ++sub) {
+              const uint64_t b_desc = t_desc0 + (((rt.slot * G::kSub + sub) * G::kTSlot) >> 4);
               const uint64_t a_desc = w_desc0 + (((rt.slot * G::kSub + sub) * kWBytes) >> 4);
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k) {   // +32 bytes along K per step: +2 in the >>4 address field
@@ -895,10 +923,11 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
                   mma_bf16(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, accumulate);
               }
             }
+            if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.empty[rt.slot]), 0x3);
+            else mma_commit(smem_addr(&ctl.empty[rt.slot]));
           }
-          if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.empty[rt.slot]), 0x3);
-          else mma_commit(smem_addr(&ctl.empty[rt.slot]));
           rt.next(ST);
+        }
         }
         if (!ok) break;
         if constexpr (kPair) mma_commit_pair(smem_addr(&ctl.acc_full[acc]), 0x3);
@@ -1095,12 +1124,12 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
           tma_load_3d_hint(q_ring + rq.slot * kQSlotBytes, &p.w_map, qfull, kc * (kQRowBytes / 4), w_row, ti.e, pol);
           pending |= 1u << rq.slot;
           pend_phase = (pend_phase & ~(1u << rq.slot)) | (rq.phase << rq.slot);
-          rq.next(kQStages);
+          rq.next(static_cast<uint32_t>(QS));
         }
         if (!ok) break;
       }
       if (!ok) {
-        for (int s = 0; s < kQStages; ++s)
+        for (int s = 0; s < QS; ++s)
           if (pending & (1u << s)) wait_phase_for(smem_addr(&ctl.qfull[s]), (pend_phase >> s) & 1u, kDrainLimitNs);
         atomicOr(p.status, kStatusTimeout);
       }
@@ -1113,27 +1142,33 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
     // across tiles); in a handled stage it converts kDqSubsPerWarp 64-K sub-slabs of
     // its row (8 packed words each) into 32 TMEM columns of bf16 pairs each.  The
     // arithmetic needs only the packed slab, so it runs as soon as the slab lands;
-    // only the TMEM store waits for the slot (the MMAs that last read it completed).
-    // With as many groups as stage slots, group g always fills slot g, and its warps
-    // step straight from one of their stages to the next.  A slot cannot move past a
-    // phase this warp still waits for, because releasing it needs this warp's arrival.
-    static_assert(kDqGroups == static_cast<int>(kAStages), "group g always fills stage slot g");
+    // only the TMEM store waits, for the MMAs of stage s - kAStages, the last readers
+    // of the slab set.  With as many groups as slab sets, group g always fills set g,
+    // and its warps step straight from one of their stages to the next.  The barrier
+    // of stage s - kAStages cannot move past the phase this warp waits for, because
+    // its next phase needs the stage after it in this group, i.e. this warp's arrival.
+    static_assert(kDqGroups == static_cast<int>(kAStages), "group g always fills TMEM slab set g");
     const uint32_t dw = static_cast<uint32_t>(warp - 7);
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
-    const uint32_t grp = dw / kDqWarpsPerStage;   // also the stage slot this warp fills
+    const uint32_t grp = dw / kDqWarpsPerStage;   // also the TMEM slab set this warp fills
     const uint32_t sub0 = ((dw % kDqWarpsPerStage) >> 2) * kDqSubsPerWarp;   // first sub-slab of this warp
     const uint32_t r = quad * 32u + static_cast<uint32_t>(lane);
     const int spr = p.K / p.group_size;   // scales per weight row
     const unsigned short *sbits = reinterpret_cast<const unsigned short *>(p.scales);
     const uint32_t lane_field = (quad * 32u) << 16;
-    const uint32_t kb_mod = static_cast<uint32_t>(KB) % kDqGroups;
-    uint32_t aphase = 0;      // phase of this warp's stage slot (flips on every use)
-    uint32_t base_mod = 0;    // stages of earlier tiles, modulo kDqGroups
-    uint32_t chunk_base = 0;  // packed chunks of earlier tiles
-    // The weight stage's `full` barrier lives in the leader CTA of a pair.
-    const uint32_t full_g = (kPair ? map_to_rank(smem_addr(&ctl.full[0]), 0) : smem_addr(&ctl.full[0])) +
-                            grp * static_cast<uint32_t>(sizeof(uint64_t));
-    const uint32_t empty_g = smem_addr(&ctl.empty[grp]);
+    uint32_t s_next = grp;      // next stage (counted across tiles) of this warp's group
+    uint32_t tile_base = 0;     // stages of earlier tiles
+    // Barrier slot and phase of stage s_next (s_next % ST and its use count's parity), and
+    // of this group's previous stage, s_next - kDqGroups, kept incrementally: ST is a
+    // runtime multiple of kDqGroups, and a division by it costs tens of instructions.
+    uint32_t fslot = grp, fphase = 0, eslot = 0, ephase = 0;
+    bool has_prev = false;
+    uint32_t chunk_base = 0;    // packed chunks of earlier tiles
+    // A stage's `full` barrier lives in the leader CTA of a pair; `empty` in each CTA
+    // (the leader's commit arrives on both).
+    const uint32_t full0 = kPair ? map_to_rank(smem_addr(&ctl.full[0]), 0) : smem_addr(&ctl.full[0]);
+    const uint32_t empty0 = smem_addr(&ctl.empty[0]);
+    constexpr uint32_t kBarBytes = static_cast<uint32_t>(sizeof(uint64_t));
     bool ok = true;
     TileSource reader(dynamic, unit0, units, total);
     for (;;) {
@@ -1145,9 +1180,9 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
       const uint32_t n = ti.n0 + rank * kBlockN + r;
       const bool row_ok = n < static_cast<uint32_t>(p.N);
       const unsigned short *srow = sbits + (static_cast<size_t>(ti.e) * p.N + (row_ok ? n : 0)) * spr;
-      // This group's stages of the tile: kb = kb0, kb0 + kDqGroups, ...
-      const int kb0 = static_cast<int>((grp + kDqGroups - base_mod) % kDqGroups);
-      for (int kb = kb0; kb < KB && ok; kb += kDqGroups) {
+      // This group's stages of the tile: kb = s_next - tile_base, then every kDqGroups-th.
+      for (; s_next < tile_base + static_cast<uint32_t>(KB) && ok; s_next += kDqGroups) {
+        const int kb = static_cast<int>(s_next - tile_base);
         // Scales of this thread's sub-slabs; zero past K (the last stage's second
         // half when K is an odd multiple of 64) or past N, so the weights there are
         // zero, matching the zero-filled tokens.  Loaded first: the waits below
@@ -1162,7 +1197,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
         // Packed chunk of this stage (slot and phase from the chunk count) and the
         // stage's half of it; 16-byte piece c of row r sits at piece c ^ (r % 8).
         const uint32_t chunk = chunk_base + static_cast<uint32_t>(kb) / kQChunkStages;
-        const uint32_t qslot = chunk % kQStages, qphase = (chunk / kQStages) & 1u;
+        const uint32_t qslot = chunk & static_cast<uint32_t>(QS - 1), qphase = (chunk >> q_shift) & 1u;
         const uint32_t piece0 = (static_cast<uint32_t>(kb) % kQChunkStages) * (kSub4 * 2);
         if (!__all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.qfull[qslot]), qphase, abort))) {
           ok = false;   // the warp aborts together
@@ -1192,24 +1227,34 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
           mbar_arrive(smem_addr(&ctl.qempty[qslot]));
           if (kb == KB - 1 && (KB % kQChunkStages) != 0) mbar_arrive(smem_addr(&ctl.qempty[qslot]));
         }
-        if (!__all_sync(0xffffffffu, wait_phase(empty_g, aphase ^ 1u, abort))) {
-          ok = false;
-          break;
+        if (has_prev) {   // the MMAs of stage s - kAStages (this group's previous) read this slab set
+          if (!__all_sync(0xffffffffu, wait_phase(empty0 + eslot * kBarBytes, ephase, abort))) {
+            ok = false;
+            break;
+          }
         }
-        tc_fence_after_sync();   // the MMAs' reads of this TMEM stage precede the overwrite
+        tc_fence_after_sync();   // the MMAs' reads of this TMEM slab set precede the overwrite
 #pragma unroll
         for (int i = 0; i < kDqSubsPerWarp; ++i)
           tmem_st_x32(tmem_base + lane_field + a_slab_col(grp, sub0 + i), cols[i]);
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) {
-          if constexpr (kPair) mbar_arrive_cluster_relaxed(full_g); else mbar_arrive_relaxed(full_g);   // TMEM stores done
+        if (lane == 0) {   // TMEM stores done
+          const uint32_t fb = full0 + fslot * kBarBytes;
+          if constexpr (kPair) mbar_arrive_cluster_relaxed(fb); else mbar_arrive_relaxed(fb);
         }
-        aphase ^= 1u;
+        eslot = fslot;
+        ephase = fphase;
+        has_prev = true;
+        fslot += kDqGroups;
+        if (fslot >= ST) {
+          fslot -= ST;
+          fphase ^= 1u;
+        }
       }
       if (!ok) break;
-      base_mod = (base_mod + kb_mod) % kDqGroups;
+      tile_base += static_cast<uint32_t>(KB);
       chunk_base += static_cast<uint32_t>((KB + kQChunkStages - 1) / kQChunkStages);
     }
     if (!ok) atomicOr(p.status, kStatusTimeout);

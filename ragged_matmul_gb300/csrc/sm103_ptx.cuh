@@ -259,6 +259,78 @@ __device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tme
       : "memory");
 }
 
+// One pipeline stage of the 4-bit kernel, from the wait for its operands to the commit
+// that frees them: up to `tries` suspended tests of the stage's `full` barrier (phase
+// `parity`; kPair: at cluster scope, relaxed), a warp vote so that every lane agrees,
+// and, once it completed, a tcgen05 fence, eight MMAs over 128 of K (A in tensor
+// memory: two 64-K slabs at a0 and a1, 8 columns per K step of 16; B in shared memory:
+// two sub-slab descriptors whose low words are b0 and b1, high word bhi, +32 bytes per
+// K step) and a commit of all of them to `empty` (kPair: cta_group::2, multicast to both
+// CTAs' barriers).  Returns 1 when the stage was issued, 0 when the barrier had not
+// completed after the tests (the caller checks its clock and tries again).
+//
+// Everything is one instruction stream with a single elect: the issuing warp shares its
+// SM sub-partition with dequantisation warps that keep the issue port busy, and each
+// instruction of its own costs it tens of cycles there.  A descriptor step adds to the
+// low word only: the 14-bit start-address field holds shared-memory addresses >> 4,
+// below 256 KB, so the step never carries out of it.  `accumulate` = 0 only for a
+// tile's first stage: its first MMA then overwrites the accumulator.
+#define GMM_TS_MMA(CG, A, B, P) "@e tcgen05.mma.cta_group::" CG ".kind::f16 [%1], [" A "], " B ", %7, " P ";\n\t"
+#define GMM_TS_STAGE(CG, WAIT)                                                                 \
+  "{\n\t.reg .pred e, p, t, r, v;\n\t.reg .b32 l, a, c, n;\n\t.reg .b64 b;\n\t"                      \
+  "mov.u32 n, 0;\n\t"                                                                         \
+  "GMM_W%=:\n\t" WAIT " r, [%10], %11, 1048576;\n\t"                                           \
+  "vote.sync.all.pred v, r, 0xffffffff;\n\t"                                                 \
+  "@v bra.uni GMM_G%=;\n\t"                                                                   \
+  "add.u32 n, n, 1;\n\t"                                                                      \
+  "setp.lt.u32 t, n, %12;\n\t"                                                                \
+  "@t bra.uni GMM_W%=;\n\t"                                                                   \
+  "mov.u32 %0, 0;\n\t"                                                                        \
+  "bra.uni GMM_E%=;\n\t"                                                                      \
+  "GMM_G%=:\n\t"                                                                              \
+  "tcgen05.fence::after_thread_sync;\n\t"                                                     \
+  "elect.sync l|e, 0xffffffff;\n\t"                                                          \
+  "setp.ne.b32 p, %8, 0;\n\t"                                                                 \
+  "setp.eq.b32 t, %8, %8;\n\t"                                                                \
+  "mov.b64 b, {%4, %6};\n\t" GMM_TS_MMA(CG, "%2", "b", "p")                                  \
+  "add.u32 a, %2, 8;\n\tadd.u32 c, %4, 2;\n\tmov.b64 b, {c, %6};\n\t" GMM_TS_MMA(CG, "a", "b", "t")  \
+  "add.u32 a, %2, 16;\n\tadd.u32 c, %4, 4;\n\tmov.b64 b, {c, %6};\n\t" GMM_TS_MMA(CG, "a", "b", "t") \
+  "add.u32 a, %2, 24;\n\tadd.u32 c, %4, 6;\n\tmov.b64 b, {c, %6};\n\t" GMM_TS_MMA(CG, "a", "b", "t") \
+  "mov.b64 b, {%5, %6};\n\t" GMM_TS_MMA(CG, "%3", "b", "t")                                  \
+  "add.u32 a, %3, 8;\n\tadd.u32 c, %5, 2;\n\tmov.b64 b, {c, %6};\n\t" GMM_TS_MMA(CG, "a", "b", "t")  \
+  "add.u32 a, %3, 16;\n\tadd.u32 c, %5, 4;\n\tmov.b64 b, {c, %6};\n\t" GMM_TS_MMA(CG, "a", "b", "t") \
+  "add.u32 a, %3, 24;\n\tadd.u32 c, %5, 6;\n\tmov.b64 b, {c, %6};\n\t" GMM_TS_MMA(CG, "a", "b", "t")
+
+template <bool kPair>
+__device__ __forceinline__ uint32_t mma_stage_ts_x8(uint32_t full, uint32_t parity, uint32_t tries, uint32_t d_tmem,
+                                                    uint32_t a0, uint32_t a1, uint32_t b0, uint32_t b1, uint32_t bhi,
+                                                    uint32_t idesc, uint32_t accumulate, uint32_t empty) {
+  uint32_t issued;
+  if constexpr (kPair) {
+    asm volatile(GMM_TS_STAGE("2", "mbarrier.try_wait.parity.relaxed.cluster.shared::cta.b64")
+                 "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+                 " [%9], %13;\n\t"
+                 "mov.u32 %0, 1;\n\t"
+                 "GMM_E%=:\n\t}"
+                 : "=r"(issued)
+                 : "r"(d_tmem), "r"(a0), "r"(a1), "r"(b0), "r"(b1), "r"(bhi), "r"(idesc), "r"(accumulate), "r"(empty),
+                   "r"(full), "r"(parity), "r"(tries), "h"(static_cast<uint16_t>(3))
+                 : "memory");
+  } else {
+    asm volatile(GMM_TS_STAGE("1", "mbarrier.try_wait.parity.shared::cta.b64")
+                 "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t"
+                 "mov.u32 %0, 1;\n\t"
+                 "GMM_E%=:\n\t}"
+                 : "=r"(issued)
+                 : "r"(d_tmem), "r"(a0), "r"(a1), "r"(b0), "r"(b1), "r"(bhi), "r"(idesc), "r"(accumulate), "r"(empty),
+                   "r"(full), "r"(parity), "r"(tries)
+                 : "memory");
+  }
+  return issued;
+}
+#undef GMM_TS_STAGE
+#undef GMM_TS_MMA
+
 // Arrive once on `bar` when every tcgen05.mma issued so far (by this warp) has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
