@@ -388,7 +388,7 @@ def dtype_name(r):
 def kernel_name(r, variant):
     if is_fp8(r) and fp8_gran(r)[2] < r.K:
         return "gmm_fp8_block_kernel"
-    pair = variant == "pair" or (variant is None and not r.int4)
+    pair = variant != "single"   # the library runs CTA pairs unless told otherwise
     return "gmm_grouped_kernel<%s, %s, %s>" % ("true" if r.int4 else "false", "true" if pair else "false",
                                                "true" if is_fp8(r) else "false")
 

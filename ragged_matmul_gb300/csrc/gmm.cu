@@ -44,7 +44,9 @@ struct DeviceGuard {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// GMM_DEBUG=1: report the CUDA call behind a GMM_ERR_CUDA on stderr (diagnostics only).
+// GMM_DEBUG=1: report the CUDA call behind a GMM_ERR_CUDA on stderr, and (when set as
+// a handle is created) the handle's ring depths and each of its grouped-kernel launches'
+// layout (diagnostics only).
 void debug_report(const char *what, int code, const char *msg) {
   static const bool on = getenv("GMM_DEBUG") != nullptr;
   if (on) fprintf(stderr, "gmm: %s failed: %d %s\n", what, code, msg ? msg : "");
@@ -53,17 +55,19 @@ void debug_report(const char *what, int code, const char *msg) {
 }  // namespace
 
 // One launch configuration per kernel variant.  The grouped kernel keeps its group
-// prefix (G + 1 words) in dynamic shared memory after the rings, so its ring depth is
-// set per launch: as many stages as the rest of the budget holds for that G.
+// prefix (G + 1 words) in dynamic shared memory after the rings, so its configuration is
+// chosen per launch: the first of its candidate layouts (in order of preference) whose
+// minimum ring fits beside the prefix of that G, with as many stages as the rest holds.
 struct gmm_variant {
-  int stages = 0;           // depth of the W+T stage ring (the grouped kernel: at the largest G)
+  int stages = 0;           // depth of the W+T stage ring (grouped kernel: its first layout, one group)
   size_t smem = 0;          // dynamic shared memory of every launch
   size_t budget = 0;        // of which the kernel may use (the rest only keeps one CTA per SM)
-  size_t fixed = 0;         // grouped kernel: everything but the stage ring and the prefix
   size_t stage_bytes = 0;   // grouped kernel: one stage of the ring
   int stage_mult = 1;       // grouped kernel: the ring depth is a multiple of this (4-bit: kAStages)
   int min_stages = 2;       // grouped kernel: the shallowest ring it runs with
-  int q_stages = 0;         // 4-bit kernel: packed-ring slots
+  int layouts = 1;          // grouped kernel: candidate layouts, in order of preference
+  size_t fixed[2] = {};     // per layout: everything but the stage ring and the prefix
+  int q_stages[2] = {};     // per layout, 4-bit: packed-ring slots
   int grid = 0;             // CTAs: the SM count, or (pairs) twice the co-resident clusters of two
 };
 
@@ -75,8 +79,9 @@ struct gmm_ctx {
   gmm_variant var_fp8[2];         // e4m3 kernels, [pair]
   gmm_variant var_fp8_block;      // e4m3 with per-K-block scales (one CTA per tile)
   int smem_per_sm = 0;            // shared memory of one SM (a launch reserves more than half: one CTA per SM)
+  bool debug = false;             // GMM_DEBUG was set when the handle was created
   int use_pairs = 1;              // bf16 path: 1 = CTA-pair kernels (cta_group::2), 0 = one CTA per tile
-  int use_pairs_int4 = 0;         // 4-bit path: the same (default one CTA per tile)
+  int use_pairs_int4 = 1;         // 4-bit path: the same
   uint8_t *ws = nullptr;          // [status word | per-CTA tensor-map slots]
   size_t ws_bytes = 0;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
@@ -175,12 +180,14 @@ void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, c
   if (const char *env = getenv("GMM_CACHE_HINTS")) p.cache_hints = atoi(env) != 0;   // tuning override
 }
 
-// Stage-ring depth of a grouped-kernel launch with G groups: what the budget holds after
-// the fixed parts and the prefix, capped at kMaxStages, a multiple of stage_mult.
-int stages_for(const gmm_variant &v, int G) {
+// Stage-ring depth of a grouped-kernel launch with G groups in a layout: what the budget
+// holds after the layout's fixed parts and the prefix, capped at kMaxStages, a multiple
+// of stage_mult.
+int stages_for(const gmm_variant &v, int G, int layout) {
   const size_t prefix = (static_cast<size_t>(G + 1) * 4 + 15) & ~static_cast<size_t>(15);
-  if (v.budget < v.fixed + prefix) return 0;
-  long st = static_cast<long>((v.budget - v.fixed - prefix) / v.stage_bytes);
+  const size_t fixed = v.fixed[layout];
+  if (v.budget < fixed + prefix) return 0;
+  long st = static_cast<long>((v.budget - fixed - prefix) / v.stage_bytes);
   if (st > gmm::kMaxStages) st = gmm::kMaxStages;
   st -= st % v.stage_mult;
   return static_cast<int>(st);
@@ -205,20 +212,18 @@ int configure(gmm_variant *v, int optin, int sm_smem, int device_optin, int num_
   v->budget = static_cast<size_t>(avail);
   v->stage_bytes = G::kStageBytes;
   v->stage_mult = kInt4 ? static_cast<int>(gmm::kAStages) : 1;
-  // The deepest configuration that fits with the largest prefix (kMaxGroups), else the
-  // deepest that fits with a one-group prefix (a launch with more groups than its budget
-  // holds then returns GMM_ERR_UNSUPPORTED).
+  // Candidate layouts.  4-bit, in order of preference: the full packed ring, then half
+  // of it.  The variant is usable when at least one layout fits beside a one-group
+  // prefix; a launch whose groups' prefix leaves no layout its minimum ring returns
+  // GMM_ERR_UNSUPPORTED.
   v->min_stages = kInt4 ? static_cast<int>(gmm::kAStages) : 2;
-  v->stages = 0;
-  for (int groups : {gmm::kMaxGroups, 1}) {
-    for (int qs = gmm::kQStages; qs >= 2; qs /= 2) {   // 4-bit: full packed ring, then half of it
-      v->q_stages = kInt4 ? qs : 0;
-      v->fixed = 1024 + gmm::kEpiBytes<kInt4> + static_cast<size_t>(v->q_stages) * gmm::kQSlotBytes;
-      v->stages = stages_for(*v, groups);
-      if (v->stages >= v->min_stages || !kInt4) break;
-    }
-    if (v->stages >= v->min_stages) break;
+  v->layouts = kInt4 ? 2 : 1;
+  for (int c = 0; c < v->layouts; ++c) {
+    v->q_stages[c] = kInt4 ? (c == 0 ? gmm::kQStages : 2) : 0;
+    v->fixed[c] = 1024 + gmm::kEpiBytes<kInt4> + static_cast<size_t>(v->q_stages[c]) * gmm::kQSlotBytes;
   }
+  v->stages = 0;
+  for (int c = 0; c < v->layouts && v->stages < v->min_stages; ++c) v->stages = stages_for(*v, 1, c);
   if (v->stages < v->min_stages) return GMM_ERR_UNSUPPORTED;
   const long reserve = static_cast<long>(sm_smem) / 2 + 1024;   // more than half an SM: one CTA per SM
   const long cap = static_cast<long>(device_optin) - static_cast<long>(attr.sharedSizeBytes);
@@ -294,9 +299,15 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   cfg.gridDim = dim3(static_cast<unsigned>(v.grid));
   cfg.dynamicSmemBytes = v.smem;
   cfg.stream = stream;
-  p.num_stages = stages_for(v, p.num_groups);
-  p.q_stages = v.q_stages;
-  if (p.num_stages < v.min_stages) return GMM_ERR_UNSUPPORTED;   // the prefix of this many groups does not fit
+  int layout = 0;
+  p.num_stages = 0;
+  for (; layout < v.layouts; ++layout)
+    if ((p.num_stages = stages_for(v, p.num_groups, layout)) >= v.min_stages) break;
+  if (layout == v.layouts) return GMM_ERR_UNSUPPORTED;   // no layout's minimum ring fits beside this prefix
+  p.q_stages = v.q_stages[layout];
+  if (h->debug)
+    fprintf(stderr, "gmm: launch %s%s, %d groups: stages %d packed slots %d\n", kInt4 ? "int4" : (kFp8 ? "e4m3" : "bf16"),
+            pairs ? " pair" : "", p.num_groups, p.num_stages, p.q_stages);
   cudaError_t err;
   if (pairs) {
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -400,23 +411,24 @@ int gmm_create(gmm_handle_t *out, int num_experts, int device) {
                         configure<true, true>(&h->var[1][1], optin, sm_smem, device_optin, sms) == GMM_OK &&
                         configure<false, true, true>(&h->var_fp8[1], optin, sm_smem, device_optin, sms) == GMM_OK;
   h->use_pairs = pairs_ok && !(variant && std::strcmp(variant, "single") == 0);
-  // The 4-bit path runs one CTA per tile unless GMM_VARIANT=pair: its pair kernel's
-  // cross-CTA signal that both halves of a weight stage are in TMEM costs more than
-  // the halved token traffic saves.
-  h->use_pairs_int4 = pairs_ok && variant && std::strcmp(variant, "pair") == 0;
+  // The 4-bit path too: each CTA of a pair loads half of a stage's tokens (a 6-deep token
+  // ring fits), and one MMA instruction covers both CTAs' 128 weight rows, half the
+  // instructions per unit of work for the issuing warp, which shares its SM
+  // sub-partition with dequantisation warps.
+  h->use_pairs_int4 = h->use_pairs;
   if (!single_ok) {
     cudaGetLastError();
     delete h;
     return GMM_ERR_CUDA;
   }
 
-  if (getenv("GMM_DEBUG")) {
+  h->debug = getenv("GMM_DEBUG") != nullptr;
+  if (h->debug) {
     const gmm_variant *vs[7] = {&h->var[0][0], &h->var[0][1], &h->var[1][0], &h->var[1][1],
                                 &h->var_fp8[0], &h->var_fp8[1], &h->var_fp8_block};
     const char *names[7] = {"bf16", "bf16 pair", "int4", "int4 pair", "e4m3", "e4m3 pair", "e4m3 block"};
     for (int i = 0; i < 7; ++i)
-      fprintf(stderr, "gmm: %-16s stages %d packed slots %d smem %zu grid %d\n", names[i], vs[i]->stages,
-              vs[i]->q_stages, vs[i]->smem, vs[i]->grid);
+      fprintf(stderr, "gmm: %-16s stages %d smem %zu grid %d\n", names[i], vs[i]->stages, vs[i]->smem, vs[i]->grid);
   }
   h->ws_bytes = kStatusBytes + static_cast<size_t>(sms) * gmm::kMapSlotBytes;
   if (cudaMalloc(&h->ws, h->ws_bytes) != cudaSuccess ||

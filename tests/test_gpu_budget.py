@@ -27,8 +27,8 @@ IDS = [5, 0, 1, -1, 3, 2, 4, 0]
 
 
 def _create(E, budget, variant, capfd):
-    """A handle created under the budget cap; returns it with the parsed GMM_DEBUG report
-    {kernel name: (stages, packed slots)} (stages: with the largest prefix that fits)."""
+    """A handle created under the budget cap, with GMM_DEBUG on: the library then reports
+    each grouped-kernel launch's layout on stderr (see _launches)."""
     capfd.readouterr()
     saved = {k: os.environ.get(k) for k in ("GMM_SMEM_BUDGET", "GMM_VARIANT", "GMM_DEBUG")}
     os.environ.update({"GMM_SMEM_BUDGET": str(budget), "GMM_VARIANT": variant, "GMM_DEBUG": "1"})
@@ -40,45 +40,48 @@ def _create(E, budget, variant, capfd):
                 os.environ.pop(k, None)
             else:
                 os.environ[k] = v
+    capfd.readouterr()
+    return h
+
+
+def _launches(capfd):
+    """The layouts of the grouped-kernel launches since the last call, as
+    [(kernel, groups, stages, packed slots)]."""
     err = capfd.readouterr().err
-    cfg = {m.group(1).strip(): (int(m.group(2)), int(m.group(3)))
-           for m in re.finditer(r"gmm: (.+?)\s+stages (\d+) packed slots (\d+)", err)}
-    return h, cfg
+    return [(m.group(1), int(m.group(2)), int(m.group(3)), int(m.group(4))) for m in
+            re.finditer(r"gmm: launch (\w+(?: pair)?), (\d+) groups: stages (\d+) packed slots (\d+)", err)]
 
 
 @pytest.mark.parametrize("variant", ["pair", "single"])
 def test_bf16_and_4bit_with_200kb(variant, capfd):
-    """200 KB: one stage fewer for bf16, and the 4-bit kernel's packed ring at half its
-    slots (one CTA per tile) or a token ring of 3 instead of 6 (CTA pair)."""
+    """200 KB: one stage fewer for bf16 (3 instead of 4 for one CTA, 2 instead of 3 for a
+    pair); the 4-bit kernels still fit their full layouts beside the prefix of 8 groups."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    h, cfg = _create(6, 200 * 1024, variant, capfd)
+    h = _create(6, 200 * 1024, variant, capfd)
     try:
-        assert cfg["bf16"][0] == 3 and cfg["bf16 pair"][0] == 2, cfg
-        assert cfg["int4"] == (3, 2) and cfg["int4 pair"] == (3, 4), cfg
         r = wl.make_routing("b", 6, 384, 520, LOADS, IDS, a_dist=("normal", 1.0), b_dist=("normal", 1.0))
         _, _, status, _ = check_against_oracle(h, r, wl.host_values(r, 31), where=f"bf16 at 200 KB {variant}")
         assert status == binding.GMM_OK
+        assert _launches(capfd) == [("bf16 pair", 8, 2, 0) if variant == "pair" else ("bf16", 8, 3, 0)]
         r4 = wl.make_routing("b4", 6, 384, 1024, LOADS, IDS, a_dist=("normal", 1.0), b_dist=None, int4=True,
                              group_size=128)
         _, _, status, _ = check_against_oracle(h, r4, wl.host_values(r4, 32), where=f"4-bit at 200 KB {variant}")
         assert status == binding.GMM_OK
+        assert _launches(capfd) == [("int4 pair", 8, 6, 4) if variant == "pair" else ("int4", 8, 3, 4)]
     finally:
         binding.gmm_destroy(h)
 
 
 def test_dense_4bit_and_e4m3_with_170kb(capfd):
-    """170 KB: the CTA pairs' rings still fit (2 stages), the 4-bit kernel fits only with
-    a small prefix (a handful of groups) and the half packed ring; the dense 4-bit GEMM
-    (one group) and both e4m3 kernels run against the oracle."""
+    """170 KB: the 4-bit kernel fits only with the half packed ring; the dense 4-bit GEMM (one group) and both e4m3 kernels (3 stages instead of 4
+    for one scale over K) run against the oracle."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    h, cfg = _create(4, 170 * 1024, "single", capfd)
+    h = _create(4, 170 * 1024, "single", capfd)
     try:
-        assert cfg["int4"][1] == 2, cfg
-        assert cfg["bf16"][0] == 2, cfg
         # the dense 4-bit GEMM (its own entry point): one group of 300 rows
         r4 = wl.make_routing("d4", 1, 256, 512, [300], [0], a_dist=("normal", 1.0), b_dist=None, int4=True,
                              group_size=128)
@@ -90,6 +93,7 @@ def test_dense_4bit_and_e4m3_with_170kb(capfd):
                                 torch.from_numpy(np.ascontiguousarray(v4["packed"][0]).view(np.int32)).cuda(),
                                 to_dev_u16(v4["scales"][0], "cuda:0"), group_size=128)
         assert binding.gmm_query_status(h) == binding.GMM_OK
+        assert _launches(capfd) == [("int4", 1, 3, 2)]
         ref = oracle.gmm_int4(v4["a"], r4.a_offsets, v4["packed"], v4["scales"], r4.expert_ids, group_size=128)
         assert_close(bits_of(c), ref.ref32, np.ones(r4.rows, bool), where="dense 4-bit at 170 KB")
         # e4m3, one scale over K and per-K-block scales
@@ -98,6 +102,8 @@ def test_dense_4bit_and_e4m3_with_170kb(capfd):
             v8 = wl.fp8_host_values(r8, 34, gran)
             _, _, status, _ = check_fp8_against_oracle(h, r8, v8, gran, where=f"e4m3 {gran} at 170 KB")
             assert status == binding.GMM_OK
+        assert _launches(capfd)[:1] == [("e4m3", 4, 3, 0)]   # one scale over K: the grouped kernel, 3 stages
+
     finally:
         binding.gmm_destroy(h)
 
@@ -108,7 +114,7 @@ def test_budget_too_small_for_a_launch_is_reported(capfd):
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    h, _ = _create(2, 170 * 1024, "single", capfd)
+    h = _create(2, 170 * 1024, "single", capfd)
     try:
         G = 4096
         dev = "cuda:0"
