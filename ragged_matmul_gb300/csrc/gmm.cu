@@ -178,6 +178,13 @@ void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, c
   }
   p.cache_hints = 1;
   if (const char *env = getenv("GMM_CACHE_HINTS")) p.cache_hints = atoi(env) != 0;   // tuning override
+  // Test hooks of the device-timeout path (off unless set): GMM_TEST_WAIT_LIMIT_NS
+  // shortens every pipeline wait, GMM_TEST_STALL_STAGE makes the one-CTA bf16 kernel's
+  // producer skip that stage, so that the kernel gives up and reports a timeout.
+  p.wait_limit_ns = 0;
+  p.test_stall_stage = -1;
+  if (const char *env = getenv("GMM_TEST_WAIT_LIMIT_NS")) p.wait_limit_ns = strtoull(env, nullptr, 10);
+  if (const char *env = getenv("GMM_TEST_STALL_STAGE")) p.test_stall_stage = atoi(env);
 }
 
 // Stage-ring depth of a grouped-kernel launch with G groups in a layout: what the budget

@@ -91,6 +91,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   const uint32_t bias_stage = w_ring + ST * G::kWBytes;
 
   if (tid == 0) {
+    set_wait_limit(p.wait_limit_ns);
     for (uint32_t s = 0; s < ST; ++s) {
       mbar_init(smem_addr(&ctl.full[s]), 1);
       mbar_init(smem_addr(&ctl.empty[s]), 1);

@@ -164,7 +164,7 @@ constexpr uint32_t kStatusBadExpert = 2u;
 constexpr uint32_t kStatusTimeout = 4u;
 constexpr uint32_t kStatusTooLarge = 8u;
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // give up on a pipeline wait after 2 s
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // give up on a pipeline wait after 2 s (by default)
 constexpr uint32_t kSuspendNs = 1u << 20;            // longest suspension of one mbarrier test (~1 ms)
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // and on draining copies after 0.2 s
 
@@ -235,6 +235,12 @@ struct alignas(128) GmmParams {
   // Both are multiples of 256, so a tile's weight rows lie in one plane.
   int plane_s0;
   int plane_s1;
+  // Test hooks of the timeout path, both off (0 / -1) in normal use: a shorter limit on
+  // every pipeline wait, and (one-CTA bf16 kernel) a stage, counted from 0 over the
+  // launch, for which the producer issues neither copies nor its arrival, so that the
+  // stage never fills and the waits behind it give up with nothing in flight.
+  unsigned long long wait_limit_ns;
+  int test_stall_stage;
 };
 
 struct __align__(32) Tile {
@@ -282,8 +288,17 @@ struct Ring {
   }
 };
 
+// The CTA's limit on one pipeline wait: kWaitLimitNs, unless the launch asks for a
+// shorter one (GmmParams::wait_limit_ns, a test of the timeout path).  Set by thread 0
+// before the kernel's first block-wide barrier.
+__shared__ uint64_t s_wait_limit_ns;
+
+__device__ __forceinline__ void set_wait_limit(uint64_t requested) {
+  s_wait_limit_ns = requested != 0 ? requested : kWaitLimitNs;
+}
+
 // Bounded wait on an mbarrier phase.  Returns false (and raises the CTA's abort
-// flag) after kWaitLimitNs, or as soon as another role has aborted.  Each test may
+// flag) after s_wait_limit_ns, or as soon as another role has aborted.  Each test may
 // suspend the thread for up to kSuspendNs (it resumes as soon as the phase
 // completes), so a waiting role does not spin on the issue slots that the dequant,
 // epilogue and MMA-issuing warps of its SM need; the abort flag and the clock are
@@ -294,7 +309,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > s_wait_limit_ns) {
       *abort = 1;
       return false;
     }
@@ -318,7 +333,7 @@ __device__ __forceinline__ bool wait_phase_cluster(uint32_t bar, uint32_t parity
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > s_wait_limit_ns) {
       *abort = 1;
       return false;
     }
@@ -620,6 +635,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
   uint32_t *prefix = reinterpret_cast<uint32_t *>(dyn_smem + (epi_ring + kEpiBytes<kInt4> - dyn_base));
 
   if (tid == 0) {
+    set_wait_limit(p.wait_limit_ns);
     for (uint32_t s = 0; s < ST; ++s) {
       mbar_init(smem_addr(&ctl.full[s]), kFullArrivals);
       mbar_init(smem_addr(&ctl.empty[s]), 1);
@@ -691,6 +707,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
 
       const uint32_t m_rows = __ldg(p.a_offsets + p.num_groups);   // rows of one A plane
       Ring rt;
+      int issued_stages = 0;    // stages of this launch so far (the timeout test's stall counts them)
       uint32_t pending = 0;     // bit s: stage s has copies whose completion this thread has not seen
       uint32_t pend_phase = 0;  // bit s: the phase in which they complete
       bool ok = true;
@@ -779,9 +796,13 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
           for (int i = 0; i < kMaps; ++i) tensormap_acquire(slot + i * 128);
           maps_acquired = true;
         }
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = 0; kb < KB; ++kb, ++issued_stages) {
           const uint32_t full_local = smem_addr(&ctl.full[rt.slot]);
           if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
+          if (!kPair && !kInt4 && issued_stages == p.test_stall_stage) {   // test hook: this stage never fills
+            rt.next(ST);
+            continue;
+          }
           if (rank == 0) mbar_arrive_expect_tx(full_local, tx);
           const int32_t r = static_cast<int32_t>(ti.row0 + rank * my_tok + plane_row0(p, ti.n0, m_rows));
           const CUtensorMap *tok = tok_maps + (my_tok / 16u - 1u);   // copies my_tok rows high
@@ -887,7 +908,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
               const uint64_t t0 = global_timer_ns();
               bool issued = false;
               while (!issued) {
-                if (*abort || global_timer_ns() - t0 > kWaitLimitNs) break;
+                if (*abort || global_timer_ns() - t0 > s_wait_limit_ns) break;
                 issued = mma_stage_ts_x8<kPair>(full, rt.phase, 4u, d_tmem, a0, a0 + kAccCols, b0, b0 + tok_step,
                                                 t_hi, idesc, kb != 0, empty);
               }
