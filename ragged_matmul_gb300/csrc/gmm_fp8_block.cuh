@@ -181,6 +181,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
       bool ok = true;
       const uint64_t t_desc0 = smem_desc_k_sw128(t_ring);
       const uint64_t w_desc0 = smem_desc_k_sw128(w_ring);
+      const uint32_t t_lo = static_cast<uint32_t>(t_desc0), t_hi = static_cast<uint32_t>(t_desc0 >> 32);
+      const uint32_t w_lo = static_cast<uint32_t>(w_desc0), w_hi = static_cast<uint32_t>(w_desc0 >> 32);
       const uint32_t idesc = idesc_e4m3_f32(kBwCtaTok, kBwRows);
       for (uint32_t t = unit0; t < total && ok; t += units) {
         int in_block = 0;   // stage within its scale block (s % SPB, counted)
@@ -193,16 +195,14 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
           const bool staged = __all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort));
           if (!staged) { ok = false; break; }
           tc_fence_after_sync();
-          const uint64_t a_desc = t_desc0 + ((rt.slot * kBwTBytes) >> 4);
-          const uint64_t b_desc = w_desc0 + ((rt.slot * G::kWBytes) >> 4);
-          const uint32_t d_tmem = tmem_base + pb * kBwRows;
-#pragma unroll
-          for (int k = 0; k < 4; ++k)   // K = 32 e4m3 (32 bytes) per MMA
-            mma_f8(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc, (in_block | k) != 0);
-          mma_commit(smem_addr(&ctl.empty[rt.slot]));
+          // Four MMAs of K = 32 e4m3 (32 bytes) each, the stage's commit and, at the end of
+          // a K block, the commit that hands its partial to the promotion warps.
+          const bool block_end = in_block == SPB - 1 || s == KS - 1;
+          mma_stage_f8_x4(tmem_base + pb * kBwRows, t_lo + ((rt.slot * kBwTBytes) >> 4), t_hi,
+                          w_lo + ((rt.slot * G::kWBytes) >> 4), w_hi, idesc, in_block != 0,
+                          smem_addr(&ctl.empty[rt.slot]), block_end, smem_addr(&part_full[pb]));
           rt.next(ST);
-          if (in_block == SPB - 1 || s == KS - 1) {   // the block's partial is complete
-            mma_commit(smem_addr(&part_full[pb]));
+          if (block_end) {
             if (++pb == kBwBufs) {
               pb = 0;
               pb_phase ^= 1u;

@@ -629,6 +629,39 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
       : "memory");
 }
 
+// One stage of the per-K-block e4m3 kernel (128 of K): four kind::f8f6f4 MMAs, A and B
+// in shared memory (descriptors whose low words are a_lo and b_lo and high words a_hi
+// and b_hi; +32 bytes per step of K = 32), then a commit of them to `empty` and, when
+// `block_end` is non-zero, a second commit to `part` (the K block's partial is
+// complete).  One elected lane issues everything; the issuing warp shares its SM
+// sub-partition with the promotion warps.  `accumulate` = 0 for the first stage of a
+// K block: its first MMA then overwrites the partial buffer.  A descriptor step adds
+// to the low word only (shared-memory addresses >> 4 stay below 2^14: no carry).
+__device__ __forceinline__ void mma_stage_f8_x4(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                                uint32_t b_hi, uint32_t idesc, uint32_t accumulate, uint32_t empty,
+                                                uint32_t block_end, uint32_t part) {
+  asm volatile(
+      "{\n\t.reg .pred e, p, t, q;\n\t.reg .b32 l, x, y;\n\t.reg .b64 a, b;\n\t"
+      "elect.sync l|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "setp.eq.b32 t, %6, %6;\n\t"
+      "setp.ne.b32 q, %8, 0;\n\t"
+      "mov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %5, p;\n\t"
+      "add.u32 x, %1, 2;\n\tadd.u32 y, %3, 2;\n\tmov.b64 a, {x, %2};\n\tmov.b64 b, {y, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %5, t;\n\t"
+      "add.u32 x, %1, 4;\n\tadd.u32 y, %3, 4;\n\tmov.b64 a, {x, %2};\n\tmov.b64 b, {y, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %5, t;\n\t"
+      "add.u32 x, %1, 6;\n\tadd.u32 y, %3, 6;\n\tmov.b64 a, {x, %2};\n\tmov.b64 b, {y, %4};\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], a, b, %5, t;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t"
+      "and.pred q, q, e;\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate), "r"(empty), "r"(block_end),
+      "r"(part)
+      : "memory");
+}
+
 // ----------------------------------------------------------------- descriptors
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA with
