@@ -169,6 +169,20 @@ void fill_common(gmm_ctx *h, GmmParams &p, void *c, const uint32_t *a_offsets, c
   p.num_experts = h->num_experts;
   p.N = N;
   p.K = K;
+  // C as a TMA store target: {N, 2^31} rows (the real row count is on the device; the
+  // kernel only stores whole 32-row chunks inside a group through it), box 32 x 32,
+  // 64-byte swizzle (the epilogue staging layout).  Without it every chunk takes the
+  // 16-byte store path.
+  p.c_tma = 0;
+  if (h->encode != nullptr && aligned16(c)) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), 1ull << 31};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2u};
+    const cuuint32_t box[2] = {32, 32}, estr[2] = {1, 1};
+    p.c_tma = h->encode(&p.c_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
+  if (const char *env = getenv("GMM_TMA_STORE")) p.c_tma = p.c_tma && atoi(env) != 0;   // tuning override
   const double block_bytes = static_cast<double>(max_tok) * K * 2.0;
   const double band = kBandBytes / block_bytes;
   p.tok_band = band < 1.0 ? 1 : (band > 1e6 ? 1000000 : static_cast<int>(band));

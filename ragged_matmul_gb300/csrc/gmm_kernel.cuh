@@ -193,6 +193,7 @@ struct Geom {
 struct alignas(128) GmmParams {
   CUtensorMap w_map;       // bf16 path: B {K, N, E}, box {64, 128, 1}, 128 B swizzle
                            // 4-bit path: packed words {K/8, N, E}, box {8, 128, 1}, no swizzle
+  CUtensorMap c_map;       // C bf16 {N, 2^31 rows}, box {32, 32}, 64-byte swizzle (valid when c_tma)
   CUtensorMap tok_map;     // A bf16 {K, rows}, box {64, 128}; each CTA derives from it one map per
                            // box height (16, 32, ... rows) and patches the row extent on the device
   __nv_bfloat16 *c;
@@ -214,6 +215,7 @@ struct alignas(128) GmmParams {
   uint32_t *tile_counter;        // workspace, 8-byte aligned, zero between launches: [0..1] one 64-bit claim
                                  // word (tiles claimed from the front | from the back << 32), [2] CTAs finished
   int cache_hints;               // 1: L2 eviction priorities on the TMA loads (see the producer)
+  int c_tma;                     // 1: whole 32-row chunks of C leave through c_map (TMA stores)
   // Optional elementwise epilogue on the fp32 result before it is rounded to bf16:
   //   y = act(acc + bias[e, n]) * row_scale[r]      (each part optional)
   const __nv_bfloat16 *epi_bias;   // [E, N] or null
@@ -985,6 +987,10 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
     // With 8 epilogue warps, warps 2 .. 5 take the even 32-row chunks of a tile and
     // warps 6 .. 9 the odd ones.
     const uint32_t esub = static_cast<uint32_t>(warp - 2) >> 2, nsub = n_epi >> 2;
+    // Staging buffers per warp: two with 4 epilogue warps (bf16 / e4m3: 16 KB in all), one
+    // with 8, and one in the 4-bit kernel (8 KB for its 4 warps).
+    const uint32_t nbuf = kEpiBytes<kInt4> / (n_epi * kEpiRows * kEpiRowBytes);
+    uint32_t chunk_ctr = 0, outstanding = 0, last_buf = 0;   // this warp's TMA-store bookkeeping
     const uint32_t acc_empty0 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[0]), 0) : smem_addr(&ctl.acc_empty[0]);
     const uint32_t acc_empty1 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[1]), 0) : smem_addr(&ctl.acc_empty[1]);
     uint32_t acc = 0, acc_phase = 0;
@@ -1051,16 +1057,24 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
       // may read TMEM columns past ntok (inside the accumulator); those rows are not
       // stored.  The row factors of rows c0 .. c0 + 31 are in rs[0] / sc[0] and move
       // down one register every chunk.
-      const uint32_t stg = epi_ring + static_cast<uint32_t>(warp - 2) * (kEpiRows * kEpiRowBytes);
+      const uint32_t stg0 = epi_ring + static_cast<uint32_t>(warp - 2) * nbuf * (kEpiRows * kEpiRowBytes);
       // stmatrix: thread l addresses row 8g + (l % 8) of matrix i = l / 8 (block i).
       const uint32_t st_row = static_cast<uint32_t>(lane) & 7u, st_blk = static_cast<uint32_t>(lane) >> 3;
-      const uint8_t *stg_ptr = dyn_smem + (stg - dyn_base);
       for (uint32_t c0 = esub * 32u; c0 < ti.ntok; c0 += 32u * nsub) {
         uint32_t va[16], vb[16];
         tmem_ld_16x256b_x4(taddr + c0, va);
         tmem_ld_16x256b_x4(taddr + (16u << 16) + c0, vb);
+        // Staging buffer of this chunk; a TMA store that still reads it must finish first
+        // (the newest group may stay in flight while it reads the other buffer).
+        const uint32_t b = nbuf == 2u ? (chunk_ctr & 1u) : 0u;
+        const uint32_t stg = stg0 + b * (kEpiRows * kEpiRowBytes);
+        if (lane == 0 && ((outstanding >> b) & 1u)) {
+          if (last_buf == b) bulk_wait_read<0>(); else bulk_wait_read<1>();
+        }
+        outstanding &= ~(1u << b);
+        ++chunk_ctr;
         tmem_ld_wait();
-        __syncwarp();   // the previous chunk's row reads of the tile are done
+        __syncwarp();   // the previous chunk's row reads are done, and the buffer is free
 #pragma unroll
         for (uint32_t g = 0; g < 4; ++g) {
           // Row factors of this thread's two rows of the group.
@@ -1093,14 +1107,31 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
           const uint32_t row = 8 * g + st_row;
           stmatrix_x4_trans(stg + row * kEpiRowBytes + ((st_blk ^ ((row >> 1) & 3u)) << 4), w[0], w[1], w[2], w[3]);
         }
-        __syncwarp();
+        if (p.c_tma && c0 + 32u <= ti.nrows) {
+          // A whole chunk of the group's rows: the staging tile is laid out in TMA's
+          // 64-byte swizzle, so one store of the 32 x 32 box takes it to C (columns past
+          // N are clipped by the map).  The warp's memory queue then holds no C stores.
+          fence_async_smem();   // this thread's stmatrix writes, before the async proxy reads them
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.c_map, stg, static_cast<int32_t>(ncta), static_cast<int32_t>(ti.row0 + c0));
+            bulk_commit();
+          }
+          outstanding |= 1u << b;
+          last_buf = b;
+        } else {
+          // The group's last, partial chunk (a TMA store would also write the rows after
+          // the group's end): 16-byte stores masked to the group's rows.
+          __syncwarp();
+          const uint8_t *stg_ptr = dyn_smem + (stg - dyn_base);
 #pragma unroll
-        for (uint32_t pass = 0; pass < 4; ++pass) {
-          const uint32_t rl = pass * 8u + rsub;   // row within the chunk
-          const uint32_t row = c0 + rl;           // row within the tile
-          const uint4 out =
-              *reinterpret_cast<const uint4 *>(stg_ptr + rl * kEpiRowBytes + ((seg ^ ((rl >> 1) & 3u)) << 4));
-          if (cols_ok && row < ti.nrows) *reinterpret_cast<uint4 *>(crow + static_cast<size_t>(row) * p.N) = out;
+          for (uint32_t pass = 0; pass < 4; ++pass) {
+            const uint32_t rl = pass * 8u + rsub;   // row within the chunk
+            const uint32_t row = c0 + rl;           // row within the tile
+            const uint4 out =
+                *reinterpret_cast<const uint4 *>(stg_ptr + rl * kEpiRowBytes + ((seg ^ ((rl >> 1) & 3u)) << 4));
+            if (cols_ok && row < ti.nrows) *reinterpret_cast<uint4 *>(crow + static_cast<size_t>(row) * p.N) = out;
+          }
         }
 #pragma unroll
         for (int q = 0; q + 1 < kRowRegs; ++q) {
@@ -1119,6 +1150,8 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    // The staging tiles must stay readable, and C written, before this warp moves on.
+    if (lane == 0) bulk_wait_all();
   } else if (kInt4 && warp == 6) {
     // ------------------------------------------------------------ packed-slab producer (4-bit)
     if (lane == 0 && total > 0) {
