@@ -280,6 +280,13 @@ int configure_fp8_block(gmm_variant *v, int optin, int sm_smem, int device_optin
   auto kernel = gmm::gmm_fp8_block_kernel;
   cudaFuncAttributes attr;
   if (cudaFuncGetAttributes(&attr, reinterpret_cast<const void *>(kernel)) != cudaSuccess) return GMM_ERR_CUDA;
+  // The kernel moves registers from its first warpgroup to the promotion warpgroups
+  // (setmaxnreg).  The increase waits until the CTA's pool, the launch's registers a
+  // thread times its threads, covers it, so a build whose register count left the pool
+  // short would never finish: refuse it here instead.
+  if (static_cast<long>(attr.numRegs) * gmm::kBwThreads <
+      128L * gmm::kBwRegsLow + 32L * gmm::kBwPromoWarps * gmm::kBwRegsHigh)
+    return GMM_ERR_UNSUPPORTED;
   const long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024 - gmm::kBwBiasBytes;
   v->stages = static_cast<int>(budget / static_cast<long>(G::kStageBytes));
   if (v->stages > gmm::kMaxStages) v->stages = gmm::kMaxStages;

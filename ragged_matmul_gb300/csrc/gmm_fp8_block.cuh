@@ -19,27 +19,32 @@
 // one value per thread, and with gn a multiple of 32 the weight scale is one value per
 // 32-column TMEM load.  A promotion is one multiply-add per element.
 //
-// One CTA per tile of 128 token rows.  A K block of 128 is one stage, and the MMA
-// warp's own path through a stage (the partial-buffer wait, the stage wait, four
-// MMA issues, two commits; about 1,100 cycles under load) is longer than the
-// stage's tensor work (335 to 670 cycles), so the copies are not what bounds it.
+// One CTA per tile of 128 token rows.  A K block of 128 is one stage, 512 cycles of
+// tensor work at the e4m3 rate.  The promotion of a block must fit in that time, and
+// two partial buffers leave it little slack: the MMA of block kb + 2 waits for the
+// release of block kb.  So a promotion warp reads a partial 64 columns per TMEM wait
+// (two waits per block), releases the buffer as soon as its last load has landed,
+// before that half's multiply-adds, and folds two columns per paired fp32 FMA.
 // Tried and measured no better: 192- and 128-row tiles with 12 promotion warps or
 // four partial buffers, and a CTA-pair form (cta_group::2), whose every block
 // crosses CTAs twice.
 //
-// Roles (320 threads per CTA):
+// Roles (384 threads per CTA, three warpgroups):
 //   warp 0       TMA producer: per stage (128 of K) a 128-row token slab (16 KB) and
 //                the tile's 256 weight rows (32 KB), 128-byte swizzled.
 //   warp 1       TMEM allocation (512 columns: two 256-column partial buffers) and the
 //                MMA issue (kind::f8f6f4, M = 128, N = 256, 4 MMAs per stage).
-//   warps 2..9   promotion and epilogue: warp w reads TMEM lane quadrant w % 4 and
-//                weight columns 128 * ((w - 2) / 4) .. + 128 of each partial; every
+//   warps 2, 3   idle.
+//   warps 4..11  promotion and epilogue: warp w reads TMEM lane quadrant w % 4 and
+//                weight columns 128 * ((w - 4) / 4) .. + 128 of each partial; every
 //                thread owns one token row and 128 running sums.  After a tile's last
 //                block they apply the epilogue and store their row's 128 columns.
 //
-// Registers: the warps of a CTA spread over the SM's four sub-partitions, 16K
-// registers each, so ten warps leave 168 registers a thread, of which 128 are running
-// sums; the partial is read 16 columns per TMEM wait.
+// Registers: the launch gives every thread 168 (384 x 168 fills the register file).
+// The first warpgroup then drops to 56 a thread and the two promotion warpgroups take
+// 224: 128 running sums and a 64-column piece of a partial.  The host checks the
+// launch register count before the first launch, since an increase the pool cannot
+// cover would wait forever.
 //
 // Scheduling is the grouped kernel's static one (the same group scan and tile decode);
 // every wait is bounded as there.
@@ -50,13 +55,21 @@
 namespace gmm {
 
 constexpr uint32_t kBwPromoWarps = 8;              // two per TMEM lane quadrant
-constexpr int kBwThreads = 32 * (2 + kBwPromoWarps);
+constexpr uint32_t kBwFirstPromo = 4;              // warps 0..3: producer, MMA, two idle
+constexpr int kBwThreads = 32 * (kBwFirstPromo + kBwPromoWarps);
+constexpr uint32_t kBwLaunchRegs = 168;            // registers a thread at launch (the kernel's count)
+constexpr uint32_t kBwRegsLow = 56;                // producer / MMA warpgroup after reallocation
+constexpr uint32_t kBwRegsHigh = 224;              // promotion warpgroups after reallocation
+static_assert(kBwLaunchRegs * kBwThreads <= 65536, "the launch fits the register file");
+static_assert(128 * kBwRegsLow + 32 * kBwPromoWarps * kBwRegsHigh <= kBwLaunchRegs * kBwThreads,
+              "the increase is covered by the launch's pool and the decrease");
 constexpr uint32_t kBwCtaTok = 128;                // token rows per CTA (its TMEM lanes)
 constexpr uint32_t kBwRows = 256;                  // weight rows per tile (MMA N)
 constexpr uint32_t kBwBufs = kTmemCols / kBwRows;  // partial buffers in TMEM
 constexpr uint32_t kBwTBytes = kBwCtaTok * 128;    // token slab of a stage: 128 rows x 128 e4m3
 constexpr uint32_t kBwCols = kBwRows * 4 / kBwPromoWarps;   // weight columns per promotion warp
-constexpr uint32_t kBwPiece = 16;                  // columns per TMEM wait
+constexpr uint32_t kBwPiece = 64;                  // columns per TMEM wait
+static_assert(kBwCols == 2 * kBwPiece, "a block is read in two pieces");
 constexpr int kBwBiasBytes = kBwPromoWarps * kBwCols * 2;   // each promotion warp's bias columns (bf16)
 
 struct BwGeom {
@@ -67,8 +80,8 @@ struct BwGeom {
   static constexpr uint32_t kStageBytes = kBwTBytes + kWBytes;   // shared memory per stage
 };
 
-// Each promotion thread keeps kBwCols running sums and a 32-column piece of a partial
-// in registers.
+// Each promotion thread keeps kBwCols running sums and a kBwPiece-column piece of a
+// partial in registers.
 __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __grid_constant__ GmmParams p) {
   using G = BwGeom;
   __shared__ Ctrl ctl;
@@ -126,99 +139,106 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   const uint32_t unit0 = blockIdx.x;   // static share: tiles unit0, unit0 + units, ...
   const uint32_t units = gridDim.x;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
-    // The CTA's token map: the host's map with the row extent patched to a_offsets[G]
-    // (rows past the end of A are zero-filled) and 128-row boxes.
-    uint8_t *slot = p.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlotBytes;
-    if (total > 0 && lane == 0) {
-      const uint4 *src = reinterpret_cast<const uint4 *>(&p.tok_map);
-      uint4 *dst = reinterpret_cast<uint4 *>(slot);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dst[i] = src[i];
-      tensormap_set_dim1(dst, __ldg(p.a_offsets + p.num_groups));
-      tensormap_set_box1(dst, kBwCtaTok);
-      tensormap_release();
-      tensormap_acquire(slot);
-      const CUtensorMap *tok = reinterpret_cast<const CUtensorMap *>(slot);
-      prefetch_tensormap(&p.w_map);
-      const uint64_t pol_first = l2_policy_evict_first();
-      const uint64_t pol_last = l2_policy_evict_last();
-      const uint64_t pol_normal = l2_policy_evict_normal();
-      Ring rt;
-      uint32_t pending = 0, pend_phase = 0;
-      bool ok = true;
-      for (uint32_t t = unit0; t < total && ok; t += units) {
-        const Tile ti = decode_tile<G>(t, prefix, p);
-        const uint64_t w_pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
-        const uint64_t t_pol = p.cache_hints ? pol_last : pol_normal;
-        const int32_t t_row = static_cast<int32_t>(ti.row0);
-        const int32_t w_row = static_cast<int32_t>(ti.n0);
-        for (int s = 0; s < KS; ++s) {
-          const uint32_t full = smem_addr(&ctl.full[rt.slot]);
-          if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
-          mbar_arrive_expect_tx(full, G::kStageBytes);
-          const int32_t k0 = s * kBK;
-          tma_load_2d_hint(t_ring + rt.slot * kBwTBytes, tok, full, k0, t_row, t_pol);
-          tma_load_3d_hint(w_ring + rt.slot * G::kWBytes, &p.w_map, full, k0, w_row, ti.e, w_pol);
-          pending |= 1u << rt.slot;
-          pend_phase = (pend_phase & ~(1u << rt.slot)) | (rt.phase << rt.slot);
-          rt.next(ST);
+  // Register reallocation: each setmaxnreg is executed by a whole warpgroup at one
+  // place in the code, and the code after it is compiled for the new budget.  The
+  // first warpgroup gives, the promotion warpgroups take.
+  if (warp < static_cast<int>(kBwFirstPromo)) {
+    warpgroup_regs_dec<kBwRegsLow>();
+    if (warp == 0) {
+      // ------------------------------------------------------------ TMA producer
+      // The CTA's token map: the host's map with the row extent patched to a_offsets[G]
+      // (rows past the end of A are zero-filled) and 128-row boxes.
+      uint8_t *slot = p.map_slots + static_cast<size_t>(blockIdx.x) * kMapSlotBytes;
+      if (total > 0 && lane == 0) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(&p.tok_map);
+        uint4 *dst = reinterpret_cast<uint4 *>(slot);
+  #pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = src[i];
+        tensormap_set_dim1(dst, __ldg(p.a_offsets + p.num_groups));
+        tensormap_set_box1(dst, kBwCtaTok);
+        tensormap_release();
+        tensormap_acquire(slot);
+        const CUtensorMap *tok = reinterpret_cast<const CUtensorMap *>(slot);
+        prefetch_tensormap(&p.w_map);
+        const uint64_t pol_first = l2_policy_evict_first();
+        const uint64_t pol_last = l2_policy_evict_last();
+        const uint64_t pol_normal = l2_policy_evict_normal();
+        Ring rt;
+        uint32_t pending = 0, pend_phase = 0;
+        bool ok = true;
+        for (uint32_t t = unit0; t < total && ok; t += units) {
+          const Tile ti = decode_tile<G>(t, prefix, p);
+          const uint64_t w_pol = (p.cache_hints && ti.single_block) ? pol_first : pol_normal;
+          const uint64_t t_pol = p.cache_hints ? pol_last : pol_normal;
+          const int32_t t_row = static_cast<int32_t>(ti.row0);
+          const int32_t w_row = static_cast<int32_t>(ti.n0);
+          for (int s = 0; s < KS; ++s) {
+            const uint32_t full = smem_addr(&ctl.full[rt.slot]);
+            if (!wait_phase(smem_addr(&ctl.empty[rt.slot]), rt.phase ^ 1u, abort)) { ok = false; break; }
+            mbar_arrive_expect_tx(full, G::kStageBytes);
+            const int32_t k0 = s * kBK;
+            tma_load_2d_hint(t_ring + rt.slot * kBwTBytes, tok, full, k0, t_row, t_pol);
+            tma_load_3d_hint(w_ring + rt.slot * G::kWBytes, &p.w_map, full, k0, w_row, ti.e, w_pol);
+            pending |= 1u << rt.slot;
+            pend_phase = (pend_phase & ~(1u << rt.slot)) | (rt.phase << rt.slot);
+            rt.next(ST);
+          }
+        }
+        if (!ok) {
+          // Let the copies already issued land before the CTA can exit.
+          for (uint32_t s = 0; s < ST; ++s)
+            if (pending & (1u << s)) wait_phase_for(smem_addr(&ctl.full[s]), (pend_phase >> s) & 1u, kDrainLimitNs);
+          atomicOr(p.status, kStatusTimeout);
         }
       }
-      if (!ok) {
-        // Let the copies already issued land before the CTA can exit.
-        for (uint32_t s = 0; s < ST; ++s)
-          if (pending & (1u << s)) wait_phase_for(smem_addr(&ctl.full[s]), (pend_phase >> s) & 1u, kDrainLimitNs);
-        atomicOr(p.status, kStatusTimeout);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issue (whole warp, one elected lane)
-    if (total > 0) {
-      Ring rt;
-      uint32_t pb = 0, pb_phase = 0;   // partial buffer of the current block, and its use parity
-      bool ok = true;
-      const uint64_t t_desc0 = smem_desc_k_sw128(t_ring);
-      const uint64_t w_desc0 = smem_desc_k_sw128(w_ring);
-      const uint32_t t_lo = static_cast<uint32_t>(t_desc0), t_hi = static_cast<uint32_t>(t_desc0 >> 32);
-      const uint32_t w_lo = static_cast<uint32_t>(w_desc0), w_hi = static_cast<uint32_t>(w_desc0 >> 32);
-      const uint32_t idesc = idesc_e4m3_f32(kBwCtaTok, kBwRows);
-      for (uint32_t t = unit0; t < total && ok; t += units) {
-        int in_block = 0;   // stage within its scale block (s % SPB, counted)
-        for (int s = 0; s < KS; ++s, in_block = (in_block + 1 == SPB) ? 0 : in_block + 1) {
-          if (in_block == 0) {   // a new block starts in a free partial buffer
-            const bool free_ =
-                __all_sync(0xffffffffu, wait_phase(smem_addr(&part_empty[pb]), pb_phase ^ 1u, abort));
-            if (!free_) { ok = false; break; }
-          }
-          const bool staged = __all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort));
-          if (!staged) { ok = false; break; }
-          tc_fence_after_sync();
-          // Four MMAs of K = 32 e4m3 (32 bytes) each, the stage's commit and, at the end of
-          // a K block, the commit that hands its partial to the promotion warps.
-          const bool block_end = in_block == SPB - 1 || s == KS - 1;
-          mma_stage_f8_x4(tmem_base + pb * kBwRows, t_lo + ((rt.slot * kBwTBytes) >> 4), t_hi,
-                          w_lo + ((rt.slot * G::kWBytes) >> 4), w_hi, idesc, in_block != 0,
-                          smem_addr(&ctl.empty[rt.slot]), block_end, smem_addr(&part_full[pb]));
-          rt.next(ST);
-          if (block_end) {
-            if (++pb == kBwBufs) {
-              pb = 0;
-              pb_phase ^= 1u;
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issue (whole warp, one elected lane)
+      if (total > 0) {
+        Ring rt;
+        uint32_t pb = 0, pb_phase = 0;   // partial buffer of the current block, and its use parity
+        bool ok = true;
+        const uint64_t t_desc0 = smem_desc_k_sw128(t_ring);
+        const uint64_t w_desc0 = smem_desc_k_sw128(w_ring);
+        const uint32_t t_lo = static_cast<uint32_t>(t_desc0), t_hi = static_cast<uint32_t>(t_desc0 >> 32);
+        const uint32_t w_lo = static_cast<uint32_t>(w_desc0), w_hi = static_cast<uint32_t>(w_desc0 >> 32);
+        const uint32_t idesc = idesc_e4m3_f32(kBwCtaTok, kBwRows);
+        for (uint32_t t = unit0; t < total && ok; t += units) {
+          int in_block = 0;   // stage within its scale block (s % SPB, counted)
+          for (int s = 0; s < KS; ++s, in_block = (in_block + 1 == SPB) ? 0 : in_block + 1) {
+            if (in_block == 0) {   // a new block starts in a free partial buffer
+              const bool free_ =
+                  __all_sync(0xffffffffu, wait_phase(smem_addr(&part_empty[pb]), pb_phase ^ 1u, abort));
+              if (!free_) { ok = false; break; }
+            }
+            const bool staged = __all_sync(0xffffffffu, wait_phase(smem_addr(&ctl.full[rt.slot]), rt.phase, abort));
+            if (!staged) { ok = false; break; }
+            tc_fence_after_sync();
+            // Four MMAs of K = 32 e4m3 (32 bytes) each, the stage's commit and, at the end of
+            // a K block, the commit that hands its partial to the promotion warps.
+            const bool block_end = in_block == SPB - 1 || s == KS - 1;
+            mma_stage_f8_x4(tmem_base + pb * kBwRows, t_lo + ((rt.slot * kBwTBytes) >> 4), t_hi,
+                            w_lo + ((rt.slot * G::kWBytes) >> 4), w_hi, idesc, in_block != 0,
+                            smem_addr(&ctl.empty[rt.slot]), block_end, smem_addr(&part_full[pb]));
+            rt.next(ST);
+            if (block_end) {
+              if (++pb == kBwBufs) {
+                pb = 0;
+                pb_phase ^= 1u;
+              }
             }
           }
         }
+        if (!ok && lane == 0) atomicOr(p.status, kStatusTimeout);
       }
-      if (!ok && lane == 0) atomicOr(p.status, kStatusTimeout);
     }
   } else {
+    warpgroup_regs_inc<kBwRegsHigh>();
     // ------------------------------------------------------------ promotion and epilogue
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
-    const uint32_t part = static_cast<uint32_t>(warp - 2) >> 2;   // which kBwCols of the tile's columns
+    const uint32_t part = static_cast<uint32_t>(warp - kBwFirstPromo) >> 2;   // which kBwCols of the tile's columns
     // This thread's token row in the tile.
     const uint32_t trow = quad * 32 + static_cast<uint32_t>(lane);
-    __nv_bfloat16 *bias_s = reinterpret_cast<__nv_bfloat16 *>(dyn_smem + (bias_stage - dyn_base)) + (warp - 2) * kBwCols;
+    __nv_bfloat16 *bias_s = reinterpret_cast<__nv_bfloat16 *>(dyn_smem + (bias_stage - dyn_base)) + (warp - kBwFirstPromo) * kBwCols;
     const int wcols = p.w_scale_cols;
     uint32_t pb = 0, pb_phase = 0;
     bool ok = true;
@@ -264,19 +284,27 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
         tc_fence_after_sync();
         const uint32_t taddr = tmem_base + ((quad * 32u) << 16) + pb * kBwRows + part * kBwCols;
 #pragma unroll
-        for (int c = 0; c < static_cast<int>(kBwCols / kBwPiece); ++c) {
-          uint32_t v[16];
-          tmem_ld_x16(taddr + kBwPiece * c, v);
+        for (int h = 0; h < static_cast<int>(kBwCols / kBwPiece); ++h) {
+          uint32_t v0[32], v1[32];
+          tmem_ld_x32(taddr + kBwPiece * h, v0);
+          tmem_ld_x32(taddr + kBwPiece * h + 32, v1);
           tmem_ld_wait();
-          const float f = isv * wsv[c * kBwPiece / 32];
+          if (h == static_cast<int>(kBwCols / kBwPiece) - 1) {
+            // Every load of the block has landed: release the buffer before the last
+            // piece's multiply-adds.  Relaxed: the next block's scale loads just issued
+            // stay in flight instead of being waited for.
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_relaxed(smem_addr(&part_empty[pb]));
+          }
+          const float f0 = isv * wsv[2 * h], f1 = isv * wsv[2 * h + 1];
+          float *a = acc + kBwPiece * h;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) acc[kBwPiece * c + j] = fmaf(f, __uint_as_float(v[j]), acc[kBwPiece * c + j]);
+          for (int j = 0; j < 32; j += 2) {
+            fma_f32x2(a[j], a[j + 1], f0, __uint_as_float(v0[j]), __uint_as_float(v0[j + 1]));
+            fma_f32x2(a[32 + j], a[33 + j], f1, __uint_as_float(v1[j]), __uint_as_float(v1[j + 1]));
+          }
         }
-        tc_fence_before_sync();
-        __syncwarp();
-        // Relaxed: the partials' loads are complete, and the next block's scale loads
-        // just issued stay in flight instead of being waited for.
-        if (lane == 0) mbar_arrive_relaxed(smem_addr(&part_empty[pb]));
         if (++pb == kBwBufs) {
           pb = 0;
           pb_phase ^= 1u;

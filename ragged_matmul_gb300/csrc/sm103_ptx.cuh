@@ -312,6 +312,45 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&v)[16]) {
       : "r"(taddr));
 }
 
+// The same for 32 columns.
+__device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]),
+        "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]),
+        "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
+// Per-thread register budget of the calling warpgroup: every warp of the warpgroup
+// executes the same instruction.  A decrease returns registers to the CTA's pool; an
+// increase waits until the pool (registers a thread at launch x threads) has them.
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void warpgroup_regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+// (d0, d1) = a * (b0, b1) + (d0, d1) in one paired fp32 instruction; each lane is
+// rounded as fmaf.
+__device__ __forceinline__ void fma_f32x2(float &d0, float &d1, float a, float b0, float b1) {
+  asm("{\n\t.reg .b64 x, y, z;\n\t"
+      "mov.b64 x, {%2, %2};\n\t"
+      "mov.b64 y, {%3, %4};\n\t"
+      "mov.b64 z, {%0, %1};\n\t"
+      "fma.rn.f32x2 z, x, y, z;\n\t"
+      "mov.b64 {%0, %1}, z;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a), "f"(b0), "f"(b1));
+}
+
 // 16 TMEM lanes x 32 columns in the 16x256b shape (four repeats of 16 lanes x 8
 // columns).  In repeat j (v[4j] .. v[4j + 3]) thread t holds lane t/4, columns
 // 8j + 2(t%4) and 8j + 2(t%4) + 1 (v[4j], v[4j + 1]), and the same two columns of
