@@ -274,7 +274,8 @@ int configure(gmm_variant *v, int optin, int sm_smem, int device_optin, int num_
   return GMM_OK;
 }
 
-// The per-K-block e4m3 kernel: as many stages as fit, one CTA per SM.
+// The per-K-block e4m3 kernel: as many stages as fit beside the group prefix (sized at
+// each launch, as for the grouped kernel), one CTA per SM.
 int configure_fp8_block(gmm_variant *v, int optin, int sm_smem, int device_optin, int num_sms) {
   using G = gmm::BwGeom;
   auto kernel = gmm::gmm_fp8_block_kernel;
@@ -287,13 +288,20 @@ int configure_fp8_block(gmm_variant *v, int optin, int sm_smem, int device_optin
   if (static_cast<long>(attr.numRegs) * gmm::kBwThreads <
       128L * gmm::kBwRegsLow + 32L * gmm::kBwPromoWarps * gmm::kBwRegsHigh)
     return GMM_ERR_UNSUPPORTED;
-  const long budget = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes) - 1024 - gmm::kBwBiasBytes;
-  v->stages = static_cast<int>(budget / static_cast<long>(G::kStageBytes));
-  if (v->stages > gmm::kMaxStages) v->stages = gmm::kMaxStages;
-  if (v->stages < 2) return GMM_ERR_UNSUPPORTED;
-  const long used = static_cast<long>(v->stages) * G::kStageBytes + gmm::kBwBiasBytes + 1024;
+  const long avail = static_cast<long>(optin) - static_cast<long>(attr.sharedSizeBytes);
+  if (avail <= 0) return GMM_ERR_UNSUPPORTED;
+  v->budget = static_cast<size_t>(avail);
+  v->stage_bytes = G::kStageBytes;
+  v->stage_mult = 1;
+  v->min_stages = 2;
+  v->layouts = 1;
+  v->q_stages[0] = 0;
+  v->fixed[0] = static_cast<size_t>(gmm::kBwFixedBytes);
+  v->stages = stages_for(*v, 1, 0);
+  if (v->stages < v->min_stages) return GMM_ERR_UNSUPPORTED;
+  const long reserve = static_cast<long>(sm_smem) / 2 + 1024;   // more than half an SM: one CTA per SM
   const long cap = static_cast<long>(device_optin) - static_cast<long>(attr.sharedSizeBytes);
-  v->smem = static_cast<size_t>(std::min(cap, std::max(used, static_cast<long>(sm_smem) / 2 + 1024)));
+  v->smem = static_cast<size_t>(std::min(cap, std::max(avail, reserve)));
   if (cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel), cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(v->smem)) != cudaSuccess)
     return GMM_ERR_CUDA;
@@ -304,7 +312,10 @@ int configure_fp8_block(gmm_variant *v, int optin, int sm_smem, int device_optin
 int launch_fp8_block(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   DeviceGuard guard(h->device);
   const gmm_variant &v = h->var_fp8_block;
-  p.num_stages = v.stages;
+  p.num_stages = stages_for(v, p.num_groups, 0);
+  if (p.num_stages < v.min_stages) return GMM_ERR_UNSUPPORTED;   // the prefix leaves no room for the ring
+  if (h->debug)
+    fprintf(stderr, "gmm: launch e4m3 block, %d groups: stages %d packed slots 0\n", p.num_groups, p.num_stages);
   gmm::gmm_fp8_block_kernel<<<v.grid, gmm::kBwThreads, v.smem, stream>>>(p);
   const cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) {

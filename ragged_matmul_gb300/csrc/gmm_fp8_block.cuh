@@ -71,6 +71,10 @@ constexpr uint32_t kBwCols = kBwRows * 4 / kBwPromoWarps;   // weight columns pe
 constexpr uint32_t kBwPiece = 64;                  // columns per TMEM wait
 static_assert(kBwCols == 2 * kBwPiece, "a block is read in two pieces");
 constexpr int kBwBiasBytes = kBwPromoWarps * kBwCols * 2;   // each promotion warp's bias columns (bf16)
+constexpr uint32_t kBwStgBytes = 32 * 64;          // a promotion warp's C staging tile: 32 rows x 32 bf16
+// Dynamic shared memory besides the stage ring and the group prefix: alignment slack,
+// the C staging tiles and the bias columns.
+constexpr int kBwFixedBytes = 1024 + static_cast<int>(kBwPromoWarps * kBwStgBytes) + kBwBiasBytes;
 
 struct BwGeom {
   static constexpr uint32_t kRows = kBwRows;
@@ -85,7 +89,6 @@ struct BwGeom {
 __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __grid_constant__ GmmParams p) {
   using G = BwGeom;
   __shared__ Ctrl ctl;
-  __shared__ uint32_t prefix[kMaxGroups + 1];
   __shared__ uint64_t part_full[kBwBufs];    // a block's partial is in the buffer (MMA commit)
   __shared__ uint64_t part_empty[kBwBufs];   // every promotion warp has read it
   extern __shared__ uint8_t dyn_smem[];
@@ -96,12 +99,15 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   const int SPB = p.kb_stages;            // stages per scale block (gk / 128)
   const int NKB = (KS + SPB - 1) / SPB;   // scale blocks per tile
 
-  // 1024-byte aligned rings.
+  // Dynamic shared memory: the 1024-byte aligned rings, the promotion warps' C staging
+  // tiles, their bias columns and the group prefix.
   const uint32_t dyn_base = smem_addr(dyn_smem);
   const uint32_t ring = (dyn_base + 1023u) & ~1023u;
   const uint32_t t_ring = ring;
   const uint32_t w_ring = ring + ST * kBwTBytes;
-  const uint32_t bias_stage = w_ring + ST * G::kWBytes;
+  const uint32_t c_stage = w_ring + ST * G::kWBytes;
+  const uint32_t bias_stage = c_stage + kBwPromoWarps * kBwStgBytes;
+  uint32_t *prefix = reinterpret_cast<uint32_t *>(dyn_smem + (bias_stage + kBwBiasBytes - dyn_base));
 
   if (tid == 0) {
     set_wait_limit(p.wait_limit_ns);
@@ -234,49 +240,72 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
   } else {
     warpgroup_regs_inc<kBwRegsHigh>();
     // ------------------------------------------------------------ promotion and epilogue
+    const uint32_t pw = static_cast<uint32_t>(warp) - kBwFirstPromo;   // promotion warp 0..7
     const uint32_t quad = static_cast<uint32_t>(warp & 3);
-    const uint32_t part = static_cast<uint32_t>(warp - kBwFirstPromo) >> 2;   // which kBwCols of the tile's columns
+    const uint32_t part = pw >> 2;   // which kBwCols of the tile's columns
     // This thread's token row in the tile.
     const uint32_t trow = quad * 32 + static_cast<uint32_t>(lane);
-    __nv_bfloat16 *bias_s = reinterpret_cast<__nv_bfloat16 *>(dyn_smem + (bias_stage - dyn_base)) + (warp - kBwFirstPromo) * kBwCols;
+    __nv_bfloat16 *bias_s = reinterpret_cast<__nv_bfloat16 *>(dyn_smem + (bias_stage - dyn_base)) + pw * kBwCols;
+    const uint32_t stg = c_stage + pw * kBwStgBytes;   // this warp's C staging tile
+    constexpr int kChunks = static_cast<int>(kBwCols / 32);
     const int wcols = p.w_scale_cols;
+    // A tile's scale rows for this thread: its input scale row and the weight scale rows
+    // of the warp's 32-column chunks (gn is a multiple of 32), as offsets from the
+    // expert's first row (a column past N reads row 0 and is never stored).
+    struct ScaleRows {
+      const float *is_row;
+      const float *ws_e;
+      uint32_t ws_off[kChunks];
+      bool row_ok;
+    };
+    auto scale_rows = [&](const Tile &x) {
+      ScaleRows r;
+      r.row_ok = trow < x.nrows;
+      r.is_row = p.in_scale + static_cast<size_t>((x.row0 + trow) / static_cast<uint32_t>(p.scale_gm)) * p.scale_kb;
+      r.ws_e = p.w_scale + static_cast<size_t>(x.e) * wcols * p.scale_kb;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const uint32_t n = x.n0 + part * kBwCols + 32u * c;
+        r.ws_off[c] = (n < static_cast<uint32_t>(p.N) ? n / static_cast<uint32_t>(p.scale_gn) : 0u) *
+                      static_cast<uint32_t>(p.scale_kb);
+      }
+      return r;
+    };
+    // The scales of block kb + 1 are loaded while block kb is promoted, and those of the
+    // next tile's first block (with the next tile's decode) during this tile's last
+    // block, so no load's latency is waited for between blocks or between tiles.
+    float isn = 0.0f, wsn[kChunks];
+    auto load_scales = [&](const ScaleRows &r, int kb) {
+      isn = r.row_ok ? __ldg(r.is_row + kb) : 0.0f;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) wsn[c] = __ldg(r.ws_e + r.ws_off[c] + kb);
+    };
+    Tile tn{};
+    ScaleRows sr{};   // the scale rows of the tile whose next block's scales are loaded
+    if (unit0 < total) {
+      tn = decode_tile<G>(unit0, prefix, p);
+      sr = scale_rows(tn);
+      load_scales(sr, 0);
+    }
     uint32_t pb = 0, pb_phase = 0;
     bool ok = true;
     for (uint32_t t = unit0; t < total && ok; t += units) {
-      const Tile ti = decode_tile<G>(t, prefix, p);
-      const bool row_ok = trow < ti.nrows;
-      const uint32_t grow = ti.row0 + trow;
+      const Tile ti = tn;
       const uint32_t ncol0 = ti.n0 + part * kBwCols;   // first of this warp's weight columns
-      // Scale rows: this thread's input scales and the warp's 32-column weight scales
-      // (gn is a multiple of 32), loaded one block ahead of their use (loaded in the
-      // same block, their latency was exposed once per block).
-      const float *is_row = p.in_scale + static_cast<size_t>(grow / static_cast<uint32_t>(p.scale_gm)) * p.scale_kb;
-      // Weight scale rows of the 32-column chunks, as offsets from the expert's first
-      // row (a column past N reads row 0 and is never stored).
-      constexpr int kChunks = static_cast<int>(kBwCols / 32);
-      const float *ws_e = p.w_scale + static_cast<size_t>(ti.e) * wcols * p.scale_kb;
-      uint32_t ws_off[kChunks];
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        const uint32_t n = ncol0 + 32u * c;
-        ws_off[c] = (n < static_cast<uint32_t>(p.N) ? n / static_cast<uint32_t>(p.scale_gn) : 0u) *
-                    static_cast<uint32_t>(p.scale_kb);
-      }
       float acc[kBwCols];
 #pragma unroll
       for (int j = 0; j < static_cast<int>(kBwCols); ++j) acc[j] = 0.0f;
-      float isn = row_ok ? __ldg(is_row) : 0.0f, wsn[kChunks];
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) wsn[c] = __ldg(ws_e + ws_off[c]);
       for (int kb = 0; kb < NKB; ++kb) {
         const float isv = isn;
         float wsv[kChunks];
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) wsv[c] = wsn[c];
         if (kb + 1 < NKB) {
-          if (row_ok) isn = __ldg(is_row + kb + 1);
-#pragma unroll
-          for (int c = 0; c < kChunks; ++c) wsn[c] = __ldg(ws_e + ws_off[c] + kb + 1);
+          load_scales(sr, kb + 1);
+        } else if (t + units < total) {
+          tn = decode_tile<G>(t + units, prefix, p);
+          sr = scale_rows(tn);
+          load_scales(sr, 0);
         }
         int w_ok = 1;
         if (lane == 0) w_ok = wait_phase(smem_addr(&part_full[pb]), pb_phase, abort);
@@ -291,8 +320,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
           tmem_ld_wait();
           if (h == static_cast<int>(kBwCols / kBwPiece) - 1) {
             // Every load of the block has landed: release the buffer before the last
-            // piece's multiply-adds.  Relaxed: the next block's scale loads just issued
-            // stay in flight instead of being waited for.
+            // piece's multiply-adds.  Relaxed: the scale loads just issued stay in
+            // flight instead of being waited for.
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive_relaxed(smem_addr(&part_empty[pb]));
@@ -311,8 +340,12 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
         }
       }
       if (!ok) break;
-      // Epilogue: act(y + bias[e, n]) * row_scale[r] on the finished sums, 8 columns
-      // per 16-byte store (N is a multiple of 8: a group of 8 is in or past N whole).
+      // Epilogue: act(y + bias[e, n]) * row_scale[r] on the finished sums, 32 columns at
+      // a time.  When all 32 rows of the warp are in the group, a chunk is staged in
+      // this warp's tile in TMA's 64-byte swizzle (16-byte block b of row r at
+      // b ^ ((r >> 1) & 3)) and leaves through one tensor store of the 32 x 32 box,
+      // which clips the columns past N; otherwise 16-byte stores masked to the group's
+      // rows and to N (N is a multiple of 8: a group of 8 columns is in or past N whole).
       const bool fused = p.epi_bias != nullptr || p.epi_row_scale != nullptr || p.epi_act != kActNone;
       if (p.epi_bias != nullptr) {   // the warp's bias columns, staged once per tile
         __syncwarp();
@@ -325,30 +358,48 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
         }
         __syncwarp();
       }
+      const bool row_ok = trow < ti.nrows;
+      const uint32_t grow = ti.row0 + trow;
       const float rs = (p.epi_row_scale != nullptr && row_ok) ? __ldg(p.epi_row_scale + grow) : 1.0f;
+      const bool whole = p.c_tma && quad * 32u + 32u <= ti.nrows;
       __nv_bfloat16 *crow = p.c + static_cast<size_t>(grow) * p.N + ncol0;
 #pragma unroll
-      for (int q = 0; q < static_cast<int>(kBwCols / 8); ++q) {
-        float y[8];
+      for (int cc = 0; cc < kChunks; ++cc) {
+        uint32_t w[16];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) y[k] = acc[8 * q + k];
-        if (fused) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float b = p.epi_bias != nullptr ? __bfloat162float(bias_s[8 * q + k]) : 0.0f;
-            y[k] = epilogue_op(y[k], b, p.epi_act, rs);
+        for (int k = 0; k < 16; ++k) {
+          float y0 = acc[32 * cc + 2 * k], y1 = acc[32 * cc + 2 * k + 1];
+          if (fused) {
+            const float b0 = p.epi_bias != nullptr ? __bfloat162float(bias_s[32 * cc + 2 * k]) : 0.0f;
+            const float b1 = p.epi_bias != nullptr ? __bfloat162float(bias_s[32 * cc + 2 * k + 1]) : 0.0f;
+            y0 = epilogue_op(y0, b0, p.epi_act, rs);
+            y1 = epilogue_op(y1, b1, p.epi_act, rs);
           }
+          w[k] = pack_bf16x2(y0, y1);
         }
-        if (row_ok && ncol0 + 8u * q < static_cast<uint32_t>(p.N)) {
-          uint4 out;
-          out.x = pack_bf16x2(y[0], y[1]);
-          out.y = pack_bf16x2(y[2], y[3]);
-          out.z = pack_bf16x2(y[4], y[5]);
-          out.w = pack_bf16x2(y[6], y[7]);
-          *reinterpret_cast<uint4 *>(crow + 8 * q) = out;
+        if (whole) {
+          if (lane == 0) bulk_wait_read<0>();   // the previous store has read the staging tile
+          __syncwarp();
+          uint8_t *row_p = dyn_smem + (stg - dyn_base) + lane * 64;
+#pragma unroll
+          for (uint32_t b = 0; b < 4; ++b)
+            *reinterpret_cast<uint4 *>(row_p + ((b ^ ((static_cast<uint32_t>(lane) >> 1) & 3u)) << 4)) =
+                make_uint4(w[4 * b], w[4 * b + 1], w[4 * b + 2], w[4 * b + 3]);
+          fence_async_smem();   // this thread's staging writes, before the async proxy reads them
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&p.c_map, stg, static_cast<int32_t>(ncol0 + 32u * cc), static_cast<int32_t>(ti.row0 + quad * 32u));
+            bulk_commit();
+          }
+        } else if (row_ok) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (ncol0 + 32u * cc + 8u * q < static_cast<uint32_t>(p.N))
+              *reinterpret_cast<uint4 *>(crow + 32 * cc + 8 * q) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
         }
       }
     }
+    if (lane == 0) bulk_wait_all();   // the tensor stores have read their staging tiles
     if (!ok && lane == 0) atomicOr(p.status, kStatusTimeout);
   }
 
