@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
       return r;
     };
     // The scales of block kb + 1 are loaded while block kb is promoted, and those of the
-    // next tile's first block (with the next tile's decode) during this tile's last
-    // block, so no load's latency is waited for between blocks or between tiles.
+    // next tile's first block (with the next tile's decode) before this tile's epilogue,
+    // so no load's latency is waited for between blocks or between tiles.
     float isn = 0.0f, wsn[kChunks];
     auto load_scales = [&](const ScaleRows &r, int kb) {
       isn = r.row_ok ? __ldg(r.is_row + kb) : 0.0f;
@@ -300,13 +300,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
         float wsv[kChunks];
 #pragma unroll
         for (int c = 0; c < kChunks; ++c) wsv[c] = wsn[c];
-        if (kb + 1 < NKB) {
-          load_scales(sr, kb + 1);
-        } else if (t + units < total) {
-          tn = decode_tile<G>(t + units, prefix, p);
-          sr = scale_rows(tn);
-          load_scales(sr, 0);
-        }
+        if (kb + 1 < NKB) load_scales(sr, kb + 1);
         int w_ok = 1;
         if (lane == 0) w_ok = wait_phase(smem_addr(&part_full[pb]), pb_phase, abort);
         if (!__shfl_sync(0xffffffffu, w_ok, 0)) { ok = false; break; }
@@ -340,6 +334,11 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
         }
       }
       if (!ok) break;
+      if (t + units < total) {   // the next tile, and its first block's scales (in flight during the epilogue)
+        tn = decode_tile<G>(t + units, prefix, p);
+        sr = scale_rows(tn);
+        load_scales(sr, 0);
+      }
       // Epilogue: act(y + bias[e, n]) * row_scale[r] on the finished sums, 32 columns at
       // a time.  When all 32 rows of the warp are in the group, a chunk is staged in
       // this warp's tile in TMA's 64-byte swizzle (16-byte block b of row r at
