@@ -20,14 +20,20 @@
 // 32-column TMEM load.  A promotion is one multiply-add per element.
 //
 // One CTA per tile of 128 token rows.  A K block of 128 is one stage, 512 cycles of
-// tensor work at the e4m3 rate.  The promotion of a block must fit in that time, and
-// two partial buffers leave it little slack: the MMA of block kb + 2 waits for the
-// release of block kb.  So a promotion warp reads a partial 64 columns per TMEM wait
-// (two waits per block), releases the buffer as soon as its last load has landed,
-// before that half's multiply-adds, and folds two columns per paired fp32 FMA.
+// tensor work at the e4m3 rate.  Two partial buffers leave the promotion little
+// slack: the MMA of block kb + 2 waits for the release of block kb.  So a promotion
+// warp reads a partial 64 columns per TMEM wait (two waits per block), releases the
+// buffer as soon as its last load has landed, before that piece's multiply-adds, and
+// folds two columns per paired fp32 FMA.  A microbenchmark of this pipeline alone
+// (operands fixed in shared memory) runs a block in ~740 cycles with the promotion's
+// loads and multiply-adds, against 512 with an immediate release: the fp32 work (one
+// multiply-add per element, half the MMA time per block on each SM sub-partition)
+// and the barrier round trips do not fit beside one block of MMAs.
 // Tried and measured no better: 192- and 128-row tiles with 12 promotion warps or
-// four partial buffers, and a CTA-pair form (cta_group::2), whose every block
-// crosses CTAs twice.
+// four partial buffers, a CTA-pair form (cta_group::2), whose every block crosses CTAs
+// twice, N = 128 halves of each block with their own barriers, spinning instead of
+// suspended barrier waits, a warp that stages the scales in shared memory, and
+// 32-byte direct stores of C instead of the tensor stores.
 //
 // Roles (384 threads per CTA, three warpgroups):
 //   warp 0       TMA producer: per stage (128 of K) a 128-row token slab (16 KB) and
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
       if (total > 0 && lane == 0) {
         const uint4 *src = reinterpret_cast<const uint4 *>(&p.tok_map);
         uint4 *dst = reinterpret_cast<uint4 *>(slot);
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < 8; ++i) dst[i] = src[i];
         tensormap_set_dim1(dst, __ldg(p.a_offsets + p.num_groups));
         tensormap_set_box1(dst, kBwCtaTok);
