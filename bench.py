@@ -4,13 +4,15 @@
                     [--impl ours|reference]
 
 With no --workload (or --workload all) one run measures the five configurations
-of the mixture-of-experts shapes in turn: tiny (E=4, 60 rows, N=K=256), decode
+of the mixture-of-experts shapes in turn, tiny (E=4, 60 rows, N=K=256), decode
 (2048 rows over 64 experts, K=2048, N=2816), prefill (32768 rows over 8 experts,
 K=4096, N=14336), fine_grained (32768 rows over 128 experts with 13 skipped,
 K=7168, N=4096) and int4 (8192 rows over 64 experts of packed 4-bit weights,
-K=N=4096).  Each gets its own timed region, roofline, end-to-end number, CPU
-oracle baseline with a parity check of the timed output, and clock record, under
-"configs".  The top-level line repeats the entry of prefill, the largest of them.
+K=N=4096), then fp8_block_prefill (the prefill shape with e4m3 operands and fp32
+scales per 128 of K).  Each gets its own timed region, roofline, end-to-end number,
+CPU oracle baseline with a parity check of the timed output, and clock record, under
+"configs".  The top-level line repeats the entry of prefill, the largest of the five
+mixture-of-experts shapes.
 
 One step = one gmm_run (gmm_run_int4 for the 4-bit workload) over the whole
 workload: every group, every row, all N columns.  Inputs are seeded synthetic
@@ -349,9 +351,10 @@ def sample_desc(r, s):
 
 # ------------------------------------------------------------------ main
 
-# The configurations of the default run, in order; the headline of the JSON line is the
-# largest of them.
-DEFAULT_CONFIGS = ("tiny", "decode", "prefill", "fine_grained", "int4")
+# The configurations of the default run, in order: the five mixture-of-experts shapes,
+# then the prefill shape with e4m3 operands and per-K-block scales (the block-scaled
+# kernel).  The headline of the JSON line is prefill, the largest of the five.
+DEFAULT_CONFIGS = ("tiny", "decode", "prefill", "fine_grained", "int4", "fp8_block_prefill")
 HEADLINE = "prefill"
 
 
@@ -625,7 +628,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="all", choices=["all", *wl.WORKLOAD_NAMES],
                     help="'all' (default): the five configurations tiny, decode, prefill, fine_grained "
-                         "and int4, each timed in turn, prefill as the headline")
+                         "and int4, then fp8_block_prefill, each timed in turn, prefill as the headline")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--oracle-seconds", type=float, default=3.0,
                     help="CPU oracle work per step of the reference arm / per cpu_baseline pass")
