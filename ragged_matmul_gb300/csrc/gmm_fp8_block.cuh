@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kBwThreads, 1) gmm_fp8_block_kernel(const __gr
           }
           w[k] = pack_bf16x2(y0, y1);
         }
-        if (whole) {
+        if (whole && ncol0 + 32u * cc < static_cast<uint32_t>(p.N)) {   // (a box wholly past N: nothing to store)
           if (lane == 0) bulk_wait_read<0>();   // the previous store has read the staging tile
           __syncwarp();
           uint8_t *row_p = dyn_smem + (stg - dyn_base) + lane * 64;

@@ -1107,10 +1107,11 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
           const uint32_t row = 8 * g + st_row;
           stmatrix_x4_trans(stg + row * kEpiRowBytes + ((st_blk ^ ((row >> 1) & 3u)) << 4), w[0], w[1], w[2], w[3]);
         }
-        if (p.c_tma && c0 + 32u <= ti.nrows) {
+        if (p.c_tma && c0 + 32u <= ti.nrows && ncta < static_cast<uint32_t>(p.N)) {
           // A whole chunk of the group's rows: the staging tile is laid out in TMA's
           // 64-byte swizzle, so one store of the 32 x 32 box takes it to C (columns past
-          // N are clipped by the map).  The warp's memory queue then holds no C stores.
+          // N are clipped by the map; a box wholly past N is not issued).  The warp's
+          // memory queue then holds no C stores.
           fence_async_smem();   // this thread's stmatrix writes, before the async proxy reads them
           __syncwarp();
           if (lane == 0) {
