@@ -333,7 +333,7 @@ int launch(gmm_ctx *h, GmmParams &p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cudaLaunchAttribute attr[1];
-  // Short K: 8 epilogue warps (the bf16 / e4m3 kernel reads its warp count from blockDim).
+  // Short K: 12 epilogue warps (the bf16 / e4m3 kernel reads its warp count from blockDim).
   cfg.blockDim = dim3(kInt4 ? gmm::kInt4Threads : (p.K <= gmm::kWideEpilogueMaxK ? gmm::kThreadsWide : gmm::kThreads));
   cfg.gridDim = dim3(static_cast<unsigned>(v.grid));
   cfg.dynamicSmemBytes = v.smem;

@@ -58,8 +58,9 @@
 //                shared-memory staging tile (the transpose from weight-row lanes
 //                to C rows) -> 16-byte stores to C, masking token rows past the
 //                group's end and columns past N; two accumulators let it overlap
-//                the next tile's main loop.  A 320-thread launch (bf16 / e4m3 with
-//                short K) adds warps 6..9, which take alternate 32-row chunks.
+//                the next tile's main loop.  A 448-thread launch (bf16 / e4m3 with
+//                short K) adds warps 6..13: the three warps of a TMEM lane quadrant
+//                take every third 32-row chunk.
 //   warp 6       (4-bit) TMA producer of packed slabs.
 //   warps 7..18  (4-bit) dequantisation.
 //
@@ -87,9 +88,10 @@ constexpr int kMaxStages = 12;                // deepest W+T stage ring
 constexpr int kMaxGroups = 4096;
 constexpr int kThreads = 192;                 // bf16 kernel: producer, MMA, 4 epilogue warps
 // With short K a tile is a few stages, and storing its accumulator takes longer than
-// computing it: the bf16 / e4m3 kernel then runs 8 epilogue warps, two per TMEM lane
-// quadrant, taking alternate 32-row chunks.
-constexpr int kThreadsWide = 320;
+// computing it: the bf16 / e4m3 kernel then runs 12 epilogue warps, three per TMEM lane
+// quadrant, each taking every third 32-row chunk (lora_qkv, K = 64: 0.0407 ms with 8
+// warps, 0.0371 with 12; 16 would leave 96 registers a thread and spill).
+constexpr int kThreadsWide = 448;
 constexpr int kWideEpilogueMaxK = 512;
 // 4-bit kernel: 64-wide K sub-slabs per stage, and the dequantisation warps.  The
 // 12 warps form kDqGroups groups that take the stages in turn (stage s goes to group
@@ -122,9 +124,9 @@ static_assert(kQRowBytes == 128, "the packed chunk is one 128-byte swizzle row p
 // of bank conflicts.
 constexpr uint32_t kEpiRows = 32;
 constexpr uint32_t kEpiRowBytes = 64;
-constexpr int kEpiStageBytes = 8 * kEpiRows * kEpiRowBytes;   // up to 8 epilogue warps
+constexpr int kEpiStageBytes = 12 * kEpiRows * kEpiRowBytes;   // up to 12 epilogue warps
 template <bool kInt4>
-constexpr uint32_t kEpiBytes = kInt4 ? kEpiStageBytes / 2 : kEpiStageBytes;   // the 4-bit kernel has 4
+constexpr uint32_t kEpiBytes = kInt4 ? 4 * kEpiRows * kEpiRowBytes : kEpiStageBytes;   // the 4-bit kernel has 4
 constexpr uint32_t kAccCols = 256;            // TMEM columns per accumulator
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 // 4-bit kernel: dequantised weight slabs live in TMEM (128 lanes = weight rows, 32
@@ -600,7 +602,7 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
     gmm_grouped_kernel(const __grid_constant__ GmmParams p) {
   static_assert(!(kInt4 && kFp8), "the e4m3 path has its weights in shared memory");
   using G = Geom<kInt4, kPair>;
-  // Epilogue warps 2 .. 2 + n_epi - 1: 4, or 8 in a wide launch (bf16 / e4m3 only).
+  // Epilogue warps 2 .. 2 + n_epi - 1: 4, or 12 in a wide launch (bf16 / e4m3 only).
   const uint32_t n_epi = kInt4 ? 4u : blockDim.x / 32u - 2u;
   const uint32_t epi_arrivals = (kPair ? 2u : 1u) * n_epi;   // one per epilogue warp of each CTA
   constexpr uint32_t kDequantWarps = kDequantThreads / 32;
@@ -984,12 +986,12 @@ __global__ void __launch_bounds__(kInt4 ? kInt4Threads : kThreadsWide, 1)
       if (lane == 0) mbar_arrive(smem_addr(&ctl.maps_ready));
     }
     const uint32_t quad = static_cast<uint32_t>(warp & 3);   // TMEM lanes this warp may read
-    // With 8 epilogue warps, warps 2 .. 5 take the even 32-row chunks of a tile and
-    // warps 6 .. 9 the odd ones.
+    // With 12 epilogue warps, warps 2 .. 5 take 32-row chunks 0, 3, 6 of a tile, warps
+    // 6 .. 9 chunks 1, 4, 7 and warps 10 .. 13 chunks 2, 5.
     const uint32_t esub = static_cast<uint32_t>(warp - 2) >> 2, nsub = n_epi >> 2;
-    // Staging buffers per warp: two with 4 epilogue warps (bf16 / e4m3: 16 KB in all), one
-    // with 8, and one in the 4-bit kernel (8 KB for its 4 warps).
-    const uint32_t nbuf = kEpiBytes<kInt4> / (n_epi * kEpiRows * kEpiRowBytes);
+    // Staging buffers per warp: two with 4 epilogue warps (bf16 / e4m3: 16 of the 24 KB),
+    // one with 12, and one in the 4-bit kernel (8 KB for its 4 warps).
+    const uint32_t nbuf = kEpiBytes<kInt4> / (n_epi * kEpiRows * kEpiRowBytes) >= 2u ? 2u : 1u;
     uint32_t chunk_ctr = 0, outstanding = 0, last_buf = 0;   // this warp's TMA-store bookkeeping
     const uint32_t acc_empty0 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[0]), 0) : smem_addr(&ctl.acc_empty[0]);
     const uint32_t acc_empty1 = kPair ? map_to_rank(smem_addr(&ctl.acc_empty[1]), 0) : smem_addr(&ctl.acc_empty[1]);
