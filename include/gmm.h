@@ -67,13 +67,15 @@ typedef struct gmm_ctx *gmm_handle_t;
  * the host-side set-up that the grouped GEMM page's launcher does before its
  * persistent kernel (Modular "grouped_matmul_sm100_persistent", description: it
  * builds the TMA descriptors and picks the pipeline depth from the shared memory
- * available): here the ring depths of every kernel are sized from the device's
- * opt-in shared memory once, and the tensor maps are built per call.
+ * available): here every kernel's shared-memory budget is read from the device's
+ * opt-in shared memory once, each launch sizes its rings beside that call's group
+ * prefix, and the tensor maps are built per call.
  * Allocates the handle's device workspace on `device` (cudaMalloc).  The
  * caller's current device is left unchanged.
  * Errors: GMM_ERR_INVALID_ARG (out == NULL, num_experts < 1),
  *         GMM_ERR_NO_DEVICE (no such device, or not compute capability 10.3),
- *         GMM_ERR_CUDA (allocation failed).  *out is NULL on error.
+ *         GMM_ERR_CUDA (allocation failed, or a kernel's launch configuration could
+ *         not be set up).  *out is NULL on error.
  */
 int gmm_create(gmm_handle_t *out, int num_experts, int device);
 
